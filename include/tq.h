@@ -1,0 +1,148 @@
+/*
+ * tq.h - C ABI of libtq, the ternary-weight linear layer for NVIDIA B300 (sm_103a).
+ *
+ * The method (sources cited by page title and section):
+ *   - Weights are ternary t in {-1, 0, +1} times a scale; one FP16 scale per group of weights
+ *     (cosmocat.dev "27B 大模型塞进 5.9GB：三值量化，凭什么「不崩」？", section 一 and section 二 ②:
+ *     128 weights per group; tantan.ink/?p=490, install command: the MoE build uses "g64").
+ *   - Trits are stored packed: base-3, 20 trits per 32-bit integer, about 1.6 bits per weight
+ *     (tantan.ink/?p=490, section "为什么 1.58bit 没变成乱码", point 3), or 2 bits per trit.
+ *   - Weights were Hadamard-rotated offline; at inference the matching fast transform, O(n log n),
+ *     is applied to the activations (cosmocat.dev, section 二 ①).
+ *   - Kernels compute directly on the packed format; decompressing to floats in memory would give
+ *     back the savings (cosmocat.dev, section 二 ③).
+ *   - MoE: 256 routed experts, 8 active per token, router gate in full precision
+ *     (tantan.ink/?p=490, point 1).
+ *
+ * Conventions for every entry point:
+ *   - Data pointers are DEVICE pointers owned by the caller.  The library allocates nothing and
+ *     frees nothing; scratch space is a caller-provided workspace of at least *_workspace_bytes()
+ *     bytes, 256-byte aligned.
+ *   - Work is enqueued asynchronously on ``stream`` (a cudaStream_t passed as void*; NULL = the
+ *     legacy default stream).  No entry point synchronizes.
+ *   - Argument errors are detected on the host before anything is launched and returned
+ *     synchronously (TQ_ERR_INVALID_ARG / TQ_ERR_UNSUPPORTED / TQ_ERR_MISALIGNED /
+ *     TQ_ERR_WORKSPACE).  A failed launch returns TQ_ERR_CUDA.  Data errors found on the device
+ *     (a non-canonical code word, a trit outside {-1,0,1}, a bounded wait that ran out) are
+ *     recorded in a device status word read by tq_device_status().
+ *   - Layouts are row-major.  codes [N][P] uint32 with P = tq_row_pitch_words();
+ *     scales [N][ceil(K/group)] FP16; activations [rows][K] bf16; MoE weights stacked per expert.
+ *   - bf16 and FP16 values are passed as their 16-bit patterns (uint16_t).
+ *   - Single GPU.  There is no CPU fallback: without a CUDA device every compute call returns
+ *     TQ_ERR_CUDA.
+ */
+#ifndef TQ_H_
+#define TQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  TQ_OK = 0,
+  TQ_ERR_INVALID_ARG = 1,   /* null pointer, non-positive size, inconsistent descriptor */
+  TQ_ERR_UNSUPPORTED = 2,   /* valid but not implemented: group not 64/128, K not a multiple of 128, ... */
+  TQ_ERR_MISALIGNED = 3,    /* a pointer is not 16-byte aligned (workspace: 256-byte) */
+  TQ_ERR_INVALID_CODE = 4,  /* device-reported: code word not canonical, or trit outside {-1,0,1} */
+  TQ_ERR_CUDA = 5,          /* a CUDA runtime call or launch failed */
+  TQ_ERR_TIMEOUT = 6,       /* device-reported: a bounded wait inside a kernel ran out */
+  TQ_ERR_WORKSPACE = 7,     /* workspace smaller than the matching *_workspace_bytes() */
+  TQ_ERR_RANGE = 8          /* device-reported: a transformed activation is outside the FP16 range */
+} tq_status;
+
+typedef enum {
+  TQ_PACK_B3 = 1,   /* base-3: word = sum_{i<20} (t[20j+i]+1) * 3^i; pad trits t=0; row pitch multiple of 4 words */
+  TQ_PACK_2BIT = 2  /* 2-bit : word = sum_{i<16} (t[16j+i]+1) << 2i;  field 3 invalid; pad trits t=0 */
+} tq_packing;
+
+/* One ternary weight matrix W [N][K] (y = W x~). */
+typedef struct {
+  int32_t N;          /* output features: rows of W, >= 1 */
+  int32_t K;          /* input features (reduction dim), >= 1 */
+  int32_t group;      /* weights per FP16 scale along K: 64 or 128 */
+  int32_t packing;    /* tq_packing */
+  int32_t fwht_block; /* 128: apply the block Walsh-Hadamard transform to the input; 0: input used as given */
+} tq_desc;
+
+/* ---- format sizes (host only, no device access) ------------------------------------------------
+ * Row pitch in uint32 words: base-3 roundup(ceil(K/20), 4), 2-bit roundup(ceil(K/16), 4).
+ * (tantan.ink/?p=490, point 3: 20 trits per 32-bit word.)  Return 0 for an invalid descriptor. */
+size_t tq_row_pitch_words(const tq_desc* d);
+size_t tq_packed_bytes(const tq_desc* d);      /* N * pitch * 4 */
+size_t tq_scale_bytes(const tq_desc* d);       /* N * ceil(K/group) * 2 (cosmocat.dev, section 二 ②) */
+
+/* ---- tq_pack: int8 trits [N][K] -> codes [N][P] --------------------------------------------------
+ * Packs row-contiguous trits across group boundaries; trits past K and whole padding words hold
+ * t = 0.  A trit outside {-1,0,1} records TQ_ERR_INVALID_CODE in the device status (its word is
+ * written as if the trit were 0).  trits: device, 1-byte aligned; codes: device, 16-byte aligned. */
+tq_status tq_pack(const tq_desc* d, const int8_t* trits, uint32_t* codes, void* stream);
+
+/* ---- tq_unpack: codes [N][P] -> int8 trits [N][K] ------------------------------------------------
+ * Digit i of a base-3 word v is (v / 3^i) mod 3, t = digit - 1; field i of a 2-bit word is
+ * (v >> 2i) & 3.  invalid_words (device int32, may be NULL) receives the number of words in the
+ * whole pitch that are not valid encodings (base-3: v > 3^20 - 1; 2-bit: a field equal to 3); it is
+ * overwritten, not accumulated.  Invalid words are decoded as written (digits taken mod 3 / field 3
+ * -> t = 2 is clamped to 0).  A non-zero count is also recorded as TQ_ERR_INVALID_CODE. */
+tq_status tq_unpack(const tq_desc* d, const uint32_t* codes, int8_t* trits, int32_t* invalid_words,
+                    void* stream);
+
+/* ---- tq_fwht: x~[r, 128b + i] = sum_c H[i][c] x[r, 128b + c] / sqrt(block) -----------------------
+ * Block Walsh-Hadamard transform (Sylvester order) of each row of x (bf16 [rows][K]); block must be
+ * 128 and K a multiple of it (cosmocat.dev, section 二 ①).  out_fp16 = 0: out is float [rows][K];
+ * out_fp16 = 1: out is FP16 [rows][K] (values beyond the FP16 range record TQ_ERR_RANGE). */
+tq_status tq_fwht(const uint16_t* x, void* out, int out_fp16, int rows, int K, int block, void* stream);
+
+/* ---- tq_gemv: decode GEMV, y[b][n] = sum_k s[n][k/group] * t[n][k] * x~[b][k] ----------------------
+ * x: bf16 [batch][K], 1 <= batch <= 16; x~ = block FWHT of x (or x itself when fwht_block = 0).
+ * y: float [batch][N].  Requires K a multiple of 128.  Streams each code word from HBM once per call.
+ * workspace >= tq_gemv_workspace_bytes(d, batch).  Calls on one stream are ordered; two calls that
+ * share a workspace must not overlap in time. */
+size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch);
+tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                  int batch, float* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- tq_moe_route: top-k experts per token --------------------------------------------------------
+ * logits: float [T][E] (router at full precision, tantan.ink/?p=490 point 1).  idx: int32 [T][topk]
+ * in the order (logit descending, expert index ascending); gate: float [T][topk] =
+ * softmax over the topk chosen logits.  E <= 256, topk <= 8 (the pages' top-8 of 256). */
+tq_status tq_moe_route(const float* logits, int T, int E, int topk, int32_t* idx, float* gate, void* stream);
+
+/* ---- tq_moe_gemv: routed SwiGLU expert layer at decode time ----------------------------------------
+ * For each token: route (as tq_moe_route); x~ = FWHT(x); for each chosen expert e:
+ * g = Wg[e] x~, u = Wu[e] x~ (gate_up rows 0..F-1 then F..2F-1), h = silu(g) * u,
+ * y_e = Wd[e] FWHT(h); y = sum_j gate_j y_{e_j} in slot order j = 0..topk-1 (deterministic).
+ * gate_up: desc with N = 2F, K = H; down: desc with N = H, K = F (same packing/group/fwht).
+ * gu_codes [E][2F][P_H], gu_scales [E][2F][H/group], d_codes [E][H][P_F], d_scales [E][H][F/group].
+ * x: bf16 [T][H]; idx/gate as tq_moe_route; h_out: float [T][topk][F] or NULL; y: float [T][H].
+ * Each active expert's codes are read once per call for all the tokens routed to it. */
+size_t tq_moe_workspace_bytes(int T, int E, int topk, int H, int F);
+tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, int E, int topk,
+                      const uint32_t* gu_codes, const uint16_t* gu_scales,
+                      const uint32_t* d_codes, const uint16_t* d_scales,
+                      const float* router_logits, const uint16_t* x, int T,
+                      int32_t* topk_idx, float* topk_gate, float* h_out, float* y,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- tq_gemm: batched prefill, Y[m][n] = bf16( sum_k s[n][k/group] t[n][k] x~[m][k] ) -------------
+ * x: bf16 [M][K]; y: bf16 [M][N]; fp32 accumulation.  x~ is held as FP16 (|x~| must stay below
+ * 65504, else TQ_ERR_RANGE is recorded).  Requires K a multiple of 128.
+ * workspace >= tq_gemm_workspace_bytes(d, M). */
+size_t tq_gemm_workspace_bytes(const tq_desc* d, int M);
+tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                  int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- status ---------------------------------------------------------------------------------------
+ * Reads the device status word of the current device (the first error any kernel recorded since the
+ * last read), stores it in *status (TQ_OK if none) and clears it.  This call synchronizes the device. */
+tq_status tq_device_status(int32_t* status);
+const char* tq_status_str(tq_status s);
+int tq_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TQ_H_ */

@@ -1,0 +1,92 @@
+// libtq host entry points that do not launch compute: sizes, status, version.
+#include <cstring>
+
+#include "tq_internal.cuh"
+#include "tq_kernels.cuh"
+
+namespace tq {
+
+__device__ int g_status = 0;
+
+namespace {
+constexpr int kMaxDevices = 64;
+int* g_status_addr[kMaxDevices] = {nullptr};
+}  // namespace
+
+// Address of this device's status word; looked up once per device (current device at call time).
+int* status_ptr() {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (!g_status_addr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
+      (void)cudaGetLastError();
+      return nullptr;
+    }
+    g_status_addr[dev] = static_cast<int*>(p);
+  }
+  return g_status_addr[dev];
+}
+
+tq_status check_linear_desc(const tq_desc* d) {
+  if (!d || d->N < 1 || d->K < 1) return TQ_ERR_INVALID_ARG;
+  if (d->packing != TQ_PACK_B3 && d->packing != TQ_PACK_2BIT) return TQ_ERR_INVALID_ARG;
+  if (d->group != 64 && d->group != 128) return TQ_ERR_UNSUPPORTED;
+  if (d->fwht_block != 0 && d->fwht_block != kFwhtBlock) return TQ_ERR_UNSUPPORTED;
+  if (d->K % kFwhtBlock != 0) return TQ_ERR_UNSUPPORTED;
+  return TQ_OK;
+}
+
+}  // namespace tq
+
+using namespace tq;
+
+static bool desc_ok(const tq_desc* d) {
+  return d && d->N >= 1 && d->K >= 1 && (d->packing == TQ_PACK_B3 || d->packing == TQ_PACK_2BIT);
+}
+
+extern "C" size_t tq_row_pitch_words(const tq_desc* d) {
+  return desc_ok(d) ? static_cast<size_t>(pitch_words(d->K, d->packing)) : 0;
+}
+
+extern "C" size_t tq_packed_bytes(const tq_desc* d) {
+  return desc_ok(d) ? static_cast<size_t>(d->N) * pitch_words(d->K, d->packing) * 4 : 0;
+}
+
+extern "C" size_t tq_scale_bytes(const tq_desc* d) {
+  if (!desc_ok(d) || d->group < 1) return 0;
+  return static_cast<size_t>(d->N) * groups_of(d->K, d->group) * 2;
+}
+
+extern "C" tq_status tq_device_status(int32_t* out) {
+  if (!out) return TQ_ERR_INVALID_ARG;
+  int* p = status_ptr();
+  if (!p) return TQ_ERR_CUDA;
+  int v = 0;
+  if (cudaDeviceSynchronize() != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+  const int zero = 0;
+  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ERR_CUDA;
+  *out = v;
+  return TQ_OK;
+}
+
+extern "C" const char* tq_status_str(tq_status s) {
+  switch (s) {
+    case TQ_OK: return "ok";
+    case TQ_ERR_INVALID_ARG: return "invalid argument";
+    case TQ_ERR_UNSUPPORTED: return "unsupported shape or option";
+    case TQ_ERR_MISALIGNED: return "misaligned pointer";
+    case TQ_ERR_INVALID_CODE: return "invalid packed code or trit";
+    case TQ_ERR_CUDA: return "CUDA error";
+    case TQ_ERR_TIMEOUT: return "bounded device wait timed out";
+    case TQ_ERR_WORKSPACE: return "workspace too small";
+    case TQ_ERR_RANGE: return "transformed activation outside FP16 range";
+  }
+  return "unknown status";
+}
+
+extern "C" int tq_version(void) { return 1; }

@@ -1,0 +1,60 @@
+// Entry points of the dense ternary contraction: tq_gemv (decode) and tq_gemm (prefill).
+#include "tq_internal.cuh"
+#include "tq_kernels.cuh"
+#include "tq_simple.cuh"
+
+namespace tq {
+namespace {
+
+tq_status check_ptrs(const uint32_t* codes, const uint16_t* scales, const uint16_t* x, const void* y,
+                     const void* ws) {
+  if (!codes || !scales || !x || !y || !ws) return TQ_ERR_INVALID_ARG;
+  if (!aligned(codes, 16) || !aligned(scales, 16) || !aligned(x, 16) || !aligned(y, 16)) return TQ_ERR_MISALIGNED;
+  if (!aligned(ws, 256)) return TQ_ERR_MISALIGNED;
+  return TQ_OK;
+}
+
+}  // namespace
+}  // namespace tq
+
+using namespace tq;
+
+extern "C" size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch) {
+  if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return 0;
+  return align256(static_cast<size_t>(batch) * d->K * sizeof(float));
+}
+
+extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                             int batch, float* y, void* workspace, size_t workspace_bytes, void* stream) {
+  tq_status st = check_linear_desc(d);
+  if (st != TQ_OK) return st;
+  if (batch < 1 || batch > kMaxBatch) return TQ_ERR_INVALID_ARG;
+  if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
+  if (workspace_bytes < tq_gemv_workspace_bytes(d, batch)) return TQ_ERR_WORKSPACE;
+  if (!status_ptr()) return TQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* xt = static_cast<float*>(workspace);
+  if (launch_fwht_bf16(x, xt, 0, batch, d->K, d->fwht_block != 0, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  if (launch_gemv_simple(d, codes, scales, xt, batch, y, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  return TQ_OK;
+}
+
+extern "C" size_t tq_gemm_workspace_bytes(const tq_desc* d, int M) {
+  if (check_linear_desc(d) != TQ_OK || M < 1) return 0;
+  return align256(static_cast<size_t>(M) * d->K * sizeof(float));
+}
+
+extern "C" tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                             int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream) {
+  tq_status st = check_linear_desc(d);
+  if (st != TQ_OK) return st;
+  if (M < 1) return TQ_ERR_INVALID_ARG;
+  if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
+  if (workspace_bytes < tq_gemm_workspace_bytes(d, M)) return TQ_ERR_WORKSPACE;
+  if (!status_ptr()) return TQ_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  float* xt = static_cast<float*>(workspace);
+  if (launch_fwht_bf16(x, xt, 0, M, d->K, d->fwht_block != 0, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  if (launch_gemm_simple(d, codes, scales, xt, M, y, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  return TQ_OK;
+}

@@ -1,0 +1,72 @@
+"""tq_gemv (decode) against the oracle: element by element on small and ragged shapes, and on
+sampled rows of every linear of the 27B-class decode layer at its full size."""
+import numpy as np
+import pytest
+import torch
+
+import ternary_weight_quantized_unpack_b300 as tq
+from ternary_weight_quantized_unpack_b300 import inputs
+from tq_testlib import LinearCase, check_tolerance, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+B3, B2 = tq.TQ_PACK_B3, tq.TQ_PACK_2BIT
+
+
+def run(case: LinearCase):
+    y = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    return y.cpu().numpy()
+
+
+def test_single_linear_1024():
+    """K = N = 1024, batch 1, base-3, group 128, 0.5 % x20 outliers, seed 0: every output."""
+    c = inputs.SINGLE_LINEAR
+    case = LinearCase(inputs.seed_of(1), 0, c["N"], c["K"], c["group"], c["packing"], c["B"],
+                      outlier_frac=c["outlier_frac"])
+    y_ref, A = case.oracle()
+    check_tolerance(run(case), y_ref, A)
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("group", [64, 128])
+@pytest.mark.parametrize("N,K,batch", [(1, 128, 1), (33, 384, 3), (200, 1024, 16), (129, 640, 5), (7, 2560, 8),
+                                        (300, 1280, 2)])
+def test_small_ragged(packing, group, N, K, batch):
+    case = LinearCase(11, N * 7 + batch, N, K, group, packing, batch)
+    y_ref, A = case.oracle()
+    check_tolerance(run(case), y_ref, A)
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+def test_no_transform(packing):
+    case = LinearCase(12, 3, 96, 512, 128, packing, 4, fwht_block=0)
+    y_ref, A = case.oracle()
+    check_tolerance(run(case), y_ref, A)
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("batch", [1, 4, 16])
+@pytest.mark.parametrize("lin", inputs.dense_layer_linears(), ids=lambda l: l.name)
+def test_dense_layer_full_size_sampled(lin, batch, packing):
+    """Full-size weights, the launch configuration the benchmark times; 48 sampled rows checked."""
+    tid = 100 + inputs.dense_layer_linears().index(lin)
+    case = LinearCase(inputs.seed_of(2), tid, lin.N, lin.K, 128, packing, batch)
+    y = run(case)
+    rows = sample_rows(lin.N, 48, seed=tid)
+    y_ref, A = case.oracle(rows)
+    check_tolerance(y[:, rows], y_ref, A)
+
+
+def test_zero_trits_and_determinism():
+    d = tq.desc(64, 1024, 128, B3)
+    codes = tq.tq_pack(d, torch.zeros((64, 1024), dtype=torch.int8, device="cuda"))
+    scales = inputs.scales(1, 1, 64, 8, device="cuda")
+    x = inputs.activations(1, 1, 4, 1024).cuda()
+    y = tq.tq_gemv(d, codes, scales, x)
+    assert torch.count_nonzero(y).item() == 0
+    case = LinearCase(13, 1, 512, 2048, 128, B2, 16)
+    y1 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
+    y2 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
+    assert torch.equal(y1, y2)
