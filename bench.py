@@ -90,26 +90,34 @@ def measured_peaks():
 
 
 class ClockSampler:
-    """Polls NVML (SM clock, max clock, throttle reasons) in a thread while the timed region runs."""
+    """Samples SM clock, max clock and throttle reasons while the timed region runs: NVML when it
+    loads, else ``nvidia-smi -lms 20`` in a subprocess."""
 
     REASONS = {"hw_slowdown": 0x8, "sw_thermal_slowdown": 0x20, "hw_thermal_slowdown": 0x40,
                "sw_power_cap": 0x4, "hw_power_brake_slowdown": 0x80}
+    SMI_FIELDS = ["clocks.sm", "clocks.max.sm", "clocks_event_reasons.hw_slowdown",
+                  "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+                  "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, index: int):
+        self.index = index
         self.samples, self.reasons, self.max_mhz = [], set(), None
         self._stop = threading.Event()
-        self.ok = False
+        self.mode, self.err = None, None
         try:
             import pynvml
             pynvml.nvmlInit()
             self.nv = pynvml
             self.h = pynvml.nvmlDeviceGetHandleByIndex(index)
             self.max_mhz = pynvml.nvmlDeviceGetMaxClockInfo(self.h, pynvml.NVML_CLOCK_SM)
-            self.ok = True
-        except Exception:
-            self.ok = False
+            self.mode = "nvml"
+        except Exception as e:  # NVML library missing: fall back to nvidia-smi
+            self.err = repr(e)
+            import shutil
+            if shutil.which("nvidia-smi"):
+                self.mode = "nvidia-smi"
 
-    def _run(self):
+    def _run_nvml(self):
         nv = self.nv
         while not self._stop.is_set():
             try:
@@ -123,21 +131,45 @@ class ClockSampler:
             time.sleep(0.002)
 
     def __enter__(self):
-        if self.ok:
-            self.t = threading.Thread(target=self._run, daemon=True)
+        if self.mode == "nvml":
+            self.t = threading.Thread(target=self._run_nvml, daemon=True)
             self.t.start()
+        elif self.mode == "nvidia-smi":
+            import subprocess
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), "--query-gpu=" + ",".join(self.SMI_FIELDS),
+                                          "--format=csv,noheader,nounits", "-lms", "20"],
+                                         stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)   # let the first sample land before the timed region starts
         return self
 
     def __exit__(self, *a):
-        if self.ok:
+        if self.mode == "nvml":
             self._stop.set()
             self.t.join()
+        elif self.mode == "nvidia-smi":
+            time.sleep(0.05)
+            self.proc.terminate()
+            out, _ = self.proc.communicate(timeout=10)
+            names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+            for line in out.splitlines():
+                f = [x.strip() for x in line.split(",")]
+                if len(f) < 6:
+                    continue
+                try:
+                    self.samples.append(float(f[0]))
+                    self.max_mhz = float(f[1])
+                except ValueError:
+                    continue
+                for n, v in zip(names, f[2:6]):
+                    if v.lower() == "active":
+                        self.reasons.add(n)
+        return False
 
     def summary(self):
-        if not self.ok:
-            return None
+        if self.mode is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "error": self.err}
         return {"sm_mhz": statistics.median(self.samples) if self.samples else None, "sm_max_mhz": self.max_mhz,
-                "reasons": sorted(self.reasons), "samples": len(self.samples)}
+                "reasons": sorted(self.reasons), "samples": len(self.samples), "source": self.mode}
 
 
 # ----------------------------------------------------------------------------------------------
@@ -520,8 +552,8 @@ def tq_launches_per_gemv():
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--batch", type=int, default=1)
     ap.add_argument("--no-extras", dest="extras", action="store_false")

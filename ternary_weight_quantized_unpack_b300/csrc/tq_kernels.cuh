@@ -11,6 +11,11 @@ cudaError_t launch_fwht_bf16(const uint16_t* x, void* out, int out_fp16, int row
 // Block FWHT (block 128) of fp32 rows into fp32.
 cudaError_t launch_fwht_f32(const float* x, float* out, int rows, int K, cudaStream_t s);
 
+// Tensor-core decode GEMV (preparation kernel + tcgen05 kernel); workspace from gemv_tc_workspace_bytes.
+size_t gemv_tc_workspace_bytes(const tq_desc* d, int batch);
+cudaError_t launch_gemv_tc(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                           int batch, float* y, void* ws, cudaStream_t s);
+
 // Host-side descriptor checks shared by the contraction entry points.
 tq_status check_linear_desc(const tq_desc* d);
 

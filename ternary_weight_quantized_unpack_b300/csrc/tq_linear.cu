@@ -21,7 +21,7 @@ using namespace tq;
 
 extern "C" size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch) {
   if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return 0;
-  return align256(static_cast<size_t>(batch) * d->K * sizeof(float));
+  return gemv_tc_workspace_bytes(d, batch);
 }
 
 extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
@@ -33,9 +33,10 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
   if (workspace_bytes < tq_gemv_workspace_bytes(d, batch)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* xt = static_cast<float*>(workspace);
-  if (launch_fwht_bf16(x, xt, 0, batch, d->K, d->fwht_block != 0, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
-  if (launch_gemv_simple(d, codes, scales, xt, batch, y, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  if (launch_gemv_tc(d, codes, scales, x, batch, y, workspace, s) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return TQ_ERR_CUDA;
+  }
   return TQ_OK;
 }
 

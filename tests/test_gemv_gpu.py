@@ -70,3 +70,28 @@ def test_zero_trits_and_determinism():
     y1 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
     y2 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
     assert torch.equal(y1, y2)
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("mag", [1e4, 1e-6, 0.0])
+def test_activation_magnitudes(packing, mag):
+    """Per-block exponent handling: very large, very small and all-zero activations."""
+    case = LinearCase(14, 2, 160, 1280, 128, packing, 3)
+    case.x_host = (case.x_host.float() * mag).to(torch.bfloat16)
+    case.x = case.x_host.cuda()
+    y_ref, A = case.oracle()
+    y = run(case)
+    check_tolerance(y, y_ref, A)
+    if mag == 0.0:
+        assert np.count_nonzero(y) == 0
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("N,K,batch", [(200, 17408, 1), (1, 17408, 16), (1000, 640, 2), (257, 3200, 7)])
+def test_split_tiles(packing, N, K, batch):
+    """Few rows, long K: tiles are split across many CTAs and summed by the last arriver."""
+    case = LinearCase(15, N + batch, N, K, 128, packing, batch)
+    y_ref, A = case.oracle()
+    check_tolerance(run(case), y_ref, A)
+    y2 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x).cpu().numpy()
+    assert np.array_equal(y2, run(case))   # deterministic across calls
