@@ -65,7 +65,9 @@ def test_zero_trits_and_determinism():
     scales = inputs.scales(1, 1, 64, 8, device="cuda")
     x = inputs.activations(1, 1, 4, 1024).cuda()
     y = tq.tq_gemv(d, codes, scales, x)
-    assert torch.count_nonzero(y).item() == 0
+    # all-zero trits: sum |s t x~| = 0, so the bound is the absolute 1e-5 (the tensor-core path sums
+    # (t + 1) x~ and subtracts sum x~, which cancels to ~1e-6 rather than to an exact 0)
+    assert torch.max(torch.abs(y)).item() <= 1e-5
     case = LinearCase(13, 1, 512, 2048, 128, B2, 16)
     y1 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
     y2 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
