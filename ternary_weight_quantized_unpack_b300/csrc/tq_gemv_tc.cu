@@ -41,10 +41,13 @@ constexpr int kRows = 128;                // rows per tile = MMA M = TMEM lanes
 constexpr int kStageWords = 32;           // code words per row per stage (128 bytes)
 constexpr int kRowPitchSmem = 144;        // 128 B + 16 B padding: conflict-free 16-byte row reads
 constexpr int kCodeStageBytes = kRows * kRowPitchSmem;
-constexpr int kRing = 4;                  // groups in flight between the decode warps and the MMA
-constexpr int kThreads = 192;             // warps 0-3 decode, 4 producer, 5 MMA + TMEM owner
+constexpr int kKLanes = 4;                // decode warp groups working on different stages
+constexpr int kDecodeWarps = 4 * kKLanes; // 4 lane quarters x 4 K-lanes
+constexpr int kProducerWarp = kDecodeWarps;
+constexpr int kMmaWarp = kDecodeWarps + 1;
+constexpr int kThreads = 32 * (kDecodeWarps + 2);
 constexpr uint32_t kLutBytes = 2u * 243u * 32u * 4u;
-constexpr int kMaxStages = 6;
+constexpr int kMaxStages = 8;
 
 template <int PACK>
 struct Geo;
@@ -60,13 +63,9 @@ struct Geo<TQ_PACK_2BIT> {
 template <int PACK, int G>
 struct Cfg {
   static constexpr int ST = Geo<PACK>::kStageTrits;
-  static constexpr int GP = G / 2;        // TMEM columns (FP16 pairs) per group
-  static constexpr int GPS = ST / G;      // groups per stage
-  static constexpr int SLICES = G / 16;   // K=16 MMAs per group
-  static constexpr int A_COLS = kRing * GP;
-  static constexpr int D_COL0 = A_COLS;
-  static constexpr int C_COL0 = A_COLS + kRing * 16;
-  static constexpr int TMEM_COLS = (C_COL0 + 8) <= 256 ? 256 : 512;
+  static constexpr int GPS = ST / G;        // groups per stage
+  static constexpr int CPG = G / 64;        // 64-trit chunks (32 TMEM columns) per group
+  static constexpr int CPS = ST / 64;       // chunks per stage
   static constexpr uint32_t LUT_BYTES = PACK == TQ_PACK_B3 ? kLutBytes : 0u;
 };
 
@@ -96,18 +95,24 @@ constexpr LutTable make_lut() {
 }
 __device__ const LutTable g_lut = make_lut();
 
+// TMEM columns (512 allocated): K-lane j owns A chunk slots [64j, 64j+64) (2 x 32 columns) and
+// D slots [256 + 32j, 256 + 32j + 32) (2 x 16 columns); the constant correction A is at 384.
+constexpr int kTmemCols = 512;
+constexpr int kDCol0 = 256;
+constexpr int kCCol = 384;
+
 struct Params {
   const uint32_t* codes;
   const uint16_t* scales;
-  const uint8_t* xhat;      // prepared activations, one block per stage
-  const float* pow2g;       // 2^(16 + e) per group (e = exponent of the group's block)
+  const uint8_t* xhat;      // prepared activations, one block per stage (x^, corrections, 2^(16+e))
   float* y;
-  float* partial;           // [tile][part][B][128] partial outputs of split tiles
-  int* counters;            // [tile] arrivals of split tiles (zeroed by the preparation kernel)
+  float* partial;           // [unit][B][128] partial outputs, indexed by the first unit of a part
+  int* counters;            // [tile] arrivals (zeroed by the preparation kernel, reset by the last arriver)
   int* status;
   int N, K, P, ng, B, n_tiles, spr, units;
-  uint32_t xhat_stage_bytes;  // bytes of one stage block of x^ (main + correction + zero chunk)
+  uint32_t xhat_stage_bytes;  // bytes of one stage block
   uint32_t corr_offset;       // offset of the correction chunks inside a stage block
+  uint32_t pow2_offset;       // offset of the per-group 2^(16+e) floats inside a stage block
   uint32_t stage_smem;        // shared-memory bytes per pipeline stage
   int stages;                 // pipeline depth
 };
@@ -117,124 +122,128 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* s_abort) {
   *s_abort = 1;
 }
 
-// CTA that owns unit u under the static partition u_c = floor(c * units / grid).
+// Static stream-K partition: CTA c owns units [floor(c U / G), floor((c+1) U / G)).
+__device__ __forceinline__ int cta_first_unit(long long c, long long units, long long grid) {
+  return static_cast<int>(c * units / grid);
+}
 __device__ __forceinline__ int cta_of_unit(long long u, long long units, long long grid) {
   return static_cast<int>(((u + 1) * grid + units - 1) / units - 1);
 }
+// A part is the run of units of one tile that one K-lane of one CTA decodes; unit u starts a part
+// when the previous unit of its K-lane (u - kKLanes) is outside its CTA or outside its tile.
+__device__ __forceinline__ bool starts_part(int u, int t, const Params& p, long long grid) {
+  const int c = cta_of_unit(u, p.units, grid);
+  const int first = cta_first_unit(c, p.units, grid);
+  return u - kKLanes < first || u - kKLanes < t * p.spr;
+}
 
-// Sink of decoded pairs for one decode thread: stages 16 pairs in registers, writes them to the
-// current group's A slot in TMEM, hands finished groups to the MMA and folds finished MMAs into acc.
+// One decode thread of one K-lane.  Produces 64-trit chunks of FP16 pairs into its K-lane's two
+// TMEM chunk slots; waits for the MMA of each chunk in order; when the last chunk of a group
+// completes, folds the group's 128 x 16 result into acc with the group's multiplier.
 template <int PACK, int G, int NB>
-struct Decoder {
+struct Lane {
   using C = Cfg<PACK, G>;
-  uint32_t lane_tmem;   // TMEM address of this warp's lane quarter, column 0
-  uint64_t* a_full;
-  uint64_t* mma_done;
-  float* m_ring;        // [kRing][128] per-thread multipliers of groups in flight
+  uint32_t tm;          // TMEM address of this warp's lane quarter, column 0
+  uint64_t* a_full;     // [2] of this K-lane
+  uint64_t* mma_done;   // [2] of this K-lane
+  float* m_ring;        // [2][128] multipliers of the groups in flight (this K-lane)
   volatile int* s_abort;
   const Params* p;
-  int r, lane;
-  int gc, consumed;
+  int j, r, lane;
+  int cc, waited;       // chunks produced / chunks whose MMA completion has been consumed
   bool ok;
   float acc[NB];
   uint32_t stg[16];
 
-  __device__ __forceinline__ uint32_t slot_col() const { return lane_tmem + (gc % kRing) * C::GP; }
+  __device__ __forceinline__ uint32_t a_col() const { return tm + 64u * j + 32u * (cc & 1); }
 
-  __device__ __forceinline__ void consume_one() {
-    const int q = consumed;
-    const int slot = q % kRing;
-    bool w = mbar_wait(mma_done + slot, (q / kRing) & 1);
+  __device__ __forceinline__ void wait_next() {
+    const int n = waited;
+    bool w = mbar_wait(mma_done + (n & 1), (n >> 1) & 1);
     w = __all_sync(0xffffffffu, w);
     if (!w) {
       ok = false;
       if (lane == 0) fail(*p, s_abort);
       return;
     }
-    tc_fence_after();
-    uint32_t d[NB];
-    tmem_ld<NB>(lane_tmem + C::D_COL0 + slot * 16, d);
-    tmem_wait_ld();
-    const float m = m_ring[slot * kRows + r];
+    if (n % C::CPG == C::CPG - 1) {  // last chunk of a group: its accumulator is final
+      const int g = n / C::CPG;
+      tc_fence_after();
+      uint32_t d[NB];
+      tmem_ld<NB>(tm + kDCol0 + 32u * j + 16u * (g & 1), d);
+      tmem_wait_ld();
+      const float m = m_ring[(g & 1) * kRows + r];
 #pragma unroll
-    for (int b = 0; b < NB; ++b) acc[b] = fmaf(m, __uint_as_float(d[b]), acc[b]);
-    ++consumed;
+      for (int b = 0; b < NB; ++b) acc[b] = fmaf(m, __uint_as_float(d[b]), acc[b]);
+    }
+    ++waited;
   }
-  __device__ __forceinline__ void begin_group() {
-    while (ok && gc - consumed >= kRing) consume_one();
+  __device__ __forceinline__ void begin_chunk() {
+    while (ok && waited <= cc - 2) wait_next();
   }
-  __device__ __forceinline__ void end_group(float m) {
+  // group_end: this chunk is the last of its group, m = its multiplier
+  __device__ __forceinline__ void end_chunk(bool group_end, float m) {
     tmem_wait_st();
     tc_fence_before();
-    m_ring[(gc % kRing) * kRows + r] = m;
+    if (group_end) m_ring[((cc / C::CPG) & 1) * kRows + r] = m;
     __syncwarp();
-    if (lane == 0) mbar_arrive(a_full + (gc % kRing));
-    ++gc;
+    if (lane == 0) mbar_arrive(a_full + (cc & 1));
+    ++cc;
   }
   __device__ __forceinline__ void drain() {
-    while (ok && consumed < gc) consume_one();
+    while (ok && waited < cc) wait_next();
   }
 };
 
+// Per-pair work shared by both decoders: stage 16 pairs, store, close chunks.
+template <int PACK, int G, int NB, bool FULL>
+__device__ __forceinline__ void put_pair(Lane<PACK, G, NB>& L, int q, uint32_t v, int ngs,
+                                         const float (&mg)[Cfg<PACK, G>::GPS]) {
+  const int gl = (2 * q) / G;  // group of pair q (pairs are 2 trits)
+  if (!FULL && gl >= ngs) return;
+  if (q % 32 == 0) L.begin_chunk();
+  L.stg[q % 16] = v;
+  if (q % 16 == 15) tmem_st16(L.a_col() + (q % 32) - 15, L.stg);
+  if (q % 32 == 31) L.end_chunk((2 * q + 2) % G == 0, (2 * q + 2) % G == 0 ? mg[gl] : 0.f);
+}
+
 // Decode one stage (32 words) of base-3 codes: natural-order pairs (t_2j, t_2j+1).
-template <int G, int NB>
-__device__ __forceinline__ void decode_stage_b3(Decoder<TQ_PACK_B3, G, NB>& D, const uint32_t (&w)[32],
+template <int G, int NB, bool FULL>
+__device__ __forceinline__ void decode_stage_b3(Lane<TQ_PACK_B3, G, NB>& L, const uint32_t (&w)[32],
                                                 const uint32_t* __restrict__ lutA, const uint32_t* __restrict__ lutB,
                                                 int ngs, const float (&mg)[Cfg<TQ_PACK_B3, G>::GPS]) {
-  using C = Cfg<TQ_PACK_B3, G>;
-  uint32_t col = 0;
 #pragma unroll
   for (int wi = 0; wi < 32; ++wi) {
-    if ((wi * 10) / C::GP >= ngs) break;
+    if (!FULL && (wi * 20) / G >= ngs) break;
     const uint32_t v = min(w[wi], kB3Max);
-    const uint32_t hi = __umulhi(v + 1u, 2383401723u) >> 15;    // v / 3^10, exact for v < 3^20
+    const uint32_t hi = __umulhi(v + 1u, 2383401723u) >> 15;  // v / 3^10, exact for v < 3^20
     const uint32_t lo = v - hi * 59049u;
-    const uint32_t bl = __umulhi(lo, 17675008u);                  // lo / 243, exact for lo < 3^10
+    const uint32_t bl = __umulhi(lo, 17675008u);                // lo / 243, exact for lo < 3^10
     const uint32_t al = lo - bl * 243u;
     const uint32_t bh = __umulhi(hi, 17675008u);
     const uint32_t ah = hi - bh * 243u;
-    const uint32_t A0 = lutA[al * 32], B0 = lutB[bl * 32], A1 = lutA[ah * 32], B1 = lutB[bh * 32];
+    const uint32_t P0 = lutA[al * 32] | lutB[bl * 32];
+    const uint32_t P1 = lutA[ah * 32] | lutB[bh * 32];
 #pragma unroll
-    for (int j = 0; j < 10; ++j) {
-      const int q = wi * 10 + j;
-      const int gl = q / C::GP;
-      if (gl < ngs) {
-        if (q % C::GP == 0) {
-          D.begin_group();
-          col = D.slot_col();
-        }
-        const uint32_t mask = 0x00030003u << (2 * (j % 5));
-        D.stg[q % 16] = j < 5 ? ((A0 | B0) & mask) : ((A1 | B1) & mask);
-        if (q % 16 == 15) tmem_st16(col + (q % C::GP) - 15, D.stg);
-        if (q % C::GP == C::GP - 1) D.end_group(mg[gl]);
-      }
-    }
+    for (int jj = 0; jj < 10; ++jj)
+      put_pair<TQ_PACK_B3, G, NB, FULL>(L, wi * 10 + jj, (jj < 5 ? P0 : P1) & (0x00030003u << (2 * (jj % 5))), ngs,
+                                        mg);
   }
 }
 
 // Decode one stage (32 words) of 2-bit codes: pair j of a word = fields (j, j + 8).
-template <int G, int NB>
-__device__ __forceinline__ void decode_stage_2b(Decoder<TQ_PACK_2BIT, G, NB>& D, const uint32_t (&w)[32], int ngs,
+template <int G, int NB, bool FULL>
+__device__ __forceinline__ void decode_stage_2b(Lane<TQ_PACK_2BIT, G, NB>& L, const uint32_t (&w)[32], int ngs,
                                                 const float (&mg)[Cfg<TQ_PACK_2BIT, G>::GPS]) {
-  using C = Cfg<TQ_PACK_2BIT, G>;
-  uint32_t col = 0;
 #pragma unroll
   for (int wi = 0; wi < 32; ++wi) {
-    if ((wi * 8) / C::GP >= ngs) break;
+    if (!FULL && (wi * 16) / G >= ngs) break;
     const uint32_t v = w[wi];
     const uint32_t v2 = v >> 10;
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-      const int q = wi * 8 + j;
-      const int gl = q / C::GP;
-      if (q % C::GP == 0) {
-        D.begin_group();
-        col = D.slot_col();
-      }
-      D.stg[q % 16] = j < 5 ? (v & (0x00030003u << (2 * j))) : (v2 & (0x00030003u << (2 * (j - 5))));
-      if (q % 16 == 15) tmem_st16(col + (q % C::GP) - 15, D.stg);
-      if (q % C::GP == C::GP - 1) D.end_group(mg[gl]);
-    }
+    for (int jj = 0; jj < 8; ++jj)
+      put_pair<TQ_PACK_2BIT, G, NB, FULL>(
+          L, wi * 8 + jj, jj < 5 ? (v & (0x00030003u << (2 * jj))) : (v2 & (0x00030003u << (2 * (jj - 5)))), ngs, mg);
   }
 }
 
@@ -244,8 +253,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long grid = gridDim.x;
-  const int u0 = static_cast<int>(static_cast<long long>(blockIdx.x) * p.units / grid);
-  const int u1 = static_cast<int>(static_cast<long long>(blockIdx.x + 1) * p.units / grid);
+  const int u0 = cta_first_unit(blockIdx.x, p.units, grid);
+  const int u1 = cta_first_unit(blockIdx.x + 1, p.units, grid);
+  const int n_units = u1 - u0;
   const int S = p.stages;
 
   uint8_t* lut_smem = smem;
@@ -254,20 +264,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   uint64_t* codes_full = bars;
   uint64_t* xhat_full = bars + S;
   uint64_t* empty = bars + 2 * S;
-  uint64_t* a_full = bars + 3 * S;
-  uint64_t* mma_done = a_full + kRing;
-  uint64_t* lut_bar = mma_done + kRing;
+  uint64_t* a_full = bars + 3 * S;            // [kKLanes][2]
+  uint64_t* mma_done = a_full + 2 * kKLanes;  // [kKLanes][2]
+  uint64_t* lut_bar = mma_done + 2 * kKLanes;
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(lut_bar + 1);
   volatile int* s_abort = reinterpret_cast<volatile int*>(tmem_slot + 1);
-  float* m_ring = reinterpret_cast<float*>(lut_bar + 3);  // 16-byte aligned: bars start 16-aligned
+  float* m_ring = reinterpret_cast<float*>(lut_bar + 3);  // [kKLanes][2][128]
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < S; ++i) {
       mbar_init(codes_full + i, 1);
       mbar_init(xhat_full + i, 1);
-      mbar_init(empty + i, 5);  // 4 decode warps (codes read) + 1 MMA commit (x^ read)
+      mbar_init(empty + i, 5);  // the 4 warps of the stage's K-lane (codes read) + 1 MMA commit (x^ read)
     }
-    for (int i = 0; i < kRing; ++i) {
+    for (int i = 0; i < 2 * kKLanes; ++i) {
       mbar_init(a_full + i, 4);
       mbar_init(mma_done + i, 1);
     }
@@ -275,32 +285,35 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == 5) {
-    tmem_alloc(tmem_slot, C::TMEM_COLS);
+  if (warp == kMmaWarp) {
+    tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
 
-  if (warp < 4) {
-    // ------------------------------------------------------------------ decode warps (thread = row)
-    Decoder<PACK, G, NB> D;
-    D.lane_tmem = tbase + (static_cast<uint32_t>(warp * 32) << 16);
-    D.a_full = a_full;
-    D.mma_done = mma_done;
-    D.m_ring = m_ring;
-    D.s_abort = s_abort;
-    D.p = &p;
-    D.r = threadIdx.x;
-    D.lane = lane;
-    D.gc = 0;
-    D.consumed = 0;
-    D.ok = true;
-    {
+  if (warp < kDecodeWarps) {
+    // ------------------------------------------------------------- decode warps: K-lane j, quarter q
+    const int q = warp & 3, j = warp >> 2;
+    Lane<PACK, G, NB> L;
+    L.tm = tbase + (static_cast<uint32_t>(q * 32) << 16);
+    L.a_full = a_full + 2 * j;
+    L.mma_done = mma_done + 2 * j;
+    L.m_ring = m_ring + j * 2 * kRows;
+    L.s_abort = s_abort;
+    L.p = &p;
+    L.j = j;
+    L.r = q * 32 + lane;
+    L.lane = lane;
+    L.cc = 0;
+    L.waited = 0;
+    L.ok = true;
+    if (j == 0) {
       // constant A of the correction MMA: K-slots 0 and 1 hold 2^-16 (FP16 0x0100), the rest 0
       uint32_t cv[8] = {0x01000100u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      tmem_st8(D.lane_tmem + C::C_COL0, cv);
+      tmem_st8(L.tm + kCCol, cv);
+      tmem_wait_st();
     }
     const uint32_t* lutA = reinterpret_cast<const uint32_t*>(lut_smem) + lane;
     const uint32_t* lutB = lutA + 243 * 32;
@@ -308,99 +321,116 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       bool w = mbar_wait(lut_bar, 0);
       w = __all_sync(0xffffffffu, w);
       if (!w) {
-        D.ok = false;
+        L.ok = false;
         if (lane == 0) fail(p, s_abort);
       }
     }
-    pdl_wait();  // pow2g and the split counters come from the preparation kernel
     int seg_tile = -1, seg_first = 0;
-    for (int u = u0; u < u1 && D.ok; ++u) {
+    float sc[C::GPS];
+    for (int it = j; it < n_units && L.ok; it += kKLanes) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;
-      const int it = u - u0, i = it % S;
+      const int u = u0 + it, i = it % S;
       const int t = u / p.spr, st = u % p.spr;
+      const int row = t * kRows + L.r;
+      const int ngs = min(C::GPS, p.ng - st * C::GPS);
+#pragma unroll
+      for (int gl = 0; gl < C::GPS; ++gl)
+        sc[gl] = (gl < ngs && row < p.N)
+                     ? half_bits_to_float(__ldg(p.scales + static_cast<size_t>(row) * p.ng + st * C::GPS + gl))
+                     : 0.f;
       if (t != seg_tile) {
         seg_tile = t;
-        seg_first = st;
+        seg_first = u;
 #pragma unroll
-        for (int b = 0; b < NB; ++b) D.acc[b] = 0.f;
-      }
-      const int row = t * kRows + threadIdx.x;
-      const int ngs = min(C::GPS, p.ng - st * C::GPS);
-      float mg[C::GPS];
-#pragma unroll
-      for (int gl = 0; gl < C::GPS; ++gl) {
-        const int g = st * C::GPS + gl;
-        mg[gl] = (gl < ngs && row < p.N)
-                     ? half_bits_to_float(__ldg(p.scales + static_cast<size_t>(row) * p.ng + g)) * __ldg(p.pow2g + g)
-                     : 0.f;
+        for (int b = 0; b < NB; ++b) L.acc[b] = 0.f;
       }
       bool w = mbar_wait(codes_full + i, (it / S) & 1);
       w = __all_sync(0xffffffffu, w);
       if (!w) {
-        D.ok = false;
+        L.ok = false;
         if (lane == 0) fail(p, s_abort);
         break;
       }
       uint32_t cw[32];
       if (row < p.N) {
         const uint4* src = reinterpret_cast<const uint4*>(stages + static_cast<size_t>(i) * p.stage_smem +
-                                                          threadIdx.x * kRowPitchSmem);
+                                                          L.r * kRowPitchSmem);
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {
-          const uint4 v = src[q];
-          cw[4 * q] = v.x;
-          cw[4 * q + 1] = v.y;
-          cw[4 * q + 2] = v.z;
-          cw[4 * q + 3] = v.w;
+        for (int k4 = 0; k4 < 8; ++k4) {
+          const uint4 v = src[k4];
+          cw[4 * k4] = v.x;
+          cw[4 * k4 + 1] = v.y;
+          cw[4 * k4 + 2] = v.z;
+          cw[4 * k4 + 3] = v.w;
         }
       } else {
 #pragma unroll
-        for (int q = 0; q < 32; ++q) cw[q] = PACK == TQ_PACK_B3 ? kB3Zero : kB2Zero;
+        for (int k4 = 0; k4 < 32; ++k4) cw[k4] = PACK == TQ_PACK_B3 ? kB3Zero : kB2Zero;
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + i);
-      if constexpr (PACK == TQ_PACK_B3)
-        decode_stage_b3<G, NB>(D, cw, lutA, lutB, ngs, mg);
-      else
-        decode_stage_2b<G, NB>(D, cw, ngs, mg);
-      if (!D.ok) break;
-      // end of this CTA's segment of tile t: fold in the remaining groups, then write
-      if (u == u1 - 1 || (u + 1) / p.spr != t) {
-        D.drain();
-        if (!D.ok) break;
-        if (seg_first == 0 && st == p.spr - 1) {
+      // per-group multipliers s * 2^(16+e): 2^(16+e) travels with the stage's x^ block
+      w = mbar_wait(xhat_full + i, (it / S) & 1);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) {
+        L.ok = false;
+        if (lane == 0) fail(p, s_abort);
+        break;
+      }
+      const float* pw = reinterpret_cast<const float*>(stages + static_cast<size_t>(i) * p.stage_smem +
+                                                       kCodeStageBytes + p.pow2_offset);
+      float mg[C::GPS];
+#pragma unroll
+      for (int gl = 0; gl < C::GPS; ++gl) mg[gl] = sc[gl] * pw[gl];
+      if constexpr (PACK == TQ_PACK_B3) {
+        if (ngs == C::GPS)
+          decode_stage_b3<G, NB, true>(L, cw, lutA, lutB, ngs, mg);
+        else
+          decode_stage_b3<G, NB, false>(L, cw, lutA, lutB, ngs, mg);
+      } else {
+        if (ngs == C::GPS)
+          decode_stage_2b<G, NB, true>(L, cw, ngs, mg);
+        else
+          decode_stage_2b<G, NB, false>(L, cw, ngs, mg);
+      }
+      if (!L.ok) break;
+      // end of this K-lane's part of tile t: fold in its last groups, then publish
+      const int nxt = it + kKLanes;
+      if (nxt >= n_units || (u0 + nxt) / p.spr != t) {
+        L.drain();
+        if (!L.ok) break;
+        int n_parts = 0;
+        for (int uu = t * p.spr; uu < (t + 1) * p.spr; ++uu) n_parts += starts_part(uu, t, p, grid);
+        if (n_parts == 1) {
           if (row < p.N)
 #pragma unroll
             for (int b = 0; b < NB; ++b)
-              if (b < p.B) p.y[static_cast<size_t>(b) * p.N + row] = D.acc[b];
+              if (b < p.B) p.y[static_cast<size_t>(b) * p.N + row] = L.acc[b];
         } else {
-          const long long first_u = static_cast<long long>(t) * p.spr;
-          const int c_first = cta_of_unit(first_u, p.units, grid);
-          const int n_parts = cta_of_unit(first_u + p.spr - 1, p.units, grid) - c_first + 1;
-          const int part = static_cast<int>(blockIdx.x) - c_first;
-          float* pp = p.partial + (static_cast<size_t>(t) * p.spr + part) * p.B * kRows;
+          float* pp = p.partial + static_cast<size_t>(seg_first) * p.B * kRows;
 #pragma unroll
           for (int b = 0; b < NB; ++b)
-            if (b < p.B) pp[b * kRows + threadIdx.x] = D.acc[b];
-          // last-arriving warp (over all parts of the tile) sums the parts in K order: deterministic
+            if (b < p.B) pp[b * kRows + L.r] = L.acc[b];
           __threadfence();
           __syncwarp();
           int last = 0;
           if (lane == 0) {
             const int old = atomicAdd(p.counters + t, 1);
-            last = old == 4 * n_parts - 1;
+            last = old == 4 * n_parts - 1;  // 4 warps (lane quarters) per part
             if (last) p.counters[t] = 0;
             __threadfence();
           }
           last = __shfl_sync(0xffffffffu, last, 0);
           if (last) {
+            // this warp sums every part of the tile, in unit order: deterministic
             for (int rr = lane; rr < kRows; rr += 32) {
               const int rrow = t * kRows + rr;
               if (rrow >= p.N) break;
               for (int b = 0; b < p.B; ++b) {
                 float v = 0.f;
-                for (int q = 0; q < n_parts; ++q)
-                  v += __ldcg(p.partial + ((static_cast<size_t>(t) * p.spr + q) * p.B + b) * kRows + rr);
+                for (int uu = t * p.spr; uu < (t + 1) * p.spr; ++uu)
+                  if (starts_part(uu, t, p, grid))
+                    v += __ldcg(p.partial + (static_cast<size_t>(uu) * p.B + b) * kRows + rr);
                 p.y[static_cast<size_t>(b) * p.N + rrow] = v;
               }
             }
@@ -408,17 +438,17 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         }
       }
     }
-    D.drain();
-  } else if (warp == 4) {
-    // ------------------------------------------------------------------ producer warp
+    L.drain();
+  } else if (warp == kProducerWarp) {
+    // ------------------------------------------------------------- producer warp
     if (PACK == TQ_PACK_B3 && lane == 0) {
       mbar_arrive_expect_tx(lut_bar, kLutBytes);
       bulk_g2s(lut_smem, &g_lut, kLutBytes, lut_bar);
     }
     bool pdl_done = false;
-    for (int u = u0; u < u1; ++u) {
+    for (int it = 0; it < n_units; ++it) {
       if (*s_abort) break;
-      const int it = u - u0, i = it % S;
+      const int u = u0 + it, i = it % S;
       bool w = true;
       if (lane == 0) w = mbar_wait(empty + i, ((it / S) & 1) ^ 1);
       w = __shfl_sync(0xffffffffu, w, 0);
@@ -438,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
                  codes_full + i);
       if (lane == 0) {
         if (!pdl_done) {
-          pdl_wait();
+          pdl_wait();  // x^ comes from the preparation kernel
           pdl_done = true;
         }
         mbar_arrive_expect_tx(xhat_full + i, p.xhat_stage_bytes);
@@ -447,14 +477,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       }
     }
   } else if (lane == 0) {
-    // ------------------------------------------------------------------ MMA issuer (one thread)
+    // ------------------------------------------------------------- MMA issuer (one thread)
     const uint32_t idesc = idesc_f16_f32(kRows, 16);
     const uint32_t lbo = 16u * static_cast<uint32_t>(p.B), sbo = 128u;
-    int gc = 0;
+    int cc[kKLanes] = {0, 0, 0, 0};
     bool alive = true;
-    for (int u = u0; u < u1 && alive; ++u) {
+    for (int it = 0; it < n_units && alive; ++it) {
       if (*s_abort) break;
-      const int it = u - u0, i = it % S;
+      const int u = u0 + it, i = it % S, j = it % kKLanes;
       if (!mbar_wait(xhat_full + i, (it / S) & 1)) {
         fail(p, s_abort);
         break;
@@ -463,34 +493,36 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       const int st = u % p.spr;
       const int ngs = min(C::GPS, p.ng - st * C::GPS);
       const uint32_t xs = smem_addr(stages + static_cast<size_t>(i) * p.stage_smem + kCodeStageBytes);
-      const uint32_t cs = xs + p.corr_offset;
-      for (int gl = 0; gl < ngs; ++gl) {
-        const int slot = gc % kRing;
-        if (!mbar_wait(a_full + slot, (gc / kRing) & 1)) {
+      const uint32_t csx = xs + p.corr_offset;
+      for (int c = 0; c < ngs * C::CPG; ++c) {
+        const int n = cc[j];
+        if (!mbar_wait(a_full + 2 * j + (n & 1), (n >> 1) & 1)) {
           fail(p, s_abort);
           alive = false;
           break;
         }
         tc_fence_after();
-        const uint32_t d = tbase + C::D_COL0 + slot * 16;
+        const int gl = c / C::CPG, half = c % C::CPG;
+        const uint32_t d = tbase + kDCol0 + 32u * j + 16u * ((n / C::CPG) & 1);
+        const uint32_t a = tbase + 64u * j + 32u * (n & 1);
 #pragma unroll
-        for (int s = 0; s < C::SLICES; ++s) {
-          const uint32_t a = tbase + slot * C::GP + s * 8;
-          const uint64_t bd = smem_desc_noswizzle(xs + ((gl * G + 16 * s) >> 3) * lbo, lbo, sbo);
-          mma_f16_ts(d, a, bd, idesc, s > 0 ? 1u : 0u);
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int slot = gl * G + half * 64 + 16 * s4;
+          mma_f16_ts(d, a + 8u * s4, smem_desc_noswizzle(xs + (slot >> 3) * lbo, lbo, sbo), idesc,
+                     (half == 0 && s4 == 0) ? 0u : 1u);
         }
-        mma_f16_ts(d, tbase + C::C_COL0, smem_desc_noswizzle(cs + gl * lbo, lbo, sbo), idesc, 1u);
-        mma_commit(mma_done + slot);
-        ++gc;
+        if (half == C::CPG - 1) mma_f16_ts(d, tbase + kCCol, smem_desc_noswizzle(csx + gl * lbo, lbo, sbo), idesc, 1u);
+        mma_commit(mma_done + 2 * j + (n & 1));
+        cc[j] = n + 1;
       }
       mma_commit(empty + i);
     }
   }
 
   __syncthreads();
-  if (warp == 5) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
-    tmem_dealloc(tbase, C::TMEM_COLS);
+    tmem_dealloc(tbase, kTmemCols);
   }
 }
 
@@ -501,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
 template <int PACK>
 __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__ x, int B, int K, int G, int apply,
                                                     uint8_t* __restrict__ xhat, uint32_t stage_bytes,
-                                                    uint32_t corr_off, float* __restrict__ pow2g,
+                                                    uint32_t corr_off, uint32_t pow2_off,
                                                     int* __restrict__ counters, int n_counters, int* status) {
   constexpr int ST = Geo<PACK>::kStageTrits;
   pdl_launch_dependents();
@@ -591,14 +623,17 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
   }
   if (lane == 0) {
     const float p2 = __int_as_float((127 + 16 + e) << 23);  // 2^(16 + e)
-    for (int g = kb0 / G; g < (kb0 + kFwhtBlock) / G; ++g) pow2g[g] = p2;
+    for (int g = kb0 / G; g < (kb0 + kFwhtBlock) / G; ++g)
+      reinterpret_cast<float*>(sbase + pow2_off)[g - st * GPS] = p2;
   }
   if (kin == 0) {
-    // correction chunks of groups that do not exist in this stage, and the trailing zero chunk
+    // correction chunks of groups that do not exist in this stage, the trailing zero chunk, and
+    // the multipliers of the missing groups
     const int ngs = min(GPS, ng - st * GPS);
     const int n16 = (GPS + 1 - ngs) * B;
     uint4* z = reinterpret_cast<uint4*>(sbase + corr_off + ngs * 16 * B);
     for (int i = lane; i < n16; i += 32) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    for (int gl = ngs + lane; gl < GPS; gl += 32) reinterpret_cast<float*>(sbase + pow2_off)[gl] = 0.f;
   }
 }
 
@@ -607,8 +642,8 @@ __global__ void __launch_bounds__(256) xprep_kernel(const uint16_t* __restrict__
 // ---------------------------------------------------------------------------------------------
 struct Plan {
   int ST, GPS, spr, n_tiles, units, ng;
-  uint32_t stage_bytes, corr_off;
-  size_t off_pow2, off_cnt, off_part, total;
+  uint32_t stage_bytes, corr_off, pow2_off;
+  size_t off_cnt, off_part, total;
 };
 
 Plan make_plan(const tq_desc* d, int B) {
@@ -620,14 +655,13 @@ Plan make_plan(const tq_desc* d, int B) {
   pl.units = pl.n_tiles * pl.spr;
   pl.ng = d->K / d->group;
   pl.corr_off = static_cast<uint32_t>(pl.ST * 2 * B);
-  pl.stage_bytes = pl.corr_off + static_cast<uint32_t>((pl.GPS + 1) * 16 * B);
+  pl.pow2_off = pl.corr_off + static_cast<uint32_t>((pl.GPS + 1) * 16 * B);
+  pl.stage_bytes = pl.pow2_off + static_cast<uint32_t>(((pl.GPS * 4 + 15) / 16) * 16);
   size_t off = align256(static_cast<size_t>(pl.spr) * pl.stage_bytes);
-  pl.off_pow2 = off;
-  off += align256(static_cast<size_t>(pl.ng) * 4);
   pl.off_cnt = off;
   off += align256(static_cast<size_t>(pl.n_tiles) * 4);
   pl.off_part = off;
-  off += align256(static_cast<size_t>(pl.n_tiles) * pl.spr * B * kRows * 4);
+  off += align256(static_cast<size_t>(pl.units) * B * kRows * 4);
   pl.total = off;
   return pl;
 }
@@ -660,16 +694,17 @@ template <int PACK, int G, int NB>
 cudaError_t launch_main(const Params& prm0, int grid, cudaStream_t s) {
   using C = Cfg<PACK, G>;
   Params prm = prm0;
-  const size_t fixed = C::LUT_BYTES + 8 * (3 * kMaxStages + 2 * kRing + 1) + 32 + kRing * kRows * 4 + 1024;
+  auto smem_for = [&](int S) {
+    return static_cast<size_t>(C::LUT_BYTES) + static_cast<size_t>(S) * prm.stage_smem +
+           8 * (3 * S + 4 * kKLanes + 1) + 24 + kKLanes * 2 * kRows * 4;
+  };
   const int optin = max_smem_optin();
   int S = kMaxStages;
-  while (S > 2 && fixed + static_cast<size_t>(S) * prm.stage_smem > static_cast<size_t>(optin)) --S;
+  while (S > 2 && smem_for(S) > static_cast<size_t>(optin)) --S;
   prm.stages = S;
-  const size_t smem = C::LUT_BYTES + static_cast<size_t>(S) * prm.stage_smem + 8 * (3 * S + 2 * kRing + 1) + 32 +
-                      kRing * kRows * 4;
+  const size_t smem = smem_for(S);
   if (smem > static_cast<size_t>(optin)) return cudaErrorInvalidConfiguration;
-  // ask for more than half of the SM's shared memory so that exactly one CTA runs per SM (each
-  // CTA holds up to 512 TMEM columns)
+  // more than half of the SM's shared memory: exactly one CTA (and one 512-column TMEM block) per SM
   const size_t smem_req = std::max(smem, static_cast<size_t>(optin / 2 + 1024));
   auto kern = gemv_tc_kernel<PACK, G, NB>;
   static bool attr_set = false;  // per instantiation
@@ -714,7 +749,6 @@ cudaError_t launch_gemv_tc(const tq_desc* d, const uint32_t* codes, const uint16
   prm.codes = codes;
   prm.scales = scales;
   prm.xhat = base;
-  prm.pow2g = reinterpret_cast<float*>(base + pl.off_pow2);
   prm.y = y;
   prm.partial = reinterpret_cast<float*>(base + pl.off_part);
   prm.counters = reinterpret_cast<int*>(base + pl.off_cnt);
@@ -729,18 +763,18 @@ cudaError_t launch_gemv_tc(const tq_desc* d, const uint32_t* codes, const uint16
   prm.units = pl.units;
   prm.xhat_stage_bytes = pl.stage_bytes;
   prm.corr_offset = pl.corr_off;
+  prm.pow2_offset = pl.pow2_off;
   prm.stage_smem = static_cast<uint32_t>(kCodeStageBytes + ((pl.stage_bytes + 256 + 127) / 128) * 128);
   const int warps = d->K / kFwhtBlock;
   const int xblocks = (warps * 32 + 255) / 256;
   const int apply = d->fwht_block != 0;
   if (d->packing == TQ_PACK_B3)
     xprep_kernel<TQ_PACK_B3><<<xblocks, 256, 0, s>>>(x, B, d->K, d->group, apply, base, pl.stage_bytes, pl.corr_off,
-                                                      const_cast<float*>(prm.pow2g), prm.counters, pl.n_tiles,
-                                                      prm.status);
+                                                      pl.pow2_off, prm.counters, pl.n_tiles, prm.status);
   else
     xprep_kernel<TQ_PACK_2BIT><<<xblocks, 256, 0, s>>>(x, B, d->K, d->group, apply, base, pl.stage_bytes,
-                                                        pl.corr_off, const_cast<float*>(prm.pow2g), prm.counters,
-                                                        pl.n_tiles, prm.status);
+                                                        pl.corr_off, pl.pow2_off, prm.counters, pl.n_tiles,
+                                                        prm.status);
   cudaError_t e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   const int grid = std::min(num_sms(), pl.units);
