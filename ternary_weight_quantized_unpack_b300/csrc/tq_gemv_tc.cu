@@ -478,30 +478,38 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     }
   } else if (lane == 0) {
     // ------------------------------------------------------------- MMA issuer (one thread)
+    // Serves the four K-lanes round-robin: whichever K-lane has its next chunk ready gets its MMAs.
     const uint32_t idesc = idesc_f16_f32(kRows, 16);
     const uint32_t lbo = 16u * static_cast<uint32_t>(p.B), sbo = 128u;
-    int cc[kKLanes] = {0, 0, 0, 0};
-    bool alive = true;
-    for (int it = 0; it < n_units && alive; ++it) {
-      if (*s_abort) break;
-      const int u = u0 + it, i = it % S, j = it % kKLanes;
-      if (!mbar_wait(xhat_full + i, (it / S) & 1)) {
-        fail(p, s_abort);
-        break;
-      }
-      tc_fence_after();
-      const int st = u % p.spr;
-      const int ngs = min(C::GPS, p.ng - st * C::GPS);
-      const uint32_t xs = smem_addr(stages + static_cast<size_t>(i) * p.stage_smem + kCodeStageBytes);
-      const uint32_t csx = xs + p.corr_offset;
-      for (int c = 0; c < ngs * C::CPG; ++c) {
-        const int n = cc[j];
-        if (!mbar_wait(a_full + 2 * j + (n & 1), (n >> 1) & 1)) {
-          fail(p, s_abort);
-          alive = false;
-          break;
+    int it_j[kKLanes], c_j[kKLanes], n_j[kKLanes];
+    bool ready_j[kKLanes];
+#pragma unroll
+    for (int j = 0; j < kKLanes; ++j) {
+      it_j[j] = j;
+      c_j[j] = 0;
+      n_j[j] = 0;
+      ready_j[j] = false;
+    }
+    uint64_t idle_since = 0;
+    for (;;) {
+      bool progress = false, active = false;
+#pragma unroll
+      for (int j = 0; j < kKLanes; ++j) {
+        const int it = it_j[j];
+        if (it >= n_units) continue;
+        active = true;
+        const int i = it % S;
+        if (!ready_j[j]) {
+          if (!mbar_test(xhat_full + i, (it / S) & 1)) continue;
+          ready_j[j] = true;
         }
+        const int n = n_j[j];
+        if (!mbar_test(a_full + 2 * j + (n & 1), (n >> 1) & 1)) continue;
         tc_fence_after();
+        const int st = (u0 + it) % p.spr;
+        const int ngs = min(C::GPS, p.ng - st * C::GPS);
+        const uint32_t xs = smem_addr(stages + static_cast<size_t>(i) * p.stage_smem + kCodeStageBytes);
+        const int c = c_j[j];
         const int gl = c / C::CPG, half = c % C::CPG;
         const uint32_t d = tbase + kDCol0 + 32u * j + 16u * ((n / C::CPG) & 1);
         const uint32_t a = tbase + 64u * j + 32u * (n & 1);
@@ -511,11 +519,33 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
           mma_f16_ts(d, a + 8u * s4, smem_desc_noswizzle(xs + (slot >> 3) * lbo, lbo, sbo), idesc,
                      (half == 0 && s4 == 0) ? 0u : 1u);
         }
-        if (half == C::CPG - 1) mma_f16_ts(d, tbase + kCCol, smem_desc_noswizzle(csx + gl * lbo, lbo, sbo), idesc, 1u);
+        if (half == C::CPG - 1)
+          mma_f16_ts(d, tbase + kCCol, smem_desc_noswizzle(xs + p.corr_offset + gl * lbo, lbo, sbo), idesc, 1u);
         mma_commit(mma_done + 2 * j + (n & 1));
-        cc[j] = n + 1;
+        n_j[j] = n + 1;
+        if (c + 1 == ngs * C::CPG) {
+          mma_commit(empty + i);  // every MMA reading this stage's x^ has been issued
+          it_j[j] = it + kKLanes;
+          c_j[j] = 0;
+          ready_j[j] = false;
+        } else {
+          c_j[j] = c + 1;
+        }
+        progress = true;
       }
-      mma_commit(empty + i);
+      if (!active) break;
+      if (progress) {
+        idle_since = 0;
+      } else {
+        if (*s_abort) break;
+        const uint64_t now = global_timer_ns();
+        if (idle_since == 0) {
+          idle_since = now;
+        } else if (now - idle_since > kWaitNs) {
+          fail(p, s_abort);
+          break;
+        }
+      }
     }
   }
 
