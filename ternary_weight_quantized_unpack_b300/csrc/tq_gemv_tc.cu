@@ -122,19 +122,40 @@ __device__ __forceinline__ void fail(const Params& p, volatile int* s_abort) {
   *s_abort = 1;
 }
 
-// Static stream-K partition: CTA c owns units [floor(c U / G), floor((c+1) U / G)).
-__device__ __forceinline__ int cta_first_unit(long long c, long long units, long long grid) {
-  return static_cast<int>(c * units / grid);
+// Static stream-K partition: CTA c owns units [floor(c U / G), floor((c+1) U / G)); inside a CTA,
+// K-lane j owns the contiguous run [first + floor(j n / 4), first + floor((j+1) n / 4)).  Stages are
+// loaded into the ring round-robin over K-lanes (m-th unit of K-lane 0, 1, 2, 3, then m+1, ...).
+__device__ __forceinline__ int cta_first_unit(int c, int units, int grid) {
+  return static_cast<int>(static_cast<unsigned>(c) * static_cast<unsigned>(units) / static_cast<unsigned>(grid));
 }
-__device__ __forceinline__ int cta_of_unit(long long u, long long units, long long grid) {
-  return static_cast<int>(((u + 1) * grid + units - 1) / units - 1);
+__device__ __forceinline__ int cta_of_unit(int u, int units, int grid) {
+  return static_cast<int>((static_cast<unsigned>(u + 1) * static_cast<unsigned>(grid) + units - 1) /
+                          static_cast<unsigned>(units)) - 1;
 }
-// A part is the run of units of one tile that one K-lane of one CTA decodes; unit u starts a part
-// when the previous unit of its K-lane (u - kKLanes) is outside its CTA or outside its tile.
-__device__ __forceinline__ bool starts_part(int u, int t, const Params& p, long long grid) {
-  const int c = cta_of_unit(u, p.units, grid);
-  const int first = cta_first_unit(c, p.units, grid);
-  return u - kKLanes < first || u - kKLanes < t * p.spr;
+__device__ __forceinline__ int klane_begin(int j, int n) { return (j * n) >> 2; }
+// Ring position of the m-th unit of K-lane j, given the K-lane run lengths len[4].
+__device__ __forceinline__ int ring_pos(int j, int m, const int (&len)[kKLanes]) {
+  int pos = 0;
+#pragma unroll
+  for (int q = 0; q < kKLanes; ++q) pos += min(len[q], m) + ((q < j && m < len[q]) ? 1 : 0);
+  return pos;
+}
+// A part is the run of units of one tile decoded by one K-lane of one CTA; unit u starts a part when
+// it begins a tile or begins a K-lane run.
+__device__ __forceinline__ bool starts_part(int u, int spr, int units, int grid) {
+  if (u % spr == 0) return true;
+  const int c = cta_of_unit(u, units, grid);
+  const int first = cta_first_unit(c, units, grid);
+  const int n = cta_first_unit(c + 1, units, grid) - first;
+  const int d = u - first;
+  return d == 0 || d == klane_begin(1, n) || d == klane_begin(2, n) || d == klane_begin(3, n);
+}
+// Bit k set <=> unit t * spr + k starts a part (spr <= 64).  Whole warp.
+__device__ __forceinline__ unsigned long long part_mask(int t, int spr, int units, int grid, int lane) {
+  const bool a = lane < spr && starts_part(t * spr + lane, spr, units, grid);
+  const bool b = lane + 32 < spr && starts_part(t * spr + lane + 32, spr, units, grid);
+  return static_cast<unsigned long long>(__ballot_sync(0xffffffffu, a)) |
+         (static_cast<unsigned long long>(__ballot_sync(0xffffffffu, b)) << 32);
 }
 
 // One decode thread of one K-lane.  Produces 64-trit chunks of FP16 pairs into its K-lane's two
@@ -252,11 +273,16 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
   using C = Cfg<PACK, G>;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const long long grid = gridDim.x;
+  const int grid = static_cast<int>(gridDim.x);
   const int u0 = cta_first_unit(blockIdx.x, p.units, grid);
-  const int u1 = cta_first_unit(blockIdx.x + 1, p.units, grid);
-  const int n_units = u1 - u0;
+  const int n_units = cta_first_unit(blockIdx.x + 1, p.units, grid) - u0;
   const int S = p.stages;
+  int kl_len[kKLanes];
+#pragma unroll
+  for (int q = 0; q < kKLanes; ++q) kl_len[q] = klane_begin(q + 1, n_units) - klane_begin(q, n_units);
+  int max_len = 0;
+#pragma unroll
+  for (int q = 0; q < kKLanes; ++q) max_len = max(max_len, kl_len[q]);
 
   uint8_t* lut_smem = smem;
   uint8_t* stages = smem + C::LUT_BYTES;
@@ -325,11 +351,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         if (lane == 0) fail(p, s_abort);
       }
     }
-    int seg_tile = -1, seg_first = 0;
+    const int kbeg = u0 + klane_begin(j, n_units);
+    const int klen = kl_len[j];
+    int seg_first = kbeg;
     float sc[C::GPS];
-    for (int it = j; it < n_units && L.ok; it += kKLanes) {
-      if (__any_sync(0xffffffffu, *s_abort != 0)) break;
-      const int u = u0 + it, i = it % S;
+    auto load_scales = [&](int u) {
       const int t = u / p.spr, st = u % p.spr;
       const int row = t * kRows + L.r;
       const int ngs = min(C::GPS, p.ng - st * C::GPS);
@@ -338,13 +364,24 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         sc[gl] = (gl < ngs && row < p.N)
                      ? half_bits_to_float(__ldg(p.scales + static_cast<size_t>(row) * p.ng + st * C::GPS + gl))
                      : 0.f;
-      if (t != seg_tile) {
-        seg_tile = t;
-        seg_first = u;
+    };
+    if (klen > 0) load_scales(kbeg);
 #pragma unroll
-        for (int b = 0; b < NB; ++b) L.acc[b] = 0.f;
-      }
-      bool w = mbar_wait(codes_full + i, (it / S) & 1);
+    for (int b = 0; b < NB; ++b) L.acc[b] = 0.f;
+    for (int m = 0; m < klen && L.ok; ++m) {
+      if (__any_sync(0xffffffffu, *s_abort != 0)) break;
+      const int u = kbeg + m;
+      const int pos = ring_pos(j, m, kl_len);
+      const int i = pos % S;
+      const uint32_t par = (pos / S) & 1;
+      const int t = u / p.spr, st = u % p.spr;
+      const int row = t * kRows + L.r;
+      const int ngs = min(C::GPS, p.ng - st * C::GPS);
+      float cur[C::GPS];
+#pragma unroll
+      for (int gl = 0; gl < C::GPS; ++gl) cur[gl] = sc[gl];
+      if (m + 1 < klen) load_scales(u + 1);  // prefetch for the next unit
+      bool w = mbar_wait(codes_full + i, par);
       w = __all_sync(0xffffffffu, w);
       if (!w) {
         L.ok = false;
@@ -370,7 +407,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       __syncwarp();
       if (lane == 0) mbar_arrive(empty + i);
       // per-group multipliers s * 2^(16+e): 2^(16+e) travels with the stage's x^ block
-      w = mbar_wait(xhat_full + i, (it / S) & 1);
+      w = mbar_wait(xhat_full + i, par);
       w = __all_sync(0xffffffffu, w);
       if (!w) {
         L.ok = false;
@@ -381,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
                                                        kCodeStageBytes + p.pow2_offset);
       float mg[C::GPS];
 #pragma unroll
-      for (int gl = 0; gl < C::GPS; ++gl) mg[gl] = sc[gl] * pw[gl];
+      for (int gl = 0; gl < C::GPS; ++gl) mg[gl] = cur[gl] * pw[gl];
       if constexpr (PACK == TQ_PACK_B3) {
         if (ngs == C::GPS)
           decode_stage_b3<G, NB, true>(L, cw, lutA, lutB, ngs, mg);
@@ -395,12 +432,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       }
       if (!L.ok) break;
       // end of this K-lane's part of tile t: fold in its last groups, then publish
-      const int nxt = it + kKLanes;
-      if (nxt >= n_units || (u0 + nxt) / p.spr != t) {
+      if (m + 1 == klen || (u + 1) % p.spr == 0) {
         L.drain();
         if (!L.ok) break;
-        int n_parts = 0;
-        for (int uu = t * p.spr; uu < (t + 1) * p.spr; ++uu) n_parts += starts_part(uu, t, p, grid);
+        const unsigned long long mask = part_mask(t, p.spr, p.units, grid, lane);
+        const int n_parts = __popcll(mask);
         if (n_parts == 1) {
           if (row < p.N)
 #pragma unroll
@@ -428,14 +464,20 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
               if (rrow >= p.N) break;
               for (int b = 0; b < p.B; ++b) {
                 float v = 0.f;
-                for (int uu = t * p.spr; uu < (t + 1) * p.spr; ++uu)
-                  if (starts_part(uu, t, p, grid))
-                    v += __ldcg(p.partial + (static_cast<size_t>(uu) * p.B + b) * kRows + rr);
+                unsigned long long mm = mask;
+                while (mm) {
+                  const int k = __ffsll(static_cast<long long>(mm)) - 1;
+                  mm &= mm - 1;
+                  v += __ldcg(p.partial + (static_cast<size_t>(t * p.spr + k) * p.B + b) * kRows + rr);
+                }
                 p.y[static_cast<size_t>(b) * p.N + rrow] = v;
               }
             }
           }
         }
+        seg_first = u + 1;
+#pragma unroll
+        for (int b = 0; b < NB; ++b) L.acc[b] = 0.f;
       }
     }
     L.drain();
@@ -446,34 +488,45 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       bulk_g2s(lut_smem, &g_lut, kLutBytes, lut_bar);
     }
     bool pdl_done = false;
-    for (int it = 0; it < n_units; ++it) {
-      if (*s_abort) break;
-      const int u = u0 + it, i = it % S;
-      bool w = true;
-      if (lane == 0) w = mbar_wait(empty + i, ((it / S) & 1) ^ 1);
-      w = __shfl_sync(0xffffffffu, w, 0);
-      if (!w) {
-        if (lane == 0) fail(p, s_abort);
-        break;
-      }
-      const int t = u / p.spr, st = u % p.spr;
-      const int rows = min(kRows, p.N - t * kRows);
-      const int words = min(kStageWords, p.P - st * kStageWords);
-      uint8_t* cs = stages + static_cast<size_t>(i) * p.stage_smem;
-      if (lane == 0) mbar_arrive_expect_tx(codes_full + i, static_cast<uint32_t>(rows * words * 4));
-      __syncwarp();
-      const uint32_t* src = p.codes + static_cast<size_t>(t) * kRows * p.P + st * kStageWords;
-      for (int rr = lane; rr < rows; rr += 32)
-        bulk_g2s(cs + rr * kRowPitchSmem, src + static_cast<size_t>(rr) * p.P, static_cast<uint32_t>(words * 4),
-                 codes_full + i);
-      if (lane == 0) {
-        if (!pdl_done) {
-          pdl_wait();  // x^ comes from the preparation kernel
-          pdl_done = true;
+    int pos = 0;
+    bool alive = true;
+    for (int m = 0; m < max_len && alive; ++m) {
+      for (int jj = 0; jj < kKLanes; ++jj) {
+        if (m >= kl_len[jj]) continue;
+        if (*s_abort) {
+          alive = false;
+          break;
         }
-        mbar_arrive_expect_tx(xhat_full + i, p.xhat_stage_bytes);
-        bulk_g2s(cs + kCodeStageBytes, p.xhat + static_cast<size_t>(st) * p.xhat_stage_bytes, p.xhat_stage_bytes,
-                 xhat_full + i);
+        const int u = u0 + klane_begin(jj, n_units) + m;
+        const int i = pos % S;
+        bool w = true;
+        if (lane == 0) w = mbar_wait(empty + i, ((pos / S) & 1) ^ 1);
+        w = __shfl_sync(0xffffffffu, w, 0);
+        if (!w) {
+          if (lane == 0) fail(p, s_abort);
+          alive = false;
+          break;
+        }
+        const int t = u / p.spr, st = u % p.spr;
+        const int rows = min(kRows, p.N - t * kRows);
+        const int words = min(kStageWords, p.P - st * kStageWords);
+        uint8_t* cs = stages + static_cast<size_t>(i) * p.stage_smem;
+        if (lane == 0) mbar_arrive_expect_tx(codes_full + i, static_cast<uint32_t>(rows * words * 4));
+        __syncwarp();
+        const uint32_t* src = p.codes + static_cast<size_t>(t) * kRows * p.P + st * kStageWords;
+        for (int rr = lane; rr < rows; rr += 32)
+          bulk_g2s(cs + rr * kRowPitchSmem, src + static_cast<size_t>(rr) * p.P, static_cast<uint32_t>(words * 4),
+                   codes_full + i);
+        if (lane == 0) {
+          if (!pdl_done) {
+            pdl_wait();  // x^ comes from the preparation kernel
+            pdl_done = true;
+          }
+          mbar_arrive_expect_tx(xhat_full + i, p.xhat_stage_bytes);
+          bulk_g2s(cs + kCodeStageBytes, p.xhat + static_cast<size_t>(st) * p.xhat_stage_bytes, p.xhat_stage_bytes,
+                   xhat_full + i);
+        }
+        ++pos;
       }
     }
   } else if (lane == 0) {
@@ -481,11 +534,11 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     // Serves the four K-lanes round-robin: whichever K-lane has its next chunk ready gets its MMAs.
     const uint32_t idesc = idesc_f16_f32(kRows, 16);
     const uint32_t lbo = 16u * static_cast<uint32_t>(p.B), sbo = 128u;
-    int it_j[kKLanes], c_j[kKLanes], n_j[kKLanes];
+    int m_j[kKLanes], c_j[kKLanes], n_j[kKLanes];
     bool ready_j[kKLanes];
 #pragma unroll
     for (int j = 0; j < kKLanes; ++j) {
-      it_j[j] = j;
+      m_j[j] = 0;
       c_j[j] = 0;
       n_j[j] = 0;
       ready_j[j] = false;
@@ -495,18 +548,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       bool progress = false, active = false;
 #pragma unroll
       for (int j = 0; j < kKLanes; ++j) {
-        const int it = it_j[j];
-        if (it >= n_units) continue;
+        const int mm = m_j[j];
+        if (mm >= kl_len[j]) continue;
         active = true;
-        const int i = it % S;
+        const int pos = ring_pos(j, mm, kl_len);
+        const int i = pos % S;
         if (!ready_j[j]) {
-          if (!mbar_test(xhat_full + i, (it / S) & 1)) continue;
+          if (!mbar_test(xhat_full + i, (pos / S) & 1)) continue;
           ready_j[j] = true;
         }
         const int n = n_j[j];
         if (!mbar_test(a_full + 2 * j + (n & 1), (n >> 1) & 1)) continue;
         tc_fence_after();
-        const int st = (u0 + it) % p.spr;
+        const int st = (u0 + klane_begin(j, n_units) + mm) % p.spr;
         const int ngs = min(C::GPS, p.ng - st * C::GPS);
         const uint32_t xs = smem_addr(stages + static_cast<size_t>(i) * p.stage_smem + kCodeStageBytes);
         const int c = c_j[j];
@@ -525,7 +579,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         n_j[j] = n + 1;
         if (c + 1 == ngs * C::CPG) {
           mma_commit(empty + i);  // every MMA reading this stage's x^ has been issued
-          it_j[j] = it + kKLanes;
+          m_j[j] = mm + 1;
           c_j[j] = 0;
           ready_j[j] = false;
         } else {

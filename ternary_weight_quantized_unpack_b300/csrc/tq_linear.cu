@@ -21,6 +21,7 @@ using namespace tq;
 
 extern "C" size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch) {
   if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return 0;
+  if (d->K > gemv_tc_max_k(d->packing)) return 0;
   return gemv_tc_workspace_bytes(d, batch);
 }
 
@@ -29,6 +30,7 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
   tq_status st = check_linear_desc(d);
   if (st != TQ_OK) return st;
   if (batch < 1 || batch > kMaxBatch) return TQ_ERR_INVALID_ARG;
+  if (d->K > gemv_tc_max_k(d->packing)) return TQ_ERR_UNSUPPORTED;
   if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
   if (workspace_bytes < tq_gemv_workspace_bytes(d, batch)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
