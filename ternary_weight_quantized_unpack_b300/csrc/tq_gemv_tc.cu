@@ -31,6 +31,7 @@
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
 #include "tq_sm100.cuh"
+#include "tq_tmap.cuh"
 
 namespace tq {
 namespace gemv_tc {
@@ -39,13 +40,11 @@ using namespace sm100;
 
 constexpr int kRows = 128;                // rows per tile = MMA M = TMEM lanes
 constexpr int kStageWords = 32;           // code words per row per stage (128 bytes)
-constexpr int kRowPitchSmem = 144;        // 128 B + 16 B padding: conflict-free 16-byte row reads
-constexpr int kCodeStageBytes = kRows * kRowPitchSmem;
+constexpr int kCodeStageBytes = kRows * kStageWords * 4;  // 16 KB, 128B-swizzled by the TMA
 constexpr int kKLanes = 4;                // decode warp groups working on different stages
 constexpr int kDecodeWarps = 4 * kKLanes; // 4 lane quarters x 4 K-lanes
-constexpr int kProducerWarp = kDecodeWarps;
-constexpr int kMmaWarp = kDecodeWarps + 1;
-constexpr int kThreads = 32 * (kDecodeWarps + 2);
+constexpr int kProducerWarp = kDecodeWarps;  // also owns the TMEM allocation
+constexpr int kThreads = 32 * (kDecodeWarps + 1);
 constexpr uint32_t kLutBytes = 2u * 243u * 32u * 4u;
 constexpr int kMaxStages = 8;
 
@@ -102,7 +101,7 @@ constexpr int kDCol0 = 256;
 constexpr int kCCol = 384;
 
 struct Params {
-  const uint32_t* codes;
+  CUtensorMap tmap;         // codes [N][P] uint32, box 32 words x 128 rows, 128B swizzle
   const uint16_t* scales;
   const uint8_t* xhat;      // prepared activations, one block per stage (x^, corrections, 2^(16+e))
   float* y;
@@ -113,7 +112,7 @@ struct Params {
   uint32_t xhat_stage_bytes;  // bytes of one stage block
   uint32_t corr_offset;       // offset of the correction chunks inside a stage block
   uint32_t pow2_offset;       // offset of the per-group 2^(16+e) floats inside a stage block
-  uint32_t stage_smem;        // shared-memory bytes per pipeline stage
+  uint32_t stage_smem;        // shared-memory bytes per pipeline stage (multiple of 1024)
   int stages;                 // pipeline depth
 };
 
@@ -159,18 +158,25 @@ __device__ __forceinline__ unsigned long long part_mask(int t, int spr, int unit
 }
 
 // One decode thread of one K-lane.  Produces 64-trit chunks of FP16 pairs into its K-lane's two
-// TMEM chunk slots; waits for the MMA of each chunk in order; when the last chunk of a group
-// completes, folds the group's 128 x 16 result into acc with the group's multiplier.
+// TMEM chunk slots.  When the K-lane's four warps have written a chunk, the K-lane leader (lane 0 of
+// its first warp) issues the chunk's MMAs.  Chunk completions are consumed in order; when the last
+// chunk of a group completes, its 128 x 16 result is folded into acc with the group's multiplier.
 template <int PACK, int G, int NB>
 struct Lane {
   using C = Cfg<PACK, G>;
   uint32_t tm;          // TMEM address of this warp's lane quarter, column 0
+  uint32_t tbase;       // TMEM address of lane 0, column 0 (MMA operands)
   uint64_t* a_full;     // [2] of this K-lane
   uint64_t* mma_done;   // [2] of this K-lane
+  uint64_t* empty_bar;  // the current stage's "empty" barrier
   float* m_ring;        // [2][128] multipliers of the groups in flight (this K-lane)
   volatile int* s_abort;
   const Params* p;
+  uint32_t xs;          // shared address of the current stage's x^ block
+  uint32_t lbo;
+  int stage_chunks;     // chunks in the current stage
   int j, r, lane;
+  bool leader;
   int cc, waited;       // chunks produced / chunks whose MMA completion has been consumed
   bool ok;
   float acc[NB];
@@ -202,13 +208,35 @@ struct Lane {
   __device__ __forceinline__ void begin_chunk() {
     while (ok && waited <= cc - 2) wait_next();
   }
-  // group_end: this chunk is the last of its group, m = its multiplier
-  __device__ __forceinline__ void end_chunk(bool group_end, float m) {
+  // c = chunk index within the stage; group_end: last chunk of its group, m = the group's multiplier
+  __device__ __forceinline__ void end_chunk(int c, bool group_end, float m) {
     tmem_wait_st();
     tc_fence_before();
     if (group_end) m_ring[((cc / C::CPG) & 1) * kRows + r] = m;
     __syncwarp();
     if (lane == 0) mbar_arrive(a_full + (cc & 1));
+    if (leader) {
+      if (!mbar_wait(a_full + (cc & 1), (cc >> 1) & 1)) {
+        fail(*p, s_abort);
+      } else {
+        tc_fence_after();
+        const uint32_t idesc = idesc_f16_f32(kRows, 16);
+        const int gl = c / C::CPG, half = c % C::CPG;
+        const uint32_t d = tbase + kDCol0 + 32u * j + 16u * ((cc / C::CPG) & 1);
+        const uint32_t a = tbase + 64u * j + 32u * (cc & 1);
+#pragma unroll
+        for (int s4 = 0; s4 < 4; ++s4) {
+          const int slot = gl * G + half * 64 + 16 * s4;
+          mma_f16_ts(d, a + 8u * s4, smem_desc_noswizzle(xs + (slot >> 3) * lbo, lbo, 128u), idesc,
+                     (half == 0 && s4 == 0) ? 0u : 1u);
+        }
+        if (half == C::CPG - 1)
+          mma_f16_ts(d, tbase + kCCol, smem_desc_noswizzle(xs + p->corr_offset + gl * lbo, lbo, 128u), idesc, 1u);
+        mma_commit(mma_done + (cc & 1));
+        if (c == stage_chunks - 1) mma_commit(empty_bar);  // every MMA reading this stage's x^ is issued
+      }
+    }
+    __syncwarp();
     ++cc;
   }
   __device__ __forceinline__ void drain() {
@@ -225,7 +253,7 @@ __device__ __forceinline__ void put_pair(Lane<PACK, G, NB>& L, int q, uint32_t v
   if (q % 32 == 0) L.begin_chunk();
   L.stg[q % 16] = v;
   if (q % 16 == 15) tmem_st16(L.a_col() + (q % 32) - 15, L.stg);
-  if (q % 32 == 31) L.end_chunk((2 * q + 2) % G == 0, (2 * q + 2) % G == 0 ? mg[gl] : 0.f);
+  if (q % 32 == 31) L.end_chunk(q / 32, (2 * q + 2) % G == 0, (2 * q + 2) % G == 0 ? mg[gl] : 0.f);
 }
 
 // Decode one stage (32 words) of base-3 codes: natural-order pairs (t_2j, t_2j+1).
@@ -284,9 +312,9 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
 #pragma unroll
   for (int q = 0; q < kKLanes; ++q) max_len = max(max_len, kl_len[q]);
 
-  uint8_t* lut_smem = smem;
-  uint8_t* stages = smem + C::LUT_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(stages + static_cast<size_t>(S) * p.stage_smem);
+  uint8_t* stages = smem;                                               // 1024-aligned stage buffers
+  uint8_t* lut_smem = smem + static_cast<size_t>(S) * p.stage_smem;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lut_smem + C::LUT_BYTES);
   uint64_t* codes_full = bars;
   uint64_t* xhat_full = bars + S;
   uint64_t* empty = bars + 2 * S;
@@ -301,7 +329,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     for (int i = 0; i < S; ++i) {
       mbar_init(codes_full + i, 1);
       mbar_init(xhat_full + i, 1);
-      mbar_init(empty + i, 5);  // the 4 warps of the stage's K-lane (codes read) + 1 MMA commit (x^ read)
+      mbar_init(empty + i, 5);  // the 4 warps of the stage's K-lane (codes read) + the leader's commit (x^ read)
     }
     for (int i = 0; i < 2 * kKLanes; ++i) {
       mbar_init(a_full + i, 4);
@@ -311,36 +339,43 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     *s_abort = 0;
     fence_mbar_init();
   }
-  if (warp == kMmaWarp) {
+  if (warp == kProducerWarp) {
     tmem_alloc(tmem_slot, kTmemCols);
     tmem_relinquish();
+    if (lane == 0) tma_prefetch_desc(&p.tmap);
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tmem_slot;
+  if (warp < 4) {
+    // constant A of the correction MMA: K-slots 0 and 1 hold 2^-16 (FP16 0x0100), the rest 0
+    uint32_t cv[8] = {0x01000100u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+    tmem_st8(tbase + (static_cast<uint32_t>(warp * 32) << 16) + kCCol, cv);
+    tmem_wait_st();
+    tc_fence_before();
+  }
+  __syncthreads();
+  tc_fence_after();
 
   if (warp < kDecodeWarps) {
     // ------------------------------------------------------------- decode warps: K-lane j, quarter q
     const int q = warp & 3, j = warp >> 2;
     Lane<PACK, G, NB> L;
     L.tm = tbase + (static_cast<uint32_t>(q * 32) << 16);
+    L.tbase = tbase;
     L.a_full = a_full + 2 * j;
     L.mma_done = mma_done + 2 * j;
     L.m_ring = m_ring + j * 2 * kRows;
     L.s_abort = s_abort;
     L.p = &p;
+    L.lbo = 16u * static_cast<uint32_t>(p.B);
     L.j = j;
     L.r = q * 32 + lane;
     L.lane = lane;
+    L.leader = q == 0 && lane == 0;
     L.cc = 0;
     L.waited = 0;
     L.ok = true;
-    if (j == 0) {
-      // constant A of the correction MMA: K-slots 0 and 1 hold 2^-16 (FP16 0x0100), the rest 0
-      uint32_t cv[8] = {0x01000100u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
-      tmem_st8(L.tm + kCCol, cv);
-      tmem_wait_st();
-    }
     const uint32_t* lutA = reinterpret_cast<const uint32_t*>(lut_smem) + lane;
     const uint32_t* lutB = lutA + 243 * 32;
     if (PACK == TQ_PACK_B3) {
@@ -368,6 +403,7 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
     if (klen > 0) load_scales(kbeg);
 #pragma unroll
     for (int b = 0; b < NB; ++b) L.acc[b] = 0.f;
+    const int swz = L.r & 7;
     for (int m = 0; m < klen && L.ok; ++m) {
       if (__any_sync(0xffffffffu, *s_abort != 0)) break;
       const int u = kbeg + m;
@@ -389,18 +425,19 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         break;
       }
       uint32_t cw[32];
-      if (row < p.N) {
-        const uint4* src = reinterpret_cast<const uint4*>(stages + static_cast<size_t>(i) * p.stage_smem +
-                                                          L.r * kRowPitchSmem);
+      {
+        // row r of the 128B-swizzled tile: 16-byte chunk k sits at position k ^ (r & 7)
+        const uint8_t* rowp = stages + static_cast<size_t>(i) * p.stage_smem + L.r * 128;
 #pragma unroll
         for (int k4 = 0; k4 < 8; ++k4) {
-          const uint4 v = src[k4];
+          const uint4 v = *reinterpret_cast<const uint4*>(rowp + ((k4 ^ swz) << 4));
           cw[4 * k4] = v.x;
           cw[4 * k4 + 1] = v.y;
           cw[4 * k4 + 2] = v.z;
           cw[4 * k4 + 3] = v.w;
         }
-      } else {
+      }
+      if (row >= p.N) {
 #pragma unroll
         for (int k4 = 0; k4 < 32; ++k4) cw[k4] = PACK == TQ_PACK_B3 ? kB3Zero : kB2Zero;
       }
@@ -414,11 +451,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
         if (lane == 0) fail(p, s_abort);
         break;
       }
-      const float* pw = reinterpret_cast<const float*>(stages + static_cast<size_t>(i) * p.stage_smem +
-                                                       kCodeStageBytes + p.pow2_offset);
+      uint8_t* xblk = stages + static_cast<size_t>(i) * p.stage_smem + kCodeStageBytes;
+      const float* pw = reinterpret_cast<const float*>(xblk + p.pow2_offset);
       float mg[C::GPS];
 #pragma unroll
       for (int gl = 0; gl < C::GPS; ++gl) mg[gl] = cur[gl] * pw[gl];
+      L.xs = smem_addr(xblk);
+      L.empty_bar = empty + i;
+      L.stage_chunks = ngs * C::CPG;
       if constexpr (PACK == TQ_PACK_B3) {
         if (ngs == C::GPS)
           decode_stage_b3<G, NB, true>(L, cw, lutA, lutB, ngs, mg);
@@ -481,43 +521,34 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
       }
     }
     L.drain();
-  } else if (warp == kProducerWarp) {
-    // ------------------------------------------------------------- producer warp
-    if (PACK == TQ_PACK_B3 && lane == 0) {
-      mbar_arrive_expect_tx(lut_bar, kLutBytes);
-      bulk_g2s(lut_smem, &g_lut, kLutBytes, lut_bar);
-    }
-    bool pdl_done = false;
-    int pos = 0;
-    bool alive = true;
-    for (int m = 0; m < max_len && alive; ++m) {
-      for (int jj = 0; jj < kKLanes; ++jj) {
-        if (m >= kl_len[jj]) continue;
-        if (*s_abort) {
-          alive = false;
-          break;
-        }
-        const int u = u0 + klane_begin(jj, n_units) + m;
-        const int i = pos % S;
-        bool w = true;
-        if (lane == 0) w = mbar_wait(empty + i, ((pos / S) & 1) ^ 1);
-        w = __shfl_sync(0xffffffffu, w, 0);
-        if (!w) {
-          if (lane == 0) fail(p, s_abort);
-          alive = false;
-          break;
-        }
-        const int t = u / p.spr, st = u % p.spr;
-        const int rows = min(kRows, p.N - t * kRows);
-        const int words = min(kStageWords, p.P - st * kStageWords);
-        uint8_t* cs = stages + static_cast<size_t>(i) * p.stage_smem;
-        if (lane == 0) mbar_arrive_expect_tx(codes_full + i, static_cast<uint32_t>(rows * words * 4));
-        __syncwarp();
-        const uint32_t* src = p.codes + static_cast<size_t>(t) * kRows * p.P + st * kStageWords;
-        for (int rr = lane; rr < rows; rr += 32)
-          bulk_g2s(cs + rr * kRowPitchSmem, src + static_cast<size_t>(rr) * p.P, static_cast<uint32_t>(words * 4),
-                   codes_full + i);
-        if (lane == 0) {
+  } else {
+    // ------------------------------------------------------------- producer warp (lane 0)
+    if (lane == 0) {
+      if (PACK == TQ_PACK_B3) {
+        mbar_arrive_expect_tx(lut_bar, kLutBytes);
+        bulk_g2s(lut_smem, &g_lut, kLutBytes, lut_bar);
+      }
+      bool pdl_done = false;
+      int pos = 0;
+      bool alive = true;
+      for (int m = 0; m < max_len && alive; ++m) {
+        for (int jj = 0; jj < kKLanes; ++jj) {
+          if (m >= kl_len[jj]) continue;
+          if (*s_abort) {
+            alive = false;
+            break;
+          }
+          const int u = u0 + klane_begin(jj, n_units) + m;
+          const int i = pos % S;
+          if (!mbar_wait(empty + i, ((pos / S) & 1) ^ 1)) {
+            fail(p, s_abort);
+            alive = false;
+            break;
+          }
+          const int t = u / p.spr, st = u % p.spr;
+          uint8_t* cs = stages + static_cast<size_t>(i) * p.stage_smem;
+          mbar_arrive_expect_tx(codes_full + i, static_cast<uint32_t>(kCodeStageBytes));
+          tma_load_2d(cs, &p.tmap, st * kStageWords, t * kRows, codes_full + i);
           if (!pdl_done) {
             pdl_wait();  // x^ comes from the preparation kernel
             pdl_done = true;
@@ -525,86 +556,14 @@ __global__ void __launch_bounds__(kThreads, 1) gemv_tc_kernel(const __grid_const
           mbar_arrive_expect_tx(xhat_full + i, p.xhat_stage_bytes);
           bulk_g2s(cs + kCodeStageBytes, p.xhat + static_cast<size_t>(st) * p.xhat_stage_bytes, p.xhat_stage_bytes,
                    xhat_full + i);
-        }
-        ++pos;
-      }
-    }
-  } else if (lane == 0) {
-    // ------------------------------------------------------------- MMA issuer (one thread)
-    // Serves the four K-lanes round-robin: whichever K-lane has its next chunk ready gets its MMAs.
-    const uint32_t idesc = idesc_f16_f32(kRows, 16);
-    const uint32_t lbo = 16u * static_cast<uint32_t>(p.B), sbo = 128u;
-    int m_j[kKLanes], c_j[kKLanes], n_j[kKLanes];
-    bool ready_j[kKLanes];
-#pragma unroll
-    for (int j = 0; j < kKLanes; ++j) {
-      m_j[j] = 0;
-      c_j[j] = 0;
-      n_j[j] = 0;
-      ready_j[j] = false;
-    }
-    uint64_t idle_since = 0;
-    for (;;) {
-      bool progress = false, active = false;
-#pragma unroll
-      for (int j = 0; j < kKLanes; ++j) {
-        const int mm = m_j[j];
-        if (mm >= kl_len[j]) continue;
-        active = true;
-        const int pos = ring_pos(j, mm, kl_len);
-        const int i = pos % S;
-        if (!ready_j[j]) {
-          if (!mbar_test(xhat_full + i, (pos / S) & 1)) continue;
-          ready_j[j] = true;
-        }
-        const int n = n_j[j];
-        if (!mbar_test(a_full + 2 * j + (n & 1), (n >> 1) & 1)) continue;
-        tc_fence_after();
-        const int st = (u0 + klane_begin(j, n_units) + mm) % p.spr;
-        const int ngs = min(C::GPS, p.ng - st * C::GPS);
-        const uint32_t xs = smem_addr(stages + static_cast<size_t>(i) * p.stage_smem + kCodeStageBytes);
-        const int c = c_j[j];
-        const int gl = c / C::CPG, half = c % C::CPG;
-        const uint32_t d = tbase + kDCol0 + 32u * j + 16u * ((n / C::CPG) & 1);
-        const uint32_t a = tbase + 64u * j + 32u * (n & 1);
-#pragma unroll
-        for (int s4 = 0; s4 < 4; ++s4) {
-          const int slot = gl * G + half * 64 + 16 * s4;
-          mma_f16_ts(d, a + 8u * s4, smem_desc_noswizzle(xs + (slot >> 3) * lbo, lbo, sbo), idesc,
-                     (half == 0 && s4 == 0) ? 0u : 1u);
-        }
-        if (half == C::CPG - 1)
-          mma_f16_ts(d, tbase + kCCol, smem_desc_noswizzle(xs + p.corr_offset + gl * lbo, lbo, sbo), idesc, 1u);
-        mma_commit(mma_done + 2 * j + (n & 1));
-        n_j[j] = n + 1;
-        if (c + 1 == ngs * C::CPG) {
-          mma_commit(empty + i);  // every MMA reading this stage's x^ has been issued
-          m_j[j] = mm + 1;
-          c_j[j] = 0;
-          ready_j[j] = false;
-        } else {
-          c_j[j] = c + 1;
-        }
-        progress = true;
-      }
-      if (!active) break;
-      if (progress) {
-        idle_since = 0;
-      } else {
-        if (*s_abort) break;
-        const uint64_t now = global_timer_ns();
-        if (idle_since == 0) {
-          idle_since = now;
-        } else if (now - idle_since > kWaitNs) {
-          fail(p, s_abort);
-          break;
+          ++pos;
         }
       }
     }
   }
 
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == kProducerWarp) {
     tc_fence_after();
     tmem_dealloc(tbase, kTmemCols);
   }
@@ -779,8 +738,8 @@ cudaError_t launch_main(const Params& prm0, int grid, cudaStream_t s) {
   using C = Cfg<PACK, G>;
   Params prm = prm0;
   auto smem_for = [&](int S) {
-    return static_cast<size_t>(C::LUT_BYTES) + static_cast<size_t>(S) * prm.stage_smem +
-           8 * (3 * S + 4 * kKLanes + 1) + 24 + kKLanes * 2 * kRows * 4;
+    return static_cast<size_t>(S) * prm.stage_smem + C::LUT_BYTES + 8 * (3 * S + 4 * kKLanes + 1) + 24 +
+           kKLanes * 2 * kRows * 4;
   };
   const int optin = max_smem_optin();
   int S = kMaxStages;
@@ -830,7 +789,10 @@ cudaError_t launch_gemv_tc(const tq_desc* d, const uint32_t* codes, const uint16
   const Plan pl = make_plan(d, B);
   uint8_t* base = static_cast<uint8_t*>(ws);
   Params prm{};
-  prm.codes = codes;
+  if (!make_tmap_2d(&prm.tmap, codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<uint64_t>(pitch_words(d->K, d->packing)),
+                    static_cast<uint64_t>(d->N), static_cast<uint64_t>(pitch_words(d->K, d->packing)) * 4,
+                    kStageWords, kRows, CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
   prm.scales = scales;
   prm.xhat = base;
   prm.y = y;
@@ -848,7 +810,7 @@ cudaError_t launch_gemv_tc(const tq_desc* d, const uint32_t* codes, const uint16
   prm.xhat_stage_bytes = pl.stage_bytes;
   prm.corr_offset = pl.corr_off;
   prm.pow2_offset = pl.pow2_off;
-  prm.stage_smem = static_cast<uint32_t>(kCodeStageBytes + ((pl.stage_bytes + 256 + 127) / 128) * 128);
+  prm.stage_smem = static_cast<uint32_t>(((kCodeStageBytes + pl.stage_bytes + 256 + 1023) / 1024) * 1024);
   const int warps = d->K / kFwhtBlock;
   const int xblocks = (warps * 32 + 255) / 256;
   const int apply = d->fwht_block != 0;
