@@ -97,8 +97,7 @@ tq_status tq_fwht(const uint16_t* x, void* out, int out_fp16, int rows, int K, i
 
 /* ---- tq_gemv: decode GEMV, y[b][n] = sum_k s[n][k/group] * t[n][k] * x~[b][k] ----------------------
  * x: bf16 [batch][K], 1 <= batch <= 16; x~ = block FWHT of x (or x itself when fwht_block = 0).
- * y: float [batch][N].  Requires K a multiple of 128 and K <= 40960 (base-3) / 32768 (2-bit), else
- * TQ_ERR_UNSUPPORTED.  Streams each code word from HBM once per call.
+ * y: float [batch][N].  Requires K a multiple of 128.  Streams each code word from HBM once per call.
  * workspace >= tq_gemv_workspace_bytes(d, batch).  Calls on one stream are ordered; two calls that
  * share a workspace must not overlap in time. */
 size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch);

@@ -21,8 +21,7 @@ using namespace tq;
 
 extern "C" size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch) {
   if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return 0;
-  if (d->K > gemv_tc_max_k(d->packing)) return 0;
-  return gemv_tc_workspace_bytes(d, batch);
+  return gemv_workspace_bytes(d, batch);
 }
 
 extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
@@ -30,12 +29,11 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
   tq_status st = check_linear_desc(d);
   if (st != TQ_OK) return st;
   if (batch < 1 || batch > kMaxBatch) return TQ_ERR_INVALID_ARG;
-  if (d->K > gemv_tc_max_k(d->packing)) return TQ_ERR_UNSUPPORTED;
   if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
   if (workspace_bytes < tq_gemv_workspace_bytes(d, batch)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_gemv_tc(d, codes, scales, x, batch, y, workspace, s) != cudaSuccess) {
+  if (launch_gemv(d, codes, scales, x, batch, y, workspace, s) != cudaSuccess) {
     (void)cudaGetLastError();
     return TQ_ERR_CUDA;
   }
