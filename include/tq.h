@@ -65,7 +65,14 @@ typedef struct {
   int32_t group;      /* weights per FP16 scale along K: 64 or 128 */
   int32_t packing;    /* tq_packing */
   int32_t fwht_block; /* 128: apply the block Walsh-Hadamard transform to the input; 0: input used as given */
+  int32_t flags;      /* 0, or TQ_STATIC_WEIGHTS (tq_gemv only; other entry points ignore it) */
 } tq_desc;
+
+/* Promise that no kernel still running on the stream when tq_gemv is called writes this matrix's
+ * codes or scales.  The GEMV kernel is launched as a programmatic dependent of the preceding kernel
+ * and may then begin streaming the weights before that kernel has finished; without the flag it
+ * reads nothing written by earlier work until the preceding kernel has completed. */
+#define TQ_STATIC_WEIGHTS 1
 
 /* ---- format sizes (host only, no device access) ------------------------------------------------
  * Row pitch in uint32 words: base-3 roundup(ceil(K/20), 4), 2-bit roundup(ceil(K/16), 4).
@@ -139,6 +146,9 @@ tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scale
  * last read), stores it in *status (TQ_OK if none) and clears it.  This call synchronizes the device. */
 tq_status tq_device_status(int32_t* status);
 const char* tq_status_str(tq_status s);
+/* The cudaError_t code of the last CUDA call that made an entry point of this library return
+ * TQ_ERR_CUDA in the calling host thread (0 if none), then clears it.  No device access. */
+int tq_last_cuda_error(void);
 int tq_version(void);
 
 #ifdef __cplusplus

@@ -19,27 +19,32 @@ LIB_PATH = os.path.join(PKG_DIR, "libtq.so")
 
 TQ_PACK_B3 = 1
 TQ_PACK_2BIT = 2
+TQ_STATIC_WEIGHTS = 1
 
 STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_MISALIGNED",
           4: "TQ_ERR_INVALID_CODE", 5: "TQ_ERR_CUDA", 6: "TQ_ERR_TIMEOUT", 7: "TQ_ERR_WORKSPACE", 8: "TQ_ERR_RANGE"}
 
 
 class TQError(RuntimeError):
-    def __init__(self, status: int, where: str):
+    def __init__(self, status: int, where: str, cuda_error: int = 0):
         self.status = status
-        super().__init__(f"{where}: {STATUS.get(status, status)}")
+        self.cuda_error = cuda_error
+        detail = f" (cudaError {cuda_error})" if cuda_error else ""
+        super().__init__(f"{where}: {STATUS.get(status, status)}{detail}")
 
 
 class tq_desc(ctypes.Structure):
     _fields_ = [("N", ctypes.c_int32), ("K", ctypes.c_int32), ("group", ctypes.c_int32),
-                ("packing", ctypes.c_int32), ("fwht_block", ctypes.c_int32)]
+                ("packing", ctypes.c_int32), ("fwht_block", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
     def __repr__(self):
-        return f"tq_desc(N={self.N}, K={self.K}, group={self.group}, packing={self.packing}, fwht_block={self.fwht_block})"
+        return (f"tq_desc(N={self.N}, K={self.K}, group={self.group}, packing={self.packing}, "
+                f"fwht_block={self.fwht_block}, flags={self.flags})")
 
 
-def desc(N: int, K: int, group: int = 128, packing: int = TQ_PACK_B3, fwht_block: int = 128) -> tq_desc:
-    return tq_desc(N, K, group, packing, fwht_block)
+def desc(N: int, K: int, group: int = 128, packing: int = TQ_PACK_B3, fwht_block: int = 128,
+         flags: int = 0) -> tq_desc:
+    return tq_desc(N, K, group, packing, fwht_block, flags)
 
 
 _P = ctypes.c_void_p
@@ -62,6 +67,7 @@ _SIGS = {
     "tq_gemm": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "tq_device_status": (_I, [ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [_I]),
+    "tq_last_cuda_error": (_I, []),
     "tq_version": (_I, []),
 }
 
@@ -98,7 +104,7 @@ def _stream(stream=None):
 
 def _check(status: int, where: str):
     if status != 0:
-        raise TQError(status, where)
+        raise TQError(status, where, lib().tq_last_cuda_error() if status == 5 else 0)
 
 
 def _ws(nbytes: int, device) -> torch.Tensor:
@@ -232,6 +238,11 @@ def tq_device_status() -> int:
 
 def tq_status_str(status: int) -> str:
     return lib().tq_status_str(status).decode()
+
+
+def tq_last_cuda_error() -> int:
+    """cudaError_t code behind the last TQ_ERR_CUDA returned in this thread (0 if none); clears it."""
+    return lib().tq_last_cuda_error()
 
 
 def tq_version() -> int:

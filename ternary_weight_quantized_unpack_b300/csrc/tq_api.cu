@@ -11,19 +11,28 @@ __device__ int g_status = 0;
 namespace {
 constexpr int kMaxDevices = 64;
 int* g_status_addr[kMaxDevices] = {nullptr};
+thread_local int g_last_cuda = 0;
 }  // namespace
+
+tq_status cuda_fail(cudaError_t e) {
+  g_last_cuda = static_cast<int>(e);
+  (void)cudaGetLastError();
+  return TQ_ERR_CUDA;
+}
 
 // Address of this device's status word; looked up once per device (current device at call time).
 int* status_ptr() {
   int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
-    (void)cudaGetLastError();
+  const cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+    cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidDevice);
     return nullptr;
   }
   if (!g_status_addr[dev]) {
     void* p = nullptr;
-    if (cudaGetSymbolAddress(&p, g_status) != cudaSuccess) {
-      (void)cudaGetLastError();
+    const cudaError_t es = cudaGetSymbolAddress(&p, g_status);
+    if (es != cudaSuccess) {
+      cuda_fail(es);
       return nullptr;
     }
     g_status_addr[dev] = static_cast<int*>(p);
@@ -37,6 +46,7 @@ tq_status check_linear_desc(const tq_desc* d) {
   if (d->group != 64 && d->group != 128) return TQ_ERR_UNSUPPORTED;
   if (d->fwht_block != 0 && d->fwht_block != kFwhtBlock) return TQ_ERR_UNSUPPORTED;
   if (d->K % kFwhtBlock != 0) return TQ_ERR_UNSUPPORTED;
+  if (d->flags & ~TQ_STATIC_WEIGHTS) return TQ_ERR_INVALID_ARG;
   return TQ_OK;
 }
 
@@ -66,10 +76,10 @@ extern "C" tq_status tq_device_status(int32_t* out) {
   int* p = status_ptr();
   if (!p) return TQ_ERR_CUDA;
   int v = 0;
-  if (cudaDeviceSynchronize() != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
-  if (cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return TQ_ERR_CUDA;
+  if (const cudaError_t e = cudaDeviceSynchronize(); e != cudaSuccess) return cuda_fail(e);
+  if (const cudaError_t e = cudaMemcpy(&v, p, sizeof(int), cudaMemcpyDeviceToHost); e != cudaSuccess) return cuda_fail(e);
   const int zero = 0;
-  if (cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return TQ_ERR_CUDA;
+  if (const cudaError_t e = cudaMemcpy(p, &zero, sizeof(int), cudaMemcpyHostToDevice); e != cudaSuccess) return cuda_fail(e);
   *out = v;
   return TQ_OK;
 }
@@ -90,3 +100,9 @@ extern "C" const char* tq_status_str(tq_status s) {
 }
 
 extern "C" int tq_version(void) { return 1; }
+
+extern "C" int tq_last_cuda_error(void) {
+  const int e = g_last_cuda;
+  g_last_cuda = 0;
+  return e;
+}

@@ -108,7 +108,10 @@ extern "C" tq_status tq_unpack(const tq_desc* d, const uint32_t* codes, int8_t* 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   int* status = status_ptr();
   if (!status) return TQ_ERR_CUDA;
-  if (invalid_words && cudaMemsetAsync(invalid_words, 0, sizeof(int32_t), s) != cudaSuccess) return TQ_ERR_CUDA;
+  if (invalid_words) {
+    const cudaError_t e = cudaMemsetAsync(invalid_words, 0, sizeof(int32_t), s);
+    if (e != cudaSuccess) return cuda_fail(e);
+  }
   const int threads = 256;
   const unsigned blocks = static_cast<unsigned>((words + threads - 1) / threads);
   unpack_kernel<<<blocks, threads, 0, s>>>(codes, trits, d->N, d->K, P, d->packing, invalid_words, status);

@@ -92,9 +92,7 @@ extern "C" tq_status tq_fwht(const uint16_t* x, void* out, int out_fp16, int row
   if (block != kFwhtBlock || K % kFwhtBlock != 0) return TQ_ERR_UNSUPPORTED;
   if (!aligned(x, 16) || !aligned(out, 16)) return TQ_ERR_MISALIGNED;
   if (!status_ptr()) return TQ_ERR_CUDA;
-  if (launch_fwht_bf16(x, out, out_fp16 ? 1 : 0, rows, K, 1, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TQ_ERR_CUDA;
-  }
+  const cudaError_t e = launch_fwht_bf16(x, out, out_fp16 ? 1 : 0, rows, K, 1, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   return TQ_OK;
 }

@@ -27,6 +27,7 @@
 //      the column matches the quad thread that supplied the K-slots, so one MMA yields four
 //      independent row dot products per quad: N = 4 thread columns x 2 batch rows.
 #include <algorithm>
+#include <mutex>
 
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
@@ -573,16 +574,37 @@ unsigned long long next_epoch() {
   return e;
 }
 
+// Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.  The
+// attribute belongs to the (function, device) pair, so the largest value set so far is kept per pair.
+cudaError_t ensure_smem_attr(const void* fn, size_t bytes) {
+  struct Entry {
+    const void* fn;
+    int dev;
+    size_t bytes;
+  };
+  static Entry table[256];
+  static int used = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  Entry* ent = nullptr;
+  for (int i = 0; i < used; ++i)
+    if (table[i].fn == fn && table[i].dev == dev) ent = &table[i];
+  if (ent && ent->bytes >= bytes) return cudaSuccess;
+  e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
+  if (e != cudaSuccess) return e;
+  if (!ent && used < 256) ent = &table[used++];
+  if (ent) *ent = Entry{fn, dev, bytes};
+  return cudaSuccess;
+}
+
 template <typename Kern>
 cudaError_t launch(Kern kern, const Params& prm, const Plan& pl, cudaStream_t s) {
   const int optin = max_smem_optin();
-  if (pl.smem > static_cast<size_t>(optin)) return cudaErrorInvalidConfiguration;
-  static bool attr_set = false;  // per kernel instantiation
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
+  if (pl.smem + 1024 > static_cast<size_t>(optin)) return cudaErrorInvalidConfiguration;
+  if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem); e != cudaSuccess) return e;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(pl.n_rg, pl.ksplit);
   cfg.blockDim = dim3(32 * pl.wpc);

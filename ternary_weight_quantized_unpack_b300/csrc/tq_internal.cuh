@@ -22,6 +22,10 @@ constexpr int kMaxBatch = 16;
 // (0 = none).  Defined once in tq_api.cu; kernels receive its address (status_ptr()).
 int* status_ptr();
 
+// Remembers a failed CUDA call for tq_last_cuda_error() (per host thread), clears CUDA's sticky-free
+// last-error slot and returns TQ_ERR_CUDA.
+tq_status cuda_fail(cudaError_t e);
+
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
 
 __host__ __device__ __forceinline__ int trits_per_word(int packing) {
@@ -70,8 +74,6 @@ inline bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintp
 
 #define TQ_CHECK_LAUNCH()                                   \
   do {                                                      \
-    if (cudaPeekAtLastError() != cudaSuccess) {             \
-      (void)cudaGetLastError();                             \
-      return TQ_ERR_CUDA;                                   \
-    }                                                       \
+    const cudaError_t e_ = cudaPeekAtLastError();           \
+    if (e_ != cudaSuccess) return tq::cuda_fail(e_);        \
   } while (0)

@@ -33,10 +33,8 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
   if (workspace_bytes < tq_gemv_workspace_bytes(d, batch)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_gemv(d, codes, scales, x, batch, y, workspace, s) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TQ_ERR_CUDA;
-  }
+  const cudaError_t e = launch_gemv(d, codes, scales, x, batch, y, workspace, s);
+  if (e != cudaSuccess) return cuda_fail(e);
   return TQ_OK;
 }
 
@@ -55,7 +53,7 @@ extern "C" tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   float* xt = static_cast<float*>(workspace);
-  if (launch_fwht_bf16(x, xt, 0, M, d->K, d->fwht_block != 0, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
-  if (launch_gemm_simple(d, codes, scales, xt, M, y, s) != cudaSuccess) { (void)cudaGetLastError(); return TQ_ERR_CUDA; }
+  if (const cudaError_t e = launch_fwht_bf16(x, xt, 0, M, d->K, d->fwht_block != 0, s); e != cudaSuccess) return cuda_fail(e);
+  if (const cudaError_t e = launch_gemm_simple(d, codes, scales, xt, M, y, s); e != cudaSuccess) return cuda_fail(e);
   return TQ_OK;
 }

@@ -211,10 +211,8 @@ extern "C" tq_status tq_moe_route(const float* logits, int T, int E, int topk, i
   if (!logits || !idx || !gate || T < 1 || E < 1 || topk < 1) return TQ_ERR_INVALID_ARG;
   if (E > kMaxExperts || topk > kMaxTopk || topk > E) return TQ_ERR_UNSUPPORTED;
   if (!aligned(logits, 4) || !aligned(idx, 4) || !aligned(gate, 4)) return TQ_ERR_MISALIGNED;
-  if (launch_route(logits, T, E, topk, idx, gate, static_cast<cudaStream_t>(stream)) != cudaSuccess) {
-    (void)cudaGetLastError();
-    return TQ_ERR_CUDA;
-  }
+  const cudaError_t e = launch_route(logits, T, E, topk, idx, gate, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e);
   return TQ_OK;
 }
 
@@ -288,6 +286,5 @@ extern "C" tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, in
   }
   return TQ_OK;
 fail:
-  (void)cudaGetLastError();
-  return TQ_ERR_CUDA;
+  return cuda_fail(cudaPeekAtLastError());
 }

@@ -45,7 +45,8 @@ def test_invalid_descriptors():
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 100), 1) == 0        # K not a multiple of 128
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, group=32), 1) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 17) == 0        # batch above 16
-    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 1) >= 128 * 4
+    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 1) >= 256
+    assert tq.tq_gemv_workspace_bytes(tq.desc(5120, 17408), 16) > 16 * 5120 * 4   # K-split partials
     assert tq.tq_moe_workspace_bytes(1, 257, 8, 2048, 512) == 0
     assert tq.tq_moe_workspace_bytes(8, 256, 8, 2048, 512) > 0
 
@@ -88,3 +89,16 @@ def test_status_strings_and_version():
     for s in range(9):
         assert tq.tq_status_str(s) and tq.tq_status_str(s) != "unknown status"
     assert tq.tq_status_str(99) == "unknown status"
+
+
+def test_last_cuda_error_without_device():
+    """Without a usable device a compute call returns TQ_ERR_CUDA and the CUDA code is kept for the caller."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a CUDA device is present")
+    tq.tq_last_cuda_error()  # clear
+    d = tq.desc(64, 256)
+    A16 = 0x10000
+    assert _call("tq_pack", ctypes.byref(d), A16, A16, None) == 5
+    assert tq.tq_last_cuda_error() != 0
+    assert tq.tq_last_cuda_error() == 0   # read clears it
