@@ -1,6 +1,6 @@
 // Decode GEMV: y[b][n] = sum_g s[n][g] sum_{k in g} t[n][k] x~[b][k], batch 1..16.
 //
-// The weights stream from HBM once; everything else is arranged so the stream is the bottleneck:
+// The weights stream from HBM once; everything else is arranged so that the stream is the bottleneck:
 //  * Decode is register-only.  A 2-bit digit d = t + 1 placed in mantissa bits 2i of an FP16 half
 //    with a zero exponent is the subnormal d * 2^(2i-24), exactly, so one LOP3 turns a code word into
 //    two FP16 tensor-core operands.  The position factor 2^(8-2i) and the offset t = d - 1 are folded
@@ -11,12 +11,25 @@
 //    per lane, conflict-free) places the chunk's digits into those bit fields.
 //  * The multiply-add runs on mma.sync m16n8k16 (FP16 x FP16 -> FP32).  On B300, tcgen05.mma costs
 //    ~120 cycles per K=16 step whatever N is, so with N <= 16 it retires only ~17 trits/cycle/SM;
-//    mma.sync m16n8k16 retires 126, above the ~80 the HBM rate requires.
+//    mma.sync m16n8k16 retires 126, above the ~100 the HBM rate requires.
 //  * Each group of 64 or 128 weights has its own FP16 scale (cosmocat.dev "27B 大模型塞进 5.9GB",
-//    section 二 ②): every MMA covers one group only, and the group's 16x8 result is folded into the
-//    output with one FMA per element.
-//  * The block Walsh-Hadamard transform of the activations (same page, section 二 ①) is computed by
-//    each CTA for its own K-range in the prologue, into shared memory; no separate launch.
+//    section 二 ②): every MMA covers one group only, and the group's result is folded into the
+//    output with one FMA per element.  The CTA's scales are staged in shared memory and
+//    pre-multiplied by the block factor 2^(16+e).
+//  * The block Walsh-Hadamard transform of the activations (same page, section 二 ①) is computed once
+//    per call by a small prep kernel, straight into the operand layout; every CTA bulk-copies
+//    (cp.async.bulk) the slice of its K-range into shared memory.
+//
+// Work split: a CTA holds rs x kl warps: rs row slabs, each split over kl K-lanes of ppl units
+// (a unit is 32 code words of a row: 640 trits base-3, 512 trits 2-bit; whole groups either way).
+// When K is split over several CTAs (gridDim.y <= 8) they form one thread-block cluster.  Partial
+// sums meet in shared memory: first over the K-lanes of a CTA, then over the cluster's CTAs through
+// distributed shared memory, in a fixed order, so results are deterministic without global atomics.
+// The plan is chosen per shape among those whose CTAs are all resident at once.
+//
+// Code words reach registers through a ring of plain 128-bit loads issued several steps ahead.  With
+// TQ_STATIC_WEIGHTS the first loads and the scale staging are issued before the programmatic
+// dependent-launch wait, so a chain of GEMVs keeps HBM busy across kernel boundaries.
 //
 // Two register layouts:
 //  2-bit ("shared-row"): a warp owns 16 rows; the four threads of a quad share a row and take words
@@ -27,7 +40,10 @@
 //      the column matches the quad thread that supplied the K-slots, so one MMA yields four
 //      independent row dot products per quad: N = 4 thread columns x 2 batch rows.
 #include <algorithm>
+#include <map>
 #include <mutex>
+#include <tuple>
+#include <vector>
 
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
@@ -38,19 +54,32 @@ namespace gemv {
 
 using namespace sm100;
 
-constexpr int kMaxWarps = 16;
+constexpr int kMaxThreads = 512;
+constexpr int kMaxCluster = 8;
 constexpr uint32_t kLutWords = 2u * 243u * 32u;
+constexpr uint32_t kLutBytes = kLutWords * 4u;
 
 template <int PACK>
-struct Unit {
-  static constexpr int TRITS = PACK == TQ_PACK_B3 ? 640 : 512;  // 32 code words
-  static constexpr int SLAB = PACK == TQ_PACK_B3 ? 64 : 16;     // rows per warp
+struct Geo;
+template <>
+struct Geo<TQ_PACK_B3> {
+  static constexpr int UT = 640;   // trits per unit (32 words; 5 groups of 128 or 10 of 64)
+  static constexpr int SLAB = 64;  // rows per warp
 };
+template <>
+struct Geo<TQ_PACK_2BIT> {
+  static constexpr int UT = 512;
+  static constexpr int SLAB = 16;
+};
+
+// Row length of VP[group][.]: V for each batch row, then zeros, then the block factor 2^(16+e) in the
+// last slot; a multiple of 4 floats so that every group's row is a whole number of 16-byte chunks.
+__host__ __device__ constexpr int vp_row(int B) { return (B + 1 + 3) & ~3; }
 
 // Chunk lookup table (base-3): for a 5-trit chunk c (digits d0..d4), entry "A" places the digits at
 // FP16 pair fields (lo0, hi0, lo1, hi1, lo2) and entry "B" at (hi2, lo3, hi3, lo4, hi4), where
 // loI / hiI are bits 2I / 16 + 2I.  Each entry is replicated 32 times so that lane l reads bank l.
-struct LutTable {
+struct __align__(128) LutTable {  // bulk-copied: 16-byte alignment required
   uint32_t v[kLutWords];
 };
 constexpr LutTable make_lut() {
@@ -73,243 +102,353 @@ constexpr LutTable make_lut() {
 }
 __device__ const LutTable g_lut = make_lut();
 
+// ---------------------------------------------------------------------------------------------
+// Prep kernel: x^ and VP for the whole of K, one warp per 128-block, all batch rows in registers.
+// x^ layout (halves), K-major so that any K-range is one contiguous slice starting at k * B:
+//   base-3: ((((m >> 1) * B + b) * 2 + (m & 1)) * 4 + r  for trit k = 4m + r (an MMA pair shares
+//           16 bytes);
+//   2-bit : ((((((gi*WPT + u)*2 + jj/2)*B + b)*4 + q)*2 + jj%2)*2 + pair%2)*2 + half for the trit at
+//           word u of quad thread q in group gi, pair index jp (MMA jj = jp / 2), half = trit / 8.
+// ---------------------------------------------------------------------------------------------
+struct PrepParams {
+  const uint16_t* x;
+  uint16_t* xh;
+  float* vp;
+  int* status;
+  int K, B, apply;
+};
+
+template <int PACK, int G>
+__global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ PrepParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // x may be the output of the preceding kernel; the previous call may still read xh
+  const int lane = threadIdx.x & 31;
+  const int blk = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (blk * kFwhtBlock >= p.K) return;
+  const int B = p.B, R = vp_row(B);
+  const int kb = blk * kFwhtBlock + 4 * lane;
+  float v[kMaxBatch][4];
+  float mx = 0.f;
+#pragma unroll
+  for (int b = 0; b < kMaxBatch; ++b) {
+    if (b < B) {
+      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x + static_cast<size_t>(b) * p.K + kb));
+      v[b][0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
+      v[b][1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
+      v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
+      v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
+      if (p.apply) fwht128_warp(v[b]);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[b][j]));
+    }
+  }
+  if (p.apply) mx *= 0.08838834764831845f;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  int e = 0;
+  if (mx > 0.f) {
+    const int ex = (__float_as_int(mx) >> 23) & 0xff;
+    e = (ex == 0 ? -126 : ex - 127) - 6;  // max |x~| * 2^-e in [64, 128)
+    if (e > 100) {
+      e = 100;
+      if (lane == 0) record_error(p.status, TQ_ERR_RANGE);
+    }
+    e = max(e, -100);
+  }
+  const float down = __int_as_float((127 - e) << 23) * (p.apply ? 0.08838834764831845f : 1.f);
+#pragma unroll
+  for (int b = 0; b < kMaxBatch; ++b) {
+    if (b >= B) break;
+    float vs = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int k = kb + j;
+      int pos, off;
+      if (PACK == TQ_PACK_B3) {
+        pos = ((k % 20) % 10) >> 1;
+        const int m = k >> 2, r4 = k & 3;
+        off = (((m >> 1) * B + b) * 2 + (m & 1)) * 4 + r4;
+      } else {
+        constexpr int WPT = G / 64;
+        const int gi = k / G, pg = k % G, wg = pg >> 4, f = pg & 15, jp = f & 7;
+        pos = jp < 5 ? jp : jp - 5;
+        const int qq = wg / WPT, u = wg % WPT, jj = jp >> 1;
+        off = ((((((gi * WPT + u) * 2 + (jj >> 1)) * B + b) * 4 + qq) * 2 + (jj & 1)) * 2 + (jp & 1)) * 2 + (f >> 3);
+      }
+      const float F = __int_as_float((127 + 8 - 2 * pos) << 23);
+      const __half h = __float2half_rn(v[b][j] * down * F);
+      p.xh[off] = __half_as_ushort(h);
+      vs += __half2float(h) * __int_as_float((127 - 8 + 2 * pos) << 23);
+    }
+    if (G == 128) {
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
+    } else {
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
+    }
+    if ((lane & (G == 128 ? 31 : 15)) == 0) p.vp[(kb / G) * R + b] = -1.52587890625e-05f * vs;
+  }
+  if (lane < kFwhtBlock / G) {  // per group of the block: padding zeros and the block factor
+    const int gi = blk * (kFwhtBlock / G) + lane;
+    for (int b = B; b < R - 1; ++b) p.vp[gi * R + b] = 0.f;
+    p.vp[gi * R + R - 1] = __int_as_float((127 + 16 + e) << 23);  // 2^(16 + e)
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// GEMV kernels
+// ---------------------------------------------------------------------------------------------
 struct Params {
   const uint32_t* codes;
   const uint16_t* scales;
-  const uint16_t* x;
+  const uint16_t* xh_g;  // prep output: x^ for all of K
+  const float* vp_g;     // prep output: VP[group][R]
   float* y;
-  float* partial;                  // [ksplit][B][N] when ksplit > 1
-  unsigned long long* counters;    // [row groups]: (epoch << 16) | arrivals
   int* status;
-  int N, K, P, ng, B, G;
-  int wpc;                         // warps per CTA
-  int upr;                         // K-units (32-word stages) per row
-  int ups;                         // units per K-split
-  int ksplit;
-  int apply;                       // 1: block FWHT of x
-  unsigned long long epoch;
-  uint32_t xh_off, v_off, p2_off;  // shared-memory offsets: x^, per-group sums, per-group 2^(16+e)
+  int N, K, P, ng, B, R, G;
+  int rs;     // row slabs per CTA
+  int kl;     // K-lanes per CTA
+  int ppl;    // units per K-lane
+  int upr;    // units per row
+  int early;  // 1: codes and scales may be read before the preceding kernel has completed
+  uint32_t xh_off, vp_off, sw_off, bar_off;  // shared-memory offsets: x^, VP, per-warp scales, barriers
 };
+
+// Where this thread's CTA and warp sit in the problem.
+struct Cta {
+  int warp, lane, slab, kln;
+  int RT;       // rows per CTA
+  int row0;     // first row of the CTA
+  int u0;       // first unit of the CTA
+  int k_start;  // first trit of the CTA's K-range
+  int kr;       // trits in the CTA's K-range (a multiple of 128)
+  int ngr;      // groups in the CTA's K-range
+  int g_abs0;   // first group of the CTA's K-range
+  int ua, ub;   // this warp's units [ua, ub) (empty: idle K-lane)
+};
+
+template <int PACK>
+__device__ __forceinline__ Cta cta_geometry(const Params& p) {
+  constexpr int UT = Geo<PACK>::UT, SLAB = Geo<PACK>::SLAB;
+  Cta c;
+  c.warp = threadIdx.x >> 5;
+  c.lane = threadIdx.x & 31;
+  c.slab = c.warp % p.rs;
+  c.kln = c.warp / p.rs;
+  c.RT = p.rs * SLAB;
+  c.row0 = blockIdx.x * c.RT;
+  c.u0 = blockIdx.y * p.kl * p.ppl;
+  const int u1 = min(c.u0 + p.kl * p.ppl, p.upr);
+  c.k_start = c.u0 * UT;
+  c.kr = min(u1 * UT, p.K) - c.k_start;
+  c.ngr = c.kr / p.G;
+  c.g_abs0 = c.k_start / p.G;
+  c.ua = c.u0 + c.kln * p.ppl;
+  c.ub = min(c.ua + p.ppl, u1);
+  return c;
+}
 
 __device__ __forceinline__ void mma16816(float (&c)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
                                          uint32_t b0, uint32_t b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
       "{%0,%1,%2,%3};"
       : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
-// Base-3 word -> two registers of FP16-pair bit fields: R0 holds pairs 0..4 (trits 0..9) at field
-// positions 0..4, R1 pairs 5..9 (trits 10..19).  Pair j of the word is (R & (0x00030003 << 2(j%5))).
-__device__ __forceinline__ void b3_fields(uint32_t w, const uint32_t* __restrict__ lutA,
-                                          const uint32_t* __restrict__ lutB, uint32_t& R0, uint32_t& R1) {
-  const uint32_t v = min(w, kB3Max);
-  const uint32_t hi = __umulhi(v + 1u, 2383401723u) >> 15;  // v / 3^10, exact for v < 3^20
-  const uint32_t lo = v - hi * 59049u;
-  const uint32_t bl = __umulhi(lo, 17675008u);                // lo / 243, exact for lo < 3^10
-  const uint32_t al = lo - bl * 243u;
-  const uint32_t bh = __umulhi(hi, 17675008u);
-  const uint32_t ah = hi - bh * 243u;
-  R0 = lutA[al * 32] | lutB[bl * 32];
-  R1 = lutA[ah * 32] | lutB[bh * 32];
-}
+// Scales of one unit of one warp (SR rows x NG groups), loaded one unit ahead into registers (two
+// halves per register) and staged in the warp's own shared-memory area as halves [group][row
+// position].  PERM stores rows r and r + 8 of a 16-row slab next to each other (2-bit layout).
+// Rows past N and groups past the unit load a clamped (valid) address: their values feed only
+// outputs that are never stored, which keeps the hot loops free of divergent branches.
+template <int SR, int NG, bool PERM>
+struct UnitScales {
+  static constexpr int PER_LANE = SR * NG / 32;
+  static_assert(PER_LANE % 2 == 0, "scales are packed in pairs");
+  uint32_t v[PER_LANE / 2];
 
-// ---------------------------------------------------------------------------------------------
-// Prologue: x~ for this CTA's K-range, all batch rows, into shared memory in the layout of PACK.
-// One warp per 128-block (round robin); the block exponent e is shared by the batch rows.
-// ---------------------------------------------------------------------------------------------
-template <int PACK>
-__device__ __forceinline__ void prepare_x(const Params& p, uint8_t* smem, int k_start, int kr) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int B = p.B, G = p.G;
-  uint16_t* xh = reinterpret_cast<uint16_t*>(smem + p.xh_off);
-  float* V = reinterpret_cast<float*>(smem + p.v_off);
-  float* P2 = reinterpret_cast<float*>(smem + p.p2_off);
-  const int nblk = kr / kFwhtBlock;
-  for (int blk = warp; blk < nblk; blk += p.wpc) {
-    const int kb = k_start + blk * kFwhtBlock + 4 * lane;  // absolute trit index of this lane's 4 values
-    float mx = 0.f;
-    for (int b = 0; b < B; ++b) {
-      float v[4];
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x + static_cast<size_t>(b) * p.K + kb));
-      v[0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
-      v[1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
-      v[2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
-      v[3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
-      if (p.apply) fwht128_warp(v);
+  __device__ __forceinline__ void load(const Params& p, int row_w0, int u, int ngp, int lane) {
 #pragma unroll
-      for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[j]));
-    }
-    if (p.apply) mx *= 0.08838834764831845f;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-    int e = 0;
-    if (mx > 0.f) {
-      const int ex = (__float_as_int(mx) >> 23) & 0xff;
-      e = (ex == 0 ? -126 : ex - 127) - 6;  // max |x~| * 2^-e in [64, 128)
-      if (e > 100) {
-        e = 100;
-        if (lane == 0) record_error(p.status, TQ_ERR_RANGE);
-      }
-      e = max(e, -100);
-    }
-    const float down = __int_as_float((127 - e) << 23) * (p.apply ? 0.08838834764831845f : 1.f);
-    const int prel = blk * kFwhtBlock + 4 * lane;  // trit index relative to k_start
-    for (int b = 0; b < B; ++b) {
-      float v[4];
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x + static_cast<size_t>(b) * p.K + kb));
-      v[0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
-      v[1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
-      v[2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
-      v[3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
-      if (p.apply) fwht128_warp(v);
-      float vs = 0.f;
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const int pr = prel + j;
-        int pos, off;
-        if (PACK == TQ_PACK_B3) {
-          pos = ((pr % 20) % 10) >> 1;  // k_start is a multiple of 20
-          const int m = pr >> 2, r4 = pr & 3;
-          off = ((m * B + b) * 2 + (r4 >> 1)) * 2 + (r4 & 1);  // in halves
-        } else {
-          const int gi = pr / G, pg = pr % G, wg = pg >> 4, f = pg & 15, jj = f & 7;
-          const int WPT = G / 64;
-          pos = jj < 5 ? jj : jj - 5;
-          const int qq = wg / WPT, u = wg % WPT;
-          off = (((((gi * WPT + u) * 4 + (jj >> 1)) * B + b) * 4 + qq) * 2 + (jj & 1)) * 2 + (f >> 3);
-        }
-        const float F = __int_as_float((127 + 8 - 2 * pos) << 23);
-        const __half h = __float2half_rn(v[j] * down * F);
-        xh[off] = __half_as_ushort(h);
-        vs += __half2float(h) * __int_as_float((127 - 8 + 2 * pos) << 23);
-      }
-      if (G == 128) {
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
-      } else {
-#pragma unroll
-        for (int o = 8; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
-      }
-      if ((lane & (G == 128 ? 31 : 15)) == 0) V[(prel / G) * B + b] = vs;
-    }
-    if (lane == 0) {
-      const float p2 = __int_as_float((127 + 16 + e) << 23);  // 2^(16 + e)
-      for (int gi = (blk * kFwhtBlock) / G; gi < (blk * kFwhtBlock + kFwhtBlock) / G; ++gi) P2[gi] = p2;
+    for (int j = 0; j < PER_LANE; ++j) {
+      const int e = lane + 32 * j, r = e / NG, g = min(e % NG, ngp - 1), row = min(row_w0 + r, p.N - 1);
+      const uint32_t h = __ldg(p.scales + static_cast<size_t>(row) * p.ng + u * NG + g);
+      if (j & 1)
+        v[j >> 1] |= h << 16;
+      else
+        v[j >> 1] = h;
     }
   }
+  __device__ __forceinline__ void store(uint16_t* sw, int lane) const {
+#pragma unroll
+    for (int j = 0; j < PER_LANE; ++j) {
+      const int e = lane + 32 * j, r = e / NG, g = e % NG;
+      const int pos = PERM ? (((r & 7) << 1) | (r >> 3)) : r;
+      sw[g * SR + pos] = static_cast<uint16_t>((j & 1) ? (v[j >> 1] >> 16) : (v[j >> 1] & 0xffffu));
+    }
+  }
+};
+
+// Two adjacent staged scales times the block factor, as fp32.
+__device__ __forceinline__ float2 scale_pair(const uint16_t* sw, float p2) {
+  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(sw));
+  return make_float2(f.x * p2, f.y * p2);
 }
 
-// ---------------------------------------------------------------------------------------------
-// Output: one K-split writes y directly; several K-splits write partials and the last CTA of a row
-// group (epoch-tagged arrival counter, reset by the last arriver) sums them in split order.
-// ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void store_out(const Params& p, int row, int b, float v) {
-  if (row >= p.N || b >= p.B) return;
-  if (p.ksplit == 1)
-    p.y[static_cast<size_t>(b) * p.N + row] = v;
-  else
-    p.partial[(static_cast<size_t>(blockIdx.y) * p.B + b) * p.N + row] = v;
-}
+// Shared-memory setup common to both kernels: mbarriers and the prep output slice of this CTA (after
+// the dependent-launch wait).
+struct Bars {
+  uint64_t lut, x;
+  uint32_t zero[4];  // 16 zero bytes: the B operand of lanes that supply none
+};
 
-__device__ __forceinline__ void finish_splits(const Params& p, int row0, int rows, volatile int* s_flag) {
-  if (p.ksplit == 1) return;
-  __threadfence();
-  __syncthreads();
+__device__ __forceinline__ void init_bars(Bars* bars) {
   if (threadIdx.x == 0) {
-    unsigned long long* c = p.counters + blockIdx.x;
-    unsigned long long old = *reinterpret_cast<volatile unsigned long long*>(c), nw, got;
-    int count;
-    for (;;) {
-      count = (old >> 16) == p.epoch ? static_cast<int>(old & 0xffffu) + 1 : 1;
-      nw = (p.epoch << 16) | static_cast<unsigned long long>(count);
-      got = atomicCAS(c, old, nw);
-      if (got == old) break;
-      old = got;
-    }
-    const int last = count == p.ksplit;
-    if (last) atomicExch(c, 0ull);
-    __threadfence();
-    *s_flag = last;
+    mbar_init(&bars->lut, 1);
+    mbar_init(&bars->x, 1);
+    fence_mbar_init();
+#pragma unroll
+    for (int i = 0; i < 4; ++i) bars->zero[i] = 0u;
   }
   __syncthreads();
-  if (!*s_flag) return;
-  for (int i = threadIdx.x; i < rows * p.B; i += blockDim.x) {
-    const int b = i / rows, row = row0 + i % rows;
-    if (row >= p.N) continue;
-    float v = 0.f;
-    for (int s = 0; s < p.ksplit; ++s) v += __ldcg(p.partial + (static_cast<size_t>(s) * p.B + b) * p.N + row);
-    p.y[static_cast<size_t>(b) * p.N + row] = v;
+}
+
+__device__ __forceinline__ void copy_prep_slice(const Params& p, const Cta& c, uint8_t* smem, Bars* bars) {
+  if (threadIdx.x == 0) {
+    const uint32_t xb = static_cast<uint32_t>(c.kr) * p.B * 2u;
+    const uint32_t vb = static_cast<uint32_t>(c.ngr) * p.R * 4u;
+    mbar_arrive_expect_tx(&bars->x, xb + vb);
+    bulk_g2s(smem + p.xh_off, p.xh_g + static_cast<size_t>(c.k_start) * p.B, xb, &bars->x);
+    bulk_g2s(smem + p.vp_off, p.vp_g + static_cast<size_t>(c.g_abs0) * p.R, vb, &bars->x);
   }
+}
+
+__device__ __forceinline__ void wait_bar(const Params& p, uint64_t* bar) {
+  if (!mbar_wait(bar, 0) && (threadIdx.x & 31) == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Partial sums red[kl][RT][B] (in shared memory) -> y.  K-lanes are added in lane order, then the
+// cluster's CTAs in rank order through distributed shared memory.  Every thread calls this.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, float* red) {
+  const int E = c.RT * p.B;
+  if (p.kl > 1) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      float v = red[e];
+      for (int l = 1; l < p.kl; ++l) v += red[l * E + e];
+      red[e] = v;
+    }
+    __syncthreads();
+  }
+  const int ks = static_cast<int>(gridDim.y);
+  if (ks == 1) {
+    for (int e = threadIdx.x; e < E; e += blockDim.x) {
+      const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
+      if (row < p.N) p.y[static_cast<size_t>(b) * p.N + row] = red[e];
+    }
+    return;
+  }
+  cluster_sync();  // every CTA's red[0] is complete
+  const int rank = static_cast<int>(cluster_ctarank());
+  const int chunk = (E + ks - 1) / ks;
+  const int e0 = rank * chunk, e1 = min(E, e0 + chunk);
+  const uint32_t base = smem_addr(red);
+  for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
+    float v = 0.f;
+    for (int r = 0; r < ks; ++r)
+      v += ld_cluster_f32(cluster_map(base + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(r)));
+    const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
+    if (row < p.N) p.y[static_cast<size_t>(b) * p.N + row] = v;
+  }
+  cluster_sync();  // keep this CTA's shared memory alive until the peers have read it
 }
 
 // ---------------------------------------------------------------------------------------------
 // 2-bit, shared-row layout.  NT = number of 8-column batch tiles (1: B <= 8, 2: B <= 16).
 // ---------------------------------------------------------------------------------------------
 template <int G, int NT>
-__global__ void __launch_bounds__(32 * kMaxWarps) gemv_2b_kernel(const __grid_constant__ Params p) {
-  constexpr int WPT = G / 64;  // words per thread per group per row
+__global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_constant__ Params p) {
+  constexpr int WPT = G / 64;          // words per thread per group per row
+  constexpr int GPU = 512 / G;         // groups per unit
+  constexpr int D = G == 128 ? 6 : 8;  // ring of groups in flight
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  const int u_a = blockIdx.y * p.ups, u_b = min(u_a + p.ups, p.upr);
-  const int k_start = u_a * Unit<TQ_PACK_2BIT>::TRITS;
-  const int kr = min(u_b * Unit<TQ_PACK_2BIT>::TRITS, p.K) - k_start;
-  const int ngr = kr / G;
-  const int g_abs0 = k_start / G;
-  pdl_wait();
-  prepare_x<TQ_PACK_2BIT>(p, smem, k_start, kr);
-  __syncthreads();
-
-  const int row0 = blockIdx.x * p.wpc * 16 + warp * 16;
-  const int rg = row0 + g, rg8 = rg + 8;
-  const bool vg = rg < p.N, vg8 = rg8 < p.N;
-  const uint32_t* cg = p.codes + static_cast<size_t>(vg ? rg : 0) * p.P + k_start / 16 + WPT * q;
-  const uint32_t* cg8 = p.codes + static_cast<size_t>(vg8 ? rg8 : 0) * p.P + k_start / 16 + WPT * q;
-  const uint16_t* sg = p.scales + static_cast<size_t>(vg ? rg : 0) * p.ng + g_abs0;
-  const uint16_t* sg8 = p.scales + static_cast<size_t>(vg8 ? rg8 : 0) * p.ng + g_abs0;
-  const uint32_t* xh = reinterpret_cast<const uint32_t*>(smem + p.xh_off);
-  const float* V = reinterpret_cast<const float*>(smem + p.v_off);
-  const float* P2 = reinterpret_cast<const float*>(smem + p.p2_off);
-  constexpr int D = 4;  // groups of code words prefetched
+  const Cta c = cta_geometry<TQ_PACK_2BIT>(p);
+  Bars* bars = reinterpret_cast<Bars*>(smem + p.bar_off);
+  init_bars(bars);
+  const int g = c.lane >> 2, q = c.lane & 3;
+  const int rg = c.row0 + c.slab * 16 + g, rg8 = rg + 8;
+  const bool vg = rg < p.N, vg8 = rg8 < p.N;  // rows past N compute on row 0 and are not stored
+  // this warp's groups, relative to the CTA's first group
+  const int gl_a = (c.ua - c.u0) * GPU;
+  const int gl_b = max(gl_a, min((c.ub - c.u0) * GPU, c.ngr));
+  const uint32_t* cg = p.codes + static_cast<size_t>(vg ? rg : 0) * p.P + c.k_start / 16 + WPT * q;
+  const uint32_t* cg8 = p.codes + static_cast<size_t>(vg8 ? rg8 : 0) * p.P + c.k_start / 16 + WPT * q;
+  const int row_w0 = c.row0 + c.slab * 16;
+  uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + c.warp * (GPU * 16);
+  UnitScales<16, GPU, true> us;
+  auto unit_groups = [&](int u) { return min(GPU, (min((u + 1) * 512, p.K) - u * 512) / G); };
   uint32_t buf[D][2 * WPT];
-  uint16_t sbuf[D][2];
-  auto fetch = [&](int gi, int slot) {
-    if (gi < ngr) {
 #pragma unroll
-      for (int u = 0; u < WPT; ++u) {
-        buf[slot][u] = vg ? __ldg(cg + gi * (G / 16) + u) : kB2Zero;
-        buf[slot][WPT + u] = vg8 ? __ldg(cg8 + gi * (G / 16) + u) : kB2Zero;
-      }
-      sbuf[slot][0] = vg ? __ldg(sg + gi) : static_cast<uint16_t>(0);
-      sbuf[slot][1] = vg8 ? __ldg(sg8 + gi) : static_cast<uint16_t>(0);
+  for (int d = 0; d < D; ++d)
+#pragma unroll
+    for (int u = 0; u < 2 * WPT; ++u) buf[d][u] = kB2Zero;
+  // rows past N read row 0 (their outputs are not stored); groups past the range re-read the last
+  auto fetch = [&](int gl, int slot) {
+    const int gc = min(gl, gl_b - 1);
+#pragma unroll
+    for (int u = 0; u < WPT; ++u) {
+      buf[slot][u] = __ldg(cg + gc * (G / 16) + u);
+      buf[slot][WPT + u] = __ldg(cg8 + gc * (G / 16) + u);
     }
   };
+  auto prime = [&]() {
+    if (gl_a < gl_b) {
 #pragma unroll
-  for (int d = 0; d < D - 1; ++d) fetch(d, d);
+      for (int d = 0; d < D - 1; ++d) fetch(gl_a + d, d);
+      us.load(p, row_w0, c.ua, unit_groups(c.ua), c.lane);
+    }
+  };
+  if (p.early) prime();
+  pdl_wait();
+  copy_prep_slice(p, c, smem, bars);
+  if (!p.early) prime();
+  wait_bar(p, &bars->x);
+
+  const uint32_t* xh = reinterpret_cast<const uint32_t*>(smem + p.xh_off);
+  const float* V = reinterpret_cast<const float*>(smem + p.vp_off);
   float acc[NT][4];
 #pragma unroll
   for (int t = 0; t < NT; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
 
-  for (int gi0 = 0; gi0 < ngr; gi0 += D) {
+  for (int gi0 = gl_a; gi0 < gl_b; gi0 += D) {
 #pragma unroll
     for (int d = 0; d < D; ++d) {
-      const int gi = gi0 + d;
-      if (gi >= ngr) break;
-      fetch(gi + D - 1, (d + D - 1) % D);
-      float c[NT][4];
+      const int gl = gi0 + d;
+      if (gl >= gl_b) break;
+      fetch(gl + D - 1, (d + D - 1) % D);
+      const int gu = (gl - gl_a) & (GPU - 1);  // group within the unit
+      if (gu == 0) {  // a new unit: its scales into the warp's area, the next unit's into registers
+        const int u = c.ua + (gl - gl_a) / GPU;
+        __syncwarp();
+        us.store(sw, c.lane);
+        __syncwarp();
+        if (u + 1 < c.ub) us.load(p, row_w0, u + 1, unit_groups(u + 1), c.lane);
+      }
+      float cc[NT][4];
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        const int bA = min(8 * t + 2 * q, p.B - 1), bB = min(8 * t + 2 * q + 1, p.B - 1);
-        const float vA = 8 * t + 2 * q < p.B ? -1.52587890625e-05f * V[gi * p.B + bA] : 0.f;
-        const float vB = 8 * t + 2 * q + 1 < p.B ? -1.52587890625e-05f * V[gi * p.B + bB] : 0.f;
-        c[t][0] = vA;
-        c[t][1] = vB;
-        c[t][2] = vA;
-        c[t][3] = vB;
+        // batch columns past B read a valid slot: they land only in columns that are not stored
+        const int b = min(8 * t + 2 * q, p.R - 2);
+        const float2 v = *reinterpret_cast<const float2*>(V + gl * p.R + b);
+        cc[t][0] = v.x;
+        cc[t][1] = v.y;
+        cc[t][2] = v.x;
+        cc[t][3] = v.y;
       }
 #pragma unroll
       for (int u = 0; u < WPT; ++u) {
@@ -321,353 +460,530 @@ __global__ void __launch_bounds__(32 * kMaxWarps) gemv_2b_kernel(const __grid_co
           pr[j] = j < 5 ? (w & (0x00030003u << (2 * j))) : (w2 & (0x00030003u << (2 * (j - 5))));
           pr8[j] = j < 5 ? (w8 & (0x00030003u << (2 * j))) : (w82 & (0x00030003u << (2 * (j - 5))));
         }
+        uint4 bp[NT];
 #pragma unroll
         for (int jj = 0; jj < 4; ++jj) {
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const int b = 8 * t + g;
-            const int bc = min(b, p.B - 1);
-            const uint2 bv =
-                *reinterpret_cast<const uint2*>(xh + ((((gi * WPT + u) * 4 + jj) * p.B + bc) * 4 + q) * 2);
-            const uint32_t b0 = b < p.B ? bv.x : 0u, b1 = b < p.B ? bv.y : 0u;
-            mma16816(c[t], pr[2 * jj], pr8[2 * jj], pr[2 * jj + 1], pr8[2 * jj + 1], b0, b1);
+            const int b = min(8 * t + g, p.B - 1);  // columns past B: not stored
+            if ((jj & 1) == 0)
+              bp[t] = *reinterpret_cast<const uint4*>(xh + ((((gl * WPT + u) * 2 + (jj >> 1)) * p.B + b) * 4 + q) * 4);
+            const uint32_t b0 = (jj & 1) ? bp[t].z : bp[t].x, b1 = (jj & 1) ? bp[t].w : bp[t].y;
+            mma16816(cc[t], pr[2 * jj], pr8[2 * jj], pr[2 * jj + 1], pr8[2 * jj + 1], b0, b1);
           }
         }
       }
-      const float p2 = P2[gi];
-      const float mg = half_bits_to_float(sbuf[d][0]) * p2, mg8 = half_bits_to_float(sbuf[d][1]) * p2;
+      const float2 m = scale_pair(sw + gu * 16 + 2 * g, V[gl * p.R + p.R - 1]);  // rows g, g + 8
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
-        acc[t][0] = fmaf(mg, c[t][0], acc[t][0]);
-        acc[t][1] = fmaf(mg, c[t][1], acc[t][1]);
-        acc[t][2] = fmaf(mg8, c[t][2], acc[t][2]);
-        acc[t][3] = fmaf(mg8, c[t][3], acc[t][3]);
+        acc[t][0] = fmaf(m.x, cc[t][0], acc[t][0]);
+        acc[t][1] = fmaf(m.x, cc[t][1], acc[t][1]);
+        acc[t][2] = fmaf(m.y, cc[t][2], acc[t][2]);
+        acc[t][3] = fmaf(m.y, cc[t][3], acc[t][3]);
       }
     }
   }
+
+  __syncthreads();  // the partial sums reuse the x^ region
+  float* red = reinterpret_cast<float*>(smem);
+  const int rl = c.slab * 16 + g;
+  float* r0 = red + (c.kln * c.RT + rl) * p.B;
+  float* r8 = red + (c.kln * c.RT + rl + 8) * p.B;
 #pragma unroll
   for (int t = 0; t < NT; ++t) {
-    store_out(p, rg, 8 * t + 2 * q, acc[t][0]);
-    store_out(p, rg, 8 * t + 2 * q + 1, acc[t][1]);
-    store_out(p, rg8, 8 * t + 2 * q, acc[t][2]);
-    store_out(p, rg8, 8 * t + 2 * q + 1, acc[t][3]);
+    const int b = 8 * t + 2 * q;
+    if (b < p.B) {
+      r0[b] = acc[t][0];
+      r8[b] = acc[t][2];
+    }
+    if (b + 1 < p.B) {
+      r0[b + 1] = acc[t][1];
+      r8[b + 1] = acc[t][3];
+    }
   }
-  __shared__ int s_flag;
-  finish_splits(p, blockIdx.x * p.wpc * 16, p.wpc * 16, &s_flag);
+  __syncthreads();
+  reduce_store(p, c, red);
 }
 
 // ---------------------------------------------------------------------------------------------
 // base-3, column layout.  NT = number of 2-row batch tiles (ceil(B / 2)).
 // Thread (g, q) owns rows R = r0 + 4g + q and R + 32 of its warp's 64-row slab.
 // ---------------------------------------------------------------------------------------------
+
+// Base-3 word -> the four table words of its chunks: L0/L1 (trits 0..9), L2/L3 (trits 10..19).
+__device__ __forceinline__ void b3_lut4(uint32_t w, const uint32_t* __restrict__ lutA,
+                                        const uint32_t* __restrict__ lutB, uint32_t (&L)[4]) {
+  const uint32_t v = min(w, kB3Max);
+  const uint32_t hi = __umulhi(v + 1u, 2383401723u) >> 15;  // v / 3^10, exact for v < 3^20
+  const uint32_t lo = v - hi * 59049u;
+  const uint32_t bl = __umulhi(lo, 17675008u);                // lo / 243, exact for lo < 3^10
+  const uint32_t al = lo - bl * 243u;
+  const uint32_t bh = __umulhi(hi, 17675008u);
+  const uint32_t ah = hi - bh * 243u;
+  L[0] = lutA[al * 32];
+  L[1] = lutB[bl * 32];
+  L[2] = lutA[ah * 32];
+  L[3] = lutB[bh * 32];
+}
+
+// Pair j (0..9) of a decoded word as an MMA operand register: (trit 2j, trit 2j+1) in the
+// (lo, hi) halves at field j % 5.  Fields 0, 1 come from the "A" entry, 3, 4 from "B", 2 from both.
+__device__ __forceinline__ uint32_t b3_pair(const uint32_t (&L)[4], int j) {
+  const uint32_t a = j < 5 ? L[0] : L[2], b = j < 5 ? L[1] : L[3];
+  const int f = j % 5;
+  const uint32_t m = 0x00030003u << (2 * f);
+  return f < 2 ? (a & m) : f == 2 ? ((a | b) & m) : (b & m);
+}
+
 template <int G, int NT, bool FULL>
-__device__ __forceinline__ void b3_period(const Params& p, const uint32_t* __restrict__ cR,
-                                          const uint32_t* __restrict__ cR2, bool vR, bool vR2,
-                                          const uint32_t* __restrict__ lutA, const uint32_t* __restrict__ lutB,
-                                          const uint32_t* __restrict__ xh, const float* __restrict__ V,
-                                          const float* __restrict__ P2, const uint16_t* const (&srow)[4],
-                                          const bool (&svalid)[4], int pi, int ngp, int lane, float (&acc)[NT][4]) {
-  constexpr int GP = G / 2;      // pairs per group
-  constexpr int GPS = 640 / G;   // groups per period
-  const int g = lane >> 2, q = lane & 3;
-  const int bq = q >> 1;         // batch within a tile held by this thread's accumulators
-  const bool bsup = (g & 3) == q;  // this thread supplies B (x^) values
-  const int bsel = g >> 2;         // batch within a tile it supplies
-  float c[NT][4];
-  uint4 cur = vR ? __ldg(reinterpret_cast<const uint4*>(cR)) : make_uint4(kB3Zero, kB3Zero, kB3Zero, kB3Zero);
-  uint4 cur2 = vR2 ? __ldg(reinterpret_cast<const uint4*>(cR2)) : make_uint4(kB3Zero, kB3Zero, kB3Zero, kB3Zero);
+__device__ __forceinline__ void b3_unit(const Params& p, const Cta& c, int u, int ngp, const uint4* __restrict__ cR,
+                                        const uint4* __restrict__ cR2, int s_last, uint4 (&ra)[4], uint4 (&rb)[4],
+                                        const uint32_t* __restrict__ lutA, const uint32_t* __restrict__ lutB,
+                                        const uint32_t* const (&bptr)[NT], const int (&bstr)[NT],
+                                        const float* __restrict__ V, const uint16_t* __restrict__ swr,
+                                        float (&acc)[NT][4]) {
+  constexpr int GP = G / 2;     // pairs per group
+  constexpr int GPS = 640 / G;  // groups per unit
+  const int q = c.lane & 3;
+  const int bq = q >> 1;    // batch within a tile held by this thread's accumulators
+  const int ul = u - c.u0;  // unit index within the CTA
+  float cc[NT][4];
+  uint4 bp[NT];
 #pragma unroll
-  for (int step = 0; step < 8; ++step) {
-    if (!FULL && (step * 80) / G >= ngp) break;
-    uint4 nxt = cur, nxt2 = cur2;
-    if (step < 7 && (FULL || ((step + 1) * 80) / G < ngp)) {  // never read past the row's last word
-      if (vR) nxt = __ldg(reinterpret_cast<const uint4*>(cR) + step + 1);
-      if (vR2) nxt2 = __ldg(reinterpret_cast<const uint4*>(cR2) + step + 1);
+  for (int st = 0; st < 8; ++st) {
+    if (!FULL && (st * 80) / G >= ngp) break;
+    {  // keep the ring three steps ahead (past this warp's range: re-read its last step)
+      const int s = min(u * 8 + st + 3, s_last);
+      ra[(st + 3) & 3] = __ldg(cR + s);
+      rb[(st + 3) & 3] = __ldg(cR2 + s);
     }
+    const uint4 cur = ra[st & 3], cur2 = rb[st & 3];
     const uint32_t wr[4] = {cur.x, cur.y, cur.z, cur.w};
     const uint32_t wr2[4] = {cur2.x, cur2.y, cur2.z, cur2.w};
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
-      uint32_t A0, A1, C0, C1;
-      b3_fields(wr[wi], lutA, lutB, A0, A1);
-      b3_fields(wr2[wi], lutA, lutB, C0, C1);
+      uint32_t La[4], Lb[4];
+      b3_lut4(wr[wi], lutA, lutB, La);
+      b3_lut4(wr2[wi], lutA, lutB, Lb);
 #pragma unroll
       for (int mj = 0; mj < 5; ++mj) {
-        const int pair = (step * 4 + wi) * 10 + 2 * mj;  // first pair of this MMA within the period
+        const int pair = (st * 4 + wi) * 10 + 2 * mj;  // first pair of this MMA within the unit
         const int gl = pair / GP;
         if (!FULL && gl >= ngp) break;
+        const int gla = ul * GPS + gl;  // group index within the CTA
         if (pair % GP == 0) {
           // new group: accumulators start at -2^-16 * sum(x^) of the group for their batch
-          const int gi = pi * GPS + gl;
 #pragma unroll
           for (int t = 0; t < NT; ++t) {
-            const int b = 2 * t + bq;
-            const float v0 = b < p.B ? -1.52587890625e-05f * V[gi * p.B + b] : 0.f;
-            c[t][0] = v0;
-            c[t][1] = v0;
-            c[t][2] = v0;
-            c[t][3] = v0;
+            const float v0 = V[gla * p.R + min(2 * t + bq, p.B - 1)];  // columns past B are not stored
+            cc[t][0] = v0;
+            cc[t][1] = v0;
+            cc[t][2] = v0;
+            cc[t][3] = v0;
           }
         }
-        const int j0 = (2 * mj) % 10, j1 = (2 * mj + 1) % 10;
-        const uint32_t RA = j0 < 5 ? A0 : A1, RB = j1 < 5 ? A0 : A1;
-        const uint32_t SA = j0 < 5 ? C0 : C1, SB = j1 < 5 ? C0 : C1;
-        const uint32_t a0 = RA & (0x00030003u << (2 * (j0 % 5)));
-        const uint32_t a2 = RB & (0x00030003u << (2 * (j1 % 5)));
-        const uint32_t a1 = SA & (0x00030003u << (2 * (j0 % 5)));
-        const uint32_t a3 = SB & (0x00030003u << (2 * (j1 % 5)));
-        const int m = pi * 160 + pair / 2;  // MMA index within the K-range
+        const int mloc = (st * 4 + wi) * 5 + mj;  // MMA index within the unit
+        if ((mloc & 1) == 0) {
+          const int mp = ul * 80 + (mloc >> 1);  // MMA pair index within the CTA
+#pragma unroll
+          for (int t = 0; t < NT; ++t) bp[t] = *reinterpret_cast<const uint4*>(bptr[t] + mp * bstr[t]);
+        }
+        const uint32_t a0 = b3_pair(La, 2 * mj), a2 = b3_pair(La, 2 * mj + 1);
+        const uint32_t a1 = b3_pair(Lb, 2 * mj), a3 = b3_pair(Lb, 2 * mj + 1);
 #pragma unroll
         for (int t = 0; t < NT; ++t) {
-          const int b = 2 * t + bsel;
-          uint32_t b0 = 0u, b1 = 0u;
-          if (bsup && b < p.B) {
-            const uint2 bv = *reinterpret_cast<const uint2*>(xh + (m * p.B + b) * 2);
-            b0 = bv.x;
-            b1 = bv.y;
-          }
-          mma16816(c[t], a0, a1, a2, a3, b0, b1);
+          const uint32_t b0 = (mloc & 1) ? bp[t].z : bp[t].x, b1 = (mloc & 1) ? bp[t].w : bp[t].y;
+          mma16816(cc[t], a0, a1, a2, a3, b0, b1);
         }
         if ((pair + 2) % GP == 0) {
-          const int gi = pi * GPS + gl;
-          const float p2 = P2[gi];
-          const int gabs = gi;  // srow pointers are offset to this CTA's first group
+          const float p2 = V[gla * p.R + p.R - 1];
+          const float2 m01 = scale_pair(swr + gl * 64, p2);       // rows of the accumulators 0, 1
+          const float2 m23 = scale_pair(swr + gl * 64 + 32, p2);  // rows + 32
 #pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float m_i = svalid[i] ? half_bits_to_float(__ldg(srow[i] + gabs)) * p2 : 0.f;
-#pragma unroll
-            for (int t = 0; t < NT; ++t) acc[t][i] = fmaf(m_i, c[t][i], acc[t][i]);
+          for (int t = 0; t < NT; ++t) {
+            acc[t][0] = fmaf(m01.x, cc[t][0], acc[t][0]);
+            acc[t][1] = fmaf(m01.y, cc[t][1], acc[t][1]);
+            acc[t][2] = fmaf(m23.x, cc[t][2], acc[t][2]);
+            acc[t][3] = fmaf(m23.y, cc[t][3], acc[t][3]);
           }
         }
       }
     }
-    cur = nxt;
-    cur2 = nxt2;
   }
 }
 
 template <int G, int NT>
-__global__ void __launch_bounds__(32 * kMaxWarps) gemv_b3_kernel(const __grid_constant__ Params p) {
+__global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_constant__ Params p) {
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_launch_dependents();
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, q = lane & 3;
-  // the chunk table into shared memory (it does not depend on earlier kernels)
-  {
-    const uint4* src = reinterpret_cast<const uint4*>(&g_lut);
-    uint4* dst = reinterpret_cast<uint4*>(smem);
-    for (int i = threadIdx.x; i < static_cast<int>(kLutWords / 4); i += blockDim.x) dst[i] = __ldg(src + i);
+  const Cta c = cta_geometry<TQ_PACK_B3>(p);
+  Bars* bars = reinterpret_cast<Bars*>(smem + p.bar_off);
+  init_bars(bars);
+  const int g = c.lane >> 2, q = c.lane & 3;
+  if (threadIdx.x == 0) {  // the chunk table (constant data of this library)
+    mbar_arrive_expect_tx(&bars->lut, kLutBytes);
+    bulk_g2s(smem, &g_lut, kLutBytes, &bars->lut);
   }
-  const int u_a = blockIdx.y * p.ups, u_b = min(u_a + p.ups, p.upr);
-  const int k_start = u_a * 640;
-  const int kr = min(u_b * 640, p.K) - k_start;
-  const int g_abs0 = k_start / G;
-  pdl_wait();
-  prepare_x<TQ_PACK_B3>(p, smem, k_start, kr);
-  __syncthreads();
-
-  const int r0 = blockIdx.x * p.wpc * 64 + warp * 64;
-  const int R = r0 + lane, R2 = R + 32;
-  const bool vR = R < p.N, vR2 = R2 < p.N;
-  const uint32_t* cR = p.codes + static_cast<size_t>(vR ? R : 0) * p.P + k_start / 20;
-  const uint32_t* cR2 = p.codes + static_cast<size_t>(vR2 ? R2 : 0) * p.P + k_start / 20;
-  // rows of the four accumulators this thread folds: threads (g, 2q%4) and (g, 2q%4 + 1), R and R+32
-  const int cq = (2 * q) & 3;
-  const int rows[4] = {r0 + 4 * g + cq, r0 + 4 * g + cq + 1, r0 + 32 + 4 * g + cq, r0 + 32 + 4 * g + cq + 1};
-  const uint16_t* srow[4];
-  bool svalid[4];
+  // rows past N compute on row 0 and are not stored
+  const int R = c.row0 + c.slab * 64 + c.lane, R2 = R + 32;
+  const uint4* cR = reinterpret_cast<const uint4*>(p.codes + static_cast<size_t>(R < p.N ? R : 0) * p.P);
+  const uint4* cR2 = reinterpret_cast<const uint4*>(p.codes + static_cast<size_t>(R2 < p.N ? R2 : 0) * p.P);
+  const int s_begin = c.ua * 8;
+  const int s_last = min(c.ub * 8, p.P >> 2) - 1;  // this warp's last 4-word step (a row has P / 4)
+  constexpr int GPS = 640 / G;
+  const int row_w0 = c.row0 + c.slab * 64;
+  uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + c.warp * (GPS * 64);
+  UnitScales<64, GPS, false> us;
+  auto unit_groups = [&](int u) { return min(GPS, (min((u + 1) * 640, p.K) - u * 640) / G); };
+  uint4 ra[4], rb[4];
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    svalid[i] = rows[i] < p.N;
-    srow[i] = p.scales + static_cast<size_t>(svalid[i] ? rows[i] : 0) * p.ng + g_abs0;
+    ra[i] = make_uint4(kB3Zero, kB3Zero, kB3Zero, kB3Zero);
+    rb[i] = ra[i];
   }
-  const uint32_t* lutA = reinterpret_cast<const uint32_t*>(smem) + lane;
+  auto prime = [&]() {
+    if (c.ua < c.ub) {
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        ra[i] = __ldg(cR + min(s_begin + i, s_last));
+        rb[i] = __ldg(cR2 + min(s_begin + i, s_last));
+      }
+      us.load(p, row_w0, c.ua, unit_groups(c.ua), c.lane);
+    }
+  };
+  if (p.early) prime();
+  pdl_wait();
+  copy_prep_slice(p, c, smem, bars);
+  if (!p.early) prime();
+  wait_bar(p, &bars->x);
+  wait_bar(p, &bars->lut);
+
+  const uint32_t* lutA = reinterpret_cast<const uint32_t*>(smem) + c.lane;
   const uint32_t* lutB = lutA + 243 * 32;
   const uint32_t* xh = reinterpret_cast<const uint32_t*>(smem + p.xh_off);
-  const float* V = reinterpret_cast<const float*>(smem + p.v_off);
-  const float* P2 = reinterpret_cast<const float*>(smem + p.p2_off);
+  const float* V = reinterpret_cast<const float*>(smem + p.vp_off);
+  // B operand: lane (g, q) supplies batch 2t + g/4 of tile t when g % 4 == q, else 16 zero bytes;
+  // batch rows past B read row B - 1 (their columns are not stored)
+  const uint32_t* bptr[NT];
+  int bstr[NT];
+  {
+    const bool bsup = (g & 3) == q;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      bptr[t] = bsup ? xh + min(2 * t + (g >> 2), p.B - 1) * 4 : bars->zero;
+      bstr[t] = bsup ? p.B * 4 : 0;  // words per MMA pair: 4 halves per (pair, batch row) x 2 MMAs
+    }
+  }
+  // accumulator rows: threads (g, cq) and (g, cq + 1) of the slab, R and R + 32
+  const int cq = (2 * q) & 3;
+  const int rl0 = c.slab * 64 + 4 * g + cq;
+  const uint16_t* swr = sw + 4 * g + cq;  // this thread's accumulator rows within the warp's slab
   float acc[NT][4];
 #pragma unroll
   for (int t = 0; t < NT; ++t)
 #pragma unroll
     for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
-  const int n_per = (kr + 639) / 640;
-  for (int pi = 0; pi < n_per; ++pi) {
-    const int ngp = min(640 / G, (kr - pi * 640) / G);
-    if (ngp == 640 / G)
-      b3_period<G, NT, true>(p, cR + pi * 32, cR2 + pi * 32, vR, vR2, lutA, lutB, xh, V, P2, srow, svalid, pi, ngp,
-                             lane, acc);
+  for (int u = c.ua; u < c.ub; ++u) {
+    const int ngp = unit_groups(u);
+    // this unit's scales into the warp's area, the next unit's into registers
+    __syncwarp();
+    us.store(sw, c.lane);
+    __syncwarp();
+    if (u + 1 < c.ub) us.load(p, row_w0, u + 1, unit_groups(u + 1), c.lane);
+    if (ngp == GPS)
+      b3_unit<G, NT, true>(p, c, u, ngp, cR, cR2, s_last, ra, rb, lutA, lutB, bptr, bstr, V, swr, acc);
     else
-      b3_period<G, NT, false>(p, cR + pi * 32, cR2 + pi * 32, vR, vR2, lutA, lutB, xh, V, P2, srow, svalid, pi, ngp,
-                              lane, acc);
+      b3_unit<G, NT, false>(p, c, u, ngp, cR, cR2, s_last, ra, rb, lutA, lutB, bptr, bstr, V, swr, acc);
   }
+
+  __syncthreads();  // the partial sums reuse the table / x^ region
+  float* red = reinterpret_cast<float*>(smem);
+  const int rows[4] = {rl0, rl0 + 1, rl0 + 32, rl0 + 33};
 #pragma unroll
-  for (int t = 0; t < NT; ++t)
+  for (int t = 0; t < NT; ++t) {
+    const int b = 2 * t + (q >> 1);
+    if (b < p.B) {
 #pragma unroll
-    for (int i = 0; i < 4; ++i) store_out(p, rows[i], 2 * t + (q >> 1), acc[t][i]);
-  __shared__ int s_flag;
-  finish_splits(p, blockIdx.x * p.wpc * 64, p.wpc * 64, &s_flag);
+      for (int i = 0; i < 4; ++i) red[(c.kln * c.RT + rows[i]) * p.B + b] = acc[t][i];
+    }
+  }
+  __syncthreads();
+  reduce_store(p, c, red);
 }
 
 // ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
-constexpr int kRefSMs = 148;  // plans depend only on the problem, so workspace sizes are stable
+constexpr int kSMs = 148;  // B300
+constexpr size_t kSmemLimit = 227 * 1024;
 
 struct Plan {
-  int wpc, ksplit, ups, upr, n_rg, ut;
-  size_t smem, xh_off, v_off, p2_off;
-  size_t ws_part, ws_cnt, total;
+  bool ok;
+  int rs, kl, ppl, ks, upr, n_rg;
+  size_t smem, xh_off, vp_off, sw_off, bar_off;
 };
 
-Plan make_plan(const tq_desc* d, int B) {
-  Plan pl{};
+// Shared-memory layout of a candidate split; returns the total bytes.  The partial-sum buffer of
+// the epilogue reuses the table / x^ region.
+size_t layout(Plan& pl, bool b3, int B, int G, int K) {
+  const int UT = b3 ? 640 : 512, SLAB = b3 ? 64 : 16;
+  const int RT = pl.rs * SLAB;
+  const int kr = std::min(pl.kl * pl.ppl * UT, K);
+  const int ngr = kr / G;
+  pl.xh_off = b3 ? kLutBytes : 0;
+  const size_t main = pl.xh_off + align256(static_cast<size_t>(kr) * B * 2);
+  const size_t red = static_cast<size_t>(pl.kl) * RT * B * 4;
+  pl.vp_off = align256(std::max(main, red));
+  pl.sw_off = pl.vp_off + align256(static_cast<size_t>(ngr) * vp_row(B) * 4);
+  pl.bar_off = pl.sw_off + align256(static_cast<size_t>(pl.rs) * pl.kl * (UT / G) * SLAB * 2);
+  pl.smem = pl.bar_off + 256;
+  return pl.smem;
+}
+
+// Candidate splits in order of estimated time: per-warp units x busiest-SM warps (at least 12, below
+// which a warp's own latency dominates); ties go to fewer CTAs, then to smaller clusters.
+std::vector<Plan> candidates(const tq_desc* d, int B) {
   const bool b3 = d->packing == TQ_PACK_B3;
-  pl.ut = b3 ? 640 : 512;
-  pl.upr = (d->K + pl.ut - 1) / pl.ut;
-  const int slab = b3 ? 64 : 16;
-  const int slabs = (d->N + slab - 1) / slab;
-  // warps per CTA: 16 when there are enough slabs, fewer for narrow matrices
-  pl.wpc = kMaxWarps;
-  while (pl.wpc > 4 && slabs < pl.wpc * 8) pl.wpc /= 2;
-  pl.n_rg = (slabs + pl.wpc - 1) / pl.wpc;
-  // K-splits: enough CTAs to cover the SMs, and a K-range whose activations fit in shared memory
-  const size_t lut = b3 ? kLutWords * 4 : 0;
-  const size_t budget = 200 * 1024 - lut;
-  int ks = std::max(1, (kRefSMs * (kMaxWarps / pl.wpc)) / pl.n_rg);
-  ks = std::min(ks, pl.upr);
-  auto xh_bytes = [&](int units) { return static_cast<size_t>(units) * pl.ut * 2 * B; };
-  while (ks < pl.upr && xh_bytes((pl.upr + ks - 1) / ks) > budget) ++ks;
-  pl.ups = (pl.upr + ks - 1) / ks;
-  pl.ksplit = (pl.upr + pl.ups - 1) / pl.ups;
-  const int kr = pl.ups * pl.ut;
-  const int ngr = kr / d->group;
-  pl.xh_off = lut;
-  pl.v_off = pl.xh_off + align256(xh_bytes(pl.ups));
-  pl.p2_off = pl.v_off + align256(static_cast<size_t>(ngr) * B * 4);
-  pl.smem = pl.p2_off + align256(static_cast<size_t>(ngr) * 4);
-  if (pl.ksplit > 1) {
-    pl.ws_part = 0;
-    pl.ws_cnt = align256(static_cast<size_t>(pl.ksplit) * B * d->N * 4);
-    pl.total = pl.ws_cnt + align256(static_cast<size_t>(pl.n_rg) * 8);
-  } else {
-    pl.total = 256;
+  const int UT = b3 ? 640 : 512, SLAB = b3 ? 64 : 16;
+  const int upr = (d->K + UT - 1) / UT;
+  const int slabs = (d->N + SLAB - 1) / SLAB;
+  std::vector<std::tuple<double, int, int, Plan>> list;
+  for (int kl = 1; kl <= 16; ++kl) {
+    for (int rs = 1; rs * kl <= 16; rs *= 2) {
+      for (int ks = 1; ks <= kMaxCluster; ++ks) {
+        Plan pl{};
+        pl.upr = upr;
+        pl.kl = kl;
+        pl.rs = rs;
+        pl.ks = ks;
+        pl.ppl = (upr + kl * ks - 1) / (kl * ks);
+        if ((ks - 1) * kl * pl.ppl >= upr) continue;  // a CTA without work
+        if (kl > 1 && (kl - 1) * pl.ppl >= upr) continue;  // a K-lane that can never have work
+        pl.n_rg = (slabs + rs - 1) / rs;
+        if (layout(pl, b3, B, d->group, d->K) > kSmemLimit) continue;
+        const long long C = static_cast<long long>(pl.n_rg) * ks;
+        const long long k = (C + kSMs - 1) / kSMs;
+        const double cost = pl.ppl * std::max<double>(static_cast<double>(k * rs * kl), 12.0);
+        list.emplace_back(cost, static_cast<int>(C), ks, pl);
+      }
+    }
   }
-  return pl;
-}
-
-int max_smem_optin() {
-  static int cache[64] = {0};
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 232448;
-  if (!cache[dev]) {
-    int v = 0;
-    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || v <= 0) v = 232448;
-    cache[dev] = v;
-  }
-  return cache[dev];
-}
-
-unsigned long long next_epoch() {
-  static unsigned long long e = 0x5eed1234ull;
-  e = (e + 0x9E3779B97F4A7C15ull) & 0x0000ffffffffffffull;
-  if (e == 0) e = 1;
-  return e;
+  std::stable_sort(list.begin(), list.end(), [](const auto& a, const auto& b) {
+    if (std::get<0>(a) != std::get<0>(b)) return std::get<0>(a) < std::get<0>(b);
+    if (std::get<1>(a) != std::get<1>(b)) return std::get<1>(a) < std::get<1>(b);
+    return std::get<2>(a) < std::get<2>(b);
+  });
+  std::vector<Plan> out;
+  for (auto& t : list) out.push_back(std::get<3>(t));
+  return out;
 }
 
 // Raises a kernel's dynamic shared-memory limit to at least `bytes` on the current device.  The
 // attribute belongs to the (function, device) pair, so the largest value set so far is kept per pair.
 cudaError_t ensure_smem_attr(const void* fn, size_t bytes) {
-  struct Entry {
-    const void* fn;
-    int dev;
-    size_t bytes;
-  };
-  static Entry table[256];
-  static int used = 0;
+  static std::map<std::pair<const void*, int>, size_t> done;
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
-  Entry* ent = nullptr;
-  for (int i = 0; i < used; ++i)
-    if (table[i].fn == fn && table[i].dev == dev) ent = &table[i];
-  if (ent && ent->bytes >= bytes) return cudaSuccess;
+  size_t& have = done[{fn, dev}];
+  if (have >= bytes) return cudaSuccess;
   e = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(bytes));
   if (e != cudaSuccess) return e;
-  if (!ent && used < 256) ent = &table[used++];
-  if (ent) *ent = Entry{fn, dev, bytes};
+  have = bytes;
+  return cudaSuccess;
+}
+
+cudaLaunchConfig_t launch_config(const Plan& pl, cudaStream_t s, cudaLaunchAttribute (&attr)[2]) {
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.n_rg, pl.ks);
+  cfg.blockDim = dim3(32 * pl.rs * pl.kl);
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (pl.ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = pl.ks;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  return cfg;
+}
+
+// The first candidate whose CTAs (or clusters) can all be resident at once on this device; plans
+// are cached per (kernel, shape, device).
+cudaError_t choose_plan(const void* kern, const tq_desc* d, int B, Plan* out) {
+  static std::map<std::tuple<const void*, int, int, int, int, int>, Plan> cache;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(kern, d->N, d->K, d->group, B, dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  int sms = kSMs;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = kSMs;
+  int optin = 0;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+  Plan chosen{};
+  for (const Plan& pl : candidates(d, B)) {
+    if (pl.smem > static_cast<size_t>(optin)) continue;
+    if ((e = ensure_smem_attr(kern, pl.smem)) != cudaSuccess) return e;
+    bool fits = false;
+    if (pl.ks > 1) {
+      cudaLaunchAttribute attr[2];
+      cudaLaunchConfig_t cfg = launch_config(pl, nullptr, attr);
+      int nc = 0;
+      if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        continue;
+      }
+      fits = nc >= pl.n_rg;
+    } else {
+      int bps = 0;
+      if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, kern, 32 * pl.rs * pl.kl, pl.smem) != cudaSuccess) {
+        (void)cudaGetLastError();
+        continue;
+      }
+      fits = bps > 0 && static_cast<long long>(pl.n_rg) <= static_cast<long long>(bps) * sms;
+    }
+    if (fits) {
+      chosen = pl;
+      chosen.ok = true;
+      break;
+    }
+  }
+  if (!chosen.ok) {  // nothing fits in one wave: take the best plan that launches at all
+    for (const Plan& pl : candidates(d, B)) {
+      if (pl.smem <= static_cast<size_t>(optin) && pl.ks == 1) {
+        chosen = pl;
+        chosen.ok = true;
+        break;
+      }
+    }
+  }
+  if (!chosen.ok) return cudaErrorInvalidConfiguration;
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = chosen;
+  *out = chosen;
   return cudaSuccess;
 }
 
 template <typename Kern>
-cudaError_t launch(Kern kern, const Params& prm, const Plan& pl, cudaStream_t s) {
-  const int optin = max_smem_optin();
-  if (pl.smem + 1024 > static_cast<size_t>(optin)) return cudaErrorInvalidConfiguration;
-  if (cudaError_t e = ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem); e != cudaSuccess) return e;
+cudaError_t launch_main(Kern kern, Params prm, const tq_desc* d, cudaStream_t s) {
+  Plan pl{};
+  cudaError_t e = choose_plan(reinterpret_cast<const void*>(kern), d, prm.B, &pl);
+  if (e != cudaSuccess) return e;
+  if ((e = ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem)) != cudaSuccess) return e;
+  prm.rs = pl.rs;
+  prm.kl = pl.kl;
+  prm.ppl = pl.ppl;
+  prm.upr = pl.upr;
+  prm.xh_off = static_cast<uint32_t>(pl.xh_off);
+  prm.vp_off = static_cast<uint32_t>(pl.vp_off);
+  prm.sw_off = static_cast<uint32_t>(pl.sw_off);
+  prm.bar_off = static_cast<uint32_t>(pl.bar_off);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(pl, s, attr);
+  return cudaLaunchKernelEx(&cfg, kern, prm);
+}
+
+template <int PACK, int G>
+cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.n_rg, pl.ksplit);
-  cfg.blockDim = dim3(32 * pl.wpc);
-  cfg.dynamicSmemBytes = pl.smem;
+  const int nblk = pp.K / kFwhtBlock;
+  cfg.gridDim = dim3((nblk + 3) / 4);
+  cfg.blockDim = dim3(128);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, prm);
+  return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G>, pp);
 }
 
 template <int G>
-cudaError_t launch_b3(const Params& prm, const Plan& pl, cudaStream_t s) {
+cudaError_t launch_b3(const Params& prm, const tq_desc* d, cudaStream_t s) {
   switch ((prm.B + 1) / 2) {
-    case 1: return launch(gemv_b3_kernel<G, 1>, prm, pl, s);
-    case 2: return launch(gemv_b3_kernel<G, 2>, prm, pl, s);
+    case 1: return launch_main(gemv_b3_kernel<G, 1>, prm, d, s);
+    case 2: return launch_main(gemv_b3_kernel<G, 2>, prm, d, s);
     case 3:
-    case 4: return launch(gemv_b3_kernel<G, 4>, prm, pl, s);
-    default: return launch(gemv_b3_kernel<G, 8>, prm, pl, s);
+    case 4: return launch_main(gemv_b3_kernel<G, 4>, prm, d, s);
+    default: return launch_main(gemv_b3_kernel<G, 8>, prm, d, s);
   }
 }
 
 template <int G>
-cudaError_t launch_2b(const Params& prm, const Plan& pl, cudaStream_t s) {
-  if (prm.B <= 8) return launch(gemv_2b_kernel<G, 1>, prm, pl, s);
-  return launch(gemv_2b_kernel<G, 2>, prm, pl, s);
+cudaError_t launch_2b(const Params& prm, const tq_desc* d, cudaStream_t s) {
+  if (prm.B <= 8) return launch_main(gemv_2b_kernel<G, 1>, prm, d, s);
+  return launch_main(gemv_2b_kernel<G, 2>, prm, d, s);
 }
+
+// Workspace: x^ (K x batch halves) then VP (groups x vp_row(batch) floats).
+size_t xh_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d->K) * B * 2); }
 
 }  // namespace gemv
 
-size_t gemv_workspace_bytes(const tq_desc* d, int batch) { return gemv::make_plan(d, batch).total; }
+size_t gemv_workspace_bytes(const tq_desc* d, int batch) {
+  using namespace gemv;
+  // the smallest split (one slab, one K-lane, eight CTAs along K) must fit shared memory
+  const bool b3 = d->packing == TQ_PACK_B3;
+  Plan pl{};
+  pl.upr = (d->K + (b3 ? 640 : 512) - 1) / (b3 ? 640 : 512);
+  pl.rs = 1;
+  pl.kl = 1;
+  pl.ks = std::min(kMaxCluster, pl.upr);
+  pl.ppl = (pl.upr + pl.ks - 1) / pl.ks;
+  if (layout(pl, b3, batch, d->group, d->K) > kSmemLimit) return 0;
+  return xh_bytes(d, batch) + align256(static_cast<size_t>(d->K / d->group) * vp_row(batch) * 4);
+}
 
 cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int B,
                         float* y, void* ws, cudaStream_t s) {
   using namespace gemv;
-  const Plan pl = make_plan(d, B);
+  PrepParams pp{};
+  pp.x = x;
+  pp.xh = static_cast<uint16_t*>(ws);
+  pp.vp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + xh_bytes(d, B));
+  pp.status = status_ptr();
+  pp.K = d->K;
+  pp.B = B;
+  pp.apply = d->fwht_block != 0;
+  const bool b3 = d->packing == TQ_PACK_B3;
+  cudaError_t e = b3 ? (d->group == 128 ? launch_prep<TQ_PACK_B3, 128>(pp, s) : launch_prep<TQ_PACK_B3, 64>(pp, s))
+                     : (d->group == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s) : launch_prep<TQ_PACK_2BIT, 64>(pp, s));
+  if (e != cudaSuccess) return e;
   Params prm{};
   prm.codes = codes;
   prm.scales = scales;
-  prm.x = x;
+  prm.xh_g = pp.xh;
+  prm.vp_g = pp.vp;
   prm.y = y;
-  prm.partial = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + pl.ws_part);
-  prm.counters = reinterpret_cast<unsigned long long*>(static_cast<uint8_t*>(ws) + pl.ws_cnt);
-  prm.status = status_ptr();
+  prm.status = pp.status;
   prm.N = d->N;
   prm.K = d->K;
   prm.P = pitch_words(d->K, d->packing);
   prm.ng = d->K / d->group;
   prm.B = B;
+  prm.R = vp_row(B);
   prm.G = d->group;
-  prm.wpc = pl.wpc;
-  prm.upr = pl.upr;
-  prm.ups = pl.ups;
-  prm.ksplit = pl.ksplit;
-  prm.apply = d->fwht_block != 0;
-  prm.epoch = next_epoch();
-  prm.xh_off = static_cast<uint32_t>(pl.xh_off);
-  prm.v_off = static_cast<uint32_t>(pl.v_off);
-  prm.p2_off = static_cast<uint32_t>(pl.p2_off);
-  if (d->packing == TQ_PACK_B3) return d->group == 128 ? launch_b3<128>(prm, pl, s) : launch_b3<64>(prm, pl, s);
-  return d->group == 128 ? launch_2b<128>(prm, pl, s) : launch_2b<64>(prm, pl, s);
+  prm.early = (d->flags & TQ_STATIC_WEIGHTS) != 0;
+  if (b3) return d->group == 128 ? launch_b3<128>(prm, d, s) : launch_b3<64>(prm, d, s);
+  return d->group == 128 ? launch_2b<128>(prm, d, s) : launch_2b<64>(prm, d, s);
 }
 
 }  // namespace tq

@@ -30,7 +30,9 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
   if (st != TQ_OK) return st;
   if (batch < 1 || batch > kMaxBatch) return TQ_ERR_INVALID_ARG;
   if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
-  if (workspace_bytes < tq_gemv_workspace_bytes(d, batch)) return TQ_ERR_WORKSPACE;
+  const size_t need = tq_gemv_workspace_bytes(d, batch);
+  if (need == 0) return TQ_ERR_UNSUPPORTED;  // the activations of a CTA's K-range do not fit shared memory
+  if (workspace_bytes < need) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const cudaError_t e = launch_gemv(d, codes, scales, x, batch, y, workspace, s);

@@ -45,8 +45,12 @@ def test_invalid_descriptors():
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 100), 1) == 0        # K not a multiple of 128
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, group=32), 1) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 17) == 0        # batch above 16
-    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 1) >= 256
-    assert tq.tq_gemv_workspace_bytes(tq.desc(5120, 17408), 16) > 16 * 5120 * 4   # K-split partials
+    # workspace = the transformed activations (K x batch halves) and one row of floats per group
+    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 1) == 256 + 256
+    assert tq.tq_gemv_workspace_bytes(tq.desc(5120, 17408), 16) == 17408 * 16 * 2 + 11008  # 136 x 20 floats, 256-rounded
+    assert tq.tq_gemv_workspace_bytes(tq.desc(64, 128 * 4096), 16) == 0        # activations of a CTA too large
+    assert tq.tq_gemv_workspace_bytes(tq.desc(64, 128, flags=2), 1) == 0        # unknown flag
+    assert tq.tq_gemv_workspace_bytes(tq.desc(64, 128, flags=tq.TQ_STATIC_WEIGHTS), 1) == 512
     assert tq.tq_moe_workspace_bytes(1, 257, 8, 2048, 512) == 0
     assert tq.tq_moe_workspace_bytes(8, 256, 8, 2048, 512) > 0
 
@@ -71,6 +75,10 @@ def test_host_validation_before_launch():
     assert _call("tq_gemv", bd, A16, A16, A16, 17, A16, A16, 1 << 20, None) == 1     # batch 17
     assert _call("tq_gemv", bd, A16, A16, A16, 1, A16, A16 + 16, 1 << 20, None) == 3  # workspace not 256-aligned
     assert _call("tq_gemv", bd, A16, A16, A16, 1, A16, A16, 16, None) == 7           # workspace too small
+    huge = tq.desc(64, 128 * 4096)
+    assert _call("tq_gemv", ctypes.byref(huge), A16, A16, A16, 16, A16, A16, 1 << 20, None) == 2
+    bad_flags = tq.desc(64, 256, flags=4)
+    assert _call("tq_gemv", ctypes.byref(bad_flags), A16, A16, A16, 1, A16, A16, 1 << 20, None) == 1
     bad_group = tq.desc(64, 256, group=96)
     assert _call("tq_gemv", ctypes.byref(bad_group), A16, A16, A16, 1, A16, A16, 1 << 20, None) == 2
     assert _call("tq_gemm", bd, A16, A16, A16, 0, A16, A16, 1 << 30, None) == 1

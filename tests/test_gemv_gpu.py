@@ -97,3 +97,21 @@ def test_split_tiles(packing, N, K, batch):
     check_tolerance(run(case), y_ref, A)
     y2 = tq.tq_gemv(case.desc, case.codes, case.scales, case.x).cpu().numpy()
     assert np.array_equal(y2, run(case))   # deterministic across calls
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("N,K,batch", [(300, 1280, 2), (5120, 17408, 1), (17408, 5120, 4), (129, 640, 16)])
+def test_static_weights_flag(packing, N, K, batch):
+    """TQ_STATIC_WEIGHTS only moves the first weight loads before the dependent-launch wait: the result
+    is bit-identical to the default path, also when the preceding kernel on the stream is a GEMV."""
+    case = LinearCase(16, N + batch, N, K, 128, packing, batch)
+    d_static = tq.desc(N, K, 128, packing, flags=tq.TQ_STATIC_WEIGHTS)
+    y_default = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
+    y_static = [tq.tq_gemv(d_static, case.codes, case.scales, case.x) for _ in range(3)]
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    for y in y_static:
+        assert torch.equal(y, y_default)
+    rows = sample_rows(N, 64, seed=N)
+    y_ref, A = case.oracle(rows)
+    check_tolerance(y_default.cpu().numpy()[:, rows], y_ref, A)
