@@ -199,7 +199,9 @@ class Stream:
         self.y_bufs = {l.name: torch.empty((batch, l.N), dtype=torch.float32, device=device) for l in self.linears}
         for layer in range(layers):
             for lin in self.linears:
-                d = tq.desc(lin.N, lin.K, 128, packing)
+                # the weights do not change during the stream: let each GEMV start streaming them
+                # while the previous call is still finishing
+                d = tq.desc(lin.N, lin.K, 128, packing, flags=tq.TQ_STATIC_WEIGHTS)
                 t = torch.randint(-1, 2, (lin.N, lin.K), dtype=torch.int8, device=device, generator=gen)
                 codes = tq.tq_pack(d, t)
                 del t
@@ -285,8 +287,8 @@ def per_call_durations(stream: Stream):
 
 
 def traffic_from_profiles(kernel_key: str):
-    """dram bytes per launch recorded by an ncu capture (profiles/ncu_traffic.txt), if the kernel
-    source it was taken on is unchanged."""
+    """DRAM bytes recorded by an ncu capture (profiles/ncu_traffic.txt: key, bytes, source hash), if
+    the kernel sources it was taken on are unchanged."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
@@ -434,11 +436,12 @@ def cpu_baseline(packing, batch, target_s=12.0):
 # arms
 # ----------------------------------------------------------------------------------------------
 
-def config_of(packing, batch):
-    return {"workload": "27B-class dense decode: 64 layers x {q,k,v,o,gate,up,down} ternary GEMV "
+def config_of(packing, batch, layers=None):
+    layers = LAYERS if layers is None else layers
+    return {"workload": f"27B-class dense decode: {layers} layers x {{q,k,v,o,gate,up,down}} ternary GEMV "
                         "(hidden 5120, FFN 17408, 40/8 heads x 128), distinct weights per layer",
             "packing": "base3_20_per_u32" if packing == tq.TQ_PACK_B3 else "2bit", "batch": batch,
-            "group": 128, "fwht_block": 128, "layers": LAYERS,
+            "group": 128, "fwht_block": 128, "layers": layers,
             "l2": "inputs larger than L2 (4.56 GB base-3 / 5.62 GB 2-bit of weights per step)"}
 
 
@@ -471,7 +474,7 @@ def run_tq(args, rank, world, local):
         raise SystemExit("bench.py needs a CUDA device (libtq has no CPU path)")
     peaks = measured_peaks()
     packing, batch = tq.TQ_PACK_B3, args.batch
-    st = Stream(packing, batch)
+    st = Stream(packing, batch, layers=args.layers)
     # warm-up: W eager steps, then capture one step into a graph
     for _ in range(args.warmup):
         st.step()
@@ -502,13 +505,16 @@ def run_tq(args, rank, world, local):
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32-accumulate (fp16 x~ operand, ternary weights)", "data": "synthetic",
-        "config": config_of(packing, batch),
+        "config": config_of(packing, batch, args.layers),
         "tok_s": world * batch / (ms_step * 1e-3),
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic_from_profiles("tq_gemv_call"),
-                     "kernel": "tq_gemv (FWHT prologue + decode GEMV), per call",
+                     "frac": achieved / peaks["hbm_gbs"],
+                     "traffic": traffic_from_profiles(f"dense_decode_b3_b{batch}_per_layer"),
+                     "traffic_unit": "DRAM bytes per layer (7 calls: prep + decode kernels), ncu",
+                     "kernel": "tq_gemv calls (activation prep kernel + decode GEMV kernel), per-call CUDA events",
                      "algorithmic_bytes_per_step": st.bytes_per_step, "calls_per_step": len(st.calls),
+                     "algorithmic_bytes_per_layer": st.bytes_per_step // max(1, args.layers),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": st.h2d_bytes(),
                 "d2h_bytes_per_step": st.d2h_bytes()},
@@ -518,7 +524,7 @@ def run_tq(args, rank, world, local):
     }
     del st, g, ge
     torch.cuda.empty_cache()
-    if rank == 0 and world == 1:
+    if rank == 0 and world == 1 and args.cpu:
         line["cpu_baseline"] = cpu_baseline(packing, batch)
     if args.extras and world == 1:
         ex = {"stream": [], "moe": [], "prefill": []}
@@ -545,7 +551,7 @@ def run_tq(args, rank, world, local):
 
 
 def tq_launches_per_gemv():
-    """Kernels one tq_gemv call launches (FWHT prologue + decode kernel)."""
+    """Kernels one tq_gemv call launches (activation prep kernel + decode GEMV kernel)."""
     return 2
 
 
@@ -556,7 +562,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--layers", type=int, default=LAYERS, help="layers of the weight stream (profiling runs use 1)")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
+    ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank, world, local = dist_setup()
