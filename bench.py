@@ -182,11 +182,13 @@ def linear_bytes(lin, packing, group=128):
 
 
 class Stream:
-    """64 layers x 7 ternary linears of the 27B-class shapes, distinct weights per layer."""
+    """64 layers of the 27B-class shapes, distinct weights per layer.  stacked=True calls the layer the
+    way an inference engine does (qkv, o, gate_up, down: 4 calls); stacked=False calls each of the 7
+    linears separately.  The weights read per token are the same either way."""
 
-    def __init__(self, packing, batch, layers=LAYERS, seed=inputs.seed_of(5), device="cuda"):
-        self.packing, self.batch, self.layers = packing, batch, layers
-        self.linears = inputs.dense_layer_linears()
+    def __init__(self, packing, batch, layers=LAYERS, seed=inputs.seed_of(5), device="cuda", stacked=True):
+        self.packing, self.batch, self.layers, self.stacked = packing, batch, layers, stacked
+        self.linears = inputs.stacked_layer_linears() if stacked else inputs.dense_layer_linears()
         gen = torch.Generator(device=device)
         gen.manual_seed(seed + 10 * packing + batch)
         self.calls = []  # (desc, codes, scales, x, y, ws, bytes)
@@ -436,10 +438,12 @@ def cpu_baseline(packing, batch, target_s=12.0):
 # arms
 # ----------------------------------------------------------------------------------------------
 
-def config_of(packing, batch, layers=None):
+def config_of(packing, batch, layers=None, stacked=True):
     layers = LAYERS if layers is None else layers
     return {"workload": f"27B-class dense decode: {layers} layers x {{q,k,v,o,gate,up,down}} ternary GEMV "
                         "(hidden 5120, FFN 17408, 40/8 heads x 128), distinct weights per layer",
+            "calls_per_layer": "4: qkv (q,k,v stacked, 7168 x 5120), o, gate_up (34816 x 5120), down" if stacked
+            else "7: one per linear",
             "packing": "base3_20_per_u32" if packing == tq.TQ_PACK_B3 else "2bit", "batch": batch,
             "group": 128, "fwht_block": 128, "layers": layers,
             "l2": "inputs larger than L2 (4.56 GB base-3 / 5.62 GB 2-bit of weights per step)"}
@@ -510,8 +514,8 @@ def run_tq(args, rank, world, local):
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic_from_profiles(f"dense_decode_b3_b{batch}_per_layer"),
-                     "traffic_unit": "DRAM bytes per layer (7 calls: prep + decode kernels), ncu",
+                     "traffic": traffic_from_profiles(f"dense_decode_b3_b{batch}_stacked_per_layer"),
+                     "traffic_unit": "DRAM bytes per layer (4 calls: prep + decode kernels), ncu",
                      "kernel": "tq_gemv calls (activation prep kernel + decode GEMV kernel), per-call CUDA events",
                      "algorithmic_bytes_per_step": st.bytes_per_step, "calls_per_step": len(st.calls),
                      "algorithmic_bytes_per_layer": st.bytes_per_step // max(1, args.layers),
@@ -528,14 +532,16 @@ def run_tq(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(packing, batch)
     if args.extras and world == 1:
         ex = {"stream": [], "moe": [], "prefill": []}
-        for pk, b in ((tq.TQ_PACK_B3, 8), (tq.TQ_PACK_2BIT, 1), (tq.TQ_PACK_2BIT, 8)):
-            s2 = Stream(pk, b)
+        for pk, b, stk in ((tq.TQ_PACK_B3, 8, True), (tq.TQ_PACK_2BIT, 1, True), (tq.TQ_PACK_2BIT, 8, True),
+                           (tq.TQ_PACK_B3, 1, False), (tq.TQ_PACK_2BIT, 1, False)):
+            s2 = Stream(pk, b, stacked=stk)
             s2.step()
             g2 = capture(s2.step, warm=0)
             g2.replay()
             ms2, _ = time_graph(g2, max(3, args.steps // 2), 1)
             ms2 /= max(3, args.steps // 2)
-            ex["stream"].append({"packing": "base3" if pk == tq.TQ_PACK_B3 else "2bit", "batch": b, "ms": ms2,
+            ex["stream"].append({"packing": "base3" if pk == tq.TQ_PACK_B3 else "2bit", "batch": b,
+                                 "calls_per_layer": 4 if stk else 7, "ms": ms2,
                                  "GB_s": s2.bytes_per_step / (ms2 * 1e-3) / GB, "tok_s": b / (ms2 * 1e-3)})
             del s2, g2
             torch.cuda.empty_cache()

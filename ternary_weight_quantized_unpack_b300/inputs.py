@@ -135,6 +135,18 @@ def dense_layer_linears(hidden: int = 5120, ffn: int = 17408, n_q: int = 40, n_k
     ]
 
 
+def stacked_layer_linears(hidden: int = 5120, ffn: int = 17408, n_q: int = 40, n_kv: int = 8, head_dim: int = 128):
+    """The same seven linears grouped as an inference engine calls them: q, k and v read the same input
+    and are stacked into one projection (rows q, then k, then v), gate and up likewise (rows gate, then
+    up).  Every weight is still read once per token; four calls per layer instead of seven."""
+    return [
+        Linear("qkv", (n_q + 2 * n_kv) * head_dim, hidden),
+        Linear("o", hidden, n_q * head_dim),
+        Linear("gate_up", 2 * ffn, hidden),
+        Linear("down", hidden, ffn),
+    ]
+
+
 def seed_of(config: int) -> int:
     """Seed of workload ``config`` (1..5): the single-layer case uses seed 0, workload c uses 1000*c."""
     return 0 if config == 1 else 1000 * config

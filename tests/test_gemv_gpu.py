@@ -59,6 +59,19 @@ def test_dense_layer_full_size_sampled(lin, batch, packing):
     check_tolerance(y[:, rows], y_ref, A)
 
 
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("batch", [1, 8])
+@pytest.mark.parametrize("lin", inputs.stacked_layer_linears()[::2], ids=lambda l: l.name)
+def test_stacked_projections_full_size_sampled(lin, batch, packing):
+    """The stacked qkv (7168 x 5120) and gate_up (34816 x 5120) projections the stream benchmark calls."""
+    tid = 200 + inputs.stacked_layer_linears().index(lin)
+    case = LinearCase(inputs.seed_of(5), tid, lin.N, lin.K, 128, packing, batch)
+    y = run(case)
+    rows = sample_rows(lin.N, 48, seed=tid)
+    y_ref, A = case.oracle(rows)
+    check_tolerance(y[:, rows], y_ref, A)
+
+
 def test_zero_trits_and_determinism():
     d = tq.desc(64, 1024, 128, B3)
     codes = tq.tq_pack(d, torch.zeros((64, 1024), dtype=torch.int8, device="cuda"))
