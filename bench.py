@@ -571,11 +571,24 @@ def main():
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers of the weight stream (profiling runs use 1)")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
+    ap.add_argument("--workload", choices=["stream", "prefill", "moe"], default="stream",
+                    help="stream: the headline decode line; prefill / moe: one line per shape of those workloads")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
+    elif args.workload == "prefill":
+        if rank == 0:
+            peaks = measured_peaks()
+            for shape in inputs.PREFILL["shapes"]:
+                r = bench_prefill(shape, args.steps, args.warmup)
+                r["pct_of_bf16_peak"] = 100.0 * r["TFLOP_s"] / peaks["bf16_tflops"]
+                print(json.dumps({"workload": "prefill", **r}))
+    elif args.workload == "moe":
+        if rank == 0:
+            for T in inputs.MOE["tokens"]:
+                print(json.dumps({"workload": "moe", **bench_moe(T, args.steps, args.warmup)}))
     else:
         run_tq(args, rank, world, local)
     if world > 1:

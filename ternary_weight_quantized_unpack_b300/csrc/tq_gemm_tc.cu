@@ -1,0 +1,257 @@
+// Batched prefill: Y[m][n] = bf16( sum_k x~[m][k] * s[n][k/group] * t[n][k] ), fp32 accumulation.
+//
+// Prefill is a dense contraction (M = 2048..4096 tokens), so it runs on the 5th-generation tensor
+// cores (tcgen05.mma kind::f16, accumulators in tensor memory).  The ternary weights are decoded
+// once per call into exact FP16 products s * t (t in {-1, 0, 1}, so s * t is s, -s or 0): decoding
+// inside the MMA loop would cost about one instruction per weight, and with 256 tokens of reuse per
+// weight tile the SM would need ~16 decoded weights per cycle to keep the tensor pipe busy, far above
+// its issue rate.  The one-off decode streams the packed weights from HBM (0.25 B per weight, 2-bit)
+// and writes 2 B per weight; its cost is amortised over all M tokens.
+//
+// GEMM kernel (one 128-token x 256-weight-row output tile per CTA, K in steps of 64):
+//   warp 0     TMA producer: 128B-swizzled tiles of x~ (128 x 64) and W (256 x 64) into a 4-stage ring
+//   warp 1     MMA issuer (one thread): 4 x tcgen05.mma M128 N256 K16 per stage, commit frees the stage
+//   warps 2-5  epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator, bf16 conversion, stores
+// Every mbarrier wait is bounded; a wait that runs out records TQ_ERR_TIMEOUT and the warp stops.
+// Activations are the block Walsh-Hadamard transform of x in FP16 (cosmocat.dev "27B 大模型塞进
+// 5.9GB", section 二 ①); group scales per 64 or 128 weights (same page, section 二 ②).
+#include <cuda_bf16.h>
+
+#include <map>
+#include <mutex>
+
+#include "tq_internal.cuh"
+#include "tq_kernels.cuh"
+#include "tq_sm100.cuh"
+#include "tq_tmap.cuh"
+
+namespace tq {
+namespace gemm {
+
+using namespace sm100;
+
+constexpr int BM = 128;  // tokens per tile (MMA M, TMEM lanes)
+constexpr int BN = 256;  // weight rows per tile (MMA N, TMEM columns)
+constexpr int BK = 64;   // K per stage: one 128-byte swizzle row of FP16
+constexpr int STAGES = 4;
+constexpr uint32_t kABytes = BM * BK * 2;
+constexpr uint32_t kBBytes = BN * BK * 2;
+constexpr int kThreads = 192;
+constexpr uint32_t kTmemCols = 256;
+
+struct Smem {
+  uint8_t a[STAGES][kABytes];  // each 1024-byte aligned (sizes are multiples of 1024)
+  uint8_t b[STAGES][kBBytes];
+  uint64_t full[STAGES];
+  uint64_t empty[STAGES];
+  uint64_t done;
+  uint32_t tmem;
+};
+constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment of the base to 1024
+
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, uint16_t* y,
+                   int M, int N, int K, int* status) {
+  extern __shared__ uint8_t smem_raw[];
+  Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
+  const int nk = K / BK;
+  if (threadIdx.x == 0) {
+#pragma unroll
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&sm.full[s], 1);
+      mbar_init(&sm.empty[s], 1);
+    }
+    mbar_init(&sm.done, 1);
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    tmem_alloc(&sm.tmem, kTmemCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = sm.tmem;
+
+  if (warp == 0 && lane == 0) {
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      if (kb >= STAGES && !mbar_wait(&sm.empty[s], ((kb / STAGES) & 1) ^ 1)) {
+        record_error(status, TQ_ERR_TIMEOUT);
+        break;
+      }
+      mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
+      tma_load_2d(sm.a[s], &tm_x, kb * BK, m0, &sm.full[s]);
+      tma_load_2d(sm.b[s], &tm_w, kb * BK, n0, &sm.full[s]);
+    }
+  } else if (warp == 1 && lane == 0) {
+    constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
+    for (int kb = 0; kb < nk; ++kb) {
+      const int s = kb % STAGES;
+      if (!mbar_wait(&sm.full[s], (kb / STAGES) & 1)) {
+        record_error(status, TQ_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const uint32_t a0 = smem_addr(sm.a[s]), b0 = smem_addr(sm.b[s]);
+#pragma unroll
+      for (int k = 0; k < BK / 16; ++k)
+        mma_f16_ss(tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc, (kb | k) != 0);
+      mma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
+    }
+    mma_commit(&sm.done);
+  } else if (warp >= 2) {
+    if (!mbar_wait(&sm.done, 0) && lane == 0) record_error(status, TQ_ERR_TIMEOUT);
+    tc_fence_after();
+    const int q = warp & 3;  // a warp reads TMEM lanes 32 (warp % 4) .. + 31
+    const int m = m0 + 32 * q + lane;
+    const bool vec = (N & 7) == 0;
+#pragma unroll 1
+    for (int c = 0; c < BN; c += 32) {
+      uint32_t v[32];
+      tmem_ld<32>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c), v);
+      tmem_wait_ld();
+      const int n = n0 + c;
+      if (m < M && n < N) {
+        uint16_t* dst = y + static_cast<size_t>(m) * N + n;
+        if (vec && n + 32 <= N) {
+#pragma unroll
+          for (int j = 0; j < 32; j += 8) {
+            uint4 o;
+            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[j + 2 * i]), __uint_as_float(v[j + 2 * i + 1]));
+              ow[i] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            *reinterpret_cast<uint4*>(dst + j) = o;
+          }
+        } else {
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            if (n + j < N) {
+              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
+              dst[j] = *reinterpret_cast<const uint16_t*>(&h);
+            }
+          }
+        }
+      }
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 1) tmem_dealloc(tmem, kTmemCols);
+}
+
+// ---------------------------------------------------------------------------------------------
+// Decode: codes -> W[n][k] = s[n][k / G] * t[n][k] as FP16 (exact: s, -s or 0).
+// 2-bit: one thread per word (16 trits, one group), two 16-byte stores.
+// base-3: one thread per 4 words (80 trits), digits by exact reciprocal multiplies.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint16_t signed_scale(int t, uint16_t s) {
+  return t == 0 ? static_cast<uint16_t>(0) : (t > 0 ? s : static_cast<uint16_t>(s ^ 0x8000u));
+}
+
+__global__ void decode_2b_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                                 uint16_t* __restrict__ w, int N, int K, int P, int ng, int G) {
+  const int wpr = K / 16;  // words with data per row
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(N) * wpr) return;
+  const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
+  const uint32_t word = __ldg(codes + static_cast<size_t>(n) * P + j);
+  const uint16_t s = __ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G);
+  uint32_t o[8];
+#pragma unroll
+  for (int h = 0; h < 8; ++h) {
+    const int d0 = static_cast<int>((word >> (4 * h)) & 3u), d1 = static_cast<int>((word >> (4 * h + 2)) & 3u);
+    // a field of 3 is not a valid code: it decodes as t = 0, as tq_unpack reads it
+    const int t0 = d0 == 3 ? 0 : d0 - 1, t1 = d1 == 3 ? 0 : d1 - 1;
+    o[h] = static_cast<uint32_t>(signed_scale(t0, s)) | (static_cast<uint32_t>(signed_scale(t1, s)) << 16);
+  }
+  uint4* dst = reinterpret_cast<uint4*>(w + static_cast<size_t>(n) * K + 16 * j);
+  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
+  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+}
+
+__global__ void decode_b3_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
+                                 uint16_t* __restrict__ w, int N, int K, int P, int ng, int G) {
+  const int qpr = K / 80;  // groups of 4 words (80 trits, 160 bytes of output) per row; K % 80 handled below
+  const int tail = K - qpr * 80;
+  const int per_row = qpr + (tail > 0 ? 1 : 0);
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(N) * per_row) return;
+  const int n = static_cast<int>(i / per_row), j = static_cast<int>(i - static_cast<long long>(n) * per_row);
+  const int k0 = 80 * j, kn = min(80, K - k0);
+  uint16_t* dst = w + static_cast<size_t>(n) * K + k0;
+  const uint16_t* srow = scales + static_cast<size_t>(n) * ng;
+  for (int wi = 0; wi < 4; ++wi) {
+    if (20 * wi >= kn) break;
+    uint32_t v = min(__ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi), kB3Max);
+#pragma unroll
+    for (int d = 0; d < 20; ++d) {
+      const uint32_t qd = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
+      const int t = static_cast<int>(v - 3u * qd) - 1;
+      v = qd;
+      const int k = 20 * wi + d;
+      if (k < kn) dst[k] = signed_scale(t, __ldg(srow + (k0 + k) / G));
+    }
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+cudaError_t ensure_attr() {
+  static std::map<int, bool> done;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  if (done[dev]) return cudaSuccess;
+  e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  if (e == cudaSuccess) done[dev] = true;
+  return e;
+}
+
+}  // namespace gemm
+
+size_t gemm_workspace_bytes(const tq_desc* d, int M) {
+  return align256(static_cast<size_t>(M) * d->K * 2) + align256(static_cast<size_t>(d->N) * d->K * 2);
+}
+
+cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int M,
+                        uint16_t* y, void* ws, cudaStream_t s) {
+  using namespace gemm;
+  const int N = d->N, K = d->K, G = d->group, P = pitch_words(K, d->packing), ng = K / G;
+  uint16_t* xa = static_cast<uint16_t*>(ws);
+  uint16_t* wa = reinterpret_cast<uint16_t*>(static_cast<uint8_t*>(ws) + align256(static_cast<size_t>(M) * K * 2));
+  // x~ in FP16 (values beyond the FP16 range record TQ_ERR_RANGE)
+  cudaError_t e = launch_fwht_bf16(x, xa, 1, M, K, d->fwht_block != 0, s);
+  if (e != cudaSuccess) return e;
+  // W = s * t in FP16
+  if (d->packing == TQ_PACK_2BIT) {
+    const long long n = static_cast<long long>(N) * (K / 16);
+    decode_2b_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
+  } else {
+    const long long n = static_cast<long long>(N) * ((K + 79) / 80);
+    decode_b3_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
+  }
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
+  CUtensorMap tm_x, tm_w;
+  if (!make_tmap_2d(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, M, static_cast<uint64_t>(K) * 2, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_w, wa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, static_cast<uint64_t>(K) * 2, BK, BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if ((e = ensure_attr()) != cudaSuccess) return e;
+  // token tiles vary fastest, so the CTAs running at one time share a few weight tiles (L2 reuse)
+  const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
+  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status_ptr());
+  return cudaPeekAtLastError();
+}
+
+}  // namespace tq

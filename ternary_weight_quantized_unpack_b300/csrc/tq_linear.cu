@@ -1,7 +1,6 @@
 // Entry points of the dense ternary contraction: tq_gemv (decode) and tq_gemm (prefill).
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
-#include "tq_simple.cuh"
 
 namespace tq {
 namespace {
@@ -42,7 +41,7 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
 
 extern "C" size_t tq_gemm_workspace_bytes(const tq_desc* d, int M) {
   if (check_linear_desc(d) != TQ_OK || M < 1) return 0;
-  return align256(static_cast<size_t>(M) * d->K * sizeof(float));
+  return gemm_workspace_bytes(d, M);
 }
 
 extern "C" tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
@@ -54,8 +53,6 @@ extern "C" tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint
   if (workspace_bytes < tq_gemm_workspace_bytes(d, M)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  float* xt = static_cast<float*>(workspace);
-  if (const cudaError_t e = launch_fwht_bf16(x, xt, 0, M, d->K, d->fwht_block != 0, s); e != cudaSuccess) return cuda_fail(e);
-  if (const cudaError_t e = launch_gemm_simple(d, codes, scales, xt, M, y, s); e != cudaSuccess) return cuda_fail(e);
+  if (const cudaError_t e = launch_gemm(d, codes, scales, x, M, y, workspace, s); e != cudaSuccess) return cuda_fail(e);
   return TQ_OK;
 }

@@ -1,4 +1,4 @@
-// Device helpers and launchers of the CUDA-core contraction kernels (internal).
+// Device helper of the CUDA-core MoE kernels (internal).
 #pragma once
 
 #include "tq_internal.cuh"
@@ -36,10 +36,5 @@ __device__ __forceinline__ void row_dot_accumulate(const uint32_t* __restrict__ 
     }
   }
 }
-
-cudaError_t launch_gemv_simple(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const float* xt,
-                               int batch, float* y, cudaStream_t s);
-cudaError_t launch_gemm_simple(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const float* xt,
-                               int M, uint16_t* y, cudaStream_t s);
 
 }  // namespace tq

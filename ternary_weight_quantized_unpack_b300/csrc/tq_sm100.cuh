@@ -186,6 +186,19 @@ __device__ __forceinline__ void tmem_ld<16>(uint32_t taddr, uint32_t (&v)[16]) {
       : "memory");
 }
 
+template <>
+__device__ __forceinline__ void tmem_ld<32>(uint32_t taddr, uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, "
+      "%15, %16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+
 // ---- tcgen05: MMA -------------------------------------------------------------------------------
 // Instruction descriptor, kind::f16: D fp32, A and B FP16, both K-major, M = m, N = n.
 __host__ __device__ constexpr uint32_t idesc_f16_f32(int m, int n) {
@@ -198,6 +211,18 @@ __device__ __forceinline__ uint64_t smem_desc_noswizzle(uint32_t saddr, uint32_t
   d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
   d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
   d |= 1ull << 46;  // descriptor version for sm_100
+  return d;
+}
+// Shared-memory matrix descriptor, K-major, 128-byte swizzle: rows of 128 bytes (64 FP16 along K),
+// 16-byte chunks XOR-ed with (row % 8), 8-row groups 1024 bytes apart (the layout a TMA load with
+// CU_TENSOR_MAP_SWIZZLE_128B writes).  The tile must start on a 1024-byte boundary; a K offset inside
+// the 128-byte row is added to the start address.
+__device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= 1ull << 16;                   // leading byte offset: unused for swizzled K-major layouts
+  d |= static_cast<uint64_t>(1024 >> 4) << 32;  // stride byte offset: 8 rows x 128 bytes
+  d |= 1ull << 46;                   // descriptor version for sm_100
+  d |= 2ull << 61;                   // layout: 128-byte swizzle
   return d;
 }
 // D[tmem] (+)= A[tmem] * B[smem]^T, issued by one thread.
