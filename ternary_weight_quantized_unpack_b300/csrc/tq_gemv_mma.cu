@@ -111,12 +111,23 @@ __device__ const LutTable g_lut = make_lut();
 //           word u of quad thread q in group gi, pair index jp (MMA jj = jp / 2), half = trit / 8.
 // ---------------------------------------------------------------------------------------------
 struct PrepParams {
-  const uint16_t* x;
+  const uint16_t* x;  // modes 0, 1: bf16 rows
+  const float* gu;    // mode 2: gate / up outputs, rows of 2K floats (gate then up)
+  float* h_out;       // mode 2: optional copy of h = silu(gate) * up, rows of K floats
   uint16_t* xh;
   float* vp;
   int* status;
   int K, B, apply;
+  // 0: batch row b is x row b.  With routed-token chunks (mode 1, 2) blockIdx.z selects a chunk
+  // record {expert, count, rows[B]}: mode 1 reads x row rows[b] / topk, mode 2 forms
+  // silu(gate) * up of gu row rows[b]; slots past count are zero.  Chunk z writes its own slice.
+  int mode;
+  const int* chunks;
+  int topk;
+  size_t xh_cstride, vp_cstride;  // halves / floats per chunk
 };
+
+__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 template <int PACK, int G>
 __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ PrepParams p) {
@@ -127,16 +138,43 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
   if (blk * kFwhtBlock >= p.K) return;
   const int B = p.B, R = vp_row(B);
   const int kb = blk * kFwhtBlock + 4 * lane;
+  int count = B;
+  const int* rows = nullptr;
+  uint16_t* xh = p.xh;
+  float* vpo = p.vp;
+  if (p.mode != 0) {
+    const int z = static_cast<int>(blockIdx.z);
+    if (z >= p.chunks[0]) return;
+    const int* rec = p.chunks + 1 + static_cast<size_t>(z) * (2 + B);
+    count = rec[1];
+    rows = rec + 2;
+    xh += static_cast<size_t>(z) * p.xh_cstride;
+    vpo += static_cast<size_t>(z) * p.vp_cstride;
+  }
   float v[kMaxBatch][4];
   float mx = 0.f;
 #pragma unroll
   for (int b = 0; b < kMaxBatch; ++b) {
     if (b < B) {
-      const uint2 raw = __ldg(reinterpret_cast<const uint2*>(p.x + static_cast<size_t>(b) * p.K + kb));
-      v[b][0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
-      v[b][1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
-      v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
-      v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
+      if (b >= count) {
+        v[b][0] = v[b][1] = v[b][2] = v[b][3] = 0.f;
+      } else if (p.mode == 2) {  // h = silu(gate) * up of the assignment's gate / up row
+        const size_t a = static_cast<size_t>(rows[b]);
+        const float4 gg = *reinterpret_cast<const float4*>(p.gu + a * 2 * p.K + kb);
+        const float4 uu = *reinterpret_cast<const float4*>(p.gu + a * 2 * p.K + p.K + kb);
+        v[b][0] = silu(gg.x) * uu.x;
+        v[b][1] = silu(gg.y) * uu.y;
+        v[b][2] = silu(gg.z) * uu.z;
+        v[b][3] = silu(gg.w) * uu.w;
+        if (p.h_out) *reinterpret_cast<float4*>(p.h_out + a * p.K + kb) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
+      } else {
+        const size_t r = p.mode == 1 ? static_cast<size_t>(rows[b] / p.topk) : static_cast<size_t>(b);
+        const uint2 raw = *reinterpret_cast<const uint2*>(p.x + r * p.K + kb);
+        v[b][0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
+        v[b][1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
+        v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
+        v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
+      }
       if (p.apply) fwht128_warp(v[b]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[b][j]));
@@ -177,7 +215,7 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
       }
       const float F = __int_as_float((127 + 8 - 2 * pos) << 23);
       const __half h = __float2half_rn(v[b][j] * down * F);
-      p.xh[off] = __half_as_ushort(h);
+      xh[off] = __half_as_ushort(h);
       vs += __half2float(h) * __int_as_float((127 - 8 + 2 * pos) << 23);
     }
     if (G == 128) {
@@ -187,12 +225,12 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
     }
-    if ((lane & (G == 128 ? 31 : 15)) == 0) p.vp[(kb / G) * R + b] = -1.52587890625e-05f * vs;
+    if ((lane & (G == 128 ? 31 : 15)) == 0) vpo[(kb / G) * R + b] = -1.52587890625e-05f * vs;
   }
   if (lane < kFwhtBlock / G) {  // per group of the block: padding zeros and the block factor
     const int gi = blk * (kFwhtBlock / G) + lane;
-    for (int b = B; b < R - 1; ++b) p.vp[gi * R + b] = 0.f;
-    p.vp[gi * R + R - 1] = __int_as_float((127 + 16 + e) << 23);  // 2^(16 + e)
+    for (int b = B; b < R - 1; ++b) vpo[gi * R + b] = 0.f;
+    vpo[gi * R + R - 1] = __int_as_float((127 + 16 + e) << 23);  // 2^(16 + e)
   }
 }
 
@@ -213,7 +251,46 @@ struct Params {
   int upr;    // units per row
   int early;  // 1: codes and scales may be read before the preceding kernel has completed
   uint32_t xh_off, vp_off, sw_off, bar_off;  // shared-memory offsets: x^, VP, per-warp scales, barriers
+  // Routed-token chunks (nullptr: one dense matrix).  blockIdx.z selects record {expert, count,
+  // rows[B]} of chunks[1 + z * (2 + B)] (chunks[0] = number of records); the expert's codes and
+  // scales start expert * *_estride elements in, the chunk's prep slice z * *_cstride in, and batch
+  // slot b (< count) is stored to output row rows[b].
+  const int* chunks;
+  size_t codes_estride, scales_estride, xh_cstride, vp_cstride;
 };
+
+// Operands of this CTA: the whole call, or one chunk of routed tokens.
+struct Sel {
+  const uint32_t* codes;
+  const uint16_t* scales;
+  const uint16_t* xh;
+  const float* vp;
+  const int* rows;  // output row of each batch slot, or nullptr (slot b -> row b)
+  int count;        // batch slots holding data
+};
+
+// false: this CTA has no chunk (the grid covers the largest possible number of chunks).  With chunks
+// the record is written by the preceding kernel, so this runs after the dependent-launch wait.
+__device__ __forceinline__ bool select_operands(const Params& p, Sel& s) {
+  s.codes = p.codes;
+  s.scales = p.scales;
+  s.xh = p.xh_g;
+  s.vp = p.vp_g;
+  s.rows = nullptr;
+  s.count = p.B;
+  if (!p.chunks) return true;
+  pdl_wait();
+  const int z = static_cast<int>(blockIdx.z);
+  if (z >= p.chunks[0]) return false;
+  const int* rec = p.chunks + 1 + static_cast<size_t>(z) * (2 + p.B);
+  s.codes += static_cast<size_t>(rec[0]) * p.codes_estride;
+  s.scales += static_cast<size_t>(rec[0]) * p.scales_estride;
+  s.xh += static_cast<size_t>(z) * p.xh_cstride;
+  s.vp += static_cast<size_t>(z) * p.vp_cstride;
+  s.rows = rec + 2;
+  s.count = rec[1];
+  return true;
+}
 
 // Where this thread's CTA and warp sit in the problem.
 struct Cta {
@@ -269,11 +346,11 @@ struct UnitScales {
   static_assert(PER_LANE % 2 == 0, "scales are packed in pairs");
   uint32_t v[PER_LANE / 2];
 
-  __device__ __forceinline__ void load(const Params& p, int row_w0, int u, int ngp, int lane) {
+  __device__ __forceinline__ void load(const Params& p, const uint16_t* scales, int row_w0, int u, int ngp, int lane) {
 #pragma unroll
     for (int j = 0; j < PER_LANE; ++j) {
       const int e = lane + 32 * j, r = e / NG, g = min(e % NG, ngp - 1), row = min(row_w0 + r, p.N - 1);
-      const uint32_t h = __ldg(p.scales + static_cast<size_t>(row) * p.ng + u * NG + g);
+      const uint32_t h = __ldg(scales + static_cast<size_t>(row) * p.ng + u * NG + g);
       if (j & 1)
         v[j >> 1] |= h << 16;
       else
@@ -314,13 +391,14 @@ __device__ __forceinline__ void init_bars(Bars* bars) {
   __syncthreads();
 }
 
-__device__ __forceinline__ void copy_prep_slice(const Params& p, const Cta& c, uint8_t* smem, Bars* bars) {
+__device__ __forceinline__ void copy_prep_slice(const Params& p, const Cta& c, const Sel& sel, uint8_t* smem,
+                                                Bars* bars) {
   if (threadIdx.x == 0) {
     const uint32_t xb = static_cast<uint32_t>(c.kr) * p.B * 2u;
     const uint32_t vb = static_cast<uint32_t>(c.ngr) * p.R * 4u;
     mbar_arrive_expect_tx(&bars->x, xb + vb);
-    bulk_g2s(smem + p.xh_off, p.xh_g + static_cast<size_t>(c.k_start) * p.B, xb, &bars->x);
-    bulk_g2s(smem + p.vp_off, p.vp_g + static_cast<size_t>(c.g_abs0) * p.R, vb, &bars->x);
+    bulk_g2s(smem + p.xh_off, sel.xh + static_cast<size_t>(c.k_start) * p.B, xb, &bars->x);
+    bulk_g2s(smem + p.vp_off, sel.vp + static_cast<size_t>(c.g_abs0) * p.R, vb, &bars->x);
   }
 }
 
@@ -332,7 +410,7 @@ __device__ __forceinline__ void wait_bar(const Params& p, uint64_t* bar) {
 // Partial sums red[kl][RT][B] (in shared memory) -> y.  K-lanes are added in lane order, then the
 // cluster's CTAs in rank order through distributed shared memory.  Every thread calls this.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, float* red) {
+__device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, const Sel& sel, float* red) {
   const int E = c.RT * p.B;
   if (p.kl > 1) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
@@ -346,7 +424,7 @@ __device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, floa
   if (ks == 1) {
     for (int e = threadIdx.x; e < E; e += blockDim.x) {
       const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
-      if (row < p.N) p.y[static_cast<size_t>(b) * p.N + row] = red[e];
+      if (row < p.N && b < sel.count) p.y[static_cast<size_t>(sel.rows ? sel.rows[b] : b) * p.N + row] = red[e];
     }
     return;
   }
@@ -360,7 +438,7 @@ __device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, floa
     for (int r = 0; r < ks; ++r)
       v += ld_cluster_f32(cluster_map(base + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(r)));
     const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
-    if (row < p.N) p.y[static_cast<size_t>(b) * p.N + row] = v;
+    if (row < p.N && b < sel.count) p.y[static_cast<size_t>(sel.rows ? sel.rows[b] : b) * p.N + row] = v;
   }
   cluster_sync();  // keep this CTA's shared memory alive until the peers have read it
 }
@@ -376,6 +454,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_launch_dependents();
   const Cta c = cta_geometry<TQ_PACK_2BIT>(p);
+  Sel sel;
+  if (!select_operands(p, sel)) return;
   Bars* bars = reinterpret_cast<Bars*>(smem + p.bar_off);
   init_bars(bars);
   const int g = c.lane >> 2, q = c.lane & 3;
@@ -384,8 +464,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
   // this warp's groups, relative to the CTA's first group
   const int gl_a = (c.ua - c.u0) * GPU;
   const int gl_b = max(gl_a, min((c.ub - c.u0) * GPU, c.ngr));
-  const uint32_t* cg = p.codes + static_cast<size_t>(vg ? rg : 0) * p.P + c.k_start / 16 + WPT * q;
-  const uint32_t* cg8 = p.codes + static_cast<size_t>(vg8 ? rg8 : 0) * p.P + c.k_start / 16 + WPT * q;
+  const uint32_t* cg = sel.codes + static_cast<size_t>(vg ? rg : 0) * p.P + c.k_start / 16 + WPT * q;
+  const uint32_t* cg8 = sel.codes + static_cast<size_t>(vg8 ? rg8 : 0) * p.P + c.k_start / 16 + WPT * q;
   const int row_w0 = c.row0 + c.slab * 16;
   uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + c.warp * (GPU * 16);
   UnitScales<16, GPU, true> us;
@@ -408,12 +488,12 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
     if (gl_a < gl_b) {
 #pragma unroll
       for (int d = 0; d < D - 1; ++d) fetch(gl_a + d, d);
-      us.load(p, row_w0, c.ua, unit_groups(c.ua), c.lane);
+      us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
   };
   if (p.early) prime();
   pdl_wait();
-  copy_prep_slice(p, c, smem, bars);
+  copy_prep_slice(p, c, sel, smem, bars);
   if (!p.early) prime();
   wait_bar(p, &bars->x);
 
@@ -437,7 +517,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
         __syncwarp();
         us.store(sw, c.lane);
         __syncwarp();
-        if (u + 1 < c.ub) us.load(p, row_w0, u + 1, unit_groups(u + 1), c.lane);
+        if (u + 1 < c.ub) us.load(p, sel.scales, row_w0, u + 1, unit_groups(u + 1), c.lane);
       }
       float cc[NT][4];
 #pragma unroll
@@ -502,7 +582,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
     }
   }
   __syncthreads();
-  reduce_store(p, c, red);
+  reduce_store(p, c, sel, red);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -617,6 +697,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
   extern __shared__ __align__(16) uint8_t smem[];
   pdl_launch_dependents();
   const Cta c = cta_geometry<TQ_PACK_B3>(p);
+  Sel sel;
+  if (!select_operands(p, sel)) return;
   Bars* bars = reinterpret_cast<Bars*>(smem + p.bar_off);
   init_bars(bars);
   const int g = c.lane >> 2, q = c.lane & 3;
@@ -626,8 +708,8 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
   }
   // rows past N compute on row 0 and are not stored
   const int R = c.row0 + c.slab * 64 + c.lane, R2 = R + 32;
-  const uint4* cR = reinterpret_cast<const uint4*>(p.codes + static_cast<size_t>(R < p.N ? R : 0) * p.P);
-  const uint4* cR2 = reinterpret_cast<const uint4*>(p.codes + static_cast<size_t>(R2 < p.N ? R2 : 0) * p.P);
+  const uint4* cR = reinterpret_cast<const uint4*>(sel.codes + static_cast<size_t>(R < p.N ? R : 0) * p.P);
+  const uint4* cR2 = reinterpret_cast<const uint4*>(sel.codes + static_cast<size_t>(R2 < p.N ? R2 : 0) * p.P);
   const int s_begin = c.ua * 8;
   const int s_last = min(c.ub * 8, p.P >> 2) - 1;  // this warp's last 4-word step (a row has P / 4)
   constexpr int GPS = 640 / G;
@@ -648,12 +730,12 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
         ra[i] = __ldg(cR + min(s_begin + i, s_last));
         rb[i] = __ldg(cR2 + min(s_begin + i, s_last));
       }
-      us.load(p, row_w0, c.ua, unit_groups(c.ua), c.lane);
+      us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
   };
   if (p.early) prime();
   pdl_wait();
-  copy_prep_slice(p, c, smem, bars);
+  copy_prep_slice(p, c, sel, smem, bars);
   if (!p.early) prime();
   wait_bar(p, &bars->x);
   wait_bar(p, &bars->lut);
@@ -689,7 +771,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
     __syncwarp();
     us.store(sw, c.lane);
     __syncwarp();
-    if (u + 1 < c.ub) us.load(p, row_w0, u + 1, unit_groups(u + 1), c.lane);
+    if (u + 1 < c.ub) us.load(p, sel.scales, row_w0, u + 1, unit_groups(u + 1), c.lane);
     if (ngp == GPS)
       b3_unit<G, NT, true>(p, c, u, ngp, cR, cR2, s_last, ra, rb, lutA, lutB, bptr, bstr, V, swr, acc);
     else
@@ -708,7 +790,7 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
     }
   }
   __syncthreads();
-  reduce_store(p, c, red);
+  reduce_store(p, c, sel, red);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -795,9 +877,9 @@ cudaError_t ensure_smem_attr(const void* fn, size_t bytes) {
   return cudaSuccess;
 }
 
-cudaLaunchConfig_t launch_config(const Plan& pl, cudaStream_t s, cudaLaunchAttribute (&attr)[2]) {
+cudaLaunchConfig_t launch_config(const Plan& pl, cudaStream_t s, cudaLaunchAttribute (&attr)[2], int zdim = 1) {
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(pl.n_rg, pl.ks);
+  cfg.gridDim = dim3(pl.n_rg, pl.ks, zdim);
   cfg.blockDim = dim3(32 * pl.rs * pl.kl);
   cfg.dynamicSmemBytes = pl.smem;
   cfg.stream = s;
@@ -883,7 +965,7 @@ cudaError_t choose_plan(const void* kern, const tq_desc* d, int B, Plan* out) {
 }
 
 template <typename Kern>
-cudaError_t launch_main(Kern kern, Params prm, const tq_desc* d, cudaStream_t s) {
+cudaError_t launch_main(Kern kern, Params prm, const tq_desc* d, cudaStream_t s, int zdim) {
   Plan pl{};
   cudaError_t e = choose_plan(reinterpret_cast<const void*>(kern), d, prm.B, &pl);
   if (e != cudaSuccess) return e;
@@ -897,15 +979,15 @@ cudaError_t launch_main(Kern kern, Params prm, const tq_desc* d, cudaStream_t s)
   prm.sw_off = static_cast<uint32_t>(pl.sw_off);
   prm.bar_off = static_cast<uint32_t>(pl.bar_off);
   cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = launch_config(pl, s, attr);
+  cudaLaunchConfig_t cfg = launch_config(pl, s, attr, zdim);
   return cudaLaunchKernelEx(&cfg, kern, prm);
 }
 
 template <int PACK, int G>
-cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s) {
+cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s, int zdim) {
   cudaLaunchConfig_t cfg = {};
   const int nblk = pp.K / kFwhtBlock;
-  cfg.gridDim = dim3((nblk + 3) / 4);
+  cfg.gridDim = dim3((nblk + 3) / 4, 1, zdim);
   cfg.blockDim = dim3(128);
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -917,24 +999,52 @@ cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s) {
 }
 
 template <int G>
-cudaError_t launch_b3(const Params& prm, const tq_desc* d, cudaStream_t s) {
+cudaError_t launch_b3(const Params& prm, const tq_desc* d, cudaStream_t s, int zdim) {
   switch ((prm.B + 1) / 2) {
-    case 1: return launch_main(gemv_b3_kernel<G, 1>, prm, d, s);
-    case 2: return launch_main(gemv_b3_kernel<G, 2>, prm, d, s);
+    case 1: return launch_main(gemv_b3_kernel<G, 1>, prm, d, s, zdim);
+    case 2: return launch_main(gemv_b3_kernel<G, 2>, prm, d, s, zdim);
     case 3:
-    case 4: return launch_main(gemv_b3_kernel<G, 4>, prm, d, s);
-    default: return launch_main(gemv_b3_kernel<G, 8>, prm, d, s);
+    case 4: return launch_main(gemv_b3_kernel<G, 4>, prm, d, s, zdim);
+    default: return launch_main(gemv_b3_kernel<G, 8>, prm, d, s, zdim);
   }
 }
 
 template <int G>
-cudaError_t launch_2b(const Params& prm, const tq_desc* d, cudaStream_t s) {
-  if (prm.B <= 8) return launch_main(gemv_2b_kernel<G, 1>, prm, d, s);
-  return launch_main(gemv_2b_kernel<G, 2>, prm, d, s);
+cudaError_t launch_2b(const Params& prm, const tq_desc* d, cudaStream_t s, int zdim) {
+  if (prm.B <= 8) return launch_main(gemv_2b_kernel<G, 1>, prm, d, s, zdim);
+  return launch_main(gemv_2b_kernel<G, 2>, prm, d, s, zdim);
 }
 
-// Workspace: x^ (K x batch halves) then VP (groups x vp_row(batch) floats).
+// Prep output of one matrix (or one chunk): x^ (K x batch halves) then VP (groups x vp_row(batch)
+// floats).  Both are multiples of 256 bytes.
 size_t xh_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d->K) * B * 2); }
+size_t vp_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d->K / d->group) * vp_row(B) * 4); }
+
+// Prep kernel then decode kernel; pp and prm carry everything but the shape-derived fields.
+cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int zdim, cudaStream_t s) {
+  pp.status = status_ptr();
+  pp.K = d->K;
+  pp.B = B;
+  pp.apply = d->fwht_block != 0;
+  const bool b3 = d->packing == TQ_PACK_B3;
+  cudaError_t e = b3 ? (d->group == 128 ? launch_prep<TQ_PACK_B3, 128>(pp, s, zdim)
+                                        : launch_prep<TQ_PACK_B3, 64>(pp, s, zdim))
+                     : (d->group == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s, zdim)
+                                        : launch_prep<TQ_PACK_2BIT, 64>(pp, s, zdim));
+  if (e != cudaSuccess) return e;
+  prm.xh_g = pp.xh;
+  prm.vp_g = pp.vp;
+  prm.status = pp.status;
+  prm.N = d->N;
+  prm.K = d->K;
+  prm.P = pitch_words(d->K, d->packing);
+  prm.ng = d->K / d->group;
+  prm.B = B;
+  prm.R = vp_row(B);
+  prm.G = d->group;
+  if (b3) return d->group == 128 ? launch_b3<128>(prm, d, s, zdim) : launch_b3<64>(prm, d, s, zdim);
+  return d->group == 128 ? launch_2b<128>(prm, d, s, zdim) : launch_2b<64>(prm, d, s, zdim);
+}
 
 }  // namespace gemv
 
@@ -949,7 +1059,7 @@ size_t gemv_workspace_bytes(const tq_desc* d, int batch) {
   pl.ks = std::min(kMaxCluster, pl.upr);
   pl.ppl = (pl.upr + pl.ks - 1) / pl.ks;
   if (layout(pl, b3, batch, d->group, d->K) > kSmemLimit) return 0;
-  return xh_bytes(d, batch) + align256(static_cast<size_t>(d->K / d->group) * vp_row(batch) * 4);
+  return xh_bytes(d, batch) + vp_bytes(d, batch);
 }
 
 cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int B,
@@ -959,31 +1069,47 @@ cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t*
   pp.x = x;
   pp.xh = static_cast<uint16_t*>(ws);
   pp.vp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + xh_bytes(d, B));
-  pp.status = status_ptr();
-  pp.K = d->K;
-  pp.B = B;
-  pp.apply = d->fwht_block != 0;
-  const bool b3 = d->packing == TQ_PACK_B3;
-  cudaError_t e = b3 ? (d->group == 128 ? launch_prep<TQ_PACK_B3, 128>(pp, s) : launch_prep<TQ_PACK_B3, 64>(pp, s))
-                     : (d->group == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s) : launch_prep<TQ_PACK_2BIT, 64>(pp, s));
-  if (e != cudaSuccess) return e;
   Params prm{};
   prm.codes = codes;
   prm.scales = scales;
-  prm.xh_g = pp.xh;
-  prm.vp_g = pp.vp;
   prm.y = y;
-  prm.status = pp.status;
-  prm.N = d->N;
-  prm.K = d->K;
-  prm.P = pitch_words(d->K, d->packing);
-  prm.ng = d->K / d->group;
-  prm.B = B;
-  prm.R = vp_row(B);
-  prm.G = d->group;
   prm.early = (d->flags & TQ_STATIC_WEIGHTS) != 0;
-  if (b3) return d->group == 128 ? launch_b3<128>(prm, d, s) : launch_b3<64>(prm, d, s);
-  return d->group == 128 ? launch_2b<128>(prm, d, s) : launch_2b<64>(prm, d, s);
+  return launch_pair(d, pp, prm, B, 1, s);
+}
+
+size_t gemv_chunks_workspace_bytes(const tq_desc* d, int B, int max_chunks) {
+  using namespace gemv;
+  if (gemv_workspace_bytes(d, B) == 0) return 0;
+  return static_cast<size_t>(max_chunks) * (xh_bytes(d, B) + vp_bytes(d, B));
+}
+
+cudaError_t launch_gemv_chunks(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, size_t codes_estride,
+                               size_t scales_estride, int mode, const uint16_t* x, const float* gu, float* h_out,
+                               int topk, const int* chunks, int B, int max_chunks, float* y, void* ws,
+                               cudaStream_t s) {
+  using namespace gemv;
+  PrepParams pp{};
+  pp.x = x;
+  pp.gu = gu;
+  pp.h_out = h_out;
+  pp.xh = static_cast<uint16_t*>(ws);
+  pp.vp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + static_cast<size_t>(max_chunks) * xh_bytes(d, B));
+  pp.mode = mode;
+  pp.chunks = chunks;
+  pp.topk = topk;
+  pp.xh_cstride = xh_bytes(d, B) / 2;
+  pp.vp_cstride = vp_bytes(d, B) / 4;
+  Params prm{};
+  prm.codes = codes;
+  prm.scales = scales;
+  prm.y = y;
+  prm.early = 0;  // the expert of a chunk is known only after routing
+  prm.chunks = chunks;
+  prm.codes_estride = codes_estride;
+  prm.scales_estride = scales_estride;
+  prm.xh_cstride = pp.xh_cstride;
+  prm.vp_cstride = pp.vp_cstride;
+  return launch_pair(d, pp, prm, B, max_chunks, s);
 }
 
 }  // namespace tq

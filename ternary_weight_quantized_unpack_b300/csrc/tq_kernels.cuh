@@ -16,6 +16,18 @@ size_t gemv_workspace_bytes(const tq_desc* d, int batch);
 cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                         int batch, float* y, void* ws, cudaStream_t s);
 
+// Decode GEMV over chunks of routed tokens (expert layer).  chunks[0] = number of records (at most
+// max_chunks); record c = chunks[1 + c * (2 + B)] = {expert, count, rows[B]}.  For slot b < count the
+// input is, mode 1: row rows[b] / topk of x (bf16, K wide); mode 2: silu(gate) * up of row rows[b] of
+// gu (float, gate then up, 2K wide), copied to h_out (K wide) when h_out is not null.  Output row
+// rows[b] of y (N wide) receives the expert's product.  Codes / scales of expert e start
+// e * codes_estride / e * scales_estride elements in.
+size_t gemv_chunks_workspace_bytes(const tq_desc* d, int B, int max_chunks);
+cudaError_t launch_gemv_chunks(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, size_t codes_estride,
+                               size_t scales_estride, int mode, const uint16_t* x, const float* gu, float* h_out,
+                               int topk, const int* chunks, int B, int max_chunks, float* y, void* ws,
+                               cudaStream_t s);
+
 // Prefill GEMM (weights decoded to FP16 once per call, tcgen05 tensor cores); workspace from
 // gemm_workspace_bytes.
 size_t gemm_workspace_bytes(const tq_desc* d, int M);

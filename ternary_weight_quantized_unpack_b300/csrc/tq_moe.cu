@@ -1,11 +1,16 @@
 // Routed MoE expert layer at decode time: top-k routing of 256 experts (8 active per token, router
 // in full precision - tantan.ink/?p=490, section "为什么 1.58bit 没变成乱码", point 1), then the
-// ternary SwiGLU experts, each reading its packed codes once for all tokens routed to it.
+// ternary SwiGLU experts.  The (token, slot) assignments are sorted by expert into chunks of up to
+// 1 / 2 / 4 tokens; the gate/up and down projections run as the decode GEMV kernels over those
+// chunks (blockIdx.z = chunk), so each chunk streams its expert's packed codes once, the prep kernel
+// gathers the tokens (gate/up) or forms FWHT(silu(gate) * up) (down), and a last kernel adds the
+// expert outputs in slot order (deterministic).
 #include <float.h>
+
+#include <algorithm>
 
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
-#include "tq_simple.cuh"
 
 namespace tq {
 namespace {
@@ -66,92 +71,43 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
   }
 }
 
-// One block: per-expert counts, offsets and the (token, slot) assignment list grouped by expert,
-// each expert's entries in ascending (token, slot) order - deterministic.
-__global__ void lists_kernel(const int* __restrict__ idx, int n_assign, int E, int* __restrict__ counts,
-                             int* __restrict__ offsets, int* __restrict__ list) {
+// One block, one thread per expert: the (token, slot) assignments routed to each expert, in ascending
+// order, cut into chunks of at most CB.  table[0] = number of chunks; chunk c is the record
+// table[1 + c * (2 + CB)] = {expert, count, a_0 .. a_(CB-1)}; chunks are in expert order.  Unused
+// slots repeat a_0 (they are never read as data).  Deterministic.
+__global__ void chunks_kernel(const int* __restrict__ idx, int n_assign, int E, int CB, int* __restrict__ table) {
   __shared__ int s_off[kMaxExperts + 1];
   const int e = threadIdx.x;
   int c = 0;
   if (e < E)
     for (int a = 0; a < n_assign; ++a) c += idx[a] == e;
-  if (e < kMaxExperts) s_off[e + 1] = c;
+  s_off[e + 1] = e < E ? (c + CB - 1) / CB : 0;
   __syncthreads();
   if (threadIdx.x == 0) {
     s_off[0] = 0;
-    for (int i = 0; i < E; ++i) s_off[i + 1] += s_off[i];
+    for (int i = 0; i < kMaxExperts; ++i) s_off[i + 1] += s_off[i];
+    table[0] = s_off[kMaxExperts];
   }
   __syncthreads();
-  if (e < E) {
-    counts[e] = c;
-    offsets[e] = s_off[e];
-    int pos = s_off[e];
-    for (int a = 0; a < n_assign && pos < s_off[e] + c; ++a)
-      if (idx[a] == e) list[pos++] = a;
-  }
-  if (threadIdx.x == 0) offsets[E] = s_off[E];
-}
-
-__device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
-
-// gate/up GEMV + SwiGLU: block (expert, 8 rows), warp per row r; for every assignment routed to
-// the expert: h = silu(Wg[r] x~) * (Wu[r] x~).
-template <int PACKING>
-__global__ void __launch_bounds__(256) gate_up_kernel(const uint32_t* __restrict__ gu_codes,
-                                                      const uint16_t* __restrict__ gu_scales,
-                                                      const float* __restrict__ xt, const int* __restrict__ counts,
-                                                      const int* __restrict__ offsets, const int* __restrict__ list,
-                                                      int H, int F, int G, int topk, float* __restrict__ h,
-                                                      float* __restrict__ h_out) {
-  const int e = blockIdx.x;
-  const int cnt = counts[e];
-  if (cnt == 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.y * 8 + warp;
-  if (r >= F) return;
-  const int P = pitch_words(H, PACKING), ng = groups_of(H, G);
-  const uint32_t* wg = gu_codes + (static_cast<size_t>(e) * 2 * F + r) * P;
-  const uint32_t* wu = gu_codes + (static_cast<size_t>(e) * 2 * F + F + r) * P;
-  const uint16_t* sg = gu_scales + (static_cast<size_t>(e) * 2 * F + r) * ng;
-  const uint16_t* su = gu_scales + (static_cast<size_t>(e) * 2 * F + F + r) * ng;
-  const int off = offsets[e];
-  for (int i = 0; i < cnt; ++i) {
-    const int a = list[off + i];
-    const float* xa = xt + static_cast<size_t>(a / topk) * H;
-    float ag[1] = {0.f}, au[1] = {0.f};
-    row_dot_accumulate<PACKING, 1>(wg, sg, xa, H, H, G, 1, lane, ag);
-    row_dot_accumulate<PACKING, 1>(wu, su, xa, H, H, G, 1, lane, au);
-    const float g = warp_sum(ag[0]), u = warp_sum(au[0]);
-    if (lane == 0) {
-      const float hv = silu(g) * u;
-      h[static_cast<size_t>(a) * F + r] = hv;
-      if (h_out) h_out[static_cast<size_t>(a) * F + r] = hv;
+  if (e < E && c > 0) {
+    int chunk = s_off[e], slot = 0;
+    int* rec = table + 1 + static_cast<size_t>(chunk) * (2 + CB);
+    for (int a = 0; a < n_assign; ++a) {
+      if (idx[a] != e) continue;
+      rec[2 + slot] = a;
+      if (++slot == CB) {
+        rec[0] = e;
+        rec[1] = CB;
+        ++chunk;
+        slot = 0;
+        rec = table + 1 + static_cast<size_t>(chunk) * (2 + CB);
+      }
     }
-  }
-}
-
-template <int PACKING>
-__global__ void __launch_bounds__(256) down_kernel(const uint32_t* __restrict__ d_codes,
-                                                   const uint16_t* __restrict__ d_scales,
-                                                   const float* __restrict__ ht, const int* __restrict__ counts,
-                                                   const int* __restrict__ offsets, const int* __restrict__ list,
-                                                   int H, int F, int G, float* __restrict__ ypart) {
-  const int e = blockIdx.x;
-  const int cnt = counts[e];
-  if (cnt == 0) return;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = blockIdx.y * 8 + warp;
-  if (r >= H) return;
-  const int P = pitch_words(F, PACKING), ng = groups_of(F, G);
-  const uint32_t* wd = d_codes + (static_cast<size_t>(e) * H + r) * P;
-  const uint16_t* sd = d_scales + (static_cast<size_t>(e) * H + r) * ng;
-  const int off = offsets[e];
-  for (int i = 0; i < cnt; ++i) {
-    const int a = list[off + i];
-    float acc[1] = {0.f};
-    row_dot_accumulate<PACKING, 1>(wd, sd, ht + static_cast<size_t>(a) * F, F, F, G, 1, lane, acc);
-    const float v = warp_sum(acc[0]);
-    if (lane == 0) ypart[static_cast<size_t>(a) * H + r] = v;
+    if (slot > 0) {
+      rec[0] = e;
+      rec[1] = slot;
+      for (int j = slot; j < CB; ++j) rec[2 + j] = rec[2];
+    }
   }
 }
 
@@ -167,31 +123,32 @@ __global__ void combine_kernel(const float* __restrict__ ypart, const float* __r
   y[i] = acc;
 }
 
+// Tokens per chunk: one token never routes twice to an expert; larger batches share an expert's
+// weights among up to 2 or 4 routed tokens per pass.
+int chunk_batch(int T) { return T == 1 ? 1 : (T <= 16 ? 2 : 4); }
+
 struct MoeWs {
-  float* xt;
-  int* counts;
-  int* offsets;
-  int* list;
-  float* h;
-  float* ht;
-  float* ypart;
+  int* table;   // chunk records
+  float* gu;    // gate / up outputs per assignment [T * topk][2F]
+  float* ypart; // down outputs per assignment [T * topk][H]
+  void* prep;   // prep output of the current stage (shared by both stages)
   size_t bytes;
 };
 
-MoeWs moe_ws_layout(void* base, int T, int E, int topk, int H, int F) {
+// Sizes assume groups of 64 (more groups than 128, so enough for both).
+MoeWs moe_ws_layout(void* base, int T, int topk, int H, int F) {
   MoeWs w{};
   char* p = static_cast<char*>(base);
   size_t off = 0;
   auto take = [&](size_t bytes) { char* q = p ? p + off : nullptr; off += align256(bytes); return q; };
-  const size_t A = static_cast<size_t>(T) * topk;
-  w.xt = reinterpret_cast<float*>(take(static_cast<size_t>(T) * H * 4));
-  w.counts = reinterpret_cast<int*>(take(static_cast<size_t>(E) * 4));
-  w.offsets = reinterpret_cast<int*>(take(static_cast<size_t>(E + 1) * 4));
-  w.list = reinterpret_cast<int*>(take(A * 4));
-  w.h = reinterpret_cast<float*>(take(A * F * 4));
-  w.ht = reinterpret_cast<float*>(take(A * F * 4));
-  w.ypart = reinterpret_cast<float*>(take(A * H * 4));
-  w.bytes = off;
+  const int A = T * topk, CB = chunk_batch(T);
+  w.table = reinterpret_cast<int*>(take((1 + static_cast<size_t>(A) * (2 + CB)) * 4));
+  w.gu = reinterpret_cast<float*>(take(static_cast<size_t>(A) * 2 * F * 4));
+  w.ypart = reinterpret_cast<float*>(take(static_cast<size_t>(A) * H * 4));
+  const tq_desc gu{2 * F, H, 64, TQ_PACK_B3, kFwhtBlock, 0}, dn{H, F, 64, TQ_PACK_B3, kFwhtBlock, 0};
+  const size_t prep = std::max(gemv_chunks_workspace_bytes(&gu, CB, A), gemv_chunks_workspace_bytes(&dn, CB, A));
+  w.prep = take(prep);
+  w.bytes = prep == 0 ? 0 : off;
   return w;
 }
 
@@ -218,7 +175,8 @@ extern "C" tq_status tq_moe_route(const float* logits, int T, int E, int topk, i
 
 extern "C" size_t tq_moe_workspace_bytes(int T, int E, int topk, int H, int F) {
   if (T < 1 || E < 1 || E > kMaxExperts || topk < 1 || topk > kMaxTopk || topk > E || H < 1 || F < 1) return 0;
-  return moe_ws_layout(nullptr, T, E, topk, H, F).bytes;
+  if (H % kFwhtBlock != 0 || F % kFwhtBlock != 0) return 0;
+  return moe_ws_layout(nullptr, T, topk, H, F).bytes;
 }
 
 extern "C" tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, int E, int topk,
@@ -245,46 +203,26 @@ extern "C" tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, in
   if (workspace_bytes < tq_moe_workspace_bytes(T, E, topk, H, F)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  MoeWs w = moe_ws_layout(workspace, T, E, topk, H, F);
-  const int G = gate_up->group;
-  const int apply = gate_up->fwht_block != 0;
-  const int n_assign = T * topk;
-  if (launch_route(router_logits, T, E, topk, topk_idx, topk_gate, s) != cudaSuccess) goto fail;
-  lists_kernel<<<1, kMaxExperts, 0, s>>>(topk_idx, n_assign, E, w.counts, w.offsets, w.list);
-  if (cudaPeekAtLastError() != cudaSuccess) goto fail;
-  if (launch_fwht_bf16(x, w.xt, 0, T, H, apply, s) != cudaSuccess) goto fail;
-  {
-    dim3 grid(E, (F + 7) / 8);
-    if (gate_up->packing == TQ_PACK_B3)
-      gate_up_kernel<TQ_PACK_B3><<<grid, 256, 0, s>>>(gu_codes, gu_scales, w.xt, w.counts, w.offsets, w.list, H, F, G,
-                                                      topk, w.h, h_out);
-    else
-      gate_up_kernel<TQ_PACK_2BIT><<<grid, 256, 0, s>>>(gu_codes, gu_scales, w.xt, w.counts, w.offsets, w.list, H, F,
-                                                        G, topk, w.h, h_out);
-    if (cudaPeekAtLastError() != cudaSuccess) goto fail;
-  }
-  if (apply) {
-    if (launch_fwht_f32(w.h, w.ht, n_assign, F, s) != cudaSuccess) goto fail;
-  } else if (cudaMemcpyAsync(w.ht, w.h, static_cast<size_t>(n_assign) * F * 4, cudaMemcpyDeviceToDevice, s) !=
-             cudaSuccess) {
-    goto fail;
-  }
-  {
-    dim3 grid(E, (H + 7) / 8);
-    if (down->packing == TQ_PACK_B3)
-      down_kernel<TQ_PACK_B3><<<grid, 256, 0, s>>>(d_codes, d_scales, w.ht, w.counts, w.offsets, w.list, H, F, G,
-                                                   w.ypart);
-    else
-      down_kernel<TQ_PACK_2BIT><<<grid, 256, 0, s>>>(d_codes, d_scales, w.ht, w.counts, w.offsets, w.list, H, F, G,
-                                                     w.ypart);
-    if (cudaPeekAtLastError() != cudaSuccess) goto fail;
-  }
+  MoeWs w = moe_ws_layout(workspace, T, topk, H, F);
+  const int G = gate_up->group, A = T * topk, CB = chunk_batch(T);
+  cudaError_t e;
+  if ((e = launch_route(router_logits, T, E, topk, topk_idx, topk_gate, s)) != cudaSuccess) return cuda_fail(e);
+  chunks_kernel<<<1, kMaxExperts, 0, s>>>(topk_idx, A, E, CB, w.table);
+  if ((e = cudaPeekAtLastError()) != cudaSuccess) return cuda_fail(e);
+  // gate / up: chunk slot b holds assignment a, fed with x row a / topk; output row a of gu
+  e = launch_gemv_chunks(gate_up, gu_codes, gu_scales, static_cast<size_t>(2 * F) * pitch_words(H, gate_up->packing),
+                         static_cast<size_t>(2 * F) * (H / G), 1, x, nullptr, nullptr, topk, w.table, CB, A, w.gu,
+                         w.prep, s);
+  if (e != cudaSuccess) return cuda_fail(e);
+  // down: fed with FWHT(silu(gate) * up) of assignment a; output row a of ypart
+  e = launch_gemv_chunks(down, d_codes, d_scales, static_cast<size_t>(H) * pitch_words(F, down->packing),
+                         static_cast<size_t>(H) * (F / G), 2, nullptr, w.gu, h_out, topk, w.table, CB, A, w.ypart,
+                         w.prep, s);
+  if (e != cudaSuccess) return cuda_fail(e);
   {
     const size_t n = static_cast<size_t>(T) * H;
     combine_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(w.ypart, topk_gate, T, H, topk, y);
-    if (cudaPeekAtLastError() != cudaSuccess) goto fail;
+    if ((e = cudaPeekAtLastError()) != cudaSuccess) return cuda_fail(e);
   }
   return TQ_OK;
-fail:
-  return cuda_fail(cudaPeekAtLastError());
 }
