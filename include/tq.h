@@ -111,6 +111,18 @@ size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch);
 tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                   int batch, float* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- tq_gemv_noalloc: tq_gemv without a workspace -------------------------------------------------
+ * No counterpart on the pages: a library convenience.  Same computation, arguments, layouts and
+ * errors as tq_gemv, but the scratch lives in a fixed 1 MiB device array inside libtq, for callers
+ * that cannot provide device memory (for example a decode loop that must not call an allocator,
+ * which can synchronise the device, or a C caller without an allocator of its own).  Shapes whose
+ * tq_gemv_workspace_bytes(d, batch) exceeds 1 MiB (at batch 16: K above 31488 for groups of 64, above
+ * 32128 for groups of 128) return TQ_ERR_WORKSPACE before anything is launched.  The first call with a device current looks up that
+ * device's array; make it before any stream capture.  Nothing has to be zeroed first.  All calls on a
+ * device share the array: calls whose kernels overlap in time race on it, so serialise them. */
+tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                          int batch, float* y, void* stream);
+
 /* ---- tq_moe_route: top-k experts per token --------------------------------------------------------
  * logits: float [T][E] (router at full precision, tantan.ink/?p=490 point 1).  idx: int32 [T][topk]
  * in the order (logit descending, expert index ascending); gate: float [T][topk] =

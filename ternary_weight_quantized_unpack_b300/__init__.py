@@ -60,6 +60,7 @@ _SIGS = {
     "tq_fwht": (_I, [_P, _P, _I, _I, _I, _I, _P]),
     "tq_gemv_workspace_bytes": (_SZ, [_D, _I]),
     "tq_gemv": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+    "tq_gemv_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P]),
     "tq_moe_route": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "tq_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "tq_moe_gemv": (_I, [_D, _D, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -179,6 +180,16 @@ def tq_gemv(d: tq_desc, codes, scales, x, y=None, workspace=None, stream=None) -
         workspace = _ws(nbytes, x.device)
     _check(lib().tq_gemv(ctypes.byref(d), _ptr(codes), _ptr(scales), _ptr(x), batch, _ptr(y), _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream)), "tq_gemv")
+    return y
+
+
+def tq_gemv_noalloc(d: tq_desc, codes, scales, x, y=None, stream=None) -> torch.Tensor:
+    """tq_gemv with the scratch in the library's fixed device array (no workspace argument)."""
+    batch = x.shape[0]
+    if y is None:
+        y = torch.empty((batch, d.N), dtype=torch.float32, device=x.device)
+    _check(lib().tq_gemv_noalloc(ctypes.byref(d), _ptr(codes), _ptr(scales), _ptr(x), batch, _ptr(y),
+                                 _stream(stream)), "tq_gemv_noalloc")
     return y
 
 
