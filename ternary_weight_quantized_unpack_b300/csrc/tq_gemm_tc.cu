@@ -8,15 +8,20 @@
 // its issue rate.  The one-off decode streams the packed weights from HBM (0.25 B per weight, 2-bit)
 // and writes 2 B per weight; its cost is amortised over all M tokens.
 //
-// GEMM kernel (one 128-token x 256-weight-row output tile per CTA, K in steps of 64):
-//   warp 0     TMA producer: 128B-swizzled tiles of x~ (128 x 64) and W (256 x 64) into a 4-stage ring
-//   warp 1     MMA issuer (one thread): 4 x tcgen05.mma M128 N256 K16 per stage, commit frees the stage
-//   warps 2-5  epilogue: tcgen05.ld of the 128 x 256 fp32 accumulator, bf16 conversion, stores
+// GEMM kernel: persistent, one CTA per SM, 128-token x 256-weight-row output tiles, K in steps of 64:
+//   warp 0     TMA producer: 128B-swizzled tiles of x~ (128 x 64) and W (256 x 64) into a 4-stage
+//              ring, running ahead across tiles
+//   warp 1     MMA issuer (one thread): 4 x tcgen05.mma M128 N256 K16 per stage into one of two
+//              TMEM accumulators (2 x 256 columns); a commit frees the stage, another marks the
+//              accumulator full
+//   warps 2-5  epilogue: tcgen05.ld of a full accumulator, bf16 conversion, stores; then the
+//              accumulator is released, so one tile's epilogue overlaps the next tile's MMAs
 // Every mbarrier wait is bounded; a wait that runs out records TQ_ERR_TIMEOUT and the warp stops.
 // Activations are the block Walsh-Hadamard transform of x in FP16 (cosmocat.dev "27B 大模型塞进
 // 5.9GB", section 二 ①); group scales per 64 or 128 weights (same page, section 二 ②).
 #include <cuda_bf16.h>
 
+#include <algorithm>
 #include <map>
 #include <mutex>
 
@@ -37,14 +42,15 @@ constexpr int STAGES = 4;
 constexpr uint32_t kABytes = BM * BK * 2;
 constexpr uint32_t kBBytes = BN * BK * 2;
 constexpr int kThreads = 192;
-constexpr uint32_t kTmemCols = 256;
+constexpr uint32_t kTmemCols = 512;  // two 128 x 256 fp32 accumulators
 
 struct Smem {
   uint8_t a[STAGES][kABytes];  // each 1024-byte aligned (sizes are multiples of 1024)
   uint8_t b[STAGES][kBBytes];
   uint64_t full[STAGES];
   uint64_t empty[STAGES];
-  uint64_t done;
+  uint64_t acc_full[2];   // MMA issuer -> epilogue
+  uint64_t acc_empty[2];  // epilogue (one arrival per warp) -> MMA issuer
   uint32_t tmem;
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment of the base to 1024
@@ -55,15 +61,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int m0 = blockIdx.x * BM, n0 = blockIdx.y * BN;
   const int nk = K / BK;
+  const int n_mt = (M + BM - 1) / BM, n_tiles = n_mt * ((N + BN - 1) / BN);
+  // tile t: token tile t % n_mt, weight tile t / n_mt (the CTAs running together share few weight tiles)
   if (threadIdx.x == 0) {
 #pragma unroll
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&sm.full[s], 1);
       mbar_init(&sm.empty[s], 1);
     }
-    mbar_init(&sm.done, 1);
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&sm.acc_full[b], 1);
+      mbar_init(&sm.acc_empty[b], 4);
+    }
     fence_mbar_init();
   }
   if (warp == 1) {
@@ -76,68 +86,98 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = sm.tmem;
 
   if (warp == 0 && lane == 0) {
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (kb >= STAGES && !mbar_wait(&sm.empty[s], ((kb / STAGES) & 1) ^ 1)) {
-        record_error(status, TQ_ERR_TIMEOUT);
-        break;
+    int g = 0;  // K steps issued so far, over all tiles
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
+      const int m0 = (t % n_mt) * BM, n0 = (t / n_mt) * BN;
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int s = g % STAGES;
+        if (g >= STAGES && !mbar_wait(&sm.empty[s], ((g / STAGES) & 1) ^ 1)) {
+          record_error(status, TQ_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
+        tma_load_2d(sm.a[s], &tm_x, kb * BK, m0, &sm.full[s]);
+        tma_load_2d(sm.b[s], &tm_w, kb * BK, n0, &sm.full[s]);
       }
-      mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
-      tma_load_2d(sm.a[s], &tm_x, kb * BK, m0, &sm.full[s]);
-      tma_load_2d(sm.b[s], &tm_w, kb * BK, n0, &sm.full[s]);
     }
   } else if (warp == 1 && lane == 0) {
     constexpr uint32_t idesc = idesc_f16_f32(BM, BN);
-    for (int kb = 0; kb < nk; ++kb) {
-      const int s = kb % STAGES;
-      if (!mbar_wait(&sm.full[s], (kb / STAGES) & 1)) {
+    int g = 0, it = 0;
+    bool ok = true;
+    for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      if (it >= 2 && !mbar_wait(&sm.acc_empty[b], ((it >> 1) - 1) & 1)) {  // epilogue of tile it - 2 done
         record_error(status, TQ_ERR_TIMEOUT);
         break;
       }
       tc_fence_after();
-      const uint32_t a0 = smem_addr(sm.a[s]), b0 = smem_addr(sm.b[s]);
+      const uint32_t d = tmem + static_cast<uint32_t>(b * BN);
+      for (int kb = 0; kb < nk; ++kb, ++g) {
+        const int s = g % STAGES;
+        if (!mbar_wait(&sm.full[s], (g / STAGES) & 1)) {
+          record_error(status, TQ_ERR_TIMEOUT);
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t a0 = smem_addr(sm.a[s]), b0 = smem_addr(sm.b[s]);
 #pragma unroll
-      for (int k = 0; k < BK / 16; ++k)
-        mma_f16_ss(tmem, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc, (kb | k) != 0);
-      mma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
+        for (int k = 0; k < BK / 16; ++k)
+          mma_f16_ss(d, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc, (kb | k) != 0);
+        mma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
+      }
+      mma_commit(&sm.acc_full[b]);
     }
-    mma_commit(&sm.done);
   } else if (warp >= 2) {
-    if (!mbar_wait(&sm.done, 0) && lane == 0) record_error(status, TQ_ERR_TIMEOUT);
-    tc_fence_after();
     const int q = warp & 3;  // a warp reads TMEM lanes 32 (warp % 4) .. + 31
-    const int m = m0 + 32 * q + lane;
     const bool vec = (N & 7) == 0;
+    int it = 0;
+    for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
+      const int b = it & 1;
+      const int m0 = (t % n_mt) * BM, n0 = (t / n_mt) * BN;
+      if (!mbar_wait(&sm.acc_full[b], (it >> 1) & 1)) {
+        if (lane == 0) record_error(status, TQ_ERR_TIMEOUT);
+        break;
+      }
+      tc_fence_after();
+      const int m = m0 + 32 * q + lane;
 #pragma unroll 1
-    for (int c = 0; c < BN; c += 32) {
-      uint32_t v[32];
-      tmem_ld<32>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(c), v);
-      tmem_wait_ld();
-      const int n = n0 + c;
-      if (m < M && n < N) {
-        uint16_t* dst = y + static_cast<size_t>(m) * N + n;
-        if (vec && n + 32 <= N) {
+      for (int c = 0; c < BN; c += 32) {
+        uint32_t v[32];
+        tmem_ld<32>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN + c), v);
+        tmem_wait_ld();
+        const int n = n0 + c;
+        if (m < M && n < N) {
+          uint16_t* dst = y + static_cast<size_t>(m) * N + n;
+          if (vec && n + 32 <= N) {
 #pragma unroll
-          for (int j = 0; j < 32; j += 8) {
-            uint4 o;
-            uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
+            for (int j = 0; j < 32; j += 8) {
+              uint4 o;
+              uint32_t* ow = reinterpret_cast<uint32_t*>(&o);
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const __nv_bfloat162 h = __floats2bfloat162_rn(__uint_as_float(v[j + 2 * i]), __uint_as_float(v[j + 2 * i + 1]));
-              ow[i] = *reinterpret_cast<const uint32_t*>(&h);
+              for (int i = 0; i < 4; ++i) {
+                const __nv_bfloat162 h =
+                    __floats2bfloat162_rn(__uint_as_float(v[j + 2 * i]), __uint_as_float(v[j + 2 * i + 1]));
+                ow[i] = *reinterpret_cast<const uint32_t*>(&h);
+              }
+              *reinterpret_cast<uint4*>(dst + j) = o;
             }
-            *reinterpret_cast<uint4*>(dst + j) = o;
-          }
-        } else {
+          } else {
 #pragma unroll
-          for (int j = 0; j < 32; ++j) {
-            if (n + j < N) {
-              const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
-              dst[j] = *reinterpret_cast<const uint16_t*>(&h);
+            for (int j = 0; j < 32; ++j) {
+              if (n + j < N) {
+                const __nv_bfloat16 h = __float2bfloat16_rn(__uint_as_float(v[j]));
+                dst[j] = *reinterpret_cast<const uint16_t*>(&h);
+              }
             }
           }
         }
       }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&sm.acc_empty[b]);  // this warp is done with the accumulator
     }
   }
   tc_fence_before();
@@ -248,8 +288,12 @@ cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t*
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   if ((e = ensure_attr()) != cudaSuccess) return e;
-  // token tiles vary fastest, so the CTAs running at one time share a few weight tiles (L2 reuse)
-  const dim3 grid((M + BM - 1) / BM, (N + BN - 1) / BN);
+  // persistent: one CTA per SM, each walking the tiles with a stride of the grid
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
+  const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, sms));
   gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status_ptr());
   return cudaPeekAtLastError();
 }
