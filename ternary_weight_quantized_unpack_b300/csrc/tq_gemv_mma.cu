@@ -129,58 +129,47 @@ struct PrepParams {
 
 __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
-template <int PACK, int G>
-__global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ PrepParams p) {
-  pdl_launch_dependents();
-  pdl_wait();  // x may be the output of the preceding kernel; the previous call may still read xh
-  const int lane = threadIdx.x & 31;
-  const int blk = blockIdx.x * 4 + (threadIdx.x >> 5);
-  if (blk * kFwhtBlock >= p.K) return;
-  const int B = p.B, R = vp_row(B);
-  const int kb = blk * kFwhtBlock + 4 * lane;
-  int count = B;
-  const int* rows = nullptr;
-  uint16_t* xh = p.xh;
-  float* vpo = p.vp;
-  if (p.mode != 0) {
-    const int z = static_cast<int>(blockIdx.z);
-    if (z >= p.chunks[0]) return;
-    const int* rec = p.chunks + 1 + static_cast<size_t>(z) * (2 + B);
-    count = rec[1];
-    rows = rec + 2;
-    xh += static_cast<size_t>(z) * p.xh_cstride;
-    vpo += static_cast<size_t>(z) * p.vp_cstride;
-  }
-  float v[kMaxBatch][4];
+// x^ and VP of one 128-block (absolute index blk) for batch slots 0..B-1 (slots past count are zero).
+// xh / vpo point at the slice that starts at block blk0 (offsets are taken relative to it; blk0 is a
+// multiple of 5, so word boundaries stay at the same offsets).  One warp; MAXB >= B.
+template <int PACK, int G, int MAXB>
+__device__ __forceinline__ void prep_block(const uint16_t* __restrict__ x, const float* __restrict__ gu, float* h_out,
+                                           int* status, int K, int B, int apply, int mode, int topk, int blk,
+                                           int blk0, int count, const int* rows, uint16_t* xh, float* vpo,
+                                           int lane) {
+  const int R = vp_row(B);
+  const int kb = blk * kFwhtBlock + 4 * lane;   // absolute trit index of this lane's 4 values
+  const int kr = kb - blk0 * kFwhtBlock;        // ... relative to the slice
+  float v[MAXB][4];
   float mx = 0.f;
 #pragma unroll
-  for (int b = 0; b < kMaxBatch; ++b) {
+  for (int b = 0; b < MAXB; ++b) {
     if (b < B) {
       if (b >= count) {
         v[b][0] = v[b][1] = v[b][2] = v[b][3] = 0.f;
-      } else if (p.mode == 2) {  // h = silu(gate) * up of the assignment's gate / up row
+      } else if (mode == 2) {  // h = silu(gate) * up of the assignment's gate / up row
         const size_t a = static_cast<size_t>(rows[b]);
-        const float4 gg = *reinterpret_cast<const float4*>(p.gu + a * 2 * p.K + kb);
-        const float4 uu = *reinterpret_cast<const float4*>(p.gu + a * 2 * p.K + p.K + kb);
+        const float4 gg = *reinterpret_cast<const float4*>(gu + a * 2 * K + kb);
+        const float4 uu = *reinterpret_cast<const float4*>(gu + a * 2 * K + K + kb);
         v[b][0] = silu(gg.x) * uu.x;
         v[b][1] = silu(gg.y) * uu.y;
         v[b][2] = silu(gg.z) * uu.z;
         v[b][3] = silu(gg.w) * uu.w;
-        if (p.h_out) *reinterpret_cast<float4*>(p.h_out + a * p.K + kb) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
+        if (h_out) *reinterpret_cast<float4*>(h_out + a * K + kb) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
       } else {
-        const size_t r = p.mode == 1 ? static_cast<size_t>(rows[b] / p.topk) : static_cast<size_t>(b);
-        const uint2 raw = *reinterpret_cast<const uint2*>(p.x + r * p.K + kb);
+        const size_t r = mode == 1 ? static_cast<size_t>(rows[b] / topk) : static_cast<size_t>(b);
+        const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(x + r * K + kb));
         v[b][0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
         v[b][1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
         v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
         v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
       }
-      if (p.apply) fwht128_warp(v[b]);
+      if (apply) fwht128_warp(v[b]);
 #pragma unroll
       for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[b][j]));
     }
   }
-  if (p.apply) mx *= 0.08838834764831845f;
+  if (apply) mx *= 0.08838834764831845f;
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
   int e = 0;
@@ -189,18 +178,18 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
     e = (ex == 0 ? -126 : ex - 127) - 6;  // max |x~| * 2^-e in [64, 128)
     if (e > 100) {
       e = 100;
-      if (lane == 0) record_error(p.status, TQ_ERR_RANGE);
+      if (lane == 0) record_error(status, TQ_ERR_RANGE);
     }
     e = max(e, -100);
   }
-  const float down = __int_as_float((127 - e) << 23) * (p.apply ? 0.08838834764831845f : 1.f);
+  const float down = __int_as_float((127 - e) << 23) * (apply ? 0.08838834764831845f : 1.f);
 #pragma unroll
-  for (int b = 0; b < kMaxBatch; ++b) {
+  for (int b = 0; b < MAXB; ++b) {
     if (b >= B) break;
     float vs = 0.f;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      const int k = kb + j;
+      const int k = kr + j;
       int pos, off;
       if (PACK == TQ_PACK_B3) {
         pos = ((k % 20) % 10) >> 1;
@@ -225,13 +214,37 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
     }
-    if ((lane & (G == 128 ? 31 : 15)) == 0) vpo[(kb / G) * R + b] = -1.52587890625e-05f * vs;
+    if ((lane & (G == 128 ? 31 : 15)) == 0) vpo[(kr / G) * R + b] = -1.52587890625e-05f * vs;
   }
   if (lane < kFwhtBlock / G) {  // per group of the block: padding zeros and the block factor
-    const int gi = blk * (kFwhtBlock / G) + lane;
+    const int gi = (blk - blk0) * (kFwhtBlock / G) + lane;
     for (int b = B; b < R - 1; ++b) vpo[gi * R + b] = 0.f;
     vpo[gi * R + R - 1] = __int_as_float((127 + 16 + e) << 23);  // 2^(16 + e)
   }
+}
+
+template <int PACK, int G>
+__global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ PrepParams p) {
+  pdl_launch_dependents();
+  pdl_wait();  // x may be the output of the preceding kernel; the previous call may still read xh
+  const int lane = threadIdx.x & 31;
+  const int blk = blockIdx.x * 4 + (threadIdx.x >> 5);
+  if (blk * kFwhtBlock >= p.K) return;
+  int count = p.B;
+  const int* rows = nullptr;
+  uint16_t* xh = p.xh;
+  float* vpo = p.vp;
+  if (p.mode != 0) {
+    const int z = static_cast<int>(blockIdx.z);
+    if (z >= p.chunks[0]) return;
+    const int* rec = p.chunks + 1 + static_cast<size_t>(z) * (2 + p.B);
+    count = rec[1];
+    rows = rec + 2;
+    xh += static_cast<size_t>(z) * p.xh_cstride;
+    vpo += static_cast<size_t>(z) * p.vp_cstride;
+  }
+  prep_block<PACK, G, kMaxBatch>(p.x, p.gu, p.h_out, p.status, p.K, p.B, p.apply, p.mode, p.topk, blk, 0, count, rows,
+                                 xh, vpo, lane);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -257,6 +270,12 @@ struct Params {
   // slot b (< count) is stored to output row rows[b].
   const int* chunks;
   size_t codes_estride, scales_estride, xh_cstride, vp_cstride;
+  // fused = 1: no prep kernel; each CTA forms x^ / VP of its own K-range in shared memory from these
+  // inputs (the prep kernel's modes, see PrepParams).
+  int fused, mode, topk, apply;
+  const uint16_t* x;
+  const float* gu;
+  float* h_out;
 };
 
 // Operands of this CTA: the whole call, or one chunk of routed tokens.
@@ -406,6 +425,19 @@ __device__ __forceinline__ void wait_bar(const Params& p, uint64_t* bar) {
   if (!mbar_wait(bar, 0) && (threadIdx.x & 31) == 0) record_error(p.status, TQ_ERR_TIMEOUT);
 }
 
+// Fused alternative to the prep kernel: the CTA's warps form x^ and VP of its K-range, one 128-block
+// per warp at a time, straight into shared memory.
+template <int PACK, int G>
+__device__ __forceinline__ void fused_prologue(const Params& p, const Cta& c, const Sel& sel, uint8_t* smem) {
+  const int blk0 = c.k_start / kFwhtBlock, nblk = c.kr / kFwhtBlock;
+  const int nw = static_cast<int>(blockDim.x >> 5);
+  for (int i = c.warp; i < nblk; i += nw)
+    prep_block<PACK, G, 2>(p.x, p.gu, p.h_out, p.status, p.K, p.B, p.apply, p.mode, p.topk, blk0 + i, blk0, sel.count,
+                           sel.rows, reinterpret_cast<uint16_t*>(smem + p.xh_off),
+                           reinterpret_cast<float*>(smem + p.vp_off), c.lane);
+  __syncthreads();
+}
+
 // ---------------------------------------------------------------------------------------------
 // Partial sums red[kl][RT][B] (in shared memory) -> y.  K-lanes are added in lane order, then the
 // cluster's CTAs in rank order through distributed shared memory.  Every thread calls this.
@@ -493,9 +525,13 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
   };
   if (p.early) prime();
   pdl_wait();
-  copy_prep_slice(p, c, sel, smem, bars);
+  if (!p.fused) copy_prep_slice(p, c, sel, smem, bars);
   if (!p.early) prime();
-  wait_bar(p, &bars->x);
+  if (p.fused) {
+    fused_prologue<TQ_PACK_2BIT, G>(p, c, sel, smem);
+  } else {
+    wait_bar(p, &bars->x);
+  }
 
   const uint32_t* xh = reinterpret_cast<const uint32_t*>(smem + p.xh_off);
   const float* V = reinterpret_cast<const float*>(smem + p.vp_off);
@@ -735,9 +771,13 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
   };
   if (p.early) prime();
   pdl_wait();
-  copy_prep_slice(p, c, sel, smem, bars);
+  if (!p.fused) copy_prep_slice(p, c, sel, smem, bars);
   if (!p.early) prime();
-  wait_bar(p, &bars->x);
+  if (p.fused) {
+    fused_prologue<TQ_PACK_B3, G>(p, c, sel, smem);
+  } else {
+    wait_bar(p, &bars->x);
+  }
   wait_bar(p, &bars->lut);
 
   const uint32_t* lutA = reinterpret_cast<const uint32_t*>(smem) + c.lane;
@@ -964,25 +1004,6 @@ cudaError_t choose_plan(const void* kern, const tq_desc* d, int B, Plan* out) {
   return cudaSuccess;
 }
 
-template <typename Kern>
-cudaError_t launch_main(Kern kern, Params prm, const tq_desc* d, cudaStream_t s, int zdim) {
-  Plan pl{};
-  cudaError_t e = choose_plan(reinterpret_cast<const void*>(kern), d, prm.B, &pl);
-  if (e != cudaSuccess) return e;
-  if ((e = ensure_smem_attr(reinterpret_cast<const void*>(kern), pl.smem)) != cudaSuccess) return e;
-  prm.rs = pl.rs;
-  prm.kl = pl.kl;
-  prm.ppl = pl.ppl;
-  prm.upr = pl.upr;
-  prm.xh_off = static_cast<uint32_t>(pl.xh_off);
-  prm.vp_off = static_cast<uint32_t>(pl.vp_off);
-  prm.sw_off = static_cast<uint32_t>(pl.sw_off);
-  prm.bar_off = static_cast<uint32_t>(pl.bar_off);
-  cudaLaunchAttribute attr[2];
-  cudaLaunchConfig_t cfg = launch_config(pl, s, attr, zdim);
-  return cudaLaunchKernelEx(&cfg, kern, prm);
-}
-
 template <int PACK, int G>
 cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s, int zdim) {
   cudaLaunchConfig_t cfg = {};
@@ -998,21 +1019,24 @@ cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s, int zdim) {
   return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G>, pp);
 }
 
+// The decode kernel for a shape: packing, group and batch tiles.
 template <int G>
-cudaError_t launch_b3(const Params& prm, const tq_desc* d, cudaStream_t s, int zdim) {
-  switch ((prm.B + 1) / 2) {
-    case 1: return launch_main(gemv_b3_kernel<G, 1>, prm, d, s, zdim);
-    case 2: return launch_main(gemv_b3_kernel<G, 2>, prm, d, s, zdim);
+const void* kernel_b3(int B) {
+  switch ((B + 1) / 2) {
+    case 1: return reinterpret_cast<const void*>(gemv_b3_kernel<G, 1>);
+    case 2: return reinterpret_cast<const void*>(gemv_b3_kernel<G, 2>);
     case 3:
-    case 4: return launch_main(gemv_b3_kernel<G, 4>, prm, d, s, zdim);
-    default: return launch_main(gemv_b3_kernel<G, 8>, prm, d, s, zdim);
+    case 4: return reinterpret_cast<const void*>(gemv_b3_kernel<G, 4>);
+    default: return reinterpret_cast<const void*>(gemv_b3_kernel<G, 8>);
   }
 }
-
 template <int G>
-cudaError_t launch_2b(const Params& prm, const tq_desc* d, cudaStream_t s, int zdim) {
-  if (prm.B <= 8) return launch_main(gemv_2b_kernel<G, 1>, prm, d, s, zdim);
-  return launch_main(gemv_2b_kernel<G, 2>, prm, d, s, zdim);
+const void* kernel_2b(int B) {
+  return B <= 8 ? reinterpret_cast<const void*>(gemv_2b_kernel<G, 1>) : reinterpret_cast<const void*>(gemv_2b_kernel<G, 2>);
+}
+const void* gemv_kernel(const tq_desc* d, int B) {
+  if (d->packing == TQ_PACK_B3) return d->group == 128 ? kernel_b3<128>(B) : kernel_b3<64>(B);
+  return d->group == 128 ? kernel_2b<128>(B) : kernel_2b<64>(B);
 }
 
 // Prep output of one matrix (or one chunk): x^ (K x batch halves) then VP (groups x vp_row(batch)
@@ -1020,18 +1044,36 @@ cudaError_t launch_2b(const Params& prm, const tq_desc* d, cudaStream_t s, int z
 size_t xh_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d->K) * B * 2); }
 size_t vp_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d->K / d->group) * vp_row(B) * 4); }
 
-// Prep kernel then decode kernel; pp and prm carry everything but the shape-derived fields.
+// Prep kernel (or the fused prologue) then decode kernel; pp and prm carry everything but the
+// shape-derived fields.  For the expert layer's chunks of at most 2 tokens the prologue is fused into
+// the decode kernel (one kernel boundary less in a chain of several launches; measured faster at
+// 1 and 8 tokens); dense calls use one prep kernel that transforms the activations once for all
+// CTAs (measured faster on the decode stream).
 cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int zdim, cudaStream_t s) {
   pp.status = status_ptr();
   pp.K = d->K;
   pp.B = B;
   pp.apply = d->fwht_block != 0;
   const bool b3 = d->packing == TQ_PACK_B3;
-  cudaError_t e = b3 ? (d->group == 128 ? launch_prep<TQ_PACK_B3, 128>(pp, s, zdim)
-                                        : launch_prep<TQ_PACK_B3, 64>(pp, s, zdim))
-                     : (d->group == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s, zdim)
-                                        : launch_prep<TQ_PACK_2BIT, 64>(pp, s, zdim));
+  const void* kern = gemv_kernel(d, B);
+  Plan pl{};
+  cudaError_t e = choose_plan(kern, d, B, &pl);
   if (e != cudaSuccess) return e;
+  if ((e = ensure_smem_attr(kern, pl.smem)) != cudaSuccess) return e;
+  prm.fused = B <= 2 && prm.chunks != nullptr;
+  if (prm.fused) {
+    prm.mode = pp.mode;
+    prm.topk = pp.topk;
+    prm.apply = pp.apply;
+    prm.x = pp.x;
+    prm.gu = pp.gu;
+    prm.h_out = pp.h_out;
+  } else {
+    e = b3 ? (d->group == 128 ? launch_prep<TQ_PACK_B3, 128>(pp, s, zdim) : launch_prep<TQ_PACK_B3, 64>(pp, s, zdim))
+           : (d->group == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s, zdim)
+                              : launch_prep<TQ_PACK_2BIT, 64>(pp, s, zdim));
+    if (e != cudaSuccess) return e;
+  }
   prm.xh_g = pp.xh;
   prm.vp_g = pp.vp;
   prm.status = pp.status;
@@ -1042,8 +1084,18 @@ cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int 
   prm.B = B;
   prm.R = vp_row(B);
   prm.G = d->group;
-  if (b3) return d->group == 128 ? launch_b3<128>(prm, d, s, zdim) : launch_b3<64>(prm, d, s, zdim);
-  return d->group == 128 ? launch_2b<128>(prm, d, s, zdim) : launch_2b<64>(prm, d, s, zdim);
+  prm.rs = pl.rs;
+  prm.kl = pl.kl;
+  prm.ppl = pl.ppl;
+  prm.upr = pl.upr;
+  prm.xh_off = static_cast<uint32_t>(pl.xh_off);
+  prm.vp_off = static_cast<uint32_t>(pl.vp_off);
+  prm.sw_off = static_cast<uint32_t>(pl.sw_off);
+  prm.bar_off = static_cast<uint32_t>(pl.bar_off);
+  cudaLaunchAttribute attr[2];
+  cudaLaunchConfig_t cfg = launch_config(pl, s, attr, zdim);
+  void* args[] = {&prm};
+  return cudaLaunchKernelExC(&cfg, kern, args);
 }
 
 }  // namespace gemv
