@@ -263,6 +263,7 @@ struct Params {
   int ppl;    // units per K-lane
   int upr;    // units per row
   int early;  // 1: codes and scales may be read before the preceding kernel has completed
+  int v8;     // base-3: rows and code base are 32-byte aligned, codes are read 32 bytes at a time
   uint32_t xh_off, vp_off, sw_off, bar_off;  // shared-memory offsets: x^, VP, per-warp scales, barriers
   // Routed-token chunks (nullptr: one dense matrix).  blockIdx.z selects record {expert, count,
   // rows[B]} of chunks[1 + z * (2 + B)] (chunks[0] = number of records); the expert's codes and
@@ -668,7 +669,13 @@ __device__ __forceinline__ void b3_unit(const Params& p, const Cta& c, int u, in
 #pragma unroll
   for (int st = 0; st < 8; ++st) {
     if (!FULL && (st * 80) / G >= ngp) break;
-    {  // keep the ring three steps ahead (past this warp's range: re-read its last step)
+    if (p.v8) {  // 32-byte loads of two steps, two steps ahead (past this warp's range: its last two)
+      if ((st & 1) == 0) {
+        const int s = min(u * 8 + st + 2, s_last - 1);
+        ldg_v8(cR + s, ra[(st + 2) & 3], ra[(st + 3) & 3]);
+        ldg_v8(cR2 + s, rb[(st + 2) & 3], rb[(st + 3) & 3]);
+      }
+    } else {  // keep the ring three steps ahead (past this warp's range: re-read its last step)
       const int s = min(u * 8 + st + 3, s_last);
       ra[(st + 3) & 3] = __ldg(cR + s);
       rb[(st + 3) & 3] = __ldg(cR2 + s);
@@ -761,10 +768,18 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
   }
   auto prime = [&]() {
     if (c.ua < c.ub) {
+      if (p.v8) {
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        ra[i] = __ldg(cR + min(s_begin + i, s_last));
-        rb[i] = __ldg(cR2 + min(s_begin + i, s_last));
+        for (int i = 0; i < 4; i += 2) {
+          ldg_v8(cR + min(s_begin + i, s_last - 1), ra[i], ra[i + 1]);
+          ldg_v8(cR2 + min(s_begin + i, s_last - 1), rb[i], rb[i + 1]);
+        }
+      } else {
+#pragma unroll
+        for (int i = 0; i < 3; ++i) {
+          ra[i] = __ldg(cR + min(s_begin + i, s_last));
+          rb[i] = __ldg(cR2 + min(s_begin + i, s_last));
+        }
       }
       us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
@@ -1092,6 +1107,8 @@ cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int 
   prm.vp_off = static_cast<uint32_t>(pl.vp_off);
   prm.sw_off = static_cast<uint32_t>(pl.sw_off);
   prm.bar_off = static_cast<uint32_t>(pl.bar_off);
+  prm.v8 = b3 && prm.P % 8 == 0 && reinterpret_cast<uintptr_t>(prm.codes) % 32 == 0 &&
+           (!prm.chunks || prm.codes_estride % 8 == 0);
   cudaLaunchAttribute attr[2];
   cudaLaunchConfig_t cfg = launch_config(pl, s, attr, zdim);
   void* args[] = {&prm};
