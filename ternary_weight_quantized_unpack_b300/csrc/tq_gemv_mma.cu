@@ -511,10 +511,19 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
   // rows past N read row 0 (their outputs are not stored); groups past the range re-read the last
   auto fetch = [&](int gl, int slot) {
     const int gc = min(gl, gl_b - 1);
+    if (WPT == 2) {  // words 2q, 2q + 1 of the group: one 8-byte load per row (rows and offsets are even)
+      const uint2 a = __ldg(reinterpret_cast<const uint2*>(cg + gc * (G / 16)));
+      const uint2 b = __ldg(reinterpret_cast<const uint2*>(cg8 + gc * (G / 16)));
+      buf[slot][0] = a.x;
+      buf[slot][1] = a.y;
+      buf[slot][WPT] = b.x;
+      buf[slot][WPT + 1] = b.y;
+    } else {
 #pragma unroll
-    for (int u = 0; u < WPT; ++u) {
-      buf[slot][u] = __ldg(cg + gc * (G / 16) + u);
-      buf[slot][WPT + u] = __ldg(cg8 + gc * (G / 16) + u);
+      for (int u = 0; u < WPT; ++u) {
+        buf[slot][u] = __ldg(cg + gc * (G / 16) + u);
+        buf[slot][WPT + u] = __ldg(cg8 + gc * (G / 16) + u);
+      }
     }
   };
   auto prime = [&]() {
