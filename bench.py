@@ -3,16 +3,17 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference] [--no-extras]
 
 Default workload: decode of the 27B-class dense model's linears - the seven ternary linears of one
-decoder layer (q/k/v/o 5120x5120 / 1024x5120, gate/up 17408x5120, down 5120x17408), base-3
-packing (20 trits per uint32), group-128 FP16 scales, fused block-128 FWHT, batch 1 - run over 64
-layers with distinct weights.  A step is one decode token through all 64 x 7 linears (448 GEMV
-calls, replayed from a CUDA graph); weights (4.56 GB) are far larger than L2, so every step streams
-them from HBM.  The metric is packed-weight HBM GB/s (codes + FP16 scales, pitch included) with
-model-equivalent decode tok/s beside it.
+decoder layer (q/k/v/o 5120x5120 / 1024x5120, gate/up 17408x5120, down 5120x17408), 2-bit packing
+(--packing base3: 20 trits per uint32), group-128 FP16 scales, fused block-128 FWHT, batch 1 - run
+over 64 layers with distinct weights.  q/k/v and gate/up are stacked as an inference engine calls
+them (4 GEMV calls per layer, 256 per step, replayed from a CUDA graph); the weights (5.62 GB 2-bit,
+4.56 GB base-3, codes + FP16 scales) are far larger than L2, so every step streams them from HBM.
+The metric is packed-weight HBM GB/s (codes + FP16 scales, pitch included) with model-equivalent
+decode tok/s beside it.
 
-Other rows of the hot path are measured in the same run under "extras": 2-bit packing and batch 8 of
-the same stream, the 256-expert top-8 MoE expert layer (1 / 8 / 64 tokens), and the two prefill GEMM
-shapes.  ``--impl reference`` times the CPU oracle (fp64 numpy) on a bounded sample of the same
+Other rows of the hot path are measured in the same run under "extras": the other packing, batch 8
+and one call per linear of the same stream, the 256-expert top-8 MoE expert layer (1 / 8 / 64
+tokens), and the two prefill GEMM shapes.  ``--impl reference`` times the CPU oracle (fp64 numpy) on a bounded sample of the same
 workload, on the host cores.
 
 Multi-GPU: independent replicas, one process per GPU (torchrun); each rank streams its own copy
@@ -41,6 +42,7 @@ from ternary_weight_quantized_unpack_b300 import inputs  # noqa: E402
 
 GB = 1e9
 LAYERS = 64
+PACKINGS = {"2bit": tq.TQ_PACK_2BIT, "base3": tq.TQ_PACK_B3}
 METRIC = "packed-weight HBM GB/s (% of B300 peak) and model-equivalent decode tok/s"
 
 
@@ -452,7 +454,7 @@ def config_of(packing, batch, layers=None, stacked=True):
 def run_reference(args, rank, world):
     if rank != 0:
         return
-    packing, batch = tq.TQ_PACK_B3, 1
+    packing, batch = PACKINGS[args.packing], 1
     per_step = []
     for _ in range(args.warmup):
         oracle_sample_seconds(packing, batch, 16)
@@ -477,7 +479,7 @@ def run_tq(args, rank, world, local):
     if not torch.cuda.is_available():
         raise SystemExit("bench.py needs a CUDA device (libtq has no CPU path)")
     peaks = measured_peaks()
-    packing, batch = tq.TQ_PACK_B3, args.batch
+    packing, batch = PACKINGS[args.packing], args.batch
     st = Stream(packing, batch, layers=args.layers)
     # warm-up: W eager steps, then capture one step into a graph
     for _ in range(args.warmup):
@@ -514,7 +516,8 @@ def run_tq(args, rank, world, local):
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic_from_profiles(f"dense_decode_b3_b{batch}_stacked_per_layer"),
+                     "traffic": traffic_from_profiles(
+                         f"dense_decode_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_stacked_per_layer"),
                      "traffic_unit": "DRAM bytes per layer (4 calls: prep + decode kernels), ncu",
                      "kernel": "tq_gemv calls (activation prep kernel + decode GEMV kernel), per-call CUDA events",
                      "algorithmic_bytes_per_step": st.bytes_per_step, "calls_per_step": len(st.calls),
@@ -532,8 +535,9 @@ def run_tq(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(packing, batch)
     if args.extras and world == 1:
         ex = {"stream": [], "moe": [], "prefill": []}
-        for pk, b, stk in ((tq.TQ_PACK_B3, 8, True), (tq.TQ_PACK_2BIT, 1, True), (tq.TQ_PACK_2BIT, 8, True),
-                           (tq.TQ_PACK_B3, 1, False), (tq.TQ_PACK_2BIT, 1, False)):
+        other = tq.TQ_PACK_B3 if packing == tq.TQ_PACK_2BIT else tq.TQ_PACK_2BIT
+        for pk, b, stk in ((packing, 8, True), (other, 1, True), (other, 8, True), (packing, 1, False),
+                           (other, 1, False)):
             s2 = Stream(pk, b, stacked=stk)
             s2.step()
             g2 = capture(s2.step, warm=0)
@@ -568,6 +572,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["tq", "reference"], default="tq")
     ap.add_argument("--batch", type=int, default=1)
+    ap.add_argument("--packing", choices=sorted(PACKINGS), default="2bit",
+                    help="packing of the decode stream (the other one is measured under extras)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers of the weight stream (profiling runs use 1)")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
