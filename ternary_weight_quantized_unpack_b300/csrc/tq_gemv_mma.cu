@@ -48,6 +48,7 @@
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
 #include "tq_sm100.cuh"
+#include "tq_tmap.cuh"
 
 namespace tq {
 namespace gemv {
@@ -56,6 +57,9 @@ using namespace sm100;
 
 constexpr int kMaxThreads = 512;
 constexpr int kMaxCluster = 8;
+// With static weights, every warp asks L2 for its whole code range before the dependent-launch wait,
+// so HBM streams this call's weights while the preceding kernels finish.
+constexpr bool kPrefetchL2 = true;
 constexpr uint32_t kLutWords = 2u * 243u * 32u;
 constexpr uint32_t kLutBytes = kLutWords * 4u;
 
@@ -131,12 +135,13 @@ __device__ __forceinline__ float silu(float z) { return z / (1.f + expf(-z)); }
 
 // x^ and VP of one 128-block (absolute index blk) for batch slots 0..B-1 (slots past count are zero).
 // xh / vpo point at the slice that starts at block blk0 (offsets are taken relative to it; blk0 is a
-// multiple of 5, so word boundaries stay at the same offsets).  One warp; MAXB >= B.
-template <int PACK, int G, int MAXB>
+// multiple of 5, so word boundaries stay at the same offsets).  One warp; MAXB >= B.  XS: x (mode 0)
+// is a shared-memory copy of the slice, rows of xs_stride values starting at trit blk0 * 128.
+template <int PACK, int G, int MAXB, bool XS = false>
 __device__ __forceinline__ void prep_block(const uint16_t* __restrict__ x, const float* __restrict__ gu, float* h_out,
                                            int* status, int K, int B, int apply, int mode, int topk, int blk,
                                            int blk0, int count, const int* rows, uint16_t* xh, float* vpo,
-                                           int lane) {
+                                           int lane, int xs_stride = 0) {
   const int R = vp_row(B);
   const int kb = blk * kFwhtBlock + 4 * lane;   // absolute trit index of this lane's 4 values
   const int kr = kb - blk0 * kFwhtBlock;        // ... relative to the slice
@@ -158,7 +163,8 @@ __device__ __forceinline__ void prep_block(const uint16_t* __restrict__ x, const
         if (h_out) *reinterpret_cast<float4*>(h_out + a * K + kb) = make_float4(v[b][0], v[b][1], v[b][2], v[b][3]);
       } else {
         const size_t r = mode == 1 ? static_cast<size_t>(rows[b] / topk) : static_cast<size_t>(b);
-        const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(x + r * K + kb));
+        const uint2 raw = XS ? *reinterpret_cast<const uint2*>(x + r * xs_stride + kr)
+                             : __ldcg(reinterpret_cast<const uint2*>(x + r * K + kb));
         v[b][0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
         v[b][1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
         v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
@@ -467,9 +473,15 @@ __device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, cons
   const int e0 = rank * chunk, e1 = min(E, e0 + chunk);
   const uint32_t base = smem_addr(red);
   for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += blockDim.x) {
+    float part[kMaxCluster];  // all remote loads in flight at once, then summed in rank order
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      part[r] = r < ks ? ld_cluster_f32(cluster_map(base + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(r)))
+                       : 0.f;
     float v = 0.f;
-    for (int r = 0; r < ks; ++r)
-      v += ld_cluster_f32(cluster_map(base + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(r)));
+#pragma unroll
+    for (int r = 0; r < kMaxCluster; ++r)
+      if (r < ks) v += part[r];
     const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
     if (row < p.N && b < sel.count) p.y[static_cast<size_t>(sel.rows ? sel.rows[b] : b) * p.N + row] = v;
   }
@@ -533,6 +545,9 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
       us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
   };
+  if (kPrefetchL2 && p.early && gl_a < gl_b && c.lane < 16 && row_w0 + c.lane < p.N)
+    bulk_prefetch_l2(sel.codes + static_cast<size_t>(row_w0 + c.lane) * p.P + c.k_start / 16 + gl_a * (G / 16),
+                     static_cast<uint32_t>(gl_b - gl_a) * (G / 4));
   if (p.early) prime();
   pdl_wait();
   if (!p.fused) copy_prep_slice(p, c, sel, smem, bars);
@@ -793,6 +808,11 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
       us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
   };
+  if (kPrefetchL2 && p.early && c.ua < c.ub) {
+    const uint32_t bytes = static_cast<uint32_t>(min(c.ub * 8, p.P >> 2) - s_begin) * 16u;
+    if (R < p.N) bulk_prefetch_l2(cR + s_begin, bytes);
+    if (R2 < p.N) bulk_prefetch_l2(cR2 + s_begin, bytes);
+  }
   if (p.early) prime();
   pdl_wait();
   if (!p.fused) copy_prep_slice(p, c, sel, smem, bars);
@@ -855,6 +875,287 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
   }
   __syncthreads();
   reduce_store(p, c, sel, red);
+}
+
+// ---------------------------------------------------------------------------------------------
+// 2-bit dense decode, streamed ("stream" kernel).  One CTA per SM: nw consumer warps, each owning a
+// 16-row slab of the CTA's 16*nw-row block, and one producer warp whose elected lane streams the
+// block's codes through a ring of S shared-memory stages with 2-D TMA (32 words = 512 trits x 16*nw
+// rows per stage, 128-byte swizzle).  With static weights the ring is filled before the
+// dependent-launch wait, so the first stages of a call arrive while the preceding kernel finishes.
+// K may be split over the ks CTAs of a cluster (partial sums meet through distributed shared
+// memory in rank order).  The activations of the CTA's K-range are transformed in the CTA (small
+// batches) or bulk-copied from the prep kernel's output.  Decode, MMA and scale folding are those of
+// the shared-row layout above.
+// ---------------------------------------------------------------------------------------------
+struct SParams {
+  const uint16_t* scales;
+  const uint16_t* x;     // bf16 rows [B][K] (fused prologue)
+  const uint16_t* xh_g;  // prep kernel output (not fused)
+  const float* vp_g;
+  float* y;
+  int* status;
+  int N, K, ng, B, R;
+  int gpc;  // groups per CTA K-range (whole 128-blocks)
+  int nw;   // consumer warps
+  int S;    // ring stages
+  int fused, early, apply;
+  uint32_t stage_bytes;
+  uint32_t xh_off, vp_off, sw_off, red_off, bar_off, xs_off;  // offsets from the 1024-aligned base
+};
+
+// The scales of one stage of one warp (16 rows x NG groups starting at absolute group ga), held two
+// halves per register and staged as halves [group][row position] (rows r and r + 8 adjacent).
+template <int NG>
+struct StageScales {
+  static constexpr int PER_LANE = 16 * NG / 32;
+  uint32_t v[PER_LANE / 2];
+  __device__ __forceinline__ void load(const uint16_t* scales, int N, int ng, int row_w0, int ga, int ngs, int lane) {
+#pragma unroll
+    for (int j = 0; j < PER_LANE; ++j) {
+      const int e = lane + 32 * j, r = e / NG, g = min(e % NG, ngs - 1), row = min(row_w0 + r, N - 1);
+      const uint32_t h = __ldg(scales + static_cast<size_t>(row) * ng + ga + g);
+      if (j & 1)
+        v[j >> 1] |= h << 16;
+      else
+        v[j >> 1] = h;
+    }
+  }
+  __device__ __forceinline__ void store(uint16_t* sw, int lane) const {
+#pragma unroll
+    for (int j = 0; j < PER_LANE; ++j) {
+      const int e = lane + 32 * j, r = e / NG, g = e % NG;
+      sw[g * 16 + (((r & 7) << 1) | (r >> 3))] = static_cast<uint16_t>((j & 1) ? (v[j >> 1] >> 16) : (v[j >> 1] & 0xffffu));
+    }
+  }
+};
+
+template <int G, int NT>
+__global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_constant__ CUtensorMap tm,
+                                                                  const __grid_constant__ SParams p) {
+  constexpr int WPT = G / 64;   // words per thread per group per row
+  constexpr int GPS = 512 / G;  // groups per stage
+  constexpr int MAXB = 8 * NT;
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  pdl_launch_dependents();
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int nw = p.nw, BR = 16 * nw;
+  const int row0 = static_cast<int>(blockIdx.x) * BR;
+  const int g0 = static_cast<int>(blockIdx.y) * p.gpc;
+  const int ngc = min(p.gpc, p.ng - g0);  // groups of this CTA (> 0)
+  const int nst = (ngc + GPS - 1) / GPS;
+  const int kw0 = g0 * (G / 16);          // first code word of the K-range
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
+  uint64_t* empty = full + p.S;
+  uint64_t* xbar = empty + p.S;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < p.S; ++i) {
+      mbar_init(&full[i], 1);
+      mbar_init(&empty[i], nw);
+    }
+    mbar_init(xbar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+
+  if (warp == nw) {  // ---------------- producer ----------------
+    if (lane == 0) {
+      tma_prefetch_desc(&tm);
+      // fused: the CTA's columns of x (rows of kr bf16 values), once the preceding kernel is done
+      auto copy_x = [&]() {
+        const uint32_t rb = static_cast<uint32_t>(ngc) * G * 2u;
+        mbar_arrive_expect_tx(xbar, rb * p.B);
+        for (int b = 0; b < p.B; ++b)
+          bulk_g2s(smem + p.xs_off + static_cast<size_t>(b) * rb, p.x + static_cast<size_t>(b) * p.K + g0 * G, rb,
+                   xbar);
+      };
+      if (!p.early) {
+        pdl_wait();
+        if (p.fused) copy_x();
+      }
+      for (int s = 0; s < nst; ++s) {
+        const int slot = s % p.S;
+        if (s == p.S && p.early) {  // the ring is full: now wait for the preceding kernel
+          pdl_wait();
+          if (p.fused) copy_x();
+        }
+        if (s >= p.S && !mbar_wait(&empty[slot], ((s / p.S) + 1) & 1)) {
+          record_error(p.status, TQ_ERR_TIMEOUT);
+          break;
+        }
+        mbar_arrive_expect_tx(&full[slot], p.stage_bytes);
+        tma_load_2d(smem + static_cast<size_t>(slot) * p.stage_bytes, &tm, kw0 + 32 * s, row0, &full[slot]);
+      }
+      if (nst <= p.S && p.early) {
+        pdl_wait();
+        if (p.fused) copy_x();
+      }
+    }
+    __syncwarp();
+    pdl_wait();  // this warp also stores outputs in the cluster reduction below
+  } else {  // ---------------- consumers ----------------
+    const int g = lane >> 2, q = lane & 3;
+    const int row_w0 = row0 + 16 * warp;
+    uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + warp * (GPS * 16);
+    StageScales<GPS> us;
+    if (p.early) us.load(p.scales, p.N, p.ng, row_w0, g0, min(GPS, ngc), lane);
+    pdl_wait();
+    if (!p.early) us.load(p.scales, p.N, p.ng, row_w0, g0, min(GPS, ngc), lane);
+    uint16_t* xhs = reinterpret_cast<uint16_t*>(smem + p.xh_off);
+    float* vps = reinterpret_cast<float*>(smem + p.vp_off);
+    const int k_start = g0 * G, kr = ngc * G;
+    if (p.fused) {
+      if (!mbar_wait(xbar, 0) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      const int blk0 = k_start / kFwhtBlock, nblk = kr / kFwhtBlock;
+      const uint16_t* xs = reinterpret_cast<const uint16_t*>(smem + p.xs_off);
+      for (int i = warp; i < nblk; i += nw)
+        prep_block<TQ_PACK_2BIT, G, MAXB, true>(xs, nullptr, nullptr, p.status, p.K, p.B, p.apply, 0, 0, blk0 + i,
+                                                blk0, p.B, nullptr, xhs, vps, lane, kr);
+      named_bar_sync(1, 32 * nw);
+    } else {
+      if (threadIdx.x == 0) {
+        const uint32_t xb = static_cast<uint32_t>(kr) * p.B * 2u;
+        const uint32_t vb = static_cast<uint32_t>(ngc) * p.R * 4u;
+        mbar_arrive_expect_tx(xbar, xb + vb);
+        bulk_g2s(xhs, p.xh_g + static_cast<size_t>(k_start) * p.B, xb, xbar);
+        bulk_g2s(vps, p.vp_g + static_cast<size_t>(g0) * p.R, vb, xbar);
+      }
+      if (!mbar_wait(xbar, 0) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+    }
+    const uint32_t* xh = reinterpret_cast<const uint32_t*>(xhs);
+    const float* V = vps;
+    float acc[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t)
+#pragma unroll
+      for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
+    // this thread's bytes within a stage row: words WPT*q .. of each group, 128-byte swizzle
+    const uint32_t rA = static_cast<uint32_t>(16 * warp + g) * 128u, rB = rA + 8u * 128u;
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % p.S;
+      const int ngs = min(GPS, ngc - s * GPS);
+      __syncwarp();
+      us.store(sw, lane);
+      __syncwarp();
+      if (s + 1 < nst) us.load(p.scales, p.N, p.ng, row_w0, g0 + (s + 1) * GPS, min(GPS, ngc - (s + 1) * GPS), lane);
+      if (!mbar_wait(&full[slot], (s / p.S) & 1) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      const uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
+#pragma unroll
+      for (int j = 0; j < GPS; ++j) {
+        if (j >= ngs) break;
+        const int gl = s * GPS + j;  // group within the CTA's K-range
+        uint32_t w[2 * WPT];
+        if (WPT == 2) {
+          const uint32_t off = (static_cast<uint32_t>((2 * j + (q >> 1)) ^ g) << 4) + 8u * (q & 1);
+          const uint2 a = *reinterpret_cast<const uint2*>(st + rA + off);
+          const uint2 b = *reinterpret_cast<const uint2*>(st + rB + off);
+          w[0] = a.x;
+          w[1] = a.y;
+          w[2] = b.x;
+          w[3] = b.y;
+        } else {
+          const uint32_t off = (static_cast<uint32_t>(j ^ g) << 4) + 4u * q;
+          w[0] = *reinterpret_cast<const uint32_t*>(st + rA + off);
+          w[1] = *reinterpret_cast<const uint32_t*>(st + rB + off);
+        }
+        float cc[NT][4];
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int b = min(8 * t + 2 * q, p.R - 2);  // columns past B read a valid slot, never stored
+          const float2 v = *reinterpret_cast<const float2*>(V + gl * p.R + b);
+          cc[t][0] = v.x;
+          cc[t][1] = v.y;
+          cc[t][2] = v.x;
+          cc[t][3] = v.y;
+        }
+#pragma unroll
+        for (int u = 0; u < WPT; ++u) {
+          const uint32_t wa = w[u], w8 = w[WPT + u];
+          const uint32_t w2 = wa >> 10, w82 = w8 >> 10;
+          uint32_t pr[8], pr8[8];
+#pragma unroll
+          for (int jj = 0; jj < 8; ++jj) {
+            pr[jj] = jj < 5 ? (wa & (0x00030003u << (2 * jj))) : (w2 & (0x00030003u << (2 * (jj - 5))));
+            pr8[jj] = jj < 5 ? (w8 & (0x00030003u << (2 * jj))) : (w82 & (0x00030003u << (2 * (jj - 5))));
+          }
+          uint4 bp[NT];
+#pragma unroll
+          for (int jj = 0; jj < 4; ++jj) {
+#pragma unroll
+            for (int t = 0; t < NT; ++t) {
+              const int b = min(8 * t + g, p.B - 1);  // columns past B: not stored
+              if ((jj & 1) == 0)
+                bp[t] = *reinterpret_cast<const uint4*>(xh + ((((gl * WPT + u) * 2 + (jj >> 1)) * p.B + b) * 4 + q) * 4);
+              const uint32_t b0 = (jj & 1) ? bp[t].z : bp[t].x, b1 = (jj & 1) ? bp[t].w : bp[t].y;
+              mma16816(cc[t], pr[2 * jj], pr8[2 * jj], pr[2 * jj + 1], pr8[2 * jj + 1], b0, b1);
+            }
+          }
+        }
+        const float2 m = scale_pair(sw + j * 16 + 2 * g, V[gl * p.R + p.R - 1]);  // rows g, g + 8
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          acc[t][0] = fmaf(m.x, cc[t][0], acc[t][0]);
+          acc[t][1] = fmaf(m.x, cc[t][1], acc[t][1]);
+          acc[t][2] = fmaf(m.y, cc[t][2], acc[t][2]);
+          acc[t][3] = fmaf(m.y, cc[t][3], acc[t][3]);
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&empty[slot]);
+    }
+    const int rg = row_w0 + g, rg8 = rg + 8;
+    if (gridDim.y == 1) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int b = 8 * t + 2 * q;
+        if (rg < p.N) {
+          if (b < p.B) p.y[static_cast<size_t>(b) * p.N + rg] = acc[t][0];
+          if (b + 1 < p.B) p.y[static_cast<size_t>(b + 1) * p.N + rg] = acc[t][1];
+        }
+        if (rg8 < p.N) {
+          if (b < p.B) p.y[static_cast<size_t>(b) * p.N + rg8] = acc[t][2];
+          if (b + 1 < p.B) p.y[static_cast<size_t>(b + 1) * p.N + rg8] = acc[t][3];
+        }
+      }
+    } else {
+      float* red = reinterpret_cast<float*>(smem + p.red_off);
+      const int rl = 16 * warp + g;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int b = 8 * t + 2 * q;
+        if (b < p.B) {
+          red[rl * p.B + b] = acc[t][0];
+          red[(rl + 8) * p.B + b] = acc[t][2];
+        }
+        if (b + 1 < p.B) {
+          red[rl * p.B + b + 1] = acc[t][1];
+          red[(rl + 8) * p.B + b + 1] = acc[t][3];
+        }
+      }
+    }
+  }
+  if (gridDim.y > 1) {  // every thread of every CTA of the cluster takes part
+    cluster_sync();     // all partial sums are in place
+    const int ks = static_cast<int>(gridDim.y), rank = static_cast<int>(cluster_ctarank());
+    const int E = BR * p.B, chunk = (E + ks - 1) / ks;
+    const int e0 = rank * chunk, e1 = min(E, e0 + chunk);
+    const uint32_t base = smem_addr(smem + p.red_off);
+    for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += static_cast<int>(blockDim.x)) {
+      float part[kMaxCluster];  // all remote loads in flight at once, then summed in rank order
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        part[r] = r < ks ? ld_cluster_f32(cluster_map(base + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(r)))
+                         : 0.f;
+      float v = 0.f;
+#pragma unroll
+      for (int r = 0; r < kMaxCluster; ++r)
+        if (r < ks) v += part[r];
+      const int rl = e / p.B, b = e - rl * p.B, row = row0 + rl;
+      if (row < p.N) p.y[static_cast<size_t>(b) * p.N + row] = v;
+    }
+    cluster_sync();  // keep this CTA's shared memory alive until the peers have read it
+  }
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1073,6 +1374,240 @@ size_t vp_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d
 // the decode kernel (one kernel boundary less in a chain of several launches; measured faster at
 // 1 and 8 tokens); dense calls use one prep kernel that transforms the activations once for all
 // CTAs (measured faster on the decode stream).
+// ---- stream kernel (2-bit dense) ----
+// Batch at most this: the CTAs transform their own K-range of the activations (no prep kernel).
+constexpr int kStreamFuseMaxB = 2;
+
+struct SPlan {
+  bool ok;
+  int nw, ks, gpc, S, n_rb;
+  size_t smem;
+  uint32_t stage_bytes, xh_off, vp_off, sw_off, red_off, bar_off, xs_off;
+};
+
+// Shared-memory layout (offsets from the 1024-aligned base): ring, x^, VP, per-warp scales, partial
+// sums, barriers.  The ring takes what the rest leaves, up to 8 stages.
+bool stream_layout(SPlan& pl, int B, int G) {
+  const int BR = 16 * pl.nw, GPS = 512 / G;
+  pl.stage_bytes = static_cast<uint32_t>(BR) * 128u;
+  const size_t xh = align256(static_cast<size_t>(pl.gpc) * G * B * 2);
+  const size_t vp = align256(static_cast<size_t>(pl.gpc) * vp_row(B) * 4);
+  const size_t sw = align256(static_cast<size_t>(pl.nw) * GPS * 16 * 2);
+  const size_t red = pl.ks > 1 ? align256(static_cast<size_t>(BR) * B * 4) : 0;
+  const size_t xs = B <= kStreamFuseMaxB ? align256(static_cast<size_t>(pl.gpc) * G * B * 2) : 0;
+  const size_t bars = 256;
+  const size_t fixed = xh + vp + sw + red + xs + bars + 1024;  // + alignment slack of the base
+  if (fixed + 2 * static_cast<size_t>(pl.stage_bytes) > kSmemLimit) return false;
+  pl.S = static_cast<int>(std::min<size_t>(8, (kSmemLimit - fixed) / pl.stage_bytes));
+  size_t off = static_cast<size_t>(pl.S) * pl.stage_bytes;
+  pl.xh_off = static_cast<uint32_t>(off);
+  off += xh;
+  pl.vp_off = static_cast<uint32_t>(off);
+  off += vp;
+  pl.sw_off = static_cast<uint32_t>(off);
+  off += sw;
+  pl.red_off = static_cast<uint32_t>(off);
+  off += red;
+  pl.xs_off = static_cast<uint32_t>(off);
+  off += xs;
+  pl.bar_off = static_cast<uint32_t>(off);
+  off += bars;
+  pl.smem = off + 1024;
+  return true;
+}
+
+// Candidate splits, cheapest first: 16*nw-row blocks x ks K-ranges (whole 128-blocks), at most one
+// CTA per SM.  Cost: groups per warp x warps per SM (the decode loop is issue-bound once ~6 warps
+// share an SM); ties go to fewer CTAs.
+std::vector<SPlan> stream_candidates(const tq_desc* d, int B, int sms) {
+  const int G = d->group, ng = d->K / G, bpg = kFwhtBlock / G;
+  std::vector<std::pair<double, SPlan>> list;
+  for (int nw : {16, 8}) {
+    const int BR = 16 * nw, n_rb = (d->N + BR - 1) / BR;
+    for (int ks = 1; ks <= kMaxCluster && n_rb * ks <= sms; ++ks) {
+      int gpc = (ng + ks - 1) / ks;
+      gpc = (gpc + bpg - 1) / bpg * bpg;
+      if ((ks - 1) * gpc >= ng) continue;  // a CTA without work
+      SPlan pl{};
+      pl.nw = nw;
+      pl.ks = ks;
+      pl.gpc = gpc;
+      pl.n_rb = n_rb;
+      if (!stream_layout(pl, B, G)) continue;
+      pl.ok = true;
+      list.emplace_back(static_cast<double>(gpc) * std::max(nw, 6), pl);
+    }
+  }
+  std::stable_sort(list.begin(), list.end(), [](const auto& a, const auto& b) {
+    if (a.first != b.first) return a.first < b.first;
+    return a.second.n_rb * a.second.ks < b.second.n_rb * b.second.ks;
+  });
+  std::vector<SPlan> out;
+  for (auto& e : list) out.push_back(e.second);
+  return out;
+}
+
+template <int G, int NT>
+const void* stream_kernel_t() {
+  return reinterpret_cast<const void*>(gemv_2b_stream_kernel<G, NT>);
+}
+const void* stream_kernel(int G, int B) {
+  if (G == 128) return B <= 8 ? stream_kernel_t<128, 1>() : stream_kernel_t<128, 2>();
+  return B <= 8 ? stream_kernel_t<64, 1>() : stream_kernel_t<64, 2>();
+}
+
+// Tensor map over a code matrix [N][P] (uint32), box 32 words x BR rows, 128-byte swizzle; cached per
+// (address, N, P, BR).
+bool codes_tmap(const uint32_t* codes, int N, int P, int BR, CUtensorMap* out) {
+  static std::map<std::tuple<const void*, int, int, int>, CUtensorMap> cache;
+  static std::mutex mu;
+  const auto key = std::make_tuple(static_cast<const void*>(codes), N, P, BR);
+  std::lock_guard<std::mutex> lock(mu);
+  auto it = cache.find(key);
+  if (it != cache.end()) {
+    *out = it->second;
+    return true;
+  }
+  CUtensorMap m;
+  if (!make_tmap_2d(&m, codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<uint64_t>(P), static_cast<uint64_t>(N),
+                    static_cast<uint64_t>(P) * 4u, 32u, static_cast<uint32_t>(BR), CU_TENSOR_MAP_SWIZZLE_128B))
+    return false;
+  if (cache.size() > 4096) cache.clear();
+  cache[key] = m;
+  *out = m;
+  return true;
+}
+
+// The stream kernel's plan for a shape on the current device (cached), or !ok when it does not apply.
+cudaError_t choose_stream_plan(const tq_desc* d, int B, SPlan* out) {
+  static std::map<std::tuple<int, int, int, int, int>, SPlan> cache;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const auto key = std::make_tuple(d->N, d->K, d->group, B, dev);
+  {
+    std::lock_guard<std::mutex> lock(mu);
+    auto it = cache.find(key);
+    if (it != cache.end()) {
+      *out = it->second;
+      return cudaSuccess;
+    }
+  }
+  int sms = kSMs, optin = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = kSMs;
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess) return e;
+  SPlan pl{};
+  if (d->packing == TQ_PACK_2BIT && d->K % kFwhtBlock == 0 && B <= kMaxBatch) {
+    // the first candidate whose CTAs (clusters) are all resident at once
+    const void* kern = stream_kernel(d->group, B);
+    for (const SPlan& c : stream_candidates(d, B, sms)) {
+      if (c.smem > static_cast<size_t>(optin)) continue;
+      if ((e = ensure_smem_attr(kern, c.smem)) != cudaSuccess) return e;
+      bool fits = false;
+      if (c.ks > 1) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(c.n_rb, c.ks, 1);
+        cfg.blockDim = dim3(32 * (c.nw + 1));
+        cfg.dynamicSmemBytes = c.smem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 1;
+        attr[0].val.clusterDim.y = c.ks;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int nc = 0;
+        if (cudaOccupancyMaxActiveClusters(&nc, kern, &cfg) != cudaSuccess) {
+          (void)cudaGetLastError();
+          continue;
+        }
+        fits = nc >= c.n_rb;
+      } else {
+        fits = c.n_rb <= sms;
+      }
+      if (fits) {
+        pl = c;
+        break;
+      }
+    }
+  }
+  std::lock_guard<std::mutex> lock(mu);
+  cache[key] = pl;
+  *out = pl;
+  return cudaSuccess;
+}
+
+// Dense 2-bit GEMV through the stream kernel (plus the prep kernel above kStreamFuseMaxB).
+cudaError_t launch_stream(const tq_desc* d, const SPlan& pl, const uint32_t* codes, const uint16_t* scales,
+                          const uint16_t* x, int B, float* y, void* ws, bool early, cudaStream_t s) {
+  const int G = d->group;
+  const int P = pitch_words(d->K, d->packing);
+  CUtensorMap tm;
+  if (!codes_tmap(codes, d->N, P, 16 * pl.nw, &tm)) return cudaErrorInvalidValue;
+  SParams sp{};
+  sp.scales = scales;
+  sp.x = x;
+  sp.xh_g = static_cast<const uint16_t*>(ws);
+  sp.vp_g = reinterpret_cast<const float*>(static_cast<const uint8_t*>(ws) + xh_bytes(d, B));
+  sp.y = y;
+  sp.status = status_ptr();
+  sp.N = d->N;
+  sp.K = d->K;
+  sp.ng = d->K / G;
+  sp.B = B;
+  sp.R = vp_row(B);
+  sp.gpc = pl.gpc;
+  sp.nw = pl.nw;
+  sp.S = pl.S;
+  sp.fused = B <= kStreamFuseMaxB;
+  sp.early = early;
+  sp.apply = d->fwht_block != 0;
+  sp.stage_bytes = pl.stage_bytes;
+  sp.xh_off = pl.xh_off;
+  sp.vp_off = pl.vp_off;
+  sp.sw_off = pl.sw_off;
+  sp.red_off = pl.red_off;
+  sp.bar_off = pl.bar_off;
+  sp.xs_off = pl.xs_off;
+  cudaError_t e;
+  if (!sp.fused) {
+    PrepParams pp{};
+    pp.x = x;
+    pp.xh = static_cast<uint16_t*>(ws);
+    pp.vp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + xh_bytes(d, B));
+    pp.status = sp.status;
+    pp.K = d->K;
+    pp.B = B;
+    pp.apply = sp.apply;
+    e = G == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s, 1) : launch_prep<TQ_PACK_2BIT, 64>(pp, s, 1);
+    if (e != cudaSuccess) return e;
+  }
+  const void* kern = stream_kernel(G, B);
+  if ((e = ensure_smem_attr(kern, pl.smem)) != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(pl.n_rb, pl.ks, 1);
+  cfg.blockDim = dim3(32 * (pl.nw + 1));
+  cfg.dynamicSmemBytes = pl.smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[2];
+  int na = 0;
+  attr[na].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[na].val.programmaticStreamSerializationAllowed = 1;
+  ++na;
+  if (pl.ks > 1) {
+    attr[na].id = cudaLaunchAttributeClusterDimension;
+    attr[na].val.clusterDim.x = 1;
+    attr[na].val.clusterDim.y = pl.ks;
+    attr[na].val.clusterDim.z = 1;
+    ++na;
+  }
+  cfg.attrs = attr;
+  cfg.numAttrs = na;
+  void* args[] = {&tm, &sp};
+  return cudaLaunchKernelExC(&cfg, kern, args);
+}
+
 cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int zdim, cudaStream_t s) {
   pp.status = status_ptr();
   pp.K = d->K;
@@ -1147,6 +1682,9 @@ cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t*
   pp.x = x;
   pp.xh = static_cast<uint16_t*>(ws);
   pp.vp = reinterpret_cast<float*>(static_cast<uint8_t*>(ws) + xh_bytes(d, B));
+  SPlan spl{};
+  if (const cudaError_t e = choose_stream_plan(d, B, &spl); e != cudaSuccess) return e;
+  if (spl.ok) return launch_stream(d, spl, codes, scales, x, B, y, ws, (d->flags & TQ_STATIC_WEIGHTS) != 0, s);
   Params prm{};
   prm.codes = codes;
   prm.scales = scales;

@@ -95,6 +95,11 @@ __device__ __forceinline__ void ldg_v8(const void* ptr, uint4& a, uint4& b) {
                : "l"(ptr));
 }
 
+// ---- L2 prefetch of a global range (fire and forget; address and size multiples of 16 bytes) ----
+__device__ __forceinline__ void bulk_prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // ---- programmatic dependent launch ------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
