@@ -525,7 +525,7 @@ def run_tq(args, rank, world, local):
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
         "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": st.h2d_bytes(),
                 "d2h_bytes_per_step": st.d2h_bytes()},
-        "gpu_launches": args.steps * len(st.calls) * tq_launches_per_gemv(),
+        "gpu_launches": args.steps * sum(tq.tq_gemv_kernel_count(c[0], batch) for c in st.calls),
         "clocks": clocks,
         "source_hash": source_hash(),
     }
@@ -558,11 +558,6 @@ def run_tq(args, rank, world, local):
         line["extras"] = ex
     if rank == 0:
         print(json.dumps(line))
-
-
-def tq_launches_per_gemv():
-    """Kernels one tq_gemv call launches (activation prep kernel + decode GEMV kernel)."""
-    return 2
 
 
 def main():

@@ -111,6 +111,12 @@ size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch);
 tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                   int batch, float* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* Number of CUDA kernels one tq_gemv call with this descriptor and batch launches on the current
+ * device (1: the activation transform runs inside the decode kernel; 2: a prep kernel precedes it),
+ * or -1 for an invalid descriptor / batch or a CUDA error.  No counterpart on the pages: it lets a
+ * caller count launches, e.g. per CUDA-graph step. */
+int tq_gemv_kernel_count(const tq_desc* d, int batch);
+
 /* ---- tq_gemv_noalloc: tq_gemv without a workspace -------------------------------------------------
  * No counterpart on the pages: a library convenience.  Same computation, arguments, layouts and
  * errors as tq_gemv, but the scratch lives in a fixed 1 MiB device array inside libtq, for callers

@@ -61,6 +61,7 @@ _SIGS = {
     "tq_gemv_workspace_bytes": (_SZ, [_D, _I]),
     "tq_gemv": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "tq_gemv_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P]),
+    "tq_gemv_kernel_count": (_I, [_D, _I]),
     "tq_moe_route": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "tq_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "tq_moe_gemv": (_I, [_D, _D, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
@@ -128,6 +129,10 @@ def tq_scale_bytes(d: tq_desc) -> int:
 
 def tq_gemv_workspace_bytes(d: tq_desc, batch: int) -> int:
     return lib().tq_gemv_workspace_bytes(ctypes.byref(d), batch)
+
+
+def tq_gemv_kernel_count(d: tq_desc, batch: int) -> int:
+    return lib().tq_gemv_kernel_count(ctypes.byref(d), batch)
 
 
 def tq_gemm_workspace_bytes(d: tq_desc, M: int) -> int:

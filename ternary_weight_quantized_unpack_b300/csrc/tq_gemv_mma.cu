@@ -60,6 +60,10 @@ constexpr int kMaxCluster = 8;
 // With static weights, every warp asks L2 for its whole code range before the dependent-launch wait,
 // so HBM streams this call's weights while the preceding kernels finish.
 constexpr bool kPrefetchL2 = true;
+// Stream kernel: up to this batch the CTAs transform their own K-range of the activations (no prep
+// kernel); stages of the code ring issued before the dependent-launch wait (static weights).
+constexpr int kStreamFuseMaxB = 2;
+constexpr int kEarlyStages = 1;
 constexpr uint32_t kLutWords = 2u * 243u * 32u;
 constexpr uint32_t kLutBytes = kLutWords * 4u;
 
@@ -949,15 +953,19 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.S;
   uint64_t* xbar = empty + p.S;
+  uint64_t* rbar = xbar + 1;  // cluster leader: partial sums of the other ranks have arrived
+  const int ks = static_cast<int>(gridDim.y);
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.S; ++i) {
       mbar_init(&full[i], 1);
       mbar_init(&empty[i], nw);
     }
     mbar_init(xbar, 1);
+    mbar_init(rbar, ks > 1 ? (ks - 1) * 32 * nw : 1);
     fence_mbar_init();
   }
   __syncthreads();
+  if (ks > 1) cluster_arrive_relaxed();  // waited on before the first remote access
 
   if (warp == nw) {  // ---------------- producer ----------------
     if (lane == 0) {
@@ -970,15 +978,26 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
           bulk_g2s(smem + p.xs_off + static_cast<size_t>(b) * rb, p.x + static_cast<size_t>(b) * p.K + g0 * G, rb,
                    xbar);
       };
-      if (!p.early) {
-        pdl_wait();
-        if (p.fused) copy_x();
-      }
+      // not fused: this CTA's slices of the prep kernel's output
+      auto copy_slices = [&]() {
+        const uint32_t xb = static_cast<uint32_t>(ngc) * G * p.B * 2u;
+        const uint32_t vb = static_cast<uint32_t>(ngc) * p.R * 4u;
+        mbar_arrive_expect_tx(xbar, xb + vb);
+        bulk_g2s(smem + p.xh_off, p.xh_g + static_cast<size_t>(g0) * G * p.B, xb, xbar);
+        bulk_g2s(smem + p.vp_off, p.vp_g + static_cast<size_t>(g0) * p.R, vb, xbar);
+      };
+      // Static weights: the first kEarlyStages stages go out before the dependent-launch wait; the
+      // activations are requested next, ahead of the rest of the ring, so that they do not queue
+      // behind the whole ring's weight traffic.
+      const int early_st = p.early ? min(nst, kEarlyStages) : 0;
       for (int s = 0; s < nst; ++s) {
         const int slot = s % p.S;
-        if (s == p.S && p.early) {  // the ring is full: now wait for the preceding kernel
+        if (s == early_st) {
           pdl_wait();
-          if (p.fused) copy_x();
+          if (p.fused)
+            copy_x();
+          else
+            copy_slices();
         }
         if (s >= p.S && !mbar_wait(&empty[slot], ((s / p.S) + 1) & 1)) {
           record_error(p.status, TQ_ERR_TIMEOUT);
@@ -987,13 +1006,15 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
         mbar_arrive_expect_tx(&full[slot], p.stage_bytes);
         tma_load_2d(smem + static_cast<size_t>(slot) * p.stage_bytes, &tm, kw0 + 32 * s, row0, &full[slot]);
       }
-      if (nst <= p.S && p.early) {
+      if (early_st == nst) {
         pdl_wait();
-        if (p.fused) copy_x();
+        if (p.fused)
+          copy_x();
+        else
+          copy_slices();
       }
     }
     __syncwarp();
-    pdl_wait();  // this warp also stores outputs in the cluster reduction below
   } else {  // ---------------- consumers ----------------
     const int g = lane >> 2, q = lane & 3;
     const int row_w0 = row0 + 16 * warp;
@@ -1014,13 +1035,6 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
                                                 blk0, p.B, nullptr, xhs, vps, lane, kr);
       named_bar_sync(1, 32 * nw);
     } else {
-      if (threadIdx.x == 0) {
-        const uint32_t xb = static_cast<uint32_t>(kr) * p.B * 2u;
-        const uint32_t vb = static_cast<uint32_t>(ngc) * p.R * 4u;
-        mbar_arrive_expect_tx(xbar, xb + vb);
-        bulk_g2s(xhs, p.xh_g + static_cast<size_t>(k_start) * p.B, xb, xbar);
-        bulk_g2s(vps, p.vp_g + static_cast<size_t>(g0) * p.R, vb, xbar);
-      }
       if (!mbar_wait(xbar, 0) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
     }
     const uint32_t* xh = reinterpret_cast<const uint32_t*>(xhs);
@@ -1105,7 +1119,44 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
       if (lane == 0) mbar_arrive(&empty[slot]);
     }
     const int rg = row_w0 + g, rg8 = rg + 8;
-    if (gridDim.y == 1) {
+    const int rl = 16 * warp + g;
+    if (ks > 1 && blockIdx.y != 0) {
+      // push the partial sums into the cluster leader's buffer (slot rank - 1), then arrive on its
+      // barrier; the leader adds them to its own in rank order
+      cluster_wait();
+      const uint32_t slot0 = smem_addr(smem + p.red_off) + 4u * static_cast<uint32_t>((blockIdx.y - 1) * BR * p.B);
+      const uint32_t base = cluster_map(slot0, 0);
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int b = 8 * t + 2 * q;
+        if (b < p.B) {
+          st_cluster_f32(base + 4u * static_cast<uint32_t>(rl * p.B + b), acc[t][0]);
+          st_cluster_f32(base + 4u * static_cast<uint32_t>((rl + 8) * p.B + b), acc[t][2]);
+        }
+        if (b + 1 < p.B) {
+          st_cluster_f32(base + 4u * static_cast<uint32_t>(rl * p.B + b + 1), acc[t][1]);
+          st_cluster_f32(base + 4u * static_cast<uint32_t>((rl + 8) * p.B + b + 1), acc[t][3]);
+        }
+      }
+      mbar_arrive_remote(cluster_map(smem_addr(rbar), 0));
+    } else {
+      if (ks > 1) {
+        cluster_wait();
+        if (!mbar_wait_cluster(rbar, 0) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        const float* red = reinterpret_cast<const float*>(smem + p.red_off);
+        const int E = BR * p.B;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const int b = min(8 * t + 2 * q, p.B - 1), b1 = min(b + 1, p.B - 1);
+          for (int r = 1; r < ks; ++r) {
+            const float* rr = red + (r - 1) * E;
+            acc[t][0] += rr[rl * p.B + b];
+            acc[t][1] += rr[rl * p.B + b1];
+            acc[t][2] += rr[(rl + 8) * p.B + b];
+            acc[t][3] += rr[(rl + 8) * p.B + b1];
+          }
+        }
+      }
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const int b = 8 * t + 2 * q;
@@ -1118,44 +1169,9 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
           if (b + 1 < p.B) p.y[static_cast<size_t>(b + 1) * p.N + rg8] = acc[t][3];
         }
       }
-    } else {
-      float* red = reinterpret_cast<float*>(smem + p.red_off);
-      const int rl = 16 * warp + g;
-#pragma unroll
-      for (int t = 0; t < NT; ++t) {
-        const int b = 8 * t + 2 * q;
-        if (b < p.B) {
-          red[rl * p.B + b] = acc[t][0];
-          red[(rl + 8) * p.B + b] = acc[t][2];
-        }
-        if (b + 1 < p.B) {
-          red[rl * p.B + b + 1] = acc[t][1];
-          red[(rl + 8) * p.B + b + 1] = acc[t][3];
-        }
-      }
     }
   }
-  if (gridDim.y > 1) {  // every thread of every CTA of the cluster takes part
-    cluster_sync();     // all partial sums are in place
-    const int ks = static_cast<int>(gridDim.y), rank = static_cast<int>(cluster_ctarank());
-    const int E = BR * p.B, chunk = (E + ks - 1) / ks;
-    const int e0 = rank * chunk, e1 = min(E, e0 + chunk);
-    const uint32_t base = smem_addr(smem + p.red_off);
-    for (int e = e0 + static_cast<int>(threadIdx.x); e < e1; e += static_cast<int>(blockDim.x)) {
-      float part[kMaxCluster];  // all remote loads in flight at once, then summed in rank order
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        part[r] = r < ks ? ld_cluster_f32(cluster_map(base + 4u * static_cast<uint32_t>(e), static_cast<uint32_t>(r)))
-                         : 0.f;
-      float v = 0.f;
-#pragma unroll
-      for (int r = 0; r < kMaxCluster; ++r)
-        if (r < ks) v += part[r];
-      const int rl = e / p.B, b = e - rl * p.B, row = row0 + rl;
-      if (row < p.N) p.y[static_cast<size_t>(b) * p.N + row] = v;
-    }
-    cluster_sync();  // keep this CTA's shared memory alive until the peers have read it
-  }
+  if (ks > 1 && warp == nw) cluster_wait();  // the producer warp completes its barrier phase too
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1375,8 +1391,7 @@ size_t vp_bytes(const tq_desc* d, int B) { return align256(static_cast<size_t>(d
 // 1 and 8 tokens); dense calls use one prep kernel that transforms the activations once for all
 // CTAs (measured faster on the decode stream).
 // ---- stream kernel (2-bit dense) ----
-// Batch at most this: the CTAs transform their own K-range of the activations (no prep kernel).
-constexpr int kStreamFuseMaxB = 2;
+
 
 struct SPlan {
   bool ok;
@@ -1393,7 +1408,7 @@ bool stream_layout(SPlan& pl, int B, int G) {
   const size_t xh = align256(static_cast<size_t>(pl.gpc) * G * B * 2);
   const size_t vp = align256(static_cast<size_t>(pl.gpc) * vp_row(B) * 4);
   const size_t sw = align256(static_cast<size_t>(pl.nw) * GPS * 16 * 2);
-  const size_t red = pl.ks > 1 ? align256(static_cast<size_t>(BR) * B * 4) : 0;
+  const size_t red = align256(static_cast<size_t>(pl.ks - 1) * BR * B * 4);
   const size_t xs = B <= kStreamFuseMaxB ? align256(static_cast<size_t>(pl.gpc) * G * B * 2) : 0;
   const size_t bars = 256;
   const size_t fixed = xh + vp + sw + red + xs + bars + 1024;  // + alignment slack of the base
@@ -1691,6 +1706,16 @@ cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t*
   prm.y = y;
   prm.early = (d->flags & TQ_STATIC_WEIGHTS) != 0;
   return launch_pair(d, pp, prm, B, 1, s);
+}
+
+int gemv_kernel_count(const tq_desc* d, int B) {
+  using namespace gemv;
+  SPlan spl{};
+  if (choose_stream_plan(d, B, &spl) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return -1;
+  }
+  return spl.ok && B <= kStreamFuseMaxB ? 1 : 2;
 }
 
 size_t gemv_chunks_workspace_bytes(const tq_desc* d, int B, int max_chunks) {

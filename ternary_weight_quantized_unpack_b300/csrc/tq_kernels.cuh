@@ -16,6 +16,9 @@ size_t gemv_workspace_bytes(const tq_desc* d, int batch);
 cudaError_t launch_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                         int batch, float* y, void* ws, cudaStream_t s);
 
+// Kernels one launch_gemv call launches for this shape on the current device (-1: CUDA error).
+int gemv_kernel_count(const tq_desc* d, int batch);
+
 // Decode GEMV over chunks of routed tokens (expert layer).  chunks[0] = number of records (at most
 // max_chunks); record c = chunks[1 + c * (2 + B)] = {expert, count, rows[B]}.  For slot b < count the
 // input is, mode 1: row rows[b] / topk of x (bf16, K wide); mode 2: silu(gate) * up of row rows[b] of

@@ -39,6 +39,11 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
   return TQ_OK;
 }
 
+extern "C" int tq_gemv_kernel_count(const tq_desc* d, int batch) {
+  if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return -1;
+  return gemv_kernel_count(d, batch);
+}
+
 extern "C" size_t tq_gemm_workspace_bytes(const tq_desc* d, int M) {
   if (check_linear_desc(d) != TQ_OK || M < 1) return 0;
   return gemm_workspace_bytes(d, M);
