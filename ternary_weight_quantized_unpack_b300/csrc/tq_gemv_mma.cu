@@ -61,9 +61,12 @@ constexpr int kMaxCluster = 8;
 // so HBM streams this call's weights while the preceding kernels finish.
 constexpr bool kPrefetchL2 = true;
 // Stream kernel: up to this batch the CTAs transform their own K-range of the activations (no prep
-// kernel); stages of the code ring issued before the dependent-launch wait (static weights).
+// kernel).  kEarlyStages: stages of the code ring issued before the dependent-launch wait (static
+// weights).  Measured on the 64-layer batch-1 stream: 0 (activations requested before any weight
+// stage) 3.43 ms per token, 1: 3.47 ms, 2: 3.72 ms; with static weights only the scales are read
+// before the wait.
 constexpr int kStreamFuseMaxB = 2;
-constexpr int kEarlyStages = 1;
+constexpr int kEarlyStages = 0;
 constexpr uint32_t kLutWords = 2u * 243u * 32u;
 constexpr uint32_t kLutBytes = kLutWords * 4u;
 
@@ -905,7 +908,7 @@ struct SParams {
   int S;    // ring stages
   int fused, early, apply;
   uint32_t stage_bytes;
-  uint32_t xh_off, vp_off, sw_off, red_off, bar_off, xs_off;  // offsets from the 1024-aligned base
+  uint32_t xh_off, vp_off, sc_off, red_off, bar_off, xs_off;  // offsets from the 1024-aligned base
 };
 
 // The scales of one stage of one warp (16 rows x NG groups starting at absolute group ga), held two
@@ -968,61 +971,64 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
   if (ks > 1) cluster_arrive_relaxed();  // waited on before the first remote access
 
   if (warp == nw) {  // ---------------- producer ----------------
-    if (lane == 0) {
-      tma_prefetch_desc(&tm);
-      // fused: the CTA's columns of x (rows of kr bf16 values), once the preceding kernel is done
-      auto copy_x = [&]() {
-        const uint32_t rb = static_cast<uint32_t>(ngc) * G * 2u;
-        mbar_arrive_expect_tx(xbar, rb * p.B);
-        for (int b = 0; b < p.B; ++b)
-          bulk_g2s(smem + p.xs_off + static_cast<size_t>(b) * rb, p.x + static_cast<size_t>(b) * p.K + g0 * G, rb,
-                   xbar);
-      };
-      // not fused: this CTA's slices of the prep kernel's output
-      auto copy_slices = [&]() {
-        const uint32_t xb = static_cast<uint32_t>(ngc) * G * p.B * 2u;
-        const uint32_t vb = static_cast<uint32_t>(ngc) * p.R * 4u;
-        mbar_arrive_expect_tx(xbar, xb + vb);
-        bulk_g2s(smem + p.xh_off, p.xh_g + static_cast<size_t>(g0) * G * p.B, xb, xbar);
-        bulk_g2s(smem + p.vp_off, p.vp_g + static_cast<size_t>(g0) * p.R, vb, xbar);
-      };
-      // Static weights: the first kEarlyStages stages go out before the dependent-launch wait; the
-      // activations are requested next, ahead of the rest of the ring, so that they do not queue
-      // behind the whole ring's weight traffic.
-      const int early_st = p.early ? min(nst, kEarlyStages) : 0;
-      for (int s = 0; s < nst; ++s) {
-        const int slot = s % p.S;
-        if (s == early_st) {
-          pdl_wait();
-          if (p.fused)
-            copy_x();
-          else
-            copy_slices();
-        }
-        if (s >= p.S && !mbar_wait(&empty[slot], ((s / p.S) + 1) & 1)) {
-          record_error(p.status, TQ_ERR_TIMEOUT);
-          break;
-        }
-        mbar_arrive_expect_tx(&full[slot], p.stage_bytes);
-        tma_load_2d(smem + static_cast<size_t>(slot) * p.stage_bytes, &tm, kw0 + 32 * s, row0, &full[slot]);
-      }
-      if (early_st == nst) {
-        pdl_wait();
+    if (lane == 0) tma_prefetch_desc(&tm);
+    // fused: the CTA's columns of x (rows of kr bf16 values), once the preceding kernel is done
+    auto copy_x = [&]() {
+      const uint32_t rb = static_cast<uint32_t>(ngc) * G * 2u;
+      mbar_arrive_expect_tx(xbar, rb * p.B);
+      for (int b = 0; b < p.B; ++b)
+        bulk_g2s(smem + p.xs_off + static_cast<size_t>(b) * rb, p.x + static_cast<size_t>(b) * p.K + g0 * G, rb,
+                 xbar);
+    };
+    // not fused: this CTA's slices of the prep kernel's output
+    auto copy_slices = [&]() {
+      const uint32_t xb = static_cast<uint32_t>(ngc) * G * p.B * 2u;
+      const uint32_t vb = static_cast<uint32_t>(ngc) * p.R * 4u;
+      mbar_arrive_expect_tx(xbar, xb + vb);
+      bulk_g2s(smem + p.xh_off, p.xh_g + static_cast<size_t>(g0) * G * p.B, xb, xbar);
+      bulk_g2s(smem + p.vp_off, p.vp_g + static_cast<size_t>(g0) * p.R, vb, xbar);
+    };
+    auto wait_and_copy = [&]() {
+      pdl_wait();
+      if (lane == 0) {
         if (p.fused)
           copy_x();
         else
           copy_slices();
       }
+    };
+    const uint64_t pol = l2_evict_first_policy();  // codes are read once per call
+    // Static weights: the first kEarlyStages stages go out before the dependent-launch wait; the
+    // activations are requested next, ahead of the rest of the ring, so that they do not queue
+    // behind the whole ring's weight traffic.
+    const int early_st = p.early ? min(nst, kEarlyStages) : 0;
+    for (int s = 0; s < nst; ++s) {
+      const int slot = s % p.S;
+      if (s == early_st) wait_and_copy();
+      if (s >= p.S && !mbar_wait(&empty[slot], ((s / p.S) + 1) & 1)) {
+        if (lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        break;
+      }
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&full[slot], p.stage_bytes);
+        tma_load_2d_hint(smem + static_cast<size_t>(slot) * p.stage_bytes, &tm, kw0 + 32 * s, row0, &full[slot], pol);
+      }
     }
+    if (early_st == nst) wait_and_copy();
     __syncwarp();
   } else {  // ---------------- consumers ----------------
     const int g = lane >> 2, q = lane & 3;
     const int row_w0 = row0 + 16 * warp;
-    uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + warp * (GPS * 16);
-    StageScales<GPS> us;
-    if (p.early) us.load(p.scales, p.N, p.ng, row_w0, g0, min(GPS, ngc), lane);
-    pdl_wait();
-    if (!p.early) us.load(p.scales, p.N, p.ng, row_w0, g0, min(GPS, ngc), lane);
+    uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sc_off) + warp * (GPS * 16);
+    // scales two stages ahead: stage s uses usA (s even) or usB (s odd)
+    StageScales<GPS> usA, usB;
+    auto load_scales = [&](StageScales<GPS>& us, int s) {
+      us.load(p.scales, p.N, p.ng, row_w0, g0 + s * GPS, min(GPS, ngc - s * GPS), lane);
+    };
+    if (!p.early) pdl_wait();
+    load_scales(usA, 0);
+    if (nst > 1) load_scales(usB, 1);
+    if (p.early) pdl_wait();
     uint16_t* xhs = reinterpret_cast<uint16_t*>(smem + p.xh_off);
     float* vps = reinterpret_cast<float*>(smem + p.vp_off);
     const int k_start = g0 * G, kr = ngc * G;
@@ -1046,13 +1052,13 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
       for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
     // this thread's bytes within a stage row: words WPT*q .. of each group, 128-byte swizzle
     const uint32_t rA = static_cast<uint32_t>(16 * warp + g) * 128u, rB = rA + 8u * 128u;
-    for (int s = 0; s < nst; ++s) {
+    auto stage = [&](int s, StageScales<GPS>& us) {
       const int slot = s % p.S;
       const int ngs = min(GPS, ngc - s * GPS);
       __syncwarp();
       us.store(sw, lane);
       __syncwarp();
-      if (s + 1 < nst) us.load(p.scales, p.N, p.ng, row_w0, g0 + (s + 1) * GPS, min(GPS, ngc - (s + 1) * GPS), lane);
+      if (s + 2 < nst) load_scales(us, s + 2);
       if (!mbar_wait(&full[slot], (s / p.S) & 1) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
       const uint8_t* st = smem + static_cast<size_t>(slot) * p.stage_bytes;
 #pragma unroll
@@ -1117,6 +1123,10 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
       }
       __syncwarp();
       if (lane == 0) mbar_arrive(&empty[slot]);
+    };
+    for (int s = 0; s < nst; s += 2) {
+      stage(s, usA);
+      if (s + 1 < nst) stage(s + 1, usB);
     }
     const int rg = row_w0 + g, rg8 = rg + 8;
     const int rl = 16 * warp + g;
@@ -1397,7 +1407,7 @@ struct SPlan {
   bool ok;
   int nw, ks, gpc, S, n_rb;
   size_t smem;
-  uint32_t stage_bytes, xh_off, vp_off, sw_off, red_off, bar_off, xs_off;
+  uint32_t stage_bytes, xh_off, vp_off, sc_off, red_off, bar_off, xs_off;
 };
 
 // Shared-memory layout (offsets from the 1024-aligned base): ring, x^, VP, per-warp scales, partial
@@ -1407,7 +1417,7 @@ bool stream_layout(SPlan& pl, int B, int G) {
   pl.stage_bytes = static_cast<uint32_t>(BR) * 128u;
   const size_t xh = align256(static_cast<size_t>(pl.gpc) * G * B * 2);
   const size_t vp = align256(static_cast<size_t>(pl.gpc) * vp_row(B) * 4);
-  const size_t sw = align256(static_cast<size_t>(pl.nw) * GPS * 16 * 2);
+  const size_t sw = align256(static_cast<size_t>(pl.nw) * GPS * 16 * 2);  // per-warp scale staging
   const size_t red = align256(static_cast<size_t>(pl.ks - 1) * BR * B * 4);
   const size_t xs = B <= kStreamFuseMaxB ? align256(static_cast<size_t>(pl.gpc) * G * B * 2) : 0;
   const size_t bars = 256;
@@ -1419,7 +1429,7 @@ bool stream_layout(SPlan& pl, int B, int G) {
   off += xh;
   pl.vp_off = static_cast<uint32_t>(off);
   off += vp;
-  pl.sw_off = static_cast<uint32_t>(off);
+  pl.sc_off = static_cast<uint32_t>(off);
   off += sw;
   pl.red_off = static_cast<uint32_t>(off);
   off += red;
@@ -1581,7 +1591,7 @@ cudaError_t launch_stream(const tq_desc* d, const SPlan& pl, const uint32_t* cod
   sp.stage_bytes = pl.stage_bytes;
   sp.xh_off = pl.xh_off;
   sp.vp_off = pl.vp_off;
-  sp.sw_off = pl.sw_off;
+  sp.sc_off = pl.sc_off;
   sp.red_off = pl.red_off;
   sp.bar_off = pl.bar_off;
   sp.xs_off = pl.xs_off;
