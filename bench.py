@@ -309,6 +309,13 @@ def traffic_from_profiles(kernel_key: str):
     return None
 
 
+def traffic_per_step(packing, batch, layers):
+    """ncu DRAM bytes of one layer (profiles/ncu_traffic.txt) x layers, or None."""
+    per_layer = traffic_from_profiles(
+        f"dense_decode_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_stacked_per_layer")
+    return None if per_layer is None else per_layer * layers
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ternary_weight_quantized_unpack_b300", "csrc")
@@ -516,10 +523,10 @@ def run_tq(args, rank, world, local):
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic_from_profiles(
-                         f"dense_decode_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_stacked_per_layer"),
-                     "traffic_unit": "DRAM bytes per layer (4 calls: prep + decode kernels), ncu",
-                     "kernel": "tq_gemv calls (activation prep kernel + decode GEMV kernel), per-call CUDA events",
+                     "traffic": traffic_per_step(packing, batch, args.layers),
+                     "traffic_unit": "DRAM bytes per step: ncu bytes of one layer's launches x layers",
+                     "kernel": "tq_gemv calls (decode GEMV kernel, plus the activation prep kernel above batch 2 "
+                               "or for base-3), per-call CUDA events",
                      "algorithmic_bytes_per_step": st.bytes_per_step, "calls_per_step": len(st.calls),
                      "algorithmic_bytes_per_layer": st.bytes_per_step // max(1, args.layers),
                      "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},

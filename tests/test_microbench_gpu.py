@@ -34,3 +34,9 @@ def test_decode_loop(tmp_path):
 def test_load_pattern(tmp_path):
     out = _build_and_run(tmp_path, "load_pattern", ["-lcuda"])
     assert out.count("us per launch") == 7, out
+
+
+@pytest.mark.gpu
+def test_mma_fp8_vs_f16(tmp_path):
+    out = _build_and_run(tmp_path, "mma_fp8_vs_f16")
+    assert out.count("weights/clk/SM") == 6 and "accuracy" in out, out
