@@ -956,7 +956,6 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.bar_off);
   uint64_t* empty = full + p.S;
   uint64_t* xbar = empty + p.S;
-  uint64_t* rbar = xbar + 1;  // cluster leader: partial sums of the other ranks have arrived
   const int ks = static_cast<int>(gridDim.y);
   if (threadIdx.x == 0) {
     for (int i = 0; i < p.S; ++i) {
@@ -964,7 +963,6 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
       mbar_init(&empty[i], nw);
     }
     mbar_init(xbar, 1);
-    mbar_init(rbar, ks > 1 ? (ks - 1) * 32 * nw : 1);
     fence_mbar_init();
   }
   __syncthreads();
@@ -1131,8 +1129,8 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
     const int rg = row_w0 + g, rg8 = rg + 8;
     const int rl = 16 * warp + g;
     if (ks > 1 && blockIdx.y != 0) {
-      // push the partial sums into the cluster leader's buffer (slot rank - 1), then arrive on its
-      // barrier; the leader adds them to its own in rank order
+      // push the partial sums into the cluster leader's buffer (slot rank - 1), then arrive on the
+      // cluster barrier (release); the leader waits on it and adds them to its own in rank order
       cluster_wait();
       const uint32_t slot0 = smem_addr(smem + p.red_off) + 4u * static_cast<uint32_t>((blockIdx.y - 1) * BR * p.B);
       const uint32_t base = cluster_map(slot0, 0);
@@ -1148,11 +1146,12 @@ __global__ void __launch_bounds__(17 * 32) gemv_2b_stream_kernel(const __grid_co
           st_cluster_f32(base + 4u * static_cast<uint32_t>((rl + 8) * p.B + b + 1), acc[t][3]);
         }
       }
-      mbar_arrive_remote(cluster_map(smem_addr(rbar), 0));
+      cluster_arrive_release();
     } else {
       if (ks > 1) {
         cluster_wait();
-        if (!mbar_wait_cluster(rbar, 0) && lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        cluster_arrive_release();  // second phase: complete once every rank has pushed (or exited)
+        cluster_wait();
         const float* red = reinterpret_cast<const float*>(smem + p.red_off);
         const int E = BR * p.B;
 #pragma unroll
