@@ -61,11 +61,12 @@ constexpr int kMaxCluster = 8;
 // so HBM streams this call's weights while the preceding kernels finish.
 constexpr bool kPrefetchL2 = true;
 // Stream kernel: up to this batch the CTAs transform their own K-range of the activations (no prep
-// kernel).  kEarlyStages: stages of the code ring issued before the dependent-launch wait (static
+// kernel; measured on the 64-layer 2-bit stream: batch 4 4.39 -> 3.86 ms per token, batch 8 no
+// better than the prep kernel, 5.11 -> 5.20 ms).  kEarlyStages: stages of the code ring issued before the dependent-launch wait (static
 // weights).  Measured on the 64-layer batch-1 stream: 0 (activations requested before any weight
 // stage) 3.43 ms per token, 1: 3.47 ms, 2: 3.72 ms; with static weights only the scales are read
 // before the wait.
-constexpr int kStreamFuseMaxB = 2;
+constexpr int kStreamFuseMaxB = 4;
 constexpr int kEarlyStages = 0;
 constexpr uint32_t kLutWords = 2u * 243u * 32u;
 constexpr uint32_t kLutBytes = kLutWords * 4u;
