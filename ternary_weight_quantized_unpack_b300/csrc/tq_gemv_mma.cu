@@ -889,12 +889,13 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
 // 2-bit dense decode, streamed ("stream" kernel).  One CTA per SM: nw consumer warps, each owning a
 // 16-row slab of the CTA's 16*nw-row block, and one producer warp whose elected lane streams the
 // block's codes through a ring of S shared-memory stages with 2-D TMA (32 words = 512 trits x 16*nw
-// rows per stage, 128-byte swizzle).  With static weights the ring is filled before the
-// dependent-launch wait, so the first stages of a call arrive while the preceding kernel finishes.
-// K may be split over the ks CTAs of a cluster (partial sums meet through distributed shared
-// memory in rank order).  The activations of the CTA's K-range are transformed in the CTA (small
-// batches) or bulk-copied from the prep kernel's output.  Decode, MMA and scale folding are those of
-// the shared-row layout above.
+// rows per stage, 128-byte swizzle, L2 evict-first).  The activations are requested first after the
+// dependent-launch wait (kEarlyStages code stages may go out before it with static weights).
+// K may be split over the ks CTAs of a cluster: the other ranks push their partial sums into the
+// leader's shared memory and arrive on the cluster barrier; the leader adds them in rank order.
+// The activations of the CTA's K-range are transformed in the CTA (batch <= kStreamFuseMaxB) or
+// bulk-copied from the prep kernel's output.  Decode, MMA and scale folding are those of the
+// shared-row layout above.
 // ---------------------------------------------------------------------------------------------
 struct SParams {
   const uint16_t* scales;
