@@ -237,7 +237,8 @@ __device__ __forceinline__ void prep_block(const uint16_t* __restrict__ x, const
   }
 }
 
-template <int PACK, int G>
+// MAXB: the smallest of 1, 2, 4, 8, 16 that holds the batch (the per-row loops are unrolled over it).
+template <int PACK, int G, int MAXB>
 __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ PrepParams p) {
   pdl_launch_dependents();
   pdl_wait();  // x may be the output of the preceding kernel; the previous call may still read xh
@@ -257,7 +258,7 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
     xh += static_cast<size_t>(z) * p.xh_cstride;
     vpo += static_cast<size_t>(z) * p.vp_cstride;
   }
-  prep_block<PACK, G, kMaxBatch>(p.x, p.gu, p.h_out, p.status, p.K, p.B, p.apply, p.mode, p.topk, blk, 0, count, rows,
+  prep_block<PACK, G, MAXB>(p.x, p.gu, p.h_out, p.status, p.K, p.B, p.apply, p.mode, p.topk, blk, 0, count, rows,
                                  xh, vpo, lane);
 }
 
@@ -1368,7 +1369,11 @@ cudaError_t launch_prep(const PrepParams& pp, cudaStream_t s, int zdim) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G>, pp);
+  if (pp.B <= 1) return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G, 1>, pp);
+  if (pp.B <= 2) return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G, 2>, pp);
+  if (pp.B <= 4) return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G, 4>, pp);
+  if (pp.B <= 8) return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G, 8>, pp);
+  return cudaLaunchKernelEx(&cfg, gemv_prep_kernel<PACK, G, kMaxBatch>, pp);
 }
 
 // The decode kernel for a shape: packing, group and batch tiles.
