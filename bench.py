@@ -525,7 +525,7 @@ def run_tq(args, rank, world, local):
                      "frac": achieved / peaks["hbm_gbs"],
                      "traffic": traffic_per_step(packing, batch, args.layers),
                      "traffic_unit": "DRAM bytes per step: ncu bytes of one layer's launches x layers",
-                     "kernel": "tq_gemv calls (decode GEMV kernel, plus the activation prep kernel above batch 2 "
+                     "kernel": "tq_gemv calls (decode GEMV kernel, plus the activation prep kernel above batch 4 "
                                "or for base-3), per-call CUDA events",
                      "algorithmic_bytes_per_step": st.bytes_per_step, "calls_per_step": len(st.calls),
                      "algorithmic_bytes_per_layer": st.bytes_per_step // max(1, args.layers),
