@@ -302,8 +302,46 @@ def pin_moe_layer(O):
         assert np.allclose(out["y"][t], acc, rtol=1e-12, atol=1e-12)
 
 
+def pin_silu(O):
+    """silu(z) = z * sigmoid(z), checked against facts of the logistic function that do not restate
+    the formula: sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4 and sigmoid(-ln 3) = 1/4 (so
+    silu(+-ln 3) = +-(3/4) ln 3 and -(1/4) ln 3), silu(z) - silu(-z) = z (because
+    sigmoid(z) + sigmoid(-z) = 1), silu(z) -> z for large z and -> 0 for very negative z, and the
+    slope 1/2 at the origin."""
+    ln3 = math.log(3.0)
+    z = np.array([0.0, ln3, -ln3, 1.0, -2.5, 7.0])
+    v = O.silu(z)
+    assert v[0] == 0.0
+    assert abs(v[1] - 0.75 * ln3) <= 1e-15 and abs(v[2] + 0.25 * ln3) <= 1e-15
+    assert np.allclose(O.silu(z) - O.silu(-z), z, rtol=0, atol=1e-14)
+    assert abs(O.silu(np.array([40.0]))[0] - 40.0) <= 40.0 * 1e-15
+    assert 0 > O.silu(np.array([-40.0]))[0] > -1e-15
+    h = 1e-8
+    assert abs(O.silu(np.array([h]))[0] / h - 0.5) < 1e-7
+
+
+def pin_moe_down_from_h(O):
+    """The down-projection + combine stage restated from a given h (the form the GPU test uses to
+    check that stage on the GPU's own h) equals the full layer when given the layer's own h."""
+    r = rng(12)
+    E, H, F, group, T, k = 6, 256, 128, 64, 4, 3
+    gu_c, gu_s, d_c, d_s, x = _moe_case(O, r, E, H, F, group, T)
+    logits = r.standard_normal((T, E)).astype(np.float32)
+    out = O.moe_layer(logits, x, gu_c, gu_s, d_c, d_s, H, F, group, O.PACK_B3, topk=k)
+    downs = {e: (d_c[e], d_s[e]) for e in range(E)}
+    y, A = O.moe_down_from_h(out["h"], out["idx"], out["gate"], downs, F, group, O.PACK_B3)
+    assert np.allclose(y, out["y"], rtol=1e-12, atol=1e-12)
+    assert np.allclose(A, np.einsum("tj,tjh->th", out["gate"], out["A_d"]), rtol=1e-12, atol=1e-12)
+    # and a single routed slot reduces to one plain ternary linear on FWHT(h)
+    y1, _ = O.moe_down_from_h(out["h"][:1, :1], out["idx"][:1, :1], np.ones((1, 1)), downs, F, group, O.PACK_B3)
+    ref, _, _ = O.ternary_linear(d_c[int(out["idx"][0, 0])], d_s[int(out["idx"][0, 0])], out["h"][0, :1], F, group,
+                                 O.PACK_B3)
+    assert np.allclose(y1, ref, rtol=1e-12, atol=1e-12)
+
+
 PINS = [pin_pack_b3, pin_pack_2b, pin_unpack, pin_format_constants, pin_hadamard, pin_fwht,
-        pin_rotation_identity, pin_contraction_bruteforce, pin_special_cases, pin_moe_route, pin_moe_layer]
+        pin_rotation_identity, pin_contraction_bruteforce, pin_special_cases, pin_moe_route, pin_moe_layer,
+        pin_silu, pin_moe_down_from_h]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -315,7 +353,8 @@ def test_oracle_pin(pin):
 # planted mistakes: each mutant must fail at least one pin
 # ----------------------------------------------------------------------------------------------
 
-ORIG = {k: getattr(O_real, k) for k in ("pack", "unpack", "hadamard", "block_fwht", "moe_route", "dequant")}
+ORIG = {k: getattr(O_real, k) for k in ("pack", "unpack", "hadamard", "block_fwht", "moe_route", "dequant",
+                                        "silu", "moe_down_from_h")}
 
 
 def _pack_msd_first(trits, packing):
@@ -361,6 +400,14 @@ def _dequant_sign_flipped(trits, scales, group):
     return -ORIG["dequant"](trits, scales, group)
 
 
+def _silu_mirrored(z):
+    return z / (1.0 + np.exp(z))    # z * sigmoid(-z)
+
+
+def _down_without_gates(h, idx, gate, experts_down, F, group, packing, fwht_block=128):
+    return ORIG["moe_down_from_h"](h, idx, np.ones_like(gate), experts_down, F, group, packing, fwht_block)
+
+
 def _unpack_off_by_one(codes, K, packing):
     t, bad = ORIG["unpack"](codes, K, packing)
     return np.roll(t, 1, axis=1), bad
@@ -376,6 +423,8 @@ MUTANTS = {
     "scales repeated wrongly": dict(dequant=_dequant_tiled),
     "weight sign flipped": dict(dequant=_dequant_sign_flipped),
     "unpack shifted by one trit": dict(unpack=_unpack_off_by_one),
+    "silu with sigmoid(-z)": dict(silu=_silu_mirrored),
+    "down stage ignores the gates": dict(moe_down_from_h=_down_without_gates),
 }
 
 
