@@ -3,16 +3,16 @@
  *
  * The method (sources cited by page title and section):
  *   - Weights are ternary t in {-1, 0, +1} times a scale; one FP16 scale per group of weights
- *     (cosmocat.dev "27B 大模型塞进 5.9GB：三值量化，凭什么「不崩」？", section 一 and section 二 ②:
- *     128 weights per group; tantan.ink/?p=490, install command: the MoE build uses "g64").
+ *     ("27B 大模型塞进 5.9GB：三值量化，凭什么「不崩」？", section 一 and section 二 ②:
+ *     128 weights per group; the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, install command: the MoE build uses "g64").
  *   - Trits are stored packed: base-3, 20 trits per 32-bit integer, about 1.6 bits per weight
- *     (tantan.ink/?p=490, section "为什么 1.58bit 没变成乱码", point 3), or 2 bits per trit.
+ *     (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, section "为什么 1.58bit 没变成乱码", point 3), or 2 bits per trit.
  *   - Weights were Hadamard-rotated offline; at inference the matching fast transform, O(n log n),
- *     is applied to the activations (cosmocat.dev, section 二 ①).
+ *     is applied to the activations ("27B 大模型塞进 5.9GB", section 二 ①).
  *   - Kernels compute directly on the packed format; decompressing to floats in memory would give
- *     back the savings (cosmocat.dev, section 二 ③).
+ *     back the savings ("27B 大模型塞进 5.9GB", section 二 ③).
  *   - MoE: 256 routed experts, 8 active per token, router gate in full precision
- *     (tantan.ink/?p=490, point 1).
+ *     (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, section "为什么 1.58bit 没变成乱码", point 1).
  *
  * Conventions for every entry point:
  *   - Data pointers are DEVICE pointers owned by the caller.  The library allocates nothing and
@@ -65,7 +65,7 @@ typedef struct {
   int32_t group;      /* weights per FP16 scale along K: 64 or 128 */
   int32_t packing;    /* tq_packing */
   int32_t fwht_block; /* 128: apply the block Walsh-Hadamard transform to the input; 0: input used as given */
-  int32_t flags;      /* 0, or TQ_STATIC_WEIGHTS (tq_gemv only; other entry points ignore it) */
+  int32_t flags;      /* 0, or TQ_STATIC_WEIGHTS (tq_gemv and tq_gemv_noalloc only; other entry points ignore it) */
 } tq_desc;
 
 /* Promise that no kernel still running on the stream when tq_gemv is called writes this matrix's
@@ -76,10 +76,10 @@ typedef struct {
 
 /* ---- format sizes (host only, no device access) ------------------------------------------------
  * Row pitch in uint32 words: base-3 roundup(ceil(K/20), 4), 2-bit roundup(ceil(K/16), 4).
- * (tantan.ink/?p=490, point 3: 20 trits per 32-bit word.)  Return 0 for an invalid descriptor. */
+ * (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, point 3: 20 trits per 32-bit word.)  Return 0 for an invalid descriptor. */
 size_t tq_row_pitch_words(const tq_desc* d);
 size_t tq_packed_bytes(const tq_desc* d);      /* N * pitch * 4 */
-size_t tq_scale_bytes(const tq_desc* d);       /* N * ceil(K/group) * 2 (cosmocat.dev, section 二 ②) */
+size_t tq_scale_bytes(const tq_desc* d);       /* N * ceil(K/group) * 2 ("27B 大模型塞进 5.9GB", section 二 ②) */
 
 /* ---- tq_pack: int8 trits [N][K] -> codes [N][P] --------------------------------------------------
  * Packs row-contiguous trits across group boundaries; trits past K and whole padding words hold
@@ -98,7 +98,7 @@ tq_status tq_unpack(const tq_desc* d, const uint32_t* codes, int8_t* trits, int3
 
 /* ---- tq_fwht: x~[r, 128b + i] = sum_c H[i][c] x[r, 128b + c] / sqrt(block) -----------------------
  * Block Walsh-Hadamard transform (Sylvester order) of each row of x (bf16 [rows][K]); block must be
- * 128 and K a multiple of it (cosmocat.dev, section 二 ①).  out_fp16 = 0: out is float [rows][K];
+ * 128 and K a multiple of it ("27B 大模型塞进 5.9GB", section 二 ①).  out_fp16 = 0: out is float [rows][K];
  * out_fp16 = 1: out is FP16 [rows][K] (values beyond the FP16 range record TQ_ERR_RANGE). */
 tq_status tq_fwht(const uint16_t* x, void* out, int out_fp16, int rows, int K, int block, void* stream);
 
@@ -125,12 +125,14 @@ int tq_gemv_kernel_count(const tq_desc* d, int batch);
  * tq_gemv_workspace_bytes(d, batch) exceeds 1 MiB (at batch 16: K above 31488 for groups of 64, above
  * 32128 for groups of 128) return TQ_ERR_WORKSPACE before anything is launched.  The first call with a device current looks up that
  * device's array; make it before any stream capture.  Nothing has to be zeroed first.  All calls on a
- * device share the array: calls whose kernels overlap in time race on it, so serialise them. */
+ * device share the array: calls whose kernels overlap in time race on it, so serialise them.  The
+ * looked-up address is kept for the life of the process: do not use the library across a
+ * cudaDeviceReset() (the device copy of the array may move). */
 tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                           int batch, float* y, void* stream);
 
 /* ---- tq_moe_route: top-k experts per token --------------------------------------------------------
- * logits: float [T][E] (router at full precision, tantan.ink/?p=490 point 1).  idx: int32 [T][topk]
+ * logits: float [T][E] (router at full precision, the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, point 1).  idx: int32 [T][topk]
  * in the order (logit descending, expert index ascending); gate: float [T][topk] =
  * softmax over the topk chosen logits.  E <= 256, topk <= 8 (the pages' top-8 of 256). */
 tq_status tq_moe_route(const float* logits, int T, int E, int topk, int32_t* idx, float* gate, void* stream);
@@ -160,6 +162,8 @@ tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scale
                   int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- status ---------------------------------------------------------------------------------------
+ * The address of each device's status word is looked up once per process; do not use the library
+ * across a cudaDeviceReset().
  * Reads the device status word of the current device (the first error any kernel recorded since the
  * last read), stores it in *status (TQ_OK if none) and clears it.  This call synchronizes the device. */
 tq_status tq_device_status(int32_t* status);

@@ -10,11 +10,11 @@ pages in the order they give it.  No blocking, fusion or reordering beyond the d
 library primitives used as single steps are ``numpy.matmul`` and ``numpy.argsort``.
 
 Sources (cited by title and section):
-  [TT]  tantan.ink/?p=490, the 1.58-bit TurboQuant-MLX build of Qwen3.6-35B-A3B on a 16 GB Mac,
+  [TT]  the page on the 1.58-bit TurboQuant-MLX build of Qwen3.6-35B-A3B on a 16 GB Mac,
         section "为什么 1.58bit 没变成乱码" (why 1.58 bit does not become gibberish), points 1-3.
-  [CC]  cosmocat.dev, "27B 大模型塞进 5.9GB：三值量化，凭什么「不崩」？",
+  [CC]  "27B 大模型塞进 5.9GB：三值量化，凭什么「不崩」？",
         section 一 (what "ternary" means) and section 二 ①-③ (rotation, group scales, kernels).
-  [NX]  nxmr.cn/news/163630, Ternary-Bonsai2-27B vs GSQ-RCO, §1.1 (ternary = sign + add/sub).
+  [NX]  the Ternary-Bonsai2-27B vs GSQ-RCO comparison page, §1.1 (ternary = sign + add/sub).
 
 Readings where the pages are silent (each is listed in the design notes):
   * base-3 word = little-endian base-3 integer of the digits (t + 1); 20 digits per uint32,

@@ -1,6 +1,6 @@
 // Packing and unpacking of ternary weights.
 //
-// base-3: 20 trits per 32-bit word, word = sum_i (t_i + 1) 3^i (tantan.ink/?p=490, section
+// base-3: 20 trits per 32-bit word, word = sum_i (t_i + 1) 3^i (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, section
 // "为什么 1.58bit 没变成乱码", point 3: base-3 code, 20 ternary indices per 32-bit integer, ~1.6 bpw).
 // 2-bit : 16 trits per word, field (t + 1) at bits 2i; field 3 is not a valid code.
 // Rows are padded to a multiple of 4 words (16 bytes) so every row starts 16-byte aligned; every

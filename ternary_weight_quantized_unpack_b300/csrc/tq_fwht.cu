@@ -1,7 +1,7 @@
 // Block Walsh-Hadamard transform of activations.
 //
 // The weights were rotated by a Hadamard transform before ternarisation; inference applies the
-// matching fast transform to the activations, O(n log n) per block (cosmocat.dev
+// matching fast transform to the activations, O(n log n) per block ("27B 大模型塞进 5.9GB"
 // "27B 大模型塞进 5.9GB：三值量化，凭什么「不崩」？", section 二 ①).  Sylvester (natural) order,
 // orthonormal scaling 1/sqrt(128), block 128 along K.
 //

@@ -17,7 +17,7 @@
 //   warps 2-5  epilogue: tcgen05.ld of a full accumulator, bf16 conversion, stores; then the
 //              accumulator is released, so one tile's epilogue overlaps the next tile's MMAs
 // Every mbarrier wait is bounded; a wait that runs out records TQ_ERR_TIMEOUT and the warp stops.
-// Activations are the block Walsh-Hadamard transform of x in FP16 (cosmocat.dev "27B 大模型塞进
+// Activations are the block Walsh-Hadamard transform of x in FP16 ("27B 大模型塞进
 // 5.9GB", section 二 ①); group scales per 64 or 128 weights (same page, section 二 ②).
 #include <cuda_bf16.h>
 

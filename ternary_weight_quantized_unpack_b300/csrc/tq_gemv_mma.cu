@@ -6,18 +6,20 @@
 //    two FP16 tensor-core operands.  The position factor 2^(8-2i) and the offset t = d - 1 are folded
 //    into the activations: x^ = x~ * 2^-e * 2^(8-2i) and, per group, the accumulator starts at
 //    -2^-16 * sum(x~ 2^-e) (e: exponent of the 128-block, shared by the batch).
-//  * Base-3 words (20 trits per uint32: tantan.ink/?p=490, "为什么 1.58bit 没变成乱码", point 3) are
+//  * Base-3 words (20 trits per uint32: the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, "为什么 1.58bit 没变成乱码", point 3) are
 //    split into four 5-trit chunks by two exact reciprocal multiplies; a 243-entry table (replicated
 //    per lane, conflict-free) places the chunk's digits into those bit fields.
 //  * The multiply-add runs on mma.sync m16n8k16 (FP16 x FP16 -> FP32).  On B300, tcgen05.mma costs
 //    ~120 cycles per K=16 step whatever N is, so with N <= 16 it retires only ~17 trits/cycle/SM;
 //    mma.sync m16n8k16 retires 126, above the ~100 the HBM rate requires.
-//  * Each group of 64 or 128 weights has its own FP16 scale (cosmocat.dev "27B 大模型塞进 5.9GB",
+//  * Each group of 64 or 128 weights has its own FP16 scale ("27B 大模型塞进 5.9GB",
 //    section 二 ②): every MMA covers one group only, and the group's result is folded into the
 //    output with one FMA per element.  The CTA's scales are staged in shared memory and
 //    pre-multiplied by the block factor 2^(16+e).
-//  * The block Walsh-Hadamard transform of the activations (same page, section 二 ①) is computed once
-//    per call by a small prep kernel, straight into the operand layout; every CTA bulk-copies
+//  * The block Walsh-Hadamard transform of the activations (same page, section 二 ①) goes straight
+//    into the operand layout.  The 2-bit stream kernel transforms its own K-range inside each CTA up
+//    to batch 4, and the expert-layer GEMVs do so for chunks of at most 2 tokens; otherwise a small
+//    prep kernel transforms the activations once per call and every CTA bulk-copies
 //    (cp.async.bulk) the slice of its K-range into shared memory.
 //
 // Work split: a CTA holds rs x kl warps: rs row slabs, each split over kl K-lanes of ppl units

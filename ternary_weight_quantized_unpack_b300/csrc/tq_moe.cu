@@ -1,5 +1,5 @@
 // Routed MoE expert layer at decode time: top-k routing of 256 experts (8 active per token, router
-// in full precision - tantan.ink/?p=490, section "为什么 1.58bit 没变成乱码", point 1), then the
+// in full precision - the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, section "为什么 1.58bit 没变成乱码", point 1), then the
 // ternary SwiGLU experts.  The (token, slot) assignments are sorted by expert into chunks of up to
 // 1 / 2 / 4 tokens; the gate/up and down projections run as the decode GEMV kernels over those
 // chunks (blockIdx.z = chunk), so each chunk streams its expert's packed codes once, the prep kernel

@@ -72,3 +72,41 @@ def sample_rows(N, n, seed=0):
     """A spread of rows: first, last, and n random ones (sorted, unique)."""
     r = np.random.Generator(np.random.PCG64(seed)).choice(N, size=min(n, N), replace=False)
     return np.unique(np.concatenate([[0, N - 1], r]))
+
+
+def silu(z):
+    return z / (1 + np.exp(-z))
+
+
+def silu_prime(z):
+    s = 1 / (1 + np.exp(-z))
+    return s * (1 + z * (1 - s))
+
+
+def moe_bounds(out, down_dense, fwht_block):
+    """Tolerances of the expert layer derived from the per-linear bound 1e-3 * A + 1e-5.
+
+    out: the oracle's moe_layer result for the checked tokens; down_dense: expert -> dense W_d
+    (fp64 s * t).  Returns (hb, A_e2e, extra):
+      hb     per-output bound on h = silu(g) * u, propagated from the bounds on g and u through
+             silu (first order plus the second-order term, silu'' <= 1/2) and the product;
+      A_e2e  sum_j gate_j * A_down, the plain down-stage scale;
+      extra  the h bound carried through FWHT (a sum of |.| over each block / sqrt(block)) and |W_d|,
+             weighted by the gates, plus a relative 1e-6 for the gates' own error.
+    """
+    Eg = 1e-3 * out["A_g"] + 1e-5
+    Eu = 1e-3 * out["A_u"] + 1e-5
+    g, u = out["g"], out["u"]
+    hb = np.abs(silu(g)) * Eu + (np.abs(silu_prime(g)) * Eg + 0.25 * Eg ** 2) * (np.abs(u) + Eu) \
+        + 1e-6 * np.abs(out["h"]) + 1e-7
+    T, k, F = hb.shape
+    H = out["y"].shape[1]
+    blk = fwht_block or 1
+    dht = np.repeat(hb.reshape(T, k, -1, blk).sum(axis=3), blk, axis=2) / math.sqrt(blk)
+    extra = np.zeros((T, H))
+    for ti in range(T):
+        for j in range(k):
+            Wd_abs = np.abs(down_dense[int(out["idx"][ti, j])])
+            extra[ti] += out["gate"][ti, j] * (Wd_abs @ dht[ti, j]) + 1e-6 * np.abs(out["y_parts"][ti, j])
+    A_e2e = np.einsum("tj,tjh->th", out["gate"], out["A_d"])
+    return hb, A_e2e, extra
