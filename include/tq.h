@@ -131,6 +131,61 @@ int tq_gemv_kernel_count(const tq_desc* d, int batch);
 tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                           int batch, float* y, void* stream);
 
+/* ---- tq_seq: a decode step (a chain of dependent GEMVs) as one launch ------------------------------
+ * Decoding one token runs every linear of the model once, each on the previous one's output
+ * ("27B 大模型塞进 5.9GB", section 三: single-stream decode of the whole model; section 二 ③: kernels
+ * that compute on the packed ternary format).  tq_seq_run executes calls[0..ncalls-1] in order, with
+ * the result of issuing tq_gemv for each on one stream (same arithmetic and tolerance), in ONE
+ * cooperative kernel launch: every CTA streams its weight tiles continuously across the calls, and
+ * calls are ordered by a grid-wide barrier, so HBM does not go idle between dependent calls.
+ * The input of call j is selected by x_src:
+ *   TQ_SEQ_X_BF16        x: bf16 [batch][K] in device memory (required for call 0);
+ *   TQ_SEQ_X_PREV        the first K entries of each batch row of call j-1's y (needs N_{j-1} >= K);
+ *   TQ_SEQ_X_SWIGLU_PREV silu(y_{j-1}[b][k]) * y_{j-1}[b][K + k] (needs N_{j-1} = 2K: a stacked
+ *                        gate/up projection, gate rows first);
+ *   TQ_SEQ_X_RMS_PREV    the TQ_SEQ_X_PREV input divided by sqrt(mean_k(input^2) + 1e-6) per batch
+ *                        row (RMS normalisation with unit gain, as a pre-norm decoder applies it
+ *                        before its attention and FFN projections).
+ * Then x~ = block FWHT(input) if fwht_block = 128, y[b][n] = sum_k s t x~ (float [batch][N]).
+ * Limits: 2-bit packing; one group size for all calls; K a multiple of 8 * group (each row of scales
+ * a multiple of 16 bytes: they are fetched by TMA); N a multiple of 4; 1 <= batch <= 8; K * batch
+ * small enough for the transformed activations of the widest call to sit in shared memory (K up to
+ * about 40000 at batch 1, 5120 at batch 8); TQ_STATIC_WEIGHTS is implied (weights must not change
+ * while the plan is in use).  A call's y must not be the x of any call, nor the y of the call before
+ * it.  All pointers: device memory, 16-byte aligned.
+ *
+ * tq_seq_create checks the calls and builds a host-side plan (tensor maps of every weight matrix,
+ * work split for the current device); it allocates host memory only.  The plan needs a caller-owned
+ * device workspace of tq_seq_workspace_bytes(plan) bytes (256-byte aligned), filled once by
+ * tq_seq_upload (synchronous: copies the call records, clears the barrier words) and then used by
+ * every tq_seq_run with that plan; tq_seq_run only enqueues the launch (no allocation, no
+ * synchronisation; capturable in a CUDA graph).  Two runs that share a workspace must not overlap.
+ * A bounded wait that runs out records TQ_ERR_TIMEOUT in the device status and leaves the workspace's
+ * barrier words dirty: call tq_seq_upload again before the next run.  The plan is tied to the device
+ * that was current at creation. */
+#define TQ_SEQ_X_BF16 0
+#define TQ_SEQ_X_PREV 1
+#define TQ_SEQ_X_SWIGLU_PREV 2
+#define TQ_SEQ_X_RMS_PREV 3
+
+typedef struct {
+  tq_desc d;               /* N, K, group, packing (TQ_PACK_2BIT), fwht_block; flags ignored */
+  const uint32_t* codes;   /* [N][P] */
+  const uint16_t* scales;  /* [N][K / group] FP16 */
+  int32_t x_src;           /* TQ_SEQ_X_* */
+  const uint16_t* x;       /* bf16 [batch][K] for TQ_SEQ_X_BF16, else ignored */
+  float* y;                /* [batch][N] */
+} tq_seq_call;
+
+typedef struct tq_seq tq_seq;
+
+tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int batch, tq_seq** plan);
+size_t tq_seq_workspace_bytes(const tq_seq* plan);
+tq_status tq_seq_upload(const tq_seq* plan, void* workspace, size_t workspace_bytes);
+tq_status tq_seq_run(const tq_seq* plan, void* workspace, void* stream);
+int tq_seq_kernel_count(const tq_seq* plan);   /* kernels one tq_seq_run launches (1), -1 for NULL */
+void tq_seq_destroy(tq_seq* plan);
+
 /* ---- tq_moe_route: top-k experts per token --------------------------------------------------------
  * logits: float [T][E] (router at full precision, the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, point 1).  idx: int32 [T][topk]
  * in the order (logit descending, expert index ascending); gate: float [T][topk] =

@@ -47,6 +47,17 @@ def desc(N: int, K: int, group: int = 128, packing: int = TQ_PACK_B3, fwht_block
     return tq_desc(N, K, group, packing, fwht_block, flags)
 
 
+TQ_SEQ_X_BF16 = 0
+TQ_SEQ_X_PREV = 1
+TQ_SEQ_X_SWIGLU_PREV = 2
+TQ_SEQ_X_RMS_PREV = 3
+
+
+class tq_seq_call(ctypes.Structure):
+    _fields_ = [("d", tq_desc), ("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p), ("x_src", ctypes.c_int32),
+                ("x", ctypes.c_void_p), ("y", ctypes.c_void_p)]
+
+
 _P = ctypes.c_void_p
 _SZ = ctypes.c_size_t
 _I = ctypes.c_int
@@ -67,6 +78,12 @@ _SIGS = {
     "tq_moe_gemv": (_I, [_D, _D, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tq_gemm_workspace_bytes": (_SZ, [_D, _I]),
     "tq_gemm": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+    "tq_seq_create": (_I, [ctypes.POINTER(tq_seq_call), _I, _I, ctypes.POINTER(ctypes.c_void_p)]),
+    "tq_seq_workspace_bytes": (_SZ, [_P]),
+    "tq_seq_upload": (_I, [_P, _P, _SZ]),
+    "tq_seq_run": (_I, [_P, _P, _P]),
+    "tq_seq_kernel_count": (_I, [_P]),
+    "tq_seq_destroy": (None, [_P]),
     "tq_device_status": (_I, [ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [_I]),
     "tq_last_cuda_error": (_I, []),
@@ -244,6 +261,61 @@ def tq_gemm(d: tq_desc, codes, scales, x, y=None, workspace=None, stream=None) -
     _check(lib().tq_gemm(ctypes.byref(d), _ptr(codes), _ptr(scales), _ptr(x), M, _ptr(y), _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream)), "tq_gemm")
     return y
+
+
+# ---- decode step: a chain of GEMVs in one launch ---------------------------------------------------
+
+def tq_seq_create(calls, batch: int) -> ctypes.c_void_p:
+    """calls: sequence of (desc, codes, scales, x_src, x or None, y) -> opaque plan handle."""
+    arr = (tq_seq_call * len(calls))()
+    for i, (d, codes, scales, x_src, x, y) in enumerate(calls):
+        arr[i] = tq_seq_call(d, _ptr(codes), _ptr(scales), x_src, _ptr(x), _ptr(y))
+    h = ctypes.c_void_p()
+    _check(lib().tq_seq_create(arr, len(calls), batch, ctypes.byref(h)), "tq_seq_create")
+    return h
+
+
+def tq_seq_workspace_bytes(plan) -> int:
+    return lib().tq_seq_workspace_bytes(plan)
+
+
+def tq_seq_upload(plan, workspace: torch.Tensor):
+    _check(lib().tq_seq_upload(plan, _ptr(workspace), workspace.numel() * workspace.element_size()), "tq_seq_upload")
+
+
+def tq_seq_run(plan, workspace: torch.Tensor, stream=None):
+    _check(lib().tq_seq_run(plan, _ptr(workspace), _stream(stream)), "tq_seq_run")
+
+
+def tq_seq_kernel_count(plan) -> int:
+    return lib().tq_seq_kernel_count(plan)
+
+
+def tq_seq_destroy(plan):
+    lib().tq_seq_destroy(plan)
+
+
+class SeqPlan:
+    """A decode step (a chain of 2-bit GEMVs) prepared once and run with one launch per call of run().
+
+    calls: list of (desc, codes, scales, x_src, x, y) as tq_seq_call; the tensors are kept alive by
+    the plan.  The workspace is allocated here with torch unless one is given."""
+
+    def __init__(self, calls, batch: int, workspace: torch.Tensor | None = None):
+        self._keep = [t for c in calls for t in c[1:] if isinstance(t, torch.Tensor)]
+        self.handle = tq_seq_create(calls, batch)
+        nbytes = tq_seq_workspace_bytes(self.handle)
+        self.workspace = workspace if workspace is not None else _ws(nbytes, calls[0][1].device)
+        tq_seq_upload(self.handle, self.workspace)
+
+    def run(self, stream=None):
+        tq_seq_run(self.handle, self.workspace, stream)
+
+    def __del__(self):
+        h = getattr(self, "handle", None)
+        if h is not None and _lib is not None:
+            _lib.tq_seq_destroy(h)
+            self.handle = None
 
 
 def tq_device_status() -> int:

@@ -1,0 +1,971 @@
+// Decode step: a sequence of dependent 2-bit ternary GEMVs in one persistent launch.
+//
+// Decoding one token runs every linear of the model once, each on the previous one's output.  Issued
+// as separate kernels, every call pays a launch, an activation fetch and transform, and a tail in
+// which the weight stream stops.  Here one cooperative launch (one CTA per SM, all resident) runs the
+// whole chain:
+//
+//  * Every warp streams its own weight tiles with 2-D TMA (32 rows x 32 code words = 512 trits of
+//    each row, 128-byte swizzle, plus the matching 32 x 8 FP16 scales) into a private ring of
+//    shared-memory stages.  The ring runs ahead across call boundaries: while the grid waits on a
+//    barrier and the next input is being transformed, the next call's weights are already in flight.
+//  * Calls are ordered by one grid-wide barrier each (a counter in the workspace, bounded wait).
+//  * Work split, K-major: the items (32-row unit ru, 512-trit K slice ku) of a call are ordered by
+//    ku, then ru, and divided into equal contiguous ranges, one per CTA (and each into ranges for
+//    its warps).  A CTA therefore works on one or two K slices of many row units: it transforms only
+//    the activations of its own slices, and every item writes its own partial sums (32 rows x batch)
+//    to the workspace.  Whoever reads a call's output afterwards - the next call's input transform,
+//    and the CTA that writes the final y after the barrier - adds the partial sums of the K slices
+//    in ku order, so results do not depend on timing.
+//  * Decode and multiply-add are those of the 2-bit decode GEMV: a digit d = t + 1 in mantissa bits
+//    2i of an FP16 half is the subnormal d * 2^(2i-24), one LOP3 per operand register, mma.sync
+//    m16n8k16 with FP32 accumulation.  Each group of 64 or 128 weights has its own FP16 scale
+//    ("27B 大模型塞进 5.9GB", section 二 ②); every MMA covers one group.  The MMA's eight columns are
+//    shared by batch rows and groups: column c holds group (c / Bp) of the cycle for batch row
+//    c % Bp, so at batch 1 four (group 128) or eight (group 64) groups accumulate side by side and
+//    the scale is folded once per cycle rather than once per group.
+//  * The input of each call is the block Walsh-Hadamard transform (same page, section 二 ①) of a bf16
+//    vector, of the previous call's output, of that output divided by its root mean square (the
+//    normalisation a pre-norm decoder applies before its attention and FFN projections), or of
+//    silu(gate) * up of the previous call's output (the SwiGLU of a stacked gate/up projection).
+//    The RMS factor is a per-call scalar: the call computes W * FWHT(input) and its readers multiply
+//    by 1 / rms, formed from per-block sums of squares the input transform stores.
+#include <algorithm>
+#include <cstring>
+#include <new>
+#include <vector>
+
+#include "tq_internal.cuh"
+#include "tq_kernels.cuh"
+#include "tq_sm100.cuh"
+#include "tq_tmap.cuh"
+
+namespace tq {
+namespace seq {
+
+using namespace sm100;
+
+constexpr int kNW = 12;                        // warps per CTA
+// Ring stages per warp: three while the batch is small, two when the staging of eight batch rows needs
+// the shared memory.
+__host__ __device__ constexpr int ring_depth(int Bp) { return Bp <= 2 ? 3 : 2; }
+constexpr int kGatherKu = 12;                  // partial sums one thread adds in one go
+constexpr int kRows = 32;                      // rows per item: two 16-row MMA slabs
+constexpr int kItemTrits = 512;                // trits per item along K: 32 code words of a row
+constexpr uint32_t kCodeStage = kRows * 128u;  // one item's codes: 4 KB (128-byte swizzled rows)
+constexpr uint32_t kScaleStage = kRows * 16u;  // 8 FP16 scales per row: 512 B
+constexpr uint32_t kStageBytes = kCodeStage + kScaleStage;
+constexpr size_t kSmemLimit = 227 * 1024;
+constexpr float kRmsEps = 1e-6f;  // RMS normalisation of an input: x / sqrt(mean(x^2) + eps)
+
+// Device copy of one call; 128-byte aligned, tensor maps first (they must be 64-byte aligned).
+struct alignas(128) CallDev {
+  CUtensorMap tm_codes;   // codes [N][P] uint32, box {32 words, 32 rows}, 128-byte swizzle
+  CUtensorMap tm_scales;  // scales [N][ng] FP16, box {8 groups, 32 rows}
+  const uint16_t* x;      // mode 0: bf16 [B][K]
+  float* y;               // [B][N]
+  int T;                  // items = nru * nku (T * grid < 2^31)
+  int N, K, ng, mode, apply;
+  int nru, nku, gp;       // 32-row units, 512-trit K slices, CTAs taking part
+};
+static_assert(sizeof(CallDev) % 128 == 0, "call records are 128-byte aligned");
+
+// The fields of a call the kernel reads repeatedly, kept in registers.
+struct CallLite {
+  const uint16_t* x;
+  float* y;
+  int T, N, K, ng, mode, apply, nru, nku, gp;
+  __device__ __forceinline__ explicit CallLite(const CallDev& c)
+      : x(c.x), y(c.y), T(c.T), N(c.N), K(c.K), ng(c.ng), mode(c.mode), apply(c.apply), nru(c.nru), nku(c.nku),
+        gp(c.gp) {}
+};
+
+struct Params {
+  const CallDev* calls;
+  int ncalls, B;
+  int* status;
+  unsigned* sync;         // [0]: barrier arrivals, [1]: CTAs that have exited
+  float* part;            // partial sums: [2][items][Bp][32] (parity of the call)
+  float* ssq;             // per 128-block sums of squares of an RMS-normalised input: [2][blocks][Bp]
+  size_t part_stride;     // floats per parity of part
+  int ssq_stride;         // floats per parity of ssq
+  int nkc;                // K slices one CTA may cover (x^ capacity)
+  int stage_floats;       // capacity of the gather staging buffer
+  uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc, off_stage;
+};
+
+// ---- static work split (K-major) ---------------------------------------------------------------
+__host__ __device__ __forceinline__ int cta_start(int T, int gp, int cta) {
+  return static_cast<int>(static_cast<unsigned>(T) * static_cast<unsigned>(cta) / static_cast<unsigned>(gp));
+}
+
+// ---- waits ---------------------------------------------------------------------------------------
+__device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
+  unsigned v;
+  asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// Grid barrier number k (after call k), in two halves so that work that does not depend on it can
+// run in between: grid_arrive (every thread; thread 0 arrives once this CTA's writes are visible) and
+// grid_wait (every thread; thread 0 waits until every CTA has arrived, false if kWaitNs passed first).
+__device__ __forceinline__ void grid_arrive(unsigned* sync) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    atomicAdd(sync, 1u);
+  }
+}
+__device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag) {
+  if (threadIdx.x == 0) {
+    *flag = 1;
+    const unsigned target = (k + 1) * gridDim.x;
+    if (ld_acquire(sync) < target) {
+      const uint64_t t0 = global_timer_ns();
+      for (uint32_t i = 0;; ++i) {
+        if (ld_acquire(sync) >= target) break;
+        if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) {
+          *flag = 0;
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  return *flag != 0;
+}
+
+// ---- reading a previous call's output ---------------------------------------------------------
+// Its output scale for batch row b: 1 / rms of its own input (RMS mode), else 1.  One warp; the sum
+// of the per-block sums of squares is taken in a fixed order, so every CTA gets the same bits.
+__device__ __forceinline__ float out_scale_warp(const CallLite& c, const float* ssq, int Bp, int b, int lane) {
+  if (c.mode != 3) return 1.f;
+  float t = 0.f;
+  const int nblk = c.K / kFwhtBlock;
+  for (int k = lane; k < nblk; k += 32) t += __ldcg(ssq + k * Bp + b);
+  t = warp_sum(t);
+  return rsqrtf(t / static_cast<float>(c.K) + kRmsEps);
+}
+
+// ---- gathering a finished call's output --------------------------------------------------------
+// Segments are stored one after another: segment sg starts after the rows of the segments before it.
+__host__ __device__ __forceinline__ int seg_offset(const int (&nr)[3], int Bp, int sg) {
+  int o = 0;
+  for (int i = 0; i < sg; ++i) o += nr[i];
+  return o * Bp;
+}
+
+// Rows [r0[sg], r0[sg] + nr[sg]) (multiples of 4) of the finished call pc, for every batch row, are
+// summed from its K slices' partial sums into the staging buffer: segment sg, 4-row chunk c4, batch
+// row b at float4 index c4 * Bp + b.  A group of NSP adjacent lanes shares one chunk: lane s adds the
+// slices [s * per, (s + 1) * per) (all its loads issued before the adds), then the group combines
+// its sums by a fixed butterfly.  The result does not depend on which CTA computes it, and the whole
+// gather costs about one L2 round trip.
+__device__ __forceinline__ void gather(const CallLite& pc, const float* ppart, int B, int Bp, int nseg,
+                                       const int (&r0)[3], const int (&nr)[3], float* stage, int nthreads) {
+  int nsp = 1;
+  while (nsp * kGatherKu < pc.nku) nsp <<= 1;  // lanes per chunk (a power of two up to 32)
+  const int per = (pc.nku + nsp - 1) / nsp;    // slices per lane (<= kGatherKu)
+  const size_t step = static_cast<size_t>(pc.nru) * Bp * kRows;
+  int items[3], total = 0;
+  for (int sg = 0; sg < 3; ++sg) {
+    items[sg] = sg < nseg ? (nr[sg] / 4) * B : 0;
+    total += items[sg];
+  }
+  const int nthr = (total * nsp + 31) & ~31;  // whole warps, so every lane takes part in the shuffles
+  if (static_cast<int>(threadIdx.x) >= nthreads) return;
+  for (int t = threadIdx.x; t < nthr; t += nthreads) {
+    const int s = t % nsp;
+    int u = t / nsp, sg = 0;
+    const bool valid = u < total;
+    if (valid)
+      while (u >= items[sg]) u -= items[sg++];
+    const int b = valid ? u % B : 0, c4 = valid ? u / B : 0;
+    const int k = r0[sg] + 4 * c4;
+    const float* p0 = ppart + (static_cast<size_t>(k >> 5) * Bp + b) * kRows + (k & 31);
+    const int ku0 = s * per;
+    float4 v[kGatherKu];
+#pragma unroll
+    for (int i = 0; i < kGatherKu; ++i)
+      if (valid && i < per && ku0 + i < pc.nku) v[i] = __ldcg(reinterpret_cast<const float4*>(p0 + (ku0 + i) * step));
+    float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < kGatherKu; ++i)
+      if (valid && i < per && ku0 + i < pc.nku) {
+        a.x += v[i].x;
+        a.y += v[i].y;
+        a.z += v[i].z;
+        a.w += v[i].w;
+      }
+    for (int m = 1; m < nsp; m <<= 1) {
+      a.x += __shfl_xor_sync(0xffffffffu, a.x, m);
+      a.y += __shfl_xor_sync(0xffffffffu, a.y, m);
+      a.z += __shfl_xor_sync(0xffffffffu, a.z, m);
+      a.w += __shfl_xor_sync(0xffffffffu, a.w, m);
+    }
+    if (valid && s == 0) reinterpret_cast<float4*>(stage + seg_offset(nr, Bp, sg))[c4 * Bp + b] = a;
+  }
+}
+
+// Rows k..k+3 of the staging segment at soff (k relative to the segment start, a multiple of 4),
+// batch row b.
+__device__ __forceinline__ float4 in_row4(const float* stage, int soff, int Bp, int b, int k, float scale) {
+  float4 a = reinterpret_cast<const float4*>(stage + soff)[(k / 4) * Bp + b];
+  a.x *= scale;
+  a.y *= scale;
+  a.z *= scale;
+  a.w *= scale;
+  return a;
+}
+
+// ---- the activation transform ------------------------------------------------------------------
+// Halves of x^ for batch row b of group gi: [word slot u][pair p][quad thread q][8 halves] = 2G bytes.
+// The half at position h = 4 (m & 1) + 2 (j & 1) + (f >> 3) of the 16-byte chunk (u, p = m >> 1, q)
+// multiplies field f of word WPT * q + u, where j = f & 7 and m = j >> 1: the two B registers of
+// MMA m.  Its value is x~ * 2^-e * 2^(8 - 2 pos), pos = j < 5 ? j : j - 5 (the field's place in the
+// FP16 mantissa), e the exponent of the 128-block and batch row.
+template <int G>
+__device__ __forceinline__ uint32_t xh_offset(int t_in, int& pos) {
+  constexpr int WPT = G / 64;
+  const int wd = t_in >> 4, f = t_in & 15, j = f & 7, m = j >> 1;
+  const int q = wd / WPT, u = wd % WPT, p = m >> 1;
+  const int h = ((m & 1) << 2) | ((j & 1) << 1) | (f >> 3);
+  pos = j < 5 ? j : j - 5;
+  return static_cast<uint32_t>((((u * 2 + p) * 4 + q) << 4) + (h << 1));
+}
+
+__device__ __forceinline__ float silu_f(float z) { return z / (1.f + __expf(-z)); }
+
+// Per-lane constants of the x^ layout (the same for every block): byte offsets of the lane's four
+// values in a group's block of halves, and the position factors 2^(8 - 2 pos) and 2^(2 pos - 8).
+template <int G>
+struct LaneLayout {
+  uint32_t off[4];
+  float up[4], dn[4];
+  __device__ __forceinline__ explicit LaneLayout(int lane) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      int pos;
+      off[i] = xh_offset<G>((4 * lane + i) % G, pos);
+      up[i] = __int_as_float((127 + 8 - 2 * pos) << 23);
+      dn[i] = __int_as_float((127 - 8 + 2 * pos) << 23);
+    }
+  }
+};
+
+// x^ and V / F of one 128-block (absolute index blk, local group index lg0 of its first group) for
+// all batch rows; one warp.  ssq: RMS mode, where the block's sums of squares go (global).
+template <int G, int BP>
+__device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, const float* stage, int krow0, int krow_n, const float (&pscale)[BP], int blk, int lg0,
+                                           const LaneLayout<G>& L, uint8_t* xh, float* V, float* Fv, float* ssq,
+                                           int lane) {
+  const int k0 = blk * kFwhtBlock + 4 * lane;
+  float v[BP][4];
+#pragma unroll
+  for (int b = 0; b < BP; ++b) {
+    v[b][0] = v[b][1] = v[b][2] = v[b][3] = 0.f;
+    if (b >= p.B) continue;
+    if (c.mode == 0) {
+      const uint2 raw = __ldcg(reinterpret_cast<const uint2*>(c.x + static_cast<size_t>(b) * c.K + k0));
+      v[b][0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
+      v[b][1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
+      v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
+      v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
+    } else if (c.mode == 2) {
+      const float4 g4 = in_row4(stage, 0, BP, b, k0 - krow0, pscale[b]);
+      const float4 u4 = in_row4(stage, krow_n * BP, BP, b, k0 - krow0, pscale[b]);
+      v[b][0] = silu_f(g4.x) * u4.x;
+      v[b][1] = silu_f(g4.y) * u4.y;
+      v[b][2] = silu_f(g4.z) * u4.z;
+      v[b][3] = silu_f(g4.w) * u4.w;
+    } else {
+      const float4 a = in_row4(stage, 0, BP, b, k0 - krow0, pscale[b]);
+      v[b][0] = a.x, v[b][1] = a.y, v[b][2] = a.z, v[b][3] = a.w;
+    }
+  }
+  if (c.mode == 3) {  // sums of squares of the block's input, for the output scale of this call
+#pragma unroll
+    for (int b = 0; b < BP; ++b) {
+      const float t = warp_sum(v[b][0] * v[b][0] + v[b][1] * v[b][1] + v[b][2] * v[b][2] + v[b][3] * v[b][3]);
+      if (lane == 0 && b < p.B) ssq[blk * BP + b] = t;
+    }
+  }
+  if (c.apply) {
+#pragma unroll
+    for (int b = 0; b < BP; ++b)
+      if (b < p.B) fwht128_warp(v[b]);
+  }
+  const float norm = c.apply ? 0.08838834764831845f : 1.f;  // 1 / sqrt(128)
+  const int lg = lg0 + (4 * lane) / G;                      // local group of this lane's values
+#pragma unroll
+  for (int b = 0; b < BP; ++b) {
+    // per batch row: exponent of the block, max |x~| * 2^-e in [64, 128)
+    float mx = fmaxf(fmaxf(fabsf(v[b][0]), fabsf(v[b][1])), fmaxf(fabsf(v[b][2]), fabsf(v[b][3])));
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+    mx *= norm;
+    int e = 0;
+    if (mx > 0.f) {
+      const int ex = (__float_as_int(mx) >> 23) & 0xff;
+      e = (ex == 0 ? -126 : ex - 127) - 6;
+      if (e > 100) {
+        e = 100;
+        if (lane == 0) record_error(p.status, TQ_ERR_RANGE);
+      }
+      e = max(e, -100);
+    }
+    const float down = __int_as_float((127 - e) << 23) * norm;
+    uint8_t* gbase = xh + (static_cast<size_t>(lg) * BP + b) * (2 * G);
+    float vs = 0.f;
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const __half h = __float2half_rn(v[b][i] * down * L.up[i]);
+      *reinterpret_cast<__half*>(gbase + L.off[i]) = h;
+      vs += __half2float(h) * L.dn[i];
+    }
+    constexpr int lanes_per_group = G / 4;
+#pragma unroll
+    for (int o = lanes_per_group / 2; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
+    if ((lane & (lanes_per_group - 1)) == 0) {
+      V[lg * BP + b] = -1.52587890625e-05f * vs;                                   // -2^-16 * sum
+      Fv[lg * BP + b] = b < p.B ? __int_as_float((127 + 16 + e) << 23) : 0.f;  // 2^(16 + e)
+    }
+  }
+}
+
+// ---- MMA -------------------------------------------------------------------------------------------
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                         uint32_t b0, uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+      "{%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+// ---- the kernel ----------------------------------------------------------------------------------
+template <int G, int BP>
+__global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_constant__ Params p) {
+  constexpr int WPT = G / 64;             // code words per quad thread per group per row
+  constexpr int GPI = kItemTrits / G;     // groups per item
+  constexpr int CPG = GPI < 8 / BP ? GPI : 8 / BP;  // groups per accumulation cycle
+  constexpr int NCYC = GPI / CPG;
+  constexpr int BPI = kItemTrits / kFwhtBlock;     // 128-blocks per item
+  constexpr int kD = ring_depth(BP);
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int g = lane >> 2, q = lane & 3;
+  const int cta = static_cast<int>(blockIdx.x);
+  uint8_t* codes_st = smem + static_cast<size_t>(warp) * kD * kCodeStage;
+  const uint16_t* scales_st = reinterpret_cast<const uint16_t*>(smem + p.off_scales) + warp * kD * (kScaleStage / 2);
+  uint8_t* scales_w = smem + p.off_scales + static_cast<size_t>(warp) * kD * kScaleStage;
+  float* stage = reinterpret_cast<float*>(smem + p.off_stage);
+  uint8_t* xh = smem + p.off_xh;
+  const uint8_t* zero = smem + p.off_zero;
+  float* V = reinterpret_cast<float*>(smem + p.off_v);
+  float* Fv = reinterpret_cast<float*>(smem + p.off_f);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar) + warp * kD;
+  int* s_flag = reinterpret_cast<int*>(smem + p.off_misc);  // [0] abort, [1] barrier result
+  float* s_scale = reinterpret_cast<float*>(s_flag + 8);     // [8] output scale of the previous call
+
+  for (uint32_t i = threadIdx.x; i < 64; i += blockDim.x) reinterpret_cast<uint32_t*>(smem + p.off_zero)[i] = 0u;
+  const int vcap = (p.nkc * GPI + 8) * BP;
+  for (int i = threadIdx.x; i < vcap; i += blockDim.x) V[i] = Fv[i] = 0.f;
+  if (lane == 0)
+    for (int s = 0; s < kD; ++s) mbar_init(&full[s], 1);
+  if (threadIdx.x == 0) s_flag[0] = 0;
+  fence_mbar_init();
+  __syncthreads();
+
+  // this warp's item range of a call
+  auto warp_range = [&](const CallLite& c, int& a, int& b) {
+    if (cta >= c.gp) {
+      a = b = 0;
+      return;
+    }
+    const int ca = cta_start(c.T, c.gp, cta), cb = cta_start(c.T, c.gp, cta + 1), tc = cb - ca;
+    a = ca + (tc * warp) / kNW;
+    b = ca + (tc * (warp + 1)) / kNW;
+  };
+
+  // ---- producer state (lane 0 issues; the cursor is kept warp-uniform) ----
+  int pcall = 0, pidx = 0, pend = 0, pru = 0, pku = 0, pnru = 0;
+  auto set_call = [&]() {
+    const CallLite c(p.calls[pcall]);
+    warp_range(c, pidx, pend);
+    pnru = c.nru;
+    pku = pidx / c.nru;
+    pru = pidx - pku * c.nru;
+  };
+  set_call();
+  unsigned issued = 0, consumed = 0;
+  int ist = 0;                 // stage of the next copy
+  int cst = 0;                 // stage of the next item to consume
+  uint32_t cph = 0;            // its phase parity
+  const uint64_t pol = l2_evict_first_policy();
+  auto issue_next = [&]() {
+    while (pidx >= pend) {
+      if (++pcall >= p.ncalls) return;
+      set_call();
+    }
+    const CallDev* cd = p.calls + pcall;
+    const int s = ist;
+    ist = ist + 1 == kD ? 0 : ist + 1;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&full[s], kStageBytes);
+      tma_load_2d_hint(codes_st + static_cast<size_t>(s) * kCodeStage, &cd->tm_codes, pku * 32, pru * kRows, &full[s],
+                       pol);
+      tma_load_2d(scales_w + static_cast<size_t>(s) * kScaleStage, &cd->tm_scales, (pku * GPI) & ~7, pru * kRows,
+                  &full[s]);
+    }
+    ++issued;
+    ++pidx;
+    if (++pru == pnru) {
+      pru = 0;
+      ++pku;
+    }
+  };
+  for (int s = 0; s < kD; ++s) issue_next();
+
+  bool abort = false;
+  const LaneLayout<G> L(lane);
+  float pscale[BP];  // output scale of the previous call, per batch row
+  for (int j = 0; j < p.ncalls && !abort; ++j) {
+    const CallLite c(p.calls[j]);
+    const int par = j & 1;
+    float* part = p.part + static_cast<size_t>(par) * p.part_stride;
+    float* ssq = p.ssq + par * p.ssq_stride;
+    const float* ppart = p.part + static_cast<size_t>(par ^ 1) * p.part_stride;
+    const float* pssq = p.ssq + (par ^ 1) * p.ssq_stride;
+    const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
+    // ---- this CTA's items and the K slices they cover ----
+    int ca = 0, cb = 0, ku_lo = 0, ku_hi = -1;
+    if (cta < c.gp) {
+      ca = cta_start(c.T, c.gp, cta);
+      cb = cta_start(c.T, c.gp, cta + 1);
+      ku_lo = ca / c.nru;
+      if (cb > ca) ku_hi = (cb - 1) / c.nru;
+    }
+    const int krow0 = ku_lo * kItemTrits;                                       // first input row needed
+    const int nkrow = ku_hi >= ku_lo ? min((ku_hi + 1) * kItemTrits, c.K) - krow0 : 0;
+    // ---- the previous call's output scale (last warp) and the input rows this CTA needs, summed
+    //      from the previous call's partial sums (the other warps) ----
+    if (warp == kNW - 1) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b) {
+        const float sc = j > 0 && b < p.B ? out_scale_warp(pc, pssq, BP, b, lane) : 1.f;
+        if (lane == 0) s_scale[b] = sc;
+      }
+    }
+    if (j > 0 && c.mode != 0 && nkrow > 0) {
+      const int r0[3] = {krow0, c.K + krow0, 0}, nr[3] = {nkrow, c.mode == 2 ? nkrow : 0, 0};
+      gather(pc, ppart, p.B, BP, c.mode == 2 ? 2 : 1, r0, nr, stage, (kNW - 1) * 32);
+    }
+    __syncthreads();
+#pragma unroll
+    for (int b = 0; b < BP; ++b) pscale[b] = s_scale[b];
+    // ---- input transform of this CTA's K slices ----
+    if (cb > ca) {
+      const int blk0 = ku_lo * BPI;
+      const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
+      for (int blk = blk0 + warp; blk < blk1; blk += kNW)
+        prep_block<G, BP>(p, c, stage, krow0, nkrow, pscale, blk, (blk - blk0) * (kFwhtBlock / G), L, xh, V, Fv,
+                          ssq, lane);
+    }
+    __syncthreads();
+
+    // ---- this warp's items ----
+    int wa = 0, wb = 0;
+    warp_range(c, wa, wb);
+    const int my_slot = g / BP, my_b = g % BP;  // B operand: this lane supplies column g = slot * BP + b
+    const uint32_t rA = static_cast<uint32_t>(g) * 128u;
+    int ku = wb > wa ? wa / c.nru : 0, ru = wa - ku * c.nru;
+    for (int it = wa; it < wb; ++it) {
+      const int st = cst;
+      if (!mbar_wait(&full[st], cph)) {
+        if (lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        abort = true;
+        break;
+      }
+      const uint8_t* cs = codes_st + static_cast<size_t>(st) * kCodeStage;
+      const uint16_t* ss = scales_st + st * (kScaleStage / 2);
+      const int g_item0 = ku * GPI;                  // first group of the item
+      const int lg_item0 = (ku - ku_lo) * GPI;       // ... in this CTA's x^
+      const int ngi = min(GPI, c.ng - g_item0);      // groups in the item
+      const int gofs = g_item0 & 7;                  // its column in the scale box
+      float acc[2][4];
+#pragma unroll
+      for (int s = 0; s < 2; ++s)
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[s][i] = 0.f;
+#pragma unroll
+      for (int cy = 0; cy < NCYC; ++cy) {
+        const int gb = cy * CPG;
+        if (gb >= ngi) break;
+        const int col0 = 2 * q;
+        // independent accumulator chains per slab (batch 1: two, by word slot u or group parity)
+        constexpr int NCH = BP == 1 ? 2 : 1;
+        float cc[2][NCH][4];
+        {
+          // start values: -2^-16 * sum x^ for the columns of groups present in this cycle
+          const float2 v2 = *reinterpret_cast<const float2*>(V + (lg_item0 + gb) * BP + col0);
+          const bool ok0 = col0 < CPG * BP && gb + col0 / BP < ngi;
+          const bool ok1 = col0 + 1 < CPG * BP && gb + (col0 + 1) / BP < ngi;
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            cc[s][0][0] = cc[s][0][2] = ok0 ? v2.x : 0.f;
+            cc[s][0][1] = cc[s][0][3] = ok1 ? v2.y : 0.f;
+#pragma unroll
+            for (int ch = 1; ch < NCH; ++ch)
+#pragma unroll
+              for (int i = 0; i < 4; ++i) cc[s][ch][i] = 0.f;
+          }
+        }
+#pragma unroll
+        for (int gl = 0; gl < CPG; ++gl) {
+          const int jj = gb + gl;  // group within the item
+          if (jj >= ngi) break;
+          uint32_t wv[2][2][WPT];  // [slab][row g / g + 8][word]
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const uint8_t* r0 = cs + rA + static_cast<uint32_t>(s) * 2048u;
+            if constexpr (WPT == 2) {
+              const uint32_t off = (static_cast<uint32_t>((2 * jj + (q >> 1)) ^ g) << 4) + 8u * (q & 1);
+              const uint2 a = *reinterpret_cast<const uint2*>(r0 + off);
+              const uint2 b = *reinterpret_cast<const uint2*>(r0 + 1024u + off);
+              wv[s][0][0] = a.x;
+              wv[s][0][WPT - 1] = a.y;
+              wv[s][1][0] = b.x;
+              wv[s][1][WPT - 1] = b.y;
+            } else {
+              const uint32_t off = (static_cast<uint32_t>(jj ^ g) << 4) + 4u * q;
+              wv[s][0][0] = *reinterpret_cast<const uint32_t*>(r0 + off);
+              wv[s][1][0] = *reinterpret_cast<const uint32_t*>(r0 + 1024u + off);
+            }
+          }
+          const uint8_t* bbase = (my_slot == gl && my_b < p.B)
+                                     ? xh + (static_cast<size_t>(lg_item0 + jj) * BP + my_b) * (2 * G)
+                                     : zero;
+#pragma unroll
+          for (int u = 0; u < WPT; ++u) {
+            uint4 bq[2];
+#pragma unroll
+            for (int pp = 0; pp < 2; ++pp)
+              bq[pp] = *reinterpret_cast<const uint4*>(bbase + (((u * 2 + pp) * 4 + q) << 4));
+#pragma unroll
+            for (int s = 0; s < 2; ++s) {
+              const uint32_t w = wv[s][0][u], w8 = wv[s][1][u];
+              const uint32_t w2 = w >> 10, w82 = w8 >> 10;
+              uint32_t pr[8], pr8[8];
+#pragma unroll
+              for (int f = 0; f < 8; ++f) {
+                pr[f] = f < 5 ? (w & (0x00030003u << (2 * f))) : (w2 & (0x00030003u << (2 * (f - 5))));
+                pr8[f] = f < 5 ? (w8 & (0x00030003u << (2 * f))) : (w82 & (0x00030003u << (2 * (f - 5))));
+              }
+              const int ch = NCH == 1 ? 0 : WPT == 2 ? u : (gl & 1);
+#pragma unroll
+              for (int m = 0; m < 4; ++m) {
+                const uint4 b = bq[m >> 1];
+                mma16816(cc[s][ch], pr[2 * m], pr8[2 * m], pr[2 * m + 1], pr8[2 * m + 1], (m & 1) ? b.z : b.x,
+                         (m & 1) ? b.w : b.y);
+              }
+            }
+          }
+        }
+        // fold the cycle: acc += scale(row, group) * 2^(16 + e) * cc for each column
+        {
+          const float2 f2 = *reinterpret_cast<const float2*>(Fv + (lg_item0 + gb) * BP + col0);
+          const int sl0 = min(col0 / BP, CPG - 1), sl1 = min((col0 + 1) / BP, CPG - 1);
+#pragma unroll
+          for (int s = 0; s < 2; ++s) {
+            const uint16_t* sr = ss + (16 * s + g) * 8 + gofs + gb;
+            const float s00 = half_bits_to_float(sr[sl0]), s01 = half_bits_to_float(sr[sl1]);
+            const float s80 = half_bits_to_float(sr[64 + sl0]), s81 = half_bits_to_float(sr[64 + sl1]);
+            float t[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              t[i] = cc[s][0][i];
+#pragma unroll
+              for (int ch = 1; ch < NCH; ++ch) t[i] += cc[s][ch][i];
+            }
+            acc[s][0] = fmaf(s00 * f2.x, t[0], acc[s][0]);
+            acc[s][1] = fmaf(s01 * f2.y, t[1], acc[s][1]);
+            acc[s][2] = fmaf(s80 * f2.x, t[2], acc[s][2]);
+            acc[s][3] = fmaf(s81 * f2.y, t[3], acc[s][3]);
+          }
+        }
+      }
+      __syncwarp();
+      ++consumed;
+      if (++cst == kD) {
+        cst = 0;
+        cph ^= 1u;
+      }
+      fence_proxy_async_smem();  // this stage's reads before the copy that refills it
+      issue_next();
+      // the item's partial sums: per (row, batch row), summed over the columns of that batch row
+      {
+        float o[2][4];
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (BP == 1) {
+            o[s][0] = acc[s][0] + acc[s][1];
+            o[s][2] = acc[s][2] + acc[s][3];
+            o[s][1] = o[s][3] = 0.f;
+          } else {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[s][i] = acc[s][i];
+          }
+#pragma unroll
+          for (int m = 1; m < 4; m <<= 1) {
+            if ((2 * m) % BP != 0) continue;  // lanes q and q ^ m hold the same batch rows
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[s][i] += __shfl_xor_sync(0xffffffffu, o[s][i], m);
+          }
+        }
+        constexpr int nwq = BP >= 2 ? BP / 2 : 1;  // quad threads holding distinct batch rows
+        if (q < nwq) {
+          float* dst = part + (static_cast<size_t>(ku) * c.nru + ru) * BP * kRows;
+#pragma unroll
+          for (int s = 0; s < 2; ++s)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+              if (BP == 1 && (i & 1)) continue;
+              const int r = 16 * s + g + (i >= 2 ? 8 : 0);
+              const int b = BP == 1 ? 0 : 2 * q + (i & 1);
+              __stcg(dst + b * kRows + r, o[s][i]);
+            }
+        }
+      }
+      if (++ru == c.nru) {
+        ru = 0;
+        ++ku;
+      }
+    }
+    __syncthreads();
+    if (abort) s_flag[0] = 1;
+    __syncthreads();
+    abort = s_flag[0] != 0;
+    if (abort) break;
+    grid_arrive(p.sync);
+    // ---- while the barrier fills: the previous call's final output, this CTA's share of its rows ----
+    if (j > 0) {
+      const int fr0 = (cta * (pc.N / 4)) / static_cast<int>(gridDim.x) * 4;
+      const int fr1 = ((cta + 1) * (pc.N / 4)) / static_cast<int>(gridDim.x) * 4;
+      const int r0[3] = {fr0, 0, 0}, nr[3] = {fr1 - fr0, 0, 0};
+      gather(pc, ppart, p.B, BP, 1, r0, nr, stage, kNW * 32);
+      __syncthreads();
+      for (int e = threadIdx.x; e < (fr1 - fr0) / 4 * p.B; e += blockDim.x) {
+        const int b = e % p.B, k = 4 * (e / p.B);
+        *reinterpret_cast<float4*>(pc.y + static_cast<size_t>(b) * pc.N + fr0 + k) =
+            in_row4(stage, 0, BP, b, k, pscale[b]);
+      }
+    }
+    if (!grid_wait(p.sync, static_cast<unsigned>(j), s_flag + 1)) {
+      if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      abort = true;
+    }
+  }
+
+  if (!abort) {
+    // the last call's final output: this CTA's share of its rows
+    const int j = p.ncalls - 1;
+    const CallLite c(p.calls[j]);
+    const float* lpart = p.part + static_cast<size_t>(j & 1) * p.part_stride;
+    const float* lssq = p.ssq + (j & 1) * p.ssq_stride;
+    if (warp == 0) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b) {
+        const float sc = b < p.B ? out_scale_warp(c, lssq, BP, b, lane) : 1.f;
+        if (lane == 0) s_scale[b] = sc;
+      }
+    }
+    const int fr0 = (cta * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
+    const int fr1 = ((cta + 1) * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
+    const int r0[3] = {fr0, 0, 0}, nr[3] = {fr1 - fr0, 0, 0};
+    gather(c, lpart, p.B, BP, 1, r0, nr, stage, kNW * 32);
+    __syncthreads();
+    for (int e = threadIdx.x; e < (fr1 - fr0) / 4 * p.B; e += blockDim.x) {
+      const int b = e % p.B, k = 4 * (e / p.B);
+      *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + fr0 + k) =
+          in_row4(stage, 0, BP, b, k, s_scale[b]);
+    }
+  } else {
+    // wind down: wait (bounded) for this warp's copies still in flight before the CTA exits
+    for (; consumed < issued; ++consumed) {
+      if (!mbar_wait(&full[cst], cph)) break;
+      if (++cst == kD) {
+        cst = 0;
+        cph ^= 1u;
+      }
+    }
+  }
+  // the last CTA to leave resets the barrier words for the next launch
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.sync + 1, 1u);
+    if (prev == gridDim.x - 1 && !abort) {
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
+}  // namespace seq
+}  // namespace tq
+
+// ---------------------------------------------------------------------------------------------
+// host side
+// ---------------------------------------------------------------------------------------------
+using namespace tq;
+using namespace tq::seq;
+
+struct tq_seq {
+  std::vector<CallDev> calls;
+  int ncalls = 0, B = 0, Bp = 0, G = 0, grid = 0, nkc = 0, dev = 0, stage_floats = 0;
+  size_t smem = 0;
+  uint32_t off_scales = 0, off_xh = 0, off_zero = 0, off_v = 0, off_f = 0, off_bar = 0, off_misc = 0, off_stage = 0;
+  size_t ws_calls = 0, ws_sync = 0, ws_part = 0, ws_ssq = 0, ws_bytes = 0, part_stride = 0;
+  int ssq_stride = 0;
+  const void* kern = nullptr;
+};
+
+namespace {
+
+template <int G, int BP>
+const void* seq_kernel_t() {
+  return reinterpret_cast<const void*>(gemv_seq_kernel<G, BP>);
+}
+const void* seq_kernel(int G, int Bp) {
+  if (G == 128) {
+    switch (Bp) {
+      case 1: return seq_kernel_t<128, 1>();
+      case 2: return seq_kernel_t<128, 2>();
+      case 4: return seq_kernel_t<128, 4>();
+      default: return seq_kernel_t<128, 8>();
+    }
+  }
+  switch (Bp) {
+    case 1: return seq_kernel_t<64, 1>();
+    case 2: return seq_kernel_t<64, 2>();
+    case 4: return seq_kernel_t<64, 4>();
+    default: return seq_kernel_t<64, 8>();
+  }
+}
+
+}  // namespace
+
+extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int batch, tq_seq** out) {
+  if (!out) return TQ_ERR_INVALID_ARG;
+  *out = nullptr;
+  if (!calls || ncalls < 1 || batch < 1 || batch > 8) return TQ_ERR_INVALID_ARG;
+  const int G = calls[0].d.group;
+  int Kmax = 0;
+  for (int j = 0; j < ncalls; ++j) {
+    const tq_seq_call& c = calls[j];
+    tq_status st = check_linear_desc(&c.d);
+    if (st != TQ_OK) return st;
+    if (c.d.packing != TQ_PACK_2BIT || c.d.group != G) return TQ_ERR_UNSUPPORTED;
+    // FP16 scales are fetched by TMA: a scale row must be a multiple of 16 bytes
+    if ((c.d.K / c.d.group) % 8 != 0 || c.d.N % 4 != 0) return TQ_ERR_UNSUPPORTED;
+    if (!c.codes || !c.scales || !c.y) return TQ_ERR_INVALID_ARG;
+    if (!aligned(c.codes, 16) || !aligned(c.scales, 16) || !aligned(c.y, 16)) return TQ_ERR_MISALIGNED;
+    if (c.x_src == TQ_SEQ_X_BF16) {
+      if (!c.x) return TQ_ERR_INVALID_ARG;
+      if (!aligned(c.x, 16)) return TQ_ERR_MISALIGNED;
+    } else if (c.x_src == TQ_SEQ_X_PREV || c.x_src == TQ_SEQ_X_RMS_PREV) {
+      if (j == 0 || calls[j - 1].d.N < c.d.K) return TQ_ERR_INVALID_ARG;
+    } else if (c.x_src == TQ_SEQ_X_SWIGLU_PREV) {
+      if (j == 0 || calls[j - 1].d.N != 2 * c.d.K) return TQ_ERR_INVALID_ARG;
+    } else {
+      return TQ_ERR_INVALID_ARG;
+    }
+    Kmax = std::max(Kmax, c.d.K);
+  }
+  int dev = 0, sms = 0, optin = 0, coop = 0;
+  cudaError_t e;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev)) != cudaSuccess)
+    return cuda_fail(e);
+  if ((e = cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev)) != cudaSuccess) return cuda_fail(e);
+  if (!coop) return TQ_ERR_UNSUPPORTED;
+
+  tq_seq* s = new (std::nothrow) tq_seq();
+  if (!s) return TQ_ERR_INVALID_ARG;
+  s->ncalls = ncalls;
+  s->B = batch;
+  s->Bp = batch <= 1 ? 1 : batch <= 2 ? 2 : batch <= 4 ? 4 : 8;
+  s->G = G;
+  s->grid = sms;
+  s->dev = dev;
+  // per-call work split; the most K slices any CTA covers, the largest item count
+  s->calls.resize(ncalls);
+  long long Tmax = 0;
+  int fin_prev = 0;         // rows of the previous call one CTA finalizes
+  long long stage_rows = 4;  // largest gather of any call
+  for (int j = 0; j < ncalls; ++j) {
+    const tq_seq_call& c = calls[j];
+    CallDev& d = s->calls[j];
+    std::memset(&d, 0, sizeof(d));
+    d.x = c.x_src == TQ_SEQ_X_BF16 ? c.x : nullptr;
+    d.y = c.y;
+    d.N = c.d.N;
+    d.K = c.d.K;
+    d.ng = c.d.K / G;
+    d.mode = c.x_src;
+    d.apply = c.d.fwht_block != 0;
+    d.nru = (c.d.N + kRows - 1) / kRows;
+    d.nku = (c.d.K + kItemTrits - 1) / kItemTrits;
+    const long long T = static_cast<long long>(d.nru) * d.nku;
+    if (T * sms >= (1ll << 31)) {
+      delete s;
+      return TQ_ERR_UNSUPPORTED;
+    }
+    d.T = static_cast<int>(T);
+    d.gp = std::min(sms, d.T);
+    Tmax = std::max(Tmax, T);
+    int kmax = 0;  // most input rows one CTA transforms
+    for (int cta = 0; cta < d.gp; ++cta) {
+      const int a = cta_start(d.T, d.gp, cta), b = cta_start(d.T, d.gp, cta + 1);
+      if (b > a) kmax = std::max(kmax, std::min(((b - 1) / d.nru + 1) * kItemTrits, d.K) - (a / d.nru) * kItemTrits);
+    }
+    const int segs = c.x_src == TQ_SEQ_X_BF16 ? 0 : c.x_src == TQ_SEQ_X_SWIGLU_PREV ? 2 : 1;
+    stage_rows = std::max<long long>(stage_rows, static_cast<long long>(segs) * kmax + fin_prev);
+    fin_prev = ((d.N / 4) / sms + 1) * 4;
+    stage_rows = std::max<long long>(stage_rows, fin_prev);  // the last call's finalize
+    for (int cta = 0; cta < d.gp; ++cta) {
+      const int a = cta_start(d.T, d.gp, cta), b = cta_start(d.T, d.gp, cta + 1);
+      if (b > a) s->nkc = std::max(s->nkc, (b - 1) / d.nru - a / d.nru + 1);
+    }
+  }
+  // shared memory: rings, x^ of the CTA's K slices, zero chunk, V, F, barriers, flags, gather staging
+  const int GPI = kItemTrits / G;
+  const int kD = ring_depth(s->Bp);
+  s->stage_floats = static_cast<int>(stage_rows * s->Bp);
+  const size_t xh = align256(static_cast<size_t>(s->nkc) * GPI * s->Bp * 2 * G);
+  const size_t vf = align256(static_cast<size_t>(s->nkc * GPI + 8) * s->Bp * 4);
+  const size_t stage = align256(static_cast<size_t>(s->stage_floats) * 4);
+  size_t off = static_cast<size_t>(kNW) * kD * kCodeStage;
+  s->off_scales = static_cast<uint32_t>(off);
+  off += static_cast<size_t>(kNW) * kD * kScaleStage;
+  s->off_xh = static_cast<uint32_t>(off);
+  off += xh;
+  s->off_zero = static_cast<uint32_t>(off);
+  off += 256;
+  s->off_v = static_cast<uint32_t>(off);
+  off += vf;
+  s->off_f = static_cast<uint32_t>(off);
+  off += vf;
+  s->off_bar = static_cast<uint32_t>(off);
+  off += align256(static_cast<size_t>(kNW) * kD * 8);
+  s->off_misc = static_cast<uint32_t>(off);
+  off += 256;
+  s->off_stage = static_cast<uint32_t>(off);
+  off += stage;
+  s->smem = off + 1024;  // alignment slack of the base
+  if (s->smem > kSmemLimit || s->smem > static_cast<size_t>(optin)) {
+    delete s;
+    return TQ_ERR_UNSUPPORTED;  // the activations of the widest CTA range do not fit shared memory
+  }
+  s->kern = seq_kernel(G, s->Bp);
+  if ((e = cudaFuncSetAttribute(s->kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s->smem))) !=
+      cudaSuccess) {
+    delete s;
+    return cuda_fail(e);
+  }
+  int bps = 0;
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, s->kern, kNW * 32, s->smem)) != cudaSuccess || bps < 1) {
+    delete s;
+    return e != cudaSuccess ? cuda_fail(e) : TQ_ERR_UNSUPPORTED;
+  }
+  for (int j = 0; j < ncalls; ++j) {
+    const tq_seq_call& c = calls[j];
+    CallDev& d = s->calls[j];
+    const int P = pitch_words(c.d.K, c.d.packing);
+    if (!make_tmap_2d(&d.tm_codes, c.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<uint64_t>(P),
+                      static_cast<uint64_t>(c.d.N), static_cast<uint64_t>(P) * 4u, 32u, kRows,
+                      CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_tmap_2d(&d.tm_scales, c.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, static_cast<uint64_t>(d.ng),
+                      static_cast<uint64_t>(c.d.N), static_cast<uint64_t>(d.ng) * 2u, 8u, kRows,
+                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
+      delete s;
+      return TQ_ERR_CUDA;
+    }
+  }
+  s->part_stride = static_cast<size_t>(Tmax) * s->Bp * kRows;
+  s->ssq_stride = (Kmax / kFwhtBlock) * s->Bp;
+  s->ws_calls = align256(sizeof(CallDev) * ncalls);
+  s->ws_sync = 256;
+  s->ws_part = align256(2 * s->part_stride * 4);
+  s->ws_ssq = align256(static_cast<size_t>(2) * s->ssq_stride * 4);
+  s->ws_bytes = s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq;
+  *out = s;
+  return TQ_OK;
+}
+
+extern "C" size_t tq_seq_workspace_bytes(const tq_seq* s) { return s ? s->ws_bytes : 0; }
+
+extern "C" tq_status tq_seq_upload(const tq_seq* s, void* workspace, size_t workspace_bytes) {
+  if (!s || !workspace) return TQ_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return TQ_ERR_MISALIGNED;
+  if (workspace_bytes < s->ws_bytes) return TQ_ERR_WORKSPACE;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  cudaError_t e = cudaMemcpy(ws, s->calls.data(), sizeof(CallDev) * s->ncalls, cudaMemcpyHostToDevice);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if ((e = cudaMemset(ws + s->ws_calls, 0, s->ws_sync)) != cudaSuccess) return cuda_fail(e);
+  return TQ_OK;
+}
+
+extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) {
+  if (!s || !workspace) return TQ_ERR_INVALID_ARG;
+  if (!aligned(workspace, 256)) return TQ_ERR_MISALIGNED;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e);
+  if (dev != s->dev) return TQ_ERR_INVALID_ARG;
+  int* status = status_ptr();
+  if (!status) return TQ_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(workspace);
+  Params prm{};
+  prm.calls = reinterpret_cast<const CallDev*>(ws);
+  prm.ncalls = s->ncalls;
+  prm.B = s->B;
+  prm.status = status;
+  prm.sync = reinterpret_cast<unsigned*>(ws + s->ws_calls);
+  prm.part = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync);
+  prm.ssq = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync + s->ws_part);
+  prm.part_stride = s->part_stride;
+  prm.ssq_stride = s->ssq_stride;
+  prm.nkc = s->nkc;
+  prm.off_scales = s->off_scales;
+  prm.off_xh = s->off_xh;
+  prm.off_zero = s->off_zero;
+  prm.off_v = s->off_v;
+  prm.off_f = s->off_f;
+  prm.off_bar = s->off_bar;
+  prm.off_misc = s->off_misc;
+  prm.off_stage = s->off_stage;
+  prm.stage_floats = s->stage_floats;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(s->grid);
+  cfg.blockDim = dim3(kNW * 32);
+  cfg.dynamicSmemBytes = s->smem;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  void* args[] = {&prm};
+  if ((e = cudaLaunchKernelExC(&cfg, s->kern, args)) != cudaSuccess) return cuda_fail(e);
+  return TQ_OK;
+}
+
+extern "C" int tq_seq_kernel_count(const tq_seq* s) { return s ? 1 : -1; }
+
+extern "C" void tq_seq_destroy(tq_seq* s) { delete s; }
