@@ -26,6 +26,9 @@ Readings where the pages are silent (each is listed in the design notes):
   * MoE: top-8 by raw logit, ties to the lower expert index; gates = softmax over the 8 chosen
     logits; SwiGLU expert h = silu(gate) * up; the expert input x and the down-projection input h
     are both block-Hadamard transformed; combine = sum_j gate_j * y_j.
+  * Offline quantizer: the pages give the order (rotate, then one FP16 scale per group, then three
+    levels) but not the rounding rule; this build takes the absmean rule of BitNet b1.58 (scale =
+    mean |w'| over the group, t = the level of {-1, 0, +1} nearest to w' / scale, a tie at 1/2 to 0).
 
 Parity pins (tests/test_oracle_pins.py): every function below is checked against something other
 than itself - Python's own base-3/base-4 integer parsing, the closed form of Sylvester entries,
@@ -285,3 +288,42 @@ def moe_down_from_h(h, idx, gate, experts_down: dict, F: int, group: int, packin
             y[t] += gate[t, j] * part
             A[t] += gate[t, j] * Apart
     return y, A
+
+
+# ----------------------------------------------------------------------------------------------
+# Offline quantizer   ([CC] §二 ①: rotate the weights by a Hadamard transform before compressing;
+# §二 ②: each group of 128 weights shares one FP16 scale; 一: three levels -1, 0, +1, the scale
+# restoring the magnitude)
+# ----------------------------------------------------------------------------------------------
+
+INV_SQRT128 = math.sqrt(2.0) / 16.0   # 2^-3.5, rounded once to fp64
+
+
+def quantize(W, group: int, packing: int, fwht_block: int = 128):
+    """Dense W [N, K] (bf16 values, given as any float array) -> (codes, fp16 scales, int8 trits).
+
+    1. Rotate each row block by block (same transform as the activations'): u = W_blk @ H^T with the
+       unnormalised Sylvester H, in fp64; the rotated weight is w' = u * c with c = 2^-3.5
+       (fwht_block 0: u = W, c = 1).  For bf16 input u is exact in fp64 whenever the magnitudes in
+       one block span less than 2^38, and so are the group sums below when they span less than 2^31.
+    2. Per group of ``group`` consecutive k: m = sum |u| / group, scale S = fp16(m * c) (the product
+       rounded to fp64 once, then to fp16 to nearest even).
+    3. t = sign(u) where fp64(|u| * c) > S / 2, else 0: the nearest of S * {-1, 0, +1} to w'
+       (absmean rule), a value exactly halfway between 0 and S going to 0.
+    4. Pack t (base-3 or 2-bit, as ``pack``).
+    """
+    W = np.asarray(W, dtype=np.float64)
+    N, K = W.shape
+    assert K % 128 == 0 and group in (64, 128) and fwht_block in (0, 128)
+    if fwht_block:
+        H = hadamard(fwht_block)
+        u = np.matmul(W.reshape(N, K // fwht_block, fwht_block), H.T).reshape(N, K)
+        c = INV_SQRT128
+    else:
+        u = W.copy()
+        c = 1.0
+    m = np.abs(u).reshape(N, K // group, group).sum(axis=2) / group
+    scales = (m * c).astype(np.float16)
+    half = np.repeat(scales.astype(np.float64) / 2.0, group, axis=1)
+    trits = np.where(np.abs(u) * c > half, np.sign(u), 0.0).astype(np.int8)
+    return pack(trits, packing), scales, trits

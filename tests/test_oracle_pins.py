@@ -339,9 +339,113 @@ def pin_moe_down_from_h(O):
     assert np.allclose(y1, ref, rtol=1e-12, atol=1e-12)
 
 
+def bf16_round(a):
+    """Round float values to bf16 (nearest even) and back, with torch as the converter."""
+    import torch
+    return torch.from_numpy(np.asarray(a, dtype=np.float32)).to(torch.bfloat16).float().numpy().astype(np.float64)
+
+
+def scipy_rotation(W, block=128):
+    """w' = W_blk @ H^T / sqrt(block), with scipy's Hadamard matrix (a separate construction)."""
+    from scipy.linalg import hadamard as scipy_hadamard
+    H = scipy_hadamard(block).astype(np.float64)
+    N, K = W.shape
+    return (np.asarray(W, np.float64).reshape(N, K // block, block) @ H.T / math.sqrt(block)).reshape(N, K)
+
+
+def pin_quantize_closed_form(O):
+    """One non-zero a at column j of a 128-block rotates to a * (-1)^popcount(r & j) / sqrt(128) at
+    every r: all |w'| equal, so the scale is fp16(|a| / sqrt(128)) for each group of the block and
+    t_r = sign(a) (-1)^popcount(r & j).  Every block of a row gets its own a and j (one block is all
+    zero: scale 0, t 0), so group bookkeeping, the sign pattern and the normalisation all show.
+    Without the transform a group of 64 values 3/16 and 64 values 1/16 has mean 1/8 = its scale, and
+    the 1/16 entries sit exactly halfway between 0 and 1/8: they go to 0."""
+    r = rng(21)
+    N, nb = 3, 4
+    K = 128 * nb
+    W = np.zeros((N, K))
+    pos = {}
+    for n in range(N):
+        for b in range(nb):
+            if (n, b) == (1, 2):
+                continue
+            a = float(bf16_round([r.choice([-1, 1]) * 2.0 ** r.integers(-8, 3) * (1 + r.integers(0, 128) / 128)])[0])
+            j = int(r.integers(0, 128))
+            W[n, 128 * b + j] = a
+            pos[(n, b)] = (a, j)
+    for group in (128, 64):
+        codes, scales, trits = O.quantize(W, group, O.PACK_2BIT)
+        for n in range(N):
+            for b in range(nb):
+                gs = slice(b * 128 // group, (b + 1) * 128 // group)
+                if (n, b) not in pos:
+                    assert np.all(scales[n, gs] == 0) and np.all(trits[n, 128 * b:128 * (b + 1)] == 0)
+                    continue
+                a, j = pos[(n, b)]
+                want_s = np.float16(abs(a) / math.sqrt(128.0))
+                assert np.all(np.abs(scales[n, gs].astype(np.float64) - float(want_s)) <= float(want_s) * 2 ** -10)
+                want_t = [int(np.sign(a)) * (-1) ** popcount(rr & j) for rr in range(128)]
+                assert trits[n, 128 * b:128 * (b + 1)].tolist() == want_t
+        t_back, bad = O.unpack(codes, K, O.PACK_2BIT)
+        assert bad == 0 and np.array_equal(t_back, trits)
+    W0 = np.array([[3 / 16] * 64 + [1 / 16] * 64 + [-3 / 16] * 64 + [-1 / 16] * 64])
+    _, s0, t0 = O.quantize(W0, 128, O.PACK_B3, fwht_block=0)
+    assert s0.tolist() == [[0.125, 0.125]]
+    assert t0.tolist() == [[1] * 64 + [0] * 64 + [-1] * 64 + [0] * 64]
+
+
+def pin_quantize_nearest_level(O):
+    """On Gaussian bf16 weights with outliers: the scale is fp16 of the group's mean |w'| (w' from
+    scipy's Hadamard matrix), every t is the level of S * {-1, 0, +1} nearest to w', negating W
+    negates t, and scaling W by 4 keeps t and scales S by 4."""
+    r = rng(22)
+    N, K = 6, 512
+    W = r.standard_normal((N, K)) * 0.02
+    W[r.random((N, K)) < 0.01] *= 20
+    W = bf16_round(W)
+    wr = scipy_rotation(W)
+    for group in (128, 64):
+        _, S, t = O.quantize(W, group, O.PACK_B3)
+        mean = np.abs(wr).reshape(N, K // group, group).mean(axis=2)
+        assert np.all(np.abs(S.astype(np.float64) - mean) <= mean * 2 ** -10)
+        Sf = np.repeat(S.astype(np.float64), group, axis=1)
+        dist = np.stack([np.abs(wr - Sf * lv) for lv in (-1, 0, 1)])
+        best = dist.min(axis=0)
+        chosen = np.abs(wr - Sf * t)
+        assert np.all(chosen <= best + 1e-12 * Sf)
+        assert np.mean(t != 0) > 0.4
+        _, Sn, tn = O.quantize(-W, group, O.PACK_B3)
+        assert np.array_equal(tn, -t) and np.array_equal(Sn, S)
+        _, S4, t4 = O.quantize(4 * W, group, O.PACK_B3)
+        assert np.array_equal(t4, t) and np.array_equal(S4.astype(np.float64), 4 * S.astype(np.float64))
+
+
+def pin_quantize_round_trip(O):
+    """The rotation loses nothing: weights that are already ternary times a group scale in the
+    rotated basis, rotated back (scipy's Hadamard) and rounded to bf16, quantize back to the same
+    trits; each scale comes back as S times the group's fraction of non-zero trits (the mean |w'|)."""
+    r = rng(23)
+    N, K = 5, 768
+    for group in (128, 64):
+        for packing in (O.PACK_B3, O.PACK_2BIT):
+            T = r.integers(-1, 2, size=(N, K)).astype(np.int8)
+            S = np.exp(r.standard_normal((N, K // group)) * 0.5 - 4).astype(np.float16).astype(np.float64)
+            wr = np.repeat(S, group, axis=1) * T
+            from scipy.linalg import hadamard as scipy_hadamard
+            H = scipy_hadamard(128).astype(np.float64)
+            W = bf16_round((wr.reshape(N, K // 128, 128) @ H / math.sqrt(128)).reshape(N, K))
+            codes, S_q, t_q = O.quantize(W, group, packing)
+            assert np.array_equal(t_q, T)
+            t_back, bad = O.unpack(codes, K, packing)
+            assert bad == 0 and np.array_equal(t_back, T)
+            frac = (T != 0).reshape(N, K // group, group).mean(axis=2)
+            assert np.allclose(S_q.astype(np.float64), S * frac, rtol=4e-3, atol=0)
+
+
 PINS = [pin_pack_b3, pin_pack_2b, pin_unpack, pin_format_constants, pin_hadamard, pin_fwht,
         pin_rotation_identity, pin_contraction_bruteforce, pin_special_cases, pin_moe_route, pin_moe_layer,
-        pin_silu, pin_moe_down_from_h]
+        pin_silu, pin_moe_down_from_h, pin_quantize_closed_form, pin_quantize_nearest_level,
+        pin_quantize_round_trip]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -354,7 +458,7 @@ def test_oracle_pin(pin):
 # ----------------------------------------------------------------------------------------------
 
 ORIG = {k: getattr(O_real, k) for k in ("pack", "unpack", "hadamard", "block_fwht", "moe_route", "dequant",
-                                        "silu", "moe_down_from_h")}
+                                        "silu", "moe_down_from_h", "quantize")}
 
 
 def _pack_msd_first(trits, packing):
@@ -413,7 +517,37 @@ def _unpack_off_by_one(codes, K, packing):
     return np.roll(t, 1, axis=1), bad
 
 
+def _quantize_with(stat="mean", thr=0.5, rotate=True, c=None, ties_up=False, interleaved=False, flip=False):
+    """The quantizer with one step changed (a planted mistake)."""
+    def q(W, group, packing, fwht_block=128):
+        W = np.asarray(W, np.float64)
+        N, K = W.shape
+        if rotate and fwht_block:
+            u = (W.reshape(N, K // 128, 128) @ O_real.hadamard(128).T).reshape(N, K)
+            cc = O_real.INV_SQRT128 if c is None else c
+        else:
+            u, cc = W.copy(), 1.0
+        g = np.abs(u).reshape(N, group, K // group).transpose(0, 2, 1) if interleaved else \
+            np.abs(u).reshape(N, K // group, group)
+        m = g.max(axis=2) if stat == "max" else g.sum(axis=2) / group
+        S = (m * cc).astype(np.float16)
+        lim = np.repeat(S.astype(np.float64) * thr, group, axis=1)
+        hit = np.abs(u) * cc >= lim if ties_up else np.abs(u) * cc > lim
+        t = np.where(hit, np.sign(u), 0.0).astype(np.int8)
+        if flip:
+            t = -t
+        return O_real.pack(t, packing), S, t
+    return q
+
+
 MUTANTS = {
+    "quantize scale from max": dict(quantize=_quantize_with(stat="max")),
+    "quantize threshold 0.7 S": dict(quantize=_quantize_with(thr=0.7)),
+    "quantize without rotation": dict(quantize=_quantize_with(rotate=False)),
+    "quantize rotation unnormalised": dict(quantize=_quantize_with(c=1.0)),
+    "quantize ties to +-1": dict(quantize=_quantize_with(ties_up=True)),
+    "quantize groups interleaved": dict(quantize=_quantize_with(interleaved=True)),
+    "quantize sign flipped": dict(quantize=_quantize_with(flip=True)),
     "pack digit order reversed": dict(pack=_pack_msd_first),
     "hadamard recursion sign": dict(hadamard=_hadamard_wrong_sign),
     "fwht missing 1/sqrt(n)": dict(block_fwht=_fwht_unnormalised),
