@@ -2,18 +2,23 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl tq|reference] [--no-extras]
 
-Default workload: decode of the 27B-class dense model's linears - the seven ternary linears of one
-decoder layer (q/k/v/o 5120x5120 / 1024x5120, gate/up 17408x5120, down 5120x17408), 2-bit packing
-(--packing base3: 20 trits per uint32), group-128 FP16 scales, fused block-128 FWHT, batch 1 - run
-over 64 layers with distinct weights.  q/k/v and gate/up are stacked as an inference engine calls
-them (4 GEMV calls per layer, 256 per step, replayed from a CUDA graph); the weights (5.62 GB 2-bit,
-4.56 GB base-3, codes + FP16 scales) are far larger than L2, so every step streams them from HBM.
-The metric is packed-weight HBM GB/s (codes + FP16 scales, pitch included) with model-equivalent
-decode tok/s beside it.
+Default workload: one decode token through the linears of a 27B-class dense model - per layer the
+stacked q/k/v projection (7168 x 5120), o (5120 x 5120), the stacked gate/up projection (34816 x 5120)
+and down (5120 x 17408) - over 64 layers with distinct weights, 2-bit packing, group-128 FP16 scales,
+fused block-128 FWHT, batch 1.  The step is the dependent chain a decode step is: qkv reads the
+RMS-normalised layer input, o reads the q part of qkv's output (attention is not part of this
+library; it stands in as the identity), gate_up reads o's output RMS-normalised, down reads
+silu(gate) * up, and the next layer reads down's output.  All 256 calls run as one tq_seq launch
+(the decode-step entry point); 5.62 GB of codes + FP16 scales per token, far larger than L2, stream
+from HBM every step.  The metric is packed-weight HBM GB/s (codes + scales, pitch included) with
+model-equivalent decode tok/s beside it.
 
-Other rows of the hot path are measured in the same run under "extras": the other packing, batch 8
-and one call per linear of the same stream, the 256-expert top-8 MoE expert layer (1 / 8 / 64
-tokens), and the two prefill GEMM shapes.  ``--impl reference`` times the CPU oracle (fp64 numpy) on a bounded sample of the same
+Other rows of the hot path are measured in the same run under "extras": the same stream as 256
+separate tq_gemv launches (per-call path, both packings, batch 1 and 8), the decode step at batch 8,
+the seven linears of one layer called one by one at batch 1 / 4 / 16 in both packings (tok/s =
+batch / (64 x the sum of the seven times)), the single 1024 x 1024 base-3 linear (latency and
+L2-cold GB/s), the 256-expert top-8 MoE expert layer (1 / 8 / 64 tokens) and the two prefill GEMM
+shapes.  ``--impl reference`` times the CPU oracle (fp64 numpy) on a bounded sample of the same
 workload, on the host cores.
 
 Multi-GPU: independent replicas, one process per GPU (torchrun); each rank streams its own copy
@@ -178,11 +183,6 @@ class ClockSampler:
 # workloads
 # ----------------------------------------------------------------------------------------------
 
-def linear_bytes(lin, packing, group=128):
-    d = tq.desc(lin.N, lin.K, group, packing)
-    return tq.tq_packed_bytes(d) + tq.tq_scale_bytes(d)
-
-
 class Stream:
     """64 layers of the 27B-class shapes, distinct weights per layer.  stacked=True calls the layer the
     way an inference engine does (qkv, o, gate_up, down: 4 calls); stacked=False calls each of the 7
@@ -223,19 +223,58 @@ class Stream:
                 events[i][1].record()
 
     def step_e2e(self, y_host):
-        """Per step: H2D of each linear's activations from pinned memory, the GEMV, D2H of the output."""
-        for i, (d, codes, s, name, _) in enumerate(self.calls):
-            xd, xh = self.x_bufs[name]
-            xd.copy_(xh, non_blocking=True)
-            tq.tq_gemv(d, codes, s, xd, y=self.y_bufs[name], workspace=self.ws)
-        last = self.calls[-1][3]
-        y_host.copy_(self.y_bufs[last], non_blocking=True)
+        """One token in, one result out: H2D of the first call's input from pinned memory, every call,
+        D2H of the last call's output."""
+        name0 = self.calls[0][3]
+        xd, xh = self.x_bufs[name0]
+        xd.copy_(xh, non_blocking=True)
+        self.step()
+        y_host.copy_(self.y_bufs[self.calls[-1][3]], non_blocking=True)
 
     def h2d_bytes(self):
-        return sum(self.x_bufs[c[3]][0].numel() * 2 for c in self.calls)
+        return self.x_bufs[self.calls[0][3]][0].numel() * 2
 
     def d2h_bytes(self):
         return self.y_bufs[self.calls[-1][3]].numel() * 4
+
+
+class SeqStep:
+    """The decode step of a Stream's weights (stacked, 2-bit) as one tq_seq launch: the dependent chain
+    qkv(RMS-normalised input) -> o(q part) -> gate_up(RMS-normalised) -> down(SwiGLU) per layer."""
+
+    SRC = {"qkv": tq.TQ_SEQ_X_RMS_PREV, "o": tq.TQ_SEQ_X_PREV, "gate_up": tq.TQ_SEQ_X_RMS_PREV,
+           "down": tq.TQ_SEQ_X_SWIGLU_PREV}
+
+    def __init__(self, stream: "Stream", device="cuda"):
+        assert stream.stacked and stream.packing == tq.TQ_PACK_2BIT
+        self.batch = stream.batch
+        lins = {l.name: l for l in stream.linears}
+        self.x_dev, self.x_host = stream.x_bufs["qkv"]
+        self.ys = {n: torch.empty((self.batch, l.N), dtype=torch.float32, device=device) for n, l in lins.items()}
+        calls = []
+        for i, (d, codes, s, name, _) in enumerate(stream.calls):
+            d0 = tq.desc(d.N, d.K, d.group, d.packing, d.fwht_block)
+            src = tq.TQ_SEQ_X_BF16 if i == 0 else self.SRC[name]
+            calls.append((d0, codes, s, src, self.x_dev if i == 0 else None, self.ys[name]))
+        self.out = self.ys[stream.calls[-1][3]]
+        self.plan = tq.SeqPlan(calls, self.batch)
+        self.bytes_per_step = stream.bytes_per_step
+
+    def step(self):
+        self.plan.run()
+
+    def step_e2e(self, y_host):
+        """One token in, one result out: H2D of the input from pinned memory, the step, D2H of the
+        last call's output."""
+        self.x_dev.copy_(self.x_host, non_blocking=True)
+        self.plan.run()
+        y_host.copy_(self.out, non_blocking=True)
+
+    def h2d_bytes(self):
+        return self.x_dev.numel() * 2
+
+    def d2h_bytes(self):
+        return self.out.numel() * 4
 
 
 def capture(fn, warm=1):
@@ -279,41 +318,18 @@ class _Null:
         return False
 
 
-def per_call_durations(stream: Stream):
-    """Capture one step with external timing events around every call; replay once; per-call ms."""
-    n = len(stream.calls)
-    events = [(torch.cuda.Event(enable_timing=True, external=True), torch.cuda.Event(enable_timing=True, external=True))
-              for _ in range(n)]
-    g = capture(lambda: stream.step(events))
-    g.replay()
-    torch.cuda.synchronize()
-    return [a.elapsed_time(b) for a, b in events]
-
-
 def traffic_from_profiles(kernel_key: str):
     """DRAM bytes recorded by an ncu capture (profiles/ncu_traffic.txt: key, bytes, source hash), if
     the kernel sources it was taken on are unchanged."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    src_hash = hashlib.sha256()
-    csrc = os.path.join(ROOT, "ternary_weight_quantized_unpack_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        with open(os.path.join(csrc, f), "rb") as fh:
-            src_hash.update(fh.read())
-    cur = src_hash.hexdigest()[:16]
+    cur = source_hash()
     for line in open(p):
         parts = line.split()
         if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key and parts[2] == cur:
             return float(parts[1])
     return None
-
-
-def traffic_per_step(packing, batch, layers):
-    """ncu DRAM bytes of one layer (profiles/ncu_traffic.txt) x layers, or None."""
-    per_layer = traffic_from_profiles(
-        f"dense_decode_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_stacked_per_layer")
-    return None if per_layer is None else per_layer * layers
 
 
 def source_hash():
@@ -404,6 +420,108 @@ def bench_prefill(shape, steps, warmup, seed=inputs.seed_of(4)):
     return {"M": M, "K": K, "N": N, "ms": ms, "TFLOP_s": flops / (ms * 1e-3) / 1e12}
 
 
+def l2_cold_times(fn, reps, flush):
+    """Per-call device time of fn() after an L2 flush (a 256 MB write; the flush keeps the device busy
+    while the host enqueues the call, so no host launch latency enters the events)."""
+    times = []
+    for _ in range(reps):
+        flush.fill_(1)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        fn()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    return statistics.median(times)
+
+
+def bench_single_linear(reps, seed=inputs.seed_of(1)):
+    """The single 1024 x 1024 base-3 linear (batch 1, 0.5 % x20 outliers): latency with L2 flushed
+    before every call, and back-to-back graph replays (L2-warm)."""
+    c = inputs.SINGLE_LINEAR
+    N, K, G, pk = c["N"], c["K"], c["group"], c["packing"]
+    d = tq.desc(N, K, G, pk, c["fwht_block"])
+    codes = tq.tq_pack(d, inputs.trits(seed, 0, N, K, device="cuda"))
+    s = inputs.scales(seed, 1, N, K // G, device="cuda").contiguous()
+    x = inputs.activations(seed, 0, c["B"], K, outlier_frac=c["outlier_frac"]).cuda()
+    y = torch.empty((c["B"], N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, tq.tq_gemv_workspace_bytes(d, c["B"])), dtype=torch.uint8, device="cuda")
+    call = lambda: tq.tq_gemv(d, codes, s, x, y=y, workspace=ws)  # noqa: E731
+    for _ in range(3):
+        call()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    cold = l2_cold_times(call, reps, flush)
+    g = capture(lambda: [call() for _ in range(20)], warm=0)
+    g.replay()
+    torch.cuda.synchronize()
+    warm_ms, _ = time_graph(g, max(3, reps // 4), 1)
+    warm = warm_ms / (20 * max(3, reps // 4))
+    byts = tq.tq_packed_bytes(d) + tq.tq_scale_bytes(d)
+    return {"N": N, "K": K, "packing": "base3", "batch": c["B"], "bytes": byts,
+            "latency_us_l2_cold": cold * 1e3, "GB_s_l2_cold": byts / (cold * 1e-3) / GB,
+            "latency_us_l2_warm_back_to_back": warm * 1e3,
+            "kernels_per_call": tq.tq_gemv_kernel_count(d, c["B"])}
+
+
+def bench_layer_linears(packing, batches, reps, seed=inputs.seed_of(2)):
+    """The seven linears of one 27B-class layer, each called alone with L2 flushed before it; per
+    batch: per-linear device times and tok/s = batch / (64 x sum of the seven times)."""
+    lins = inputs.dense_layer_linears()
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed + packing)
+    ws_bytes = max(tq.tq_gemv_workspace_bytes(tq.desc(l.N, l.K, 128, packing), b) for l in lins for b in batches)
+    ws = torch.empty(max(1, ws_bytes), dtype=torch.uint8, device="cuda")
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    w = []
+    for lin in lins:
+        d = tq.desc(lin.N, lin.K, 128, packing)
+        codes = tq.tq_pack(d, torch.randint(-1, 2, (lin.N, lin.K), dtype=torch.int8, device="cuda", generator=gen))
+        s = torch.exp(torch.randn((lin.N, lin.K // 128), generator=gen, device="cuda") * 0.5 - 4).half()
+        w.append((lin, d, codes, s))
+    out = []
+    for b in batches:
+        per = {}
+        for i, (lin, d, codes, s) in enumerate(w):
+            x = inputs.activations(seed, 700 + i, b, lin.K).cuda()
+            y = torch.empty((b, lin.N), dtype=torch.float32, device="cuda")
+            call = lambda: tq.tq_gemv(d, codes, s, x, y=y, workspace=ws)  # noqa: E731
+            call()
+            per[lin.name] = l2_cold_times(call, reps, flush) * 1e3
+        tot_us = sum(per.values())
+        byts = sum(tq.tq_packed_bytes(d) + tq.tq_scale_bytes(d) for _, d, _, _ in w)
+        out.append({"packing": "base3" if packing == tq.TQ_PACK_B3 else "2bit", "batch": b,
+                    "us_per_linear_l2_cold": per, "us_sum_7": tot_us,
+                    "GB_s": byts / (tot_us * 1e-6) / GB,
+                    "tok_s_64_layers": b / (LAYERS * tot_us * 1e-6)})
+    return out
+
+
+def bench_seq(st: "Stream", steps, world=1, clocks_index=None, warmup=3):
+    """The decode step of ``st`` as one tq_seq launch, graph-replayed; returns (engine, graph, ms for
+    all steps, clocks)."""
+    eng = SeqStep(st)
+    for _ in range(warmup):
+        eng.step()
+    torch.cuda.synchronize()
+    g = capture(eng.step, warm=0)
+    g.replay()
+    torch.cuda.synchronize()
+    ms, clocks = time_graph(g, steps, world, clocks_index=clocks_index)
+    return eng, g, ms, clocks
+
+
+def bench_per_call(st: "Stream", steps, world=1, clocks_index=None, warmup=3):
+    """The step as one tq_gemv launch per call (graph-replayed); returns (graph, ms for all steps, clocks)."""
+    for _ in range(warmup):
+        st.step()
+    torch.cuda.synchronize()
+    g = capture(st.step, warm=0)
+    g.replay()
+    torch.cuda.synchronize()
+    ms, clocks = time_graph(g, steps, world, clocks_index=clocks_index)
+    return g, ms, clocks
+
+
 # ----------------------------------------------------------------------------------------------
 # CPU oracle on a bounded sample
 # ----------------------------------------------------------------------------------------------
@@ -447,39 +565,65 @@ def cpu_baseline(packing, batch, target_s=12.0):
 # arms
 # ----------------------------------------------------------------------------------------------
 
-def config_of(packing, batch, layers=None, stacked=True):
+def config_of(packing, batch, layers=None, stacked=True, seq=False):
     layers = LAYERS if layers is None else layers
     return {"workload": f"27B-class dense decode: {layers} layers x {{q,k,v,o,gate,up,down}} ternary GEMV "
                         "(hidden 5120, FFN 17408, 40/8 heads x 128), distinct weights per layer",
             "calls_per_layer": "4: qkv (q,k,v stacked, 7168 x 5120), o, gate_up (34816 x 5120), down" if stacked
             else "7: one per linear",
+            "engine": "tq_seq: the dependent chain (RMS norm -> qkv -> o -> RMS norm -> gate_up -> SwiGLU -> down) "
+                      "in one launch" if seq else "tq_gemv per call, graph-replayed",
             "packing": "base3_20_per_u32" if packing == tq.TQ_PACK_B3 else "2bit", "batch": batch,
             "group": 128, "fwht_block": 128, "layers": layers,
             "l2": "inputs larger than L2 (4.56 GB base-3 / 5.62 GB 2-bit of weights per step)"}
 
 
+def oracle_linear_bytes(lin, packing, group=128):
+    """Codes + scales of one linear, from the oracle's own size rules (no library call)."""
+    import oracle as O
+    return O.packed_bytes(lin.N, lin.K, packing) + O.scale_bytes(lin.N, lin.K, group)
+
+
 def run_reference(args, rank, world):
+    """The oracle arm: each step runs the fp64 oracle on a fixed row sample (the first 64 rows of each
+    of the seven linears of a layer) on the host cores; value = packed bytes of the sample / time."""
     if rank != 0:
         return
     packing, batch = PACKINGS[args.packing], 1
-    per_step = []
     for _ in range(args.warmup):
         oracle_sample_seconds(packing, batch, 16)
+    t0 = time.perf_counter()
+    total_b = 0
     for _ in range(args.steps):
-        s, b = oracle_sample_seconds(packing, batch, 64)
-        per_step.append(b / s / GB)
-    full_bytes = sum(linear_bytes(l, packing) for l in inputs.dense_layer_linears()) * LAYERS
-    v = statistics.median(per_step)
-    ms = full_bytes / (v * GB) * 1e3
+        _, b = oracle_sample_seconds(packing, batch, 64)
+        total_b += b
+    secs = time.perf_counter() - t0
+    v = total_b / secs / GB
+    full_bytes = sum(oracle_linear_bytes(l, packing) for l in inputs.dense_layer_linears()) * LAYERS
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "f64", "data": "synthetic", "config": config_of(packing, batch),
-            "tok_s": batch / (ms * 1e-3),
+            "warmup": args.warmup, "ms_per_step": secs / args.steps * 1e3, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": config_of(packing, batch),
+            "step": "one step = the oracle on the first 64 rows of each of the 7 linears of a layer "
+                    f"({total_b / args.steps / 1e6:.2f} MB of packed weights)",
+            "projected_ms_per_token": full_bytes / (v * GB) * 1e3,
             "cpu_baseline": {"value": v, "unit": "GB/s", "cores": blas_threads(), "kind": "oracle",
-                             "sample": "each step: fp64 numpy oracle on the first 64 rows of each of the 7 linears, "
-                                       "scaled by packed bytes to the 64-layer stream"},
+                             "sample": "each step: fp64 numpy oracle on the first 64 rows of each of the 7 "
+                                       "linears of one layer; value = packed bytes of the sample / time"},
             "e2e": {"value": v, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line))
+
+
+def e2e_time(fn, steps, world):
+    """Wall time of ``steps`` calls of fn(), each followed by a synchronize (the step's result is read
+    on the host), max over ranks."""
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        fn()
+        torch.cuda.synchronize()
+    return max_over_ranks(time.perf_counter() - t0, world)
 
 
 def run_tq(args, rank, world, local):
@@ -488,78 +632,96 @@ def run_tq(args, rank, world, local):
     peaks = measured_peaks()
     packing, batch = PACKINGS[args.packing], args.batch
     st = Stream(packing, batch, layers=args.layers)
-    # warm-up: W eager steps, then capture one step into a graph
-    for _ in range(args.warmup):
-        st.step()
-    torch.cuda.synchronize()
-    g = capture(st.step, warm=0)
-    g.replay()
-    torch.cuda.synchronize()
-    ms_total, clocks = time_graph(g, args.steps, world, clocks_index=local)
+    seq = args.engine == "seq" and packing == tq.TQ_PACK_2BIT and batch <= 8
+    if seq:
+        eng, g, ms_total, clocks = bench_seq(st, args.steps, world, clocks_index=local, warmup=args.warmup)
+        launches_per_step = tq.tq_seq_kernel_count(eng.plan.handle)
+        kernel = ("gemv_seq_kernel: the whole step (256 dependent calls) is this one persistent launch; "
+                  "duration = CUDA-event time of the graph-replayed steps / steps")
+    else:
+        eng = st
+        g, ms_total, clocks = bench_per_call(st, args.steps, world, clocks_index=local, warmup=args.warmup)
+        launches_per_step = sum(tq.tq_gemv_kernel_count(c[0], batch) for c in st.calls)
+        kernel = ("tq_gemv launches (decode GEMV kernel, plus the activation prep kernel above batch 4 or for "
+                  "base-3); duration = graph-replayed step time")
     ms_max = max_over_ranks(ms_total, world)
     ms_step = ms_max / args.steps
     bytes_all = st.bytes_per_step * args.steps * world
     value = bytes_all / (ms_max * 1e-3) / GB
-    # dominant kernel: the GEMV call, timed per call inside a captured step (external events)
-    durs = per_call_durations(st)
-    achieved = sum(c[4] for c in st.calls) / (sum(durs) * 1e-3) / GB
-    # end to end through the public API with host buffers
-    y_host = torch.empty_like(st.y_bufs[st.calls[-1][3]], device="cpu").pin_memory()
-    ge = capture(lambda: st.step_e2e(y_host), warm=1)
-    torch.cuda.synchronize()
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        ge.replay()
-        torch.cuda.synchronize()   # the step's result is read on the host
-    e2e_s = max_over_ranks(time.perf_counter() - t0, world)
+    achieved = st.bytes_per_step / (ms_step * 1e-3) / GB
+    # end to end through the public API: one token's input in from pinned host memory, one result out
+    y_host = torch.empty_like(eng.out if seq else st.y_bufs[st.calls[-1][3]], device="cpu").pin_memory()
+    for _ in range(2):
+        eng.step_e2e(y_host)
+    e2e_s = e2e_time(lambda: eng.step_e2e(y_host), args.steps, world)
     e2e_value = st.bytes_per_step * args.steps * world / e2e_s / GB
+    tkey = f"gemv_seq_2b_b{batch}_per_layer" if seq else \
+        f"dense_decode_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_stacked_per_layer"
+    per_layer = traffic_from_profiles(tkey)
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f32-accumulate (fp16 x~ operand, ternary weights)", "data": "synthetic",
-        "config": config_of(packing, batch, args.layers),
+        "config": config_of(packing, batch, args.layers, seq=seq),
         "tok_s": world * batch / (ms_step * 1e-3),
         "pct_of_hbm_peak": 100.0 * value / world / peaks["hbm_gbs"],
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"],
-                     "traffic": traffic_per_step(packing, batch, args.layers),
-                     "traffic_unit": "DRAM bytes per step: ncu bytes of one layer's launches x layers",
-                     "kernel": "tq_gemv calls (decode GEMV kernel, plus the activation prep kernel above batch 4 "
-                               "or for base-3), per-call CUDA events",
+                     "traffic": None if per_layer is None else per_layer * args.layers,
+                     "traffic_unit": "DRAM bytes per step: ncu dram__bytes_read.sum + dram__bytes_write.sum of a "
+                                     "short stream, per layer, x layers",
+                     "kernel": kernel, "kernel_ms": ms_step,
                      "algorithmic_bytes_per_step": st.bytes_per_step, "calls_per_step": len(st.calls),
                      "algorithmic_bytes_per_layer": st.bytes_per_step // max(1, args.layers),
-                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs)"},
-        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": st.h2d_bytes(),
-                "d2h_bytes_per_step": st.d2h_bytes()},
-        "gpu_launches": args.steps * sum(tq.tq_gemv_kernel_count(c[0], batch) for c in st.calls),
+                     "peak_source": peaks["source"] + " (MEASURED_PEAKS.json hbm_gbs, burst copy)"},
+        "e2e": {"value": e2e_value, "unit": "GB/s", "h2d_bytes_per_step": eng.h2d_bytes(),
+                "d2h_bytes_per_step": eng.d2h_bytes(),
+                "path": "per step: H2D of the token's bf16 input (pinned), the step, D2H of the last output, "
+                        "host synchronize"},
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "source_hash": source_hash(),
     }
-    del st, g, ge
-    torch.cuda.empty_cache()
+    del eng, g
     if rank == 0 and world == 1 and args.cpu:
         line["cpu_baseline"] = cpu_baseline(packing, batch)
     if args.extras and world == 1:
-        ex = {"stream": [], "moe": [], "prefill": []}
-        other = tq.TQ_PACK_B3 if packing == tq.TQ_PACK_2BIT else tq.TQ_PACK_2BIT
-        for pk, b, stk in ((packing, 8, True), (other, 1, True), (other, 8, True), (packing, 1, False),
-                           (other, 1, False)):
-            s2 = Stream(pk, b, stacked=stk)
-            s2.step()
-            g2 = capture(s2.step, warm=0)
-            g2.replay()
-            ms2, _ = time_graph(g2, max(3, args.steps // 2), 1)
-            ms2 /= max(3, args.steps // 2)
-            ex["stream"].append({"packing": "base3" if pk == tq.TQ_PACK_B3 else "2bit", "batch": b,
-                                 "calls_per_layer": 4 if stk else 7, "ms": ms2,
-                                 "GB_s": s2.bytes_per_step / (ms2 * 1e-3) / GB, "tok_s": b / (ms2 * 1e-3)})
+        ex = {"decode_step": [], "per_call_stream": [], "single_linear": None, "layer_linears": [],
+              "moe": [], "prefill": []}
+        reps = max(5, args.steps // 4)
+        if seq:   # the same weights called one launch per call
+            g2, ms2, _ = bench_per_call(st, reps)
+            ms2 /= reps
+            ex["per_call_stream"].append({"packing": "2bit", "batch": batch, "calls_per_layer": 4, "ms": ms2,
+                                          "GB_s": st.bytes_per_step / (ms2 * 1e-3) / GB,
+                                          "tok_s": batch / (ms2 * 1e-3)})
+            del g2
+        del st
+        torch.cuda.empty_cache()
+        for pk, b in ((tq.TQ_PACK_2BIT, 8), (tq.TQ_PACK_B3, 1), (tq.TQ_PACK_B3, 8)):
+            s2 = Stream(pk, b)
+            if pk == tq.TQ_PACK_2BIT:
+                e2, g2, ms2, _ = bench_seq(s2, reps)
+                ms2 /= reps
+                ex["decode_step"].append({"packing": "2bit", "batch": b, "engine": "tq_seq (one launch per step)",
+                                          "ms": ms2, "GB_s": s2.bytes_per_step / (ms2 * 1e-3) / GB,
+                                          "tok_s": b / (ms2 * 1e-3)})
+                del e2, g2
+            g2, ms2, _ = bench_per_call(s2, reps)
+            ms2 /= reps
+            ex["per_call_stream"].append({"packing": "base3" if pk == tq.TQ_PACK_B3 else "2bit", "batch": b,
+                                          "calls_per_layer": 4, "ms": ms2,
+                                          "GB_s": s2.bytes_per_step / (ms2 * 1e-3) / GB, "tok_s": b / (ms2 * 1e-3)})
             del s2, g2
             torch.cuda.empty_cache()
+        ex["single_linear"] = bench_single_linear(max(20, args.steps // 2))
+        for pk in (tq.TQ_PACK_2BIT, tq.TQ_PACK_B3):
+            ex["layer_linears"] += bench_layer_linears(pk, inputs.DENSE_DECODE["batches"], max(10, args.steps // 5))
+        torch.cuda.empty_cache()
         for T in inputs.MOE["tokens"]:
-            ex["moe"].append(bench_moe(T, max(5, args.steps // 2), 3))
+            ex["moe"].append(bench_moe(T, max(10, args.steps // 2), 3))
         for shape in inputs.PREFILL["shapes"]:
-            ex["prefill"].append(bench_prefill(shape, 3, 1))
+            ex["prefill"].append(bench_prefill(shape, 20, 3))
         for p in ex["prefill"]:
             p["pct_of_bf16_peak"] = 100.0 * p["TFLOP_s"] / peaks["bf16_tflops"]
         line["extras"] = ex
@@ -577,6 +739,8 @@ def main():
     ap.add_argument("--packing", choices=sorted(PACKINGS), default="2bit",
                     help="packing of the decode stream (the other one is measured under extras)")
     ap.add_argument("--layers", type=int, default=LAYERS, help="layers of the weight stream (profiling runs use 1)")
+    ap.add_argument("--engine", choices=["seq", "per_call"], default="seq",
+                    help="seq: the whole step as one tq_seq launch (2-bit, batch <= 8); per_call: one tq_gemv per call")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
     ap.add_argument("--workload", choices=["stream", "prefill", "moe"], default="stream",

@@ -96,6 +96,21 @@ tq_status tq_pack(const tq_desc* d, const int8_t* trits, uint32_t* codes, void* 
 tq_status tq_unpack(const tq_desc* d, const uint32_t* codes, int8_t* trits, int32_t* invalid_words,
                     void* stream);
 
+/* ---- tq_quantize: offline, dense bf16 W [N][K] -> codes [N][P] + FP16 scales [N][K/group] -----------
+ * The steps "27B 大模型塞进 5.9GB" puts before compression (section 二 ①: Hadamard rotation of the
+ * weights; section 二 ②: one FP16 scale per group; section 一: three levels).  The pages give no
+ * rounding rule; this uses absmean (BitNet b1.58):
+ *   u = H_128 w per 128-block of each row (unnormalised Sylvester; fwht_block = 0: u = w),
+ *   S = fp16_rn(mean_{group} |u| * c), c = 2^-3.5 (1 without the transform),
+ *   t = sign(u) if |u| * c > S / 2 else 0,
+ * all in fp64.  With fwht_block = 128 the result is the matrix tq_gemv / tq_gemm expect for the same
+ * x: W x ~= sum s t x~.  The sums are exact (and the result therefore bit-reproducible by any exact
+ * evaluation) when the magnitudes within each 128-block span less than 2^31.  A non-finite weight or
+ * a scale beyond the FP16 range records TQ_ERR_RANGE.  Requires K a multiple of 128, K <= 196608,
+ * group 64 or 128, flags 0.  w: device bf16, 16-byte aligned; codes: device, 16-byte aligned, the
+ * layout of tq_pack; scales: device. */
+tq_status tq_quantize(const tq_desc* d, const uint16_t* w, uint32_t* codes, uint16_t* scales, void* stream);
+
 /* ---- tq_fwht: x~[r, 128b + i] = sum_c H[i][c] x[r, 128b + c] / sqrt(block) -----------------------
  * Block Walsh-Hadamard transform (Sylvester order) of each row of x (bf16 [rows][K]); block must be
  * 128 and K a multiple of it ("27B 大模型塞进 5.9GB", section 二 ①).  out_fp16 = 0: out is float [rows][K];
@@ -215,6 +230,16 @@ tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, int E, int to
 size_t tq_gemm_workspace_bytes(const tq_desc* d, int M);
 tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                   int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream);
+
+/* ---- tq_selftest_wait: the bounded-wait path, made to run out on purpose ------------------------------
+ * Launches one CTA that waits on something nothing completes, with a wait limit of limit_ns
+ * (1 .. 1e9 ns) instead of the kernels' 4 s: kind 0 an mbarrier that is never arrived on (the
+ * TMA-ring wait of the decode and prefill kernels), kind 1 the grid barrier of tq_seq on a counter
+ * that no CTA arrives at (workspace: >= 4 bytes of device memory, 256-byte aligned, zeroed by this
+ * call; NULL allowed for kind 0).  The wait gives up, the kernel records TQ_ERR_TIMEOUT in the device
+ * status word (read it with tq_device_status) and returns; the context stays usable.  Diagnostic
+ * only: no result is computed. */
+tq_status tq_selftest_wait(int kind, long long limit_ns, void* workspace, void* stream);
 
 /* ---- status ---------------------------------------------------------------------------------------
  * The address of each device's status word is looked up once per process; do not use the library

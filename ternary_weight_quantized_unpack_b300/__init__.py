@@ -69,6 +69,7 @@ _SIGS = {
     "tq_pack": (_I, [_D, _P, _P, _P]),
     "tq_unpack": (_I, [_D, _P, _P, _P, _P]),
     "tq_fwht": (_I, [_P, _P, _I, _I, _I, _I, _P]),
+    "tq_quantize": (_I, [_D, _P, _P, _P, _P]),
     "tq_gemv_workspace_bytes": (_SZ, [_D, _I]),
     "tq_gemv": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "tq_gemv_noalloc": (_I, [_D, _P, _P, _P, _I, _P, _P]),
@@ -84,6 +85,7 @@ _SIGS = {
     "tq_seq_run": (_I, [_P, _P, _P]),
     "tq_seq_kernel_count": (_I, [_P]),
     "tq_seq_destroy": (None, [_P]),
+    "tq_selftest_wait": (_I, [_I, ctypes.c_longlong, _P, _P]),
     "tq_device_status": (_I, [ctypes.POINTER(ctypes.c_int32)]),
     "tq_status_str": (ctypes.c_char_p, [_I]),
     "tq_last_cuda_error": (_I, []),
@@ -180,6 +182,18 @@ def tq_unpack(d: tq_desc, codes: torch.Tensor, trits: torch.Tensor | None = None
     _check(lib().tq_unpack(ctypes.byref(d), _ptr(codes), _ptr(trits), _ptr(invalid_words), _stream(stream)),
            "tq_unpack")
     return trits, invalid_words
+
+
+def tq_quantize(d: tq_desc, w: torch.Tensor, codes: torch.Tensor | None = None, scales: torch.Tensor | None = None,
+                stream=None):
+    """bf16 W [N, K] -> (int32 codes [N, P], fp16 scales [N, K / group]): rotate, absmean-scale, ternarize, pack."""
+    assert w.dtype == torch.bfloat16 and w.is_contiguous()
+    if codes is None:
+        codes = torch.empty((d.N, tq_row_pitch_words(d)), dtype=torch.int32, device=w.device)
+    if scales is None:
+        scales = torch.empty((d.N, -(-d.K // d.group)), dtype=torch.float16, device=w.device)
+    _check(lib().tq_quantize(ctypes.byref(d), _ptr(w), _ptr(codes), _ptr(scales), _stream(stream)), "tq_quantize")
+    return codes, scales
 
 
 def tq_fwht(x: torch.Tensor, out_fp16: bool = False, block: int = 128, out: torch.Tensor | None = None,
@@ -316,6 +330,12 @@ class SeqPlan:
         if h is not None and _lib is not None:
             _lib.tq_seq_destroy(h)
             self.handle = None
+
+
+def tq_selftest_wait(kind: int, limit_ns: int, workspace: torch.Tensor | None = None, stream=None):
+    """Run the bounded-wait self-test (see include/tq.h); the timeout shows in tq_device_status()."""
+    _check(lib().tq_selftest_wait(kind, limit_ns, _ptr(workspace) if workspace is not None else None,
+                                  _stream(stream)), "tq_selftest_wait")
 
 
 def tq_device_status() -> int:

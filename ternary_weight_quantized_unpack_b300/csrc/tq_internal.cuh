@@ -53,8 +53,9 @@ __device__ __forceinline__ float warp_sum(float v) {
 // In-warp block Walsh-Hadamard transform of 128 values, 4 per lane (lane l holds elements
 // 4l..4l+3), Sylvester order, unnormalised: v <- H_128 v.  Butterfly (a, b) -> (a + b, a - b)
 // on pairs (i, i + h) for h = 1, 2 (in registers) and h = 4..64 (lane bit log2(h/4)).
-__device__ __forceinline__ void fwht128_warp(float (&v)[4]) {
-  float a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
+template <typename T>
+__device__ __forceinline__ void fwht128_warp(T (&v)[4]) {
+  T a0 = v[0] + v[1], a1 = v[0] - v[1], a2 = v[2] + v[3], a3 = v[2] - v[3];
   v[0] = a0 + a2; v[2] = a0 - a2; v[1] = a1 + a3; v[3] = a1 - a3;
   const int lane = threadIdx.x & 31;
 #pragma unroll
@@ -62,7 +63,7 @@ __device__ __forceinline__ void fwht128_warp(float (&v)[4]) {
     const bool upper = (lane & m) != 0;
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-      float p = __shfl_xor_sync(0xffffffffu, v[j], m);
+      T p = __shfl_xor_sync(0xffffffffu, v[j], m);
       v[j] = upper ? (p - v[j]) : (v[j] + p);
     }
   }

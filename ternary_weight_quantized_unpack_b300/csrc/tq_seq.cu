@@ -108,7 +108,7 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 
 // Grid barrier number k (after call k), in two halves so that work that does not depend on it can
 // run in between: grid_arrive (every thread; thread 0 arrives once this CTA's writes are visible) and
-// grid_wait (every thread; thread 0 waits until every CTA has arrived, false if kWaitNs passed first).
+// grid_wait (every thread; thread 0 waits until every CTA has arrived, false if limit_ns passed first).
 __device__ __forceinline__ void grid_arrive(unsigned* sync) {
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -116,7 +116,7 @@ __device__ __forceinline__ void grid_arrive(unsigned* sync) {
     atomicAdd(sync, 1u);
   }
 }
-__device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag) {
+__device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag, uint64_t limit_ns = kWaitNs) {
   if (threadIdx.x == 0) {
     *flag = 1;
     const unsigned target = (k + 1) * gridDim.x;
@@ -124,7 +124,7 @@ __device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag)
       const uint64_t t0 = global_timer_ns();
       for (uint32_t i = 0;; ++i) {
         if (ld_acquire(sync) >= target) break;
-        if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) {
+        if ((i & 63u) == 63u && global_timer_ns() - t0 > limit_ns) {
           *flag = 0;
           break;
         }
@@ -969,3 +969,47 @@ extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) 
 extern "C" int tq_seq_kernel_count(const tq_seq* s) { return s ? 1 : -1; }
 
 extern "C" void tq_seq_destroy(tq_seq* s) { delete s; }
+
+// ---- self-test of the bounded waits ------------------------------------------------------------
+namespace tq {
+namespace seq {
+
+// One CTA waits, with a short limit, on what nothing will complete: kind 0 an mbarrier that is
+// never arrived on (the form of every TMA-ring wait), kind 1 a grid barrier that no CTA arrives at
+// (the form of the call-boundary wait above).  The wait gives up, the kernel records TQ_ERR_TIMEOUT
+// exactly as the production kernels do and returns.
+__global__ void selftest_wait_kernel(int kind, unsigned long long limit_ns, unsigned* counter, int* status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int flag;
+  if (threadIdx.x == 0) {
+    mbar_init(&bar, 1);
+    fence_mbar_init();
+  }
+  __syncthreads();
+  bool ok;
+  if (kind == 0) {
+    ok = mbar_wait(&bar, 0, limit_ns);
+  } else {
+    ok = grid_wait(counter, 0, &flag, limit_ns);  // counter is 0 and nothing adds to it
+  }
+  if (!ok && threadIdx.x == 0) record_error(status, TQ_ERR_TIMEOUT);
+}
+
+}  // namespace seq
+}  // namespace tq
+
+extern "C" tq_status tq_selftest_wait(int kind, long long limit_ns, void* workspace, void* stream) {
+  using namespace tq;
+  if ((kind != 0 && kind != 1) || limit_ns <= 0 || limit_ns > 1000000000ll) return TQ_ERR_INVALID_ARG;
+  if (kind == 1 && !workspace) return TQ_ERR_INVALID_ARG;
+  if (workspace && !aligned(workspace, 256)) return TQ_ERR_MISALIGNED;
+  int* status = status_ptr();
+  if (!status) return TQ_ERR_CUDA;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  unsigned* counter = static_cast<unsigned*>(workspace);
+  cudaError_t e;
+  if (counter && (e = cudaMemsetAsync(counter, 0, sizeof(unsigned), st)) != cudaSuccess) return cuda_fail(e);
+  seq::selftest_wait_kernel<<<1, 32, 0, st>>>(kind, static_cast<unsigned long long>(limit_ns), counter, status);
+  if ((e = cudaGetLastError()) != cudaSuccess) return cuda_fail(e);
+  return TQ_OK;
+}

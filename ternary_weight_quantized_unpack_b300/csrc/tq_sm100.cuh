@@ -57,13 +57,14 @@ __device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
       : "memory");
   return ok != 0;
 }
-// Wait for the phase with the given parity to complete; false if kWaitNs passes first.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete; false if limit_ns passes first (the kernels
+// use kWaitNs; a shorter limit serves the self-test of this path).
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, uint64_t limit_ns = kWaitNs) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
   for (uint32_t i = 1;; ++i) {
     if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 15u) == 0 && global_timer_ns() - t0 > kWaitNs) return false;
+    if ((i & 15u) == 0 && global_timer_ns() - t0 > limit_ns) return false;
   }
 }
 

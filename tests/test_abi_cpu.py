@@ -90,6 +90,18 @@ def test_host_validation_before_launch():
     assert _call("tq_moe_gemv", ctypes.byref(gu), ctypes.byref(bad_dn), *args) == 1
     args_small_ws = [256, 8] + [A16] * 6 + [1, A16, A16, None, A16, A16, 64, None]
     assert _call("tq_moe_gemv", ctypes.byref(gu), ctypes.byref(dn), *args_small_ws) == 7
+    assert _call("tq_quantize", bd, None, A16, A16, None) == 1
+    assert _call("tq_quantize", ctypes.byref(tq.desc(64, 200)), A16, A16, A16, None) == 2     # K not a multiple of 128
+    assert _call("tq_quantize", ctypes.byref(tq.desc(64, 256, group=32)), A16, A16, A16, None) == 2
+    assert _call("tq_quantize", ctypes.byref(tq.desc(64, 256, flags=1)), A16, A16, A16, None) == 1
+    assert _call("tq_quantize", ctypes.byref(tq.desc(64, 128 * 2048)), A16, A16, A16, None) == 2  # row too long
+    assert _call("tq_quantize", bd, A16 + 8, A16, A16, None) == 3
+    assert _call("tq_quantize", bd, A16, A16, A16 + 1, None) == 3
+    assert _call("tq_selftest_wait", 2, 1000000, A16, None) == 1         # unknown kind
+    assert _call("tq_selftest_wait", 0, 0, None, None) == 1              # limit not positive
+    assert _call("tq_selftest_wait", 0, 2 * 10 ** 9, None, None) == 1    # limit above 1 s
+    assert _call("tq_selftest_wait", 1, 1000000, None, None) == 1        # kind 1 needs the counter
+    assert _call("tq_selftest_wait", 1, 1000000, A16 + 16, None) == 3    # counter not 256-aligned
 
 
 def test_status_strings_and_version():

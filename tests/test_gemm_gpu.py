@@ -45,3 +45,42 @@ def test_prefill_full_size_sampled(shape):
     x = case.x_host.float().numpy()[toks]
     y_ref, A, _ = O.ternary_linear(O.pack(t, B2), s, x, K, 128, B2, 128)
     check_bf16(y[np.ix_(toks, rows)], y_ref, A)
+
+
+def test_prefill_full_size_every_output():
+    """(M, K, N) = (2048, 5120, 17408), 2-bit, group 128: all 35.6 M outputs against the oracle."""
+    import oracle as O
+    M, K, N = inputs.PREFILL["shapes"][0]
+    case = LinearCase(inputs.seed_of(4), K, N, K, 128, B2, M)
+    y = run(case)
+    x = case.x_host.float().numpy()
+    for r0 in range(0, N, 2048):
+        rows = np.arange(r0, min(N, r0 + 2048))
+        t, s = case.host_rows(rows)
+        y_ref, A, _ = O.ternary_linear(O.pack(t, B2), s, x, K, 128, B2, 128)
+        check_bf16(y[:, rows], y_ref, A)
+
+
+@pytest.mark.parametrize("packing", [B2, B3])
+@pytest.mark.parametrize("mag", [1e3, 1e-4])
+def test_activation_magnitudes(packing, mag):
+    """Large and small activations (x~ held as FP16 without block scaling): within the tolerance."""
+    case = LinearCase(22, 3, 200, 1280, 128, packing, 130)
+    case.x_host = (case.x_host.float() * mag).to(torch.bfloat16)
+    case.x = case.x_host.cuda()
+    y_ref, A = case.oracle()
+    check_bf16(run(case), y_ref, A)
+
+
+def test_out_of_fp16_range_is_reported():
+    """|x~| beyond the FP16 range (activations ~1e5) records TQ_ERR_RANGE in the device status."""
+    case = LinearCase(23, 4, 128, 512, 128, B2, 64)
+    case.x = (case.x_host.float() * 1e5).to(torch.bfloat16).cuda()
+    tq.tq_gemm(case.desc, case.codes, case.scales, case.x)
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 8          # TQ_ERR_RANGE
+    assert tq.tq_device_status() == 0
+    # an in-range call afterwards is correct
+    case2 = LinearCase(23, 5, 128, 512, 128, B2, 64)
+    y_ref, A = case2.oracle()
+    check_bf16(run(case2), y_ref, A)

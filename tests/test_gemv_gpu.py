@@ -128,3 +128,71 @@ def test_static_weights_flag(packing, N, K, batch):
     rows = sample_rows(N, 64, seed=N)
     y_ref, A = case.oracle(rows)
     check_tolerance(y_default.cpu().numpy()[:, rows], y_ref, A)
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("batch", [2, 16])
+@pytest.mark.parametrize("N,K", [(300, 1280), (7168, 5120)])
+def test_mixed_magnitude_batch(packing, batch, N, K):
+    """Rows of one call 1e7 apart in size (even rows x 1e4, odd rows x 1e-3): each row is held to its
+    own bound 1e-3 * sum |s t x~| + 1e-5, so a small row next to a large one must keep its precision."""
+    case = LinearCase(17, batch + N, N, K, 128, packing, batch)
+    mult = torch.tensor([1e4 if b % 2 == 0 else 1e-3 for b in range(batch)]).reshape(batch, 1)
+    case.x_host = (case.x_host.float() * mult).to(torch.bfloat16)
+    case.x = case.x_host.cuda()
+    rows = np.arange(N) if N <= 1024 else sample_rows(N, 512, seed=N)
+    y_ref, A = case.oracle(rows)
+    y = run(case)
+    check_tolerance(y[:, rows], y_ref, A)
+
+
+def _graph_of(fn):
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        fn()
+    torch.cuda.synchronize()
+    return g
+
+
+@pytest.mark.parametrize("packing", [B3, B2])
+@pytest.mark.parametrize("batch", [1, 8])
+def test_stacked_projections_graph_replayed_every_output(packing, batch):
+    """The launch configuration of the per-call decode stream: the stacked qkv (7168 x 5120) and
+    gate_up (34816 x 5120) projections with TQ_STATIC_WEIGHTS, called back to back (qkv, gate_up,
+    qkv again) inside a CUDA graph; after a replay every output of every call is compared with the
+    oracle."""
+    lins = inputs.stacked_layer_linears()
+    cases = []
+    for lin in (lins[0], lins[2]):
+        tid = 300 + lins.index(lin)
+        c = LinearCase(inputs.seed_of(5), tid, lin.N, lin.K, 128, packing, batch)
+        c.desc = tq.desc(lin.N, lin.K, 128, packing, flags=tq.TQ_STATIC_WEIGHTS)
+        cases.append(c)
+    ws = torch.empty(max(tq.tq_gemv_workspace_bytes(c.desc, batch) for c in cases), dtype=torch.uint8, device="cuda")
+    ys = [torch.empty((batch, c.N), dtype=torch.float32, device="cuda") for c in cases]
+    y_again = torch.empty_like(ys[0])
+
+    def step():
+        tq.tq_gemv(cases[0].desc, cases[0].codes, cases[0].scales, cases[0].x, y=ys[0], workspace=ws)
+        tq.tq_gemv(cases[1].desc, cases[1].codes, cases[1].scales, cases[1].x, y=ys[1], workspace=ws)
+        tq.tq_gemv(cases[0].desc, cases[0].codes, cases[0].scales, cases[0].x, y=y_again, workspace=ws)
+
+    g = _graph_of(step)
+    for y in ys + [y_again]:
+        y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    for c, y in zip(cases, ys):
+        yh = y.cpu().numpy()
+        for r0 in range(0, c.N, 4096):
+            rows = np.arange(r0, min(c.N, r0 + 4096))
+            y_ref, A = c.oracle(rows)
+            check_tolerance(yh[:, rows], y_ref, A, what=f"N={c.N} rows {r0}..")
+    assert torch.equal(y_again, ys[0])

@@ -161,3 +161,16 @@ def test_rejected_on_the_host():
     ok = tq.tq_seq_create([(d, codes, scales, BF16, x, y)], 1)
     assert tq.tq_seq_kernel_count(ok) == 1
     tq.tq_seq_destroy(ok)
+
+
+@pytest.mark.parametrize("batch", [2, 8])
+def test_chain_mixed_magnitude_rows(batch):
+    """Batch rows 1e7 apart in size in one decode step (even rows x 1e4, odd rows x 1e-3): every call
+    holds each row to its own bound (per-row block exponents; RMS normalisation per row)."""
+    c = Chain(81 + batch, SMALL_G128[:4], batch)
+    mult = torch.tensor([1e4 if b % 2 == 0 else 1e-3 for b in range(batch)]).reshape(batch, 1)
+    c.x_host = (c.x_host.float() * mult).to(torch.bfloat16)
+    c.x.copy_(c.x_host.cuda())
+    ys = c.run()
+    for j in range(4):
+        c.check_call(j, ys)
