@@ -9,14 +9,16 @@
 //    each row, 128-byte swizzle, plus the matching 32 x 8 FP16 scales) into a private ring of
 //    shared-memory stages.  The ring runs ahead across call boundaries: while the grid waits on a
 //    barrier and the next input is being transformed, the next call's weights are already in flight.
-//  * Calls are ordered by one grid-wide barrier each (a counter in the workspace, bounded wait).
+//  * Calls are separated by two grid-wide barriers (a counter in the workspace, bounded waits):
+//    after the first, every partial sum of the call is written and each CTA turns its share of the
+//    call's output rows into final values (partial sums added in K order, times the output scale);
+//    after the second, the whole output is final and the next call's CTAs read the rows they need.
 //  * Work split, K-major: the items (32-row unit ru, 512-trit K slice ku) of a call are ordered by
 //    ku, then ru, and divided into equal contiguous ranges, one per CTA (and each into ranges for
 //    its warps).  A CTA therefore works on one or two K slices of many row units: it transforms only
 //    the activations of its own slices, and every item writes its own partial sums (32 rows x batch)
-//    to the workspace.  Whoever reads a call's output afterwards - the next call's input transform,
-//    and the CTA that writes the final y after the barrier - adds the partial sums of the K slices
-//    in ku order, so results do not depend on timing.
+//    to the workspace; the CTA that finalizes an output row adds its K slices' partial sums in ku
+//    order, so results do not depend on timing.
 //  * Decode and multiply-add are those of the 2-bit decode GEMV: a digit d = t + 1 in mantissa bits
 //    2i of an FP16 half is the subnormal d * 2^(2i-24), one LOP3 per operand register, mma.sync
 //    m16n8k16 with FP32 accumulation.  Each group of 64 or 128 weights has its own FP16 scale
@@ -28,8 +30,8 @@
 //    vector, of the previous call's output, of that output divided by its root mean square (the
 //    normalisation a pre-norm decoder applies before its attention and FFN projections), or of
 //    silu(gate) * up of the previous call's output (the SwiGLU of a stacked gate/up projection).
-//    The RMS factor is a per-call scalar: the call computes W * FWHT(input) and its readers multiply
-//    by 1 / rms, formed from per-block sums of squares the input transform stores.
+//    The RMS factor is a per-call scalar: the call computes W * FWHT(input) and the finalize step
+//    multiplies by 1 / rms, formed from per-block sums of squares the input transform stores.
 #include <algorithm>
 #include <cstring>
 #include <new>
@@ -85,10 +87,8 @@ struct Params {
   int ncalls, B;
   int* status;
   unsigned* sync;         // [0]: barrier arrivals, [1]: CTAs that have exited
-  float* part;            // partial sums: [2][items][Bp][32] (parity of the call)
-  float* ssq;             // per 128-block sums of squares of an RMS-normalised input: [2][blocks][Bp]
-  size_t part_stride;     // floats per parity of part
-  int ssq_stride;         // floats per parity of ssq
+  float* part;            // partial sums of the current call: [items][Bp][32]
+  float* ssq;             // per 128-block sums of squares of an RMS-normalised input: [blocks][Bp]
   int nkc;                // K slices one CTA may cover (x^ capacity)
   int stage_floats;       // capacity of the gather staging buffer
   uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc, off_stage;
@@ -217,6 +217,20 @@ __device__ __forceinline__ float4 in_row4(const float* stage, int soff, int Bp, 
   a.z *= scale;
   a.w *= scale;
   return a;
+}
+
+// Rows [r0[sg], r0[sg] + nr[sg]) (multiples of 4) of the finished call pc's final output, for every
+// batch row, into the staging buffer in the layout gather() writes.
+__device__ __forceinline__ void load_rows(const CallLite& pc, int B, int Bp, int nseg, const int (&r0)[3],
+                                          const int (&nr)[3], float* stage) {
+  for (int sg = 0; sg < nseg; ++sg) {
+    float4* dst = reinterpret_cast<float4*>(stage + seg_offset(nr, Bp, sg));
+    const int n4 = (nr[sg] / 4) * B;
+    for (int t = threadIdx.x; t < n4; t += blockDim.x) {
+      const int b = t % B, c4 = t / B;
+      dst[c4 * Bp + b] = __ldcg(reinterpret_cast<const float4*>(pc.y + static_cast<size_t>(b) * pc.N + r0[sg] + 4 * c4));
+    }
+  }
 }
 
 // ---- the activation transform ------------------------------------------------------------------
@@ -431,14 +445,12 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
 
   bool abort = false;
   const LaneLayout<G> L(lane);
-  float pscale[BP];  // output scale of the previous call, per batch row
+  float ones[BP];
+#pragma unroll
+  for (int b = 0; b < BP; ++b) ones[b] = 1.f;
+  unsigned nbar = 0;  // grid barriers passed
   for (int j = 0; j < p.ncalls && !abort; ++j) {
     const CallLite c(p.calls[j]);
-    const int par = j & 1;
-    float* part = p.part + static_cast<size_t>(par) * p.part_stride;
-    float* ssq = p.ssq + par * p.ssq_stride;
-    const float* ppart = p.part + static_cast<size_t>(par ^ 1) * p.part_stride;
-    const float* pssq = p.ssq + (par ^ 1) * p.ssq_stride;
     const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
     // ---- this CTA's items and the K slices they cover ----
     int ca = 0, cb = 0, ku_lo = 0, ku_hi = -1;
@@ -450,29 +462,19 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     }
     const int krow0 = ku_lo * kItemTrits;                                       // first input row needed
     const int nkrow = ku_hi >= ku_lo ? min((ku_hi + 1) * kItemTrits, c.K) - krow0 : 0;
-    // ---- the previous call's output scale (last warp) and the input rows this CTA needs, summed
-    //      from the previous call's partial sums (the other warps) ----
-    if (warp == kNW - 1) {
-#pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        const float sc = j > 0 && b < p.B ? out_scale_warp(pc, pssq, BP, b, lane) : 1.f;
-        if (lane == 0) s_scale[b] = sc;
-      }
-    }
+    // ---- the input rows this CTA needs: the previous call's final output ----
     if (j > 0 && c.mode != 0 && nkrow > 0) {
       const int r0[3] = {krow0, c.K + krow0, 0}, nr[3] = {nkrow, c.mode == 2 ? nkrow : 0, 0};
-      gather(pc, ppart, p.B, BP, c.mode == 2 ? 2 : 1, r0, nr, stage, (kNW - 1) * 32);
+      load_rows(pc, p.B, BP, c.mode == 2 ? 2 : 1, r0, nr, stage);
     }
     __syncthreads();
-#pragma unroll
-    for (int b = 0; b < BP; ++b) pscale[b] = s_scale[b];
     // ---- input transform of this CTA's K slices ----
     if (cb > ca) {
       const int blk0 = ku_lo * BPI;
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
-        prep_block<G, BP>(p, c, stage, krow0, nkrow, pscale, blk, (blk - blk0) * (kFwhtBlock / G), L, xh, V, Fv,
-                          ssq, lane);
+        prep_block<G, BP>(p, c, stage, krow0, nkrow, ones, blk, (blk - blk0) * (kFwhtBlock / G), L, xh, V, Fv,
+                          p.ssq, lane);
     }
     __syncthreads();
 
@@ -493,7 +495,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       const uint16_t* ss = scales_st + st * (kScaleStage / 2);
       const int g_item0 = ku * GPI;                  // first group of the item
       const int lg_item0 = (ku - ku_lo) * GPI;       // ... in this CTA's x^
-      const int ngi = min(GPI, c.ng - g_item0);      // groups in the item
+      constexpr int ngi = GPI;  // groups in the item: K is a multiple of 8 groups, so items are whole
       const int gofs = g_item0 & 7;                  // its column in the scale box
       float acc[2][4];
 #pragma unroll
@@ -627,7 +629,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
         }
         constexpr int nwq = BP >= 2 ? BP / 2 : 1;  // quad threads holding distinct batch rows
         if (q < nwq) {
-          float* dst = part + (static_cast<size_t>(ku) * c.nru + ru) * BP * kRows;
+          float* dst = p.part + (static_cast<size_t>(ku) * c.nru + ru) * BP * kRows;
 #pragma unroll
           for (int s = 0; s < 2; ++s)
 #pragma unroll
@@ -649,50 +651,46 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     __syncthreads();
     abort = s_flag[0] != 0;
     if (abort) break;
+    // ---- barrier: every partial sum and sum of squares of this call is written ----
     grid_arrive(p.sync);
-    // ---- while the barrier fills: the previous call's final output, this CTA's share of its rows ----
-    if (j > 0) {
-      const int fr0 = (cta * (pc.N / 4)) / static_cast<int>(gridDim.x) * 4;
-      const int fr1 = ((cta + 1) * (pc.N / 4)) / static_cast<int>(gridDim.x) * 4;
+    if (!grid_wait(p.sync, nbar++, s_flag + 1)) {
+      if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      abort = true;
+      break;
+    }
+    // ---- this CTA's share of the call's output rows: partial sums in ku order, times the output
+    //      scale (the last warp forms the scale while the others add) ----
+    {
+      if (warp == kNW - 1) {
+#pragma unroll
+        for (int b = 0; b < BP; ++b) {
+          const float sc = b < p.B ? out_scale_warp(c, p.ssq, BP, b, lane) : 1.f;
+          if (lane == 0) s_scale[b] = sc;
+        }
+      }
+      const int fr0 = (cta * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
+      const int fr1 = ((cta + 1) * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
       const int r0[3] = {fr0, 0, 0}, nr[3] = {fr1 - fr0, 0, 0};
-      gather(pc, ppart, p.B, BP, 1, r0, nr, stage, kNW * 32);
+      gather(c, p.part, p.B, BP, 1, r0, nr, stage, (kNW - 1) * 32);
       __syncthreads();
       for (int e = threadIdx.x; e < (fr1 - fr0) / 4 * p.B; e += blockDim.x) {
         const int b = e % p.B, k = 4 * (e / p.B);
-        *reinterpret_cast<float4*>(pc.y + static_cast<size_t>(b) * pc.N + fr0 + k) =
-            in_row4(stage, 0, BP, b, k, pscale[b]);
+        *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + fr0 + k) =
+            in_row4(stage, 0, BP, b, k, s_scale[b]);
       }
     }
-    if (!grid_wait(p.sync, static_cast<unsigned>(j), s_flag + 1)) {
-      if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
-      abort = true;
+    // ---- barrier: the whole output is final before the next call reads it or overwrites the
+    //      partial sums ----
+    if (j + 1 < p.ncalls) {
+      grid_arrive(p.sync);
+      if (!grid_wait(p.sync, nbar++, s_flag + 1)) {
+        if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        abort = true;
+      }
     }
   }
 
-  if (!abort) {
-    // the last call's final output: this CTA's share of its rows
-    const int j = p.ncalls - 1;
-    const CallLite c(p.calls[j]);
-    const float* lpart = p.part + static_cast<size_t>(j & 1) * p.part_stride;
-    const float* lssq = p.ssq + (j & 1) * p.ssq_stride;
-    if (warp == 0) {
-#pragma unroll
-      for (int b = 0; b < BP; ++b) {
-        const float sc = b < p.B ? out_scale_warp(c, lssq, BP, b, lane) : 1.f;
-        if (lane == 0) s_scale[b] = sc;
-      }
-    }
-    const int fr0 = (cta * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
-    const int fr1 = ((cta + 1) * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
-    const int r0[3] = {fr0, 0, 0}, nr[3] = {fr1 - fr0, 0, 0};
-    gather(c, lpart, p.B, BP, 1, r0, nr, stage, kNW * 32);
-    __syncthreads();
-    for (int e = threadIdx.x; e < (fr1 - fr0) / 4 * p.B; e += blockDim.x) {
-      const int b = e % p.B, k = 4 * (e / p.B);
-      *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + fr0 + k) =
-          in_row4(stage, 0, BP, b, k, s_scale[b]);
-    }
-  } else {
+  if (abort) {
     // wind down: wait (bounded) for this warp's copies still in flight before the CTA exits
     for (; consumed < issued; ++consumed) {
       if (!mbar_wait(&full[cst], cph)) break;
@@ -806,7 +804,6 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   // per-call work split; the most K slices any CTA covers, the largest item count
   s->calls.resize(ncalls);
   long long Tmax = 0;
-  int fin_prev = 0;         // rows of the previous call one CTA finalizes
   long long stage_rows = 4;  // largest gather of any call
   for (int j = 0; j < ncalls; ++j) {
     const tq_seq_call& c = calls[j];
@@ -835,9 +832,8 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
       if (b > a) kmax = std::max(kmax, std::min(((b - 1) / d.nru + 1) * kItemTrits, d.K) - (a / d.nru) * kItemTrits);
     }
     const int segs = c.x_src == TQ_SEQ_X_BF16 ? 0 : c.x_src == TQ_SEQ_X_SWIGLU_PREV ? 2 : 1;
-    stage_rows = std::max<long long>(stage_rows, static_cast<long long>(segs) * kmax + fin_prev);
-    fin_prev = ((d.N / 4) / sms + 1) * 4;
-    stage_rows = std::max<long long>(stage_rows, fin_prev);  // the last call's finalize
+    stage_rows = std::max<long long>(stage_rows, static_cast<long long>(segs) * kmax);
+    stage_rows = std::max<long long>(stage_rows, ((d.N / 4) / sms + 1) * 4);  // the rows it finalizes
     for (int cta = 0; cta < d.gp; ++cta) {
       const int a = cta_start(d.T, d.gp, cta), b = cta_start(d.T, d.gp, cta + 1);
       if (b > a) s->nkc = std::max(s->nkc, (b - 1) / d.nru - a / d.nru + 1);
@@ -901,8 +897,8 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   s->ssq_stride = (Kmax / kFwhtBlock) * s->Bp;
   s->ws_calls = align256(sizeof(CallDev) * ncalls);
   s->ws_sync = 256;
-  s->ws_part = align256(2 * s->part_stride * 4);
-  s->ws_ssq = align256(static_cast<size_t>(2) * s->ssq_stride * 4);
+  s->ws_part = align256(s->part_stride * 4);
+  s->ws_ssq = align256(static_cast<size_t>(s->ssq_stride) * 4);
   s->ws_bytes = s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq;
   *out = s;
   return TQ_OK;
@@ -939,8 +935,6 @@ extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) 
   prm.sync = reinterpret_cast<unsigned*>(ws + s->ws_calls);
   prm.part = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync);
   prm.ssq = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync + s->ws_part);
-  prm.part_stride = s->part_stride;
-  prm.ssq_stride = s->ssq_stride;
   prm.nkc = s->nkc;
   prm.off_scales = s->off_scales;
   prm.off_xh = s->off_xh;
