@@ -9,10 +9,12 @@
 //    each row, 128-byte swizzle, plus the matching 32 x 8 FP16 scales) into a private ring of
 //    shared-memory stages.  The ring runs ahead across call boundaries: while the grid waits on a
 //    barrier and the next input is being transformed, the next call's weights are already in flight.
-//  * Calls are separated by two grid-wide barriers (a counter in the workspace, bounded waits):
-//    after the first, every partial sum of the call is written and each CTA turns its share of the
-//    call's output rows into final values (partial sums added in K order, times the output scale);
-//    after the second, the whole output is final and the next call's CTAs read the rows they need.
+//  * After a call's items, one grid-wide barrier (a counter in the workspace, bounded wait): every
+//    partial sum of the call is written.  Each CTA then turns its share of the call's output rows
+//    into final values (partial sums added in K order, times the output scale) and raises its ready
+//    flag; the next call's CTAs wait (bounded) only for the flags of the CTAs that finalized the
+//    rows they read.  Partial sums and sums of squares alternate between two buffers by the parity
+//    of the call, so a CTA may start the next call while others still finalize this one.
 //  * Work split, K-major: the items (32-row unit ru, 512-trit K slice ku) of a call are ordered by
 //    ku, then ru, and divided into equal contiguous ranges, one per CTA (and each into ranges for
 //    its warps).  A CTA therefore works on one or two K slices of many row units: it transforms only
@@ -86,9 +88,11 @@ struct Params {
   const CallDev* calls;
   int ncalls, B;
   int* status;
-  unsigned* sync;         // [0]: barrier arrivals, [1]: CTAs that have exited
-  float* part;            // partial sums of the current call: [items][Bp][32]
-  float* ssq;             // per 128-block sums of squares of an RMS-normalised input: [blocks][Bp]
+  unsigned* sync;         // [0]: barrier arrivals, [1]: CTAs that have exited, [64 + cta]: ready flags
+  float* part;            // partial sums: [2][items][Bp][32] (parity of the call)
+  float* ssq;             // per 128-block sums of squares of an RMS-normalised input: [2][blocks][Bp]
+  size_t part_stride;     // floats per parity of part
+  int ssq_stride;         // floats per parity of ssq
   int nkc;                // K slices one CTA may cover (x^ capacity)
   int stage_floats;       // capacity of the gather staging buffer
   uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc, off_stage;
@@ -132,6 +136,43 @@ __device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag,
     }
     __threadfence();
   }
+  __syncthreads();
+  return *flag != 0;
+}
+
+// Ready flags: CTA c stores j + 1 in flags[c] (release) once its rows of call j's output are final.
+constexpr int kFlagBase = 64;  // flags start at this word of the sync area
+__device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
+  asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+// Rows [fr0, fr1) of an N-row output that CTA c of `grid` finalizes.
+__device__ __forceinline__ void fin_rows(int N, int c, int grid, int& fr0, int& fr1) {
+  fr0 = (c * (N / 4)) / grid * 4;
+  fr1 = ((c + 1) * (N / 4)) / grid * 4;
+}
+// Every thread t < grid whose CTA finalized any of the rows [r0[sg], r0[sg] + nr[sg]) of call pc
+// waits (bounded) for that CTA's flag to reach `want`; then the CTA synchronises.  False on timeout.
+__device__ __forceinline__ bool wait_rows_ready(const unsigned* flags, const CallLite& pc, int nseg, const int (&r0)[3],
+                                                const int (&nr)[3], unsigned want, int* flag) {
+  if (threadIdx.x == 0) *flag = 1;
+  __syncthreads();
+  const int grid = static_cast<int>(gridDim.x);
+  for (int t = threadIdx.x; t < grid; t += blockDim.x) {
+    int fr0, fr1;
+    fin_rows(pc.N, t, grid, fr0, fr1);
+    bool need = false;
+    for (int sg = 0; sg < nseg; ++sg) need = need || (fr0 < r0[sg] + nr[sg] && r0[sg] < fr1);
+    if (!need || ld_acquire(flags + t) >= want) continue;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0;; ++i) {
+      if (ld_acquire(flags + t) >= want) break;
+      if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) {
+        *flag = 0;
+        break;
+      }
+    }
+  }
+  __threadfence();
   __syncthreads();
   return *flag != 0;
 }
@@ -452,6 +493,8 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   for (int j = 0; j < p.ncalls && !abort; ++j) {
     const CallLite c(p.calls[j]);
     const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
+    float* part = p.part + static_cast<size_t>(j & 1) * p.part_stride;
+    float* ssq = p.ssq + (j & 1) * p.ssq_stride;
     // ---- this CTA's items and the K slices they cover ----
     int ca = 0, cb = 0, ku_lo = 0, ku_hi = -1;
     if (cta < c.gp) {
@@ -465,6 +508,12 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     // ---- the input rows this CTA needs: the previous call's final output ----
     if (j > 0 && c.mode != 0 && nkrow > 0) {
       const int r0[3] = {krow0, c.K + krow0, 0}, nr[3] = {nkrow, c.mode == 2 ? nkrow : 0, 0};
+      if (!wait_rows_ready(p.sync + kFlagBase, pc, c.mode == 2 ? 2 : 1, r0, nr, static_cast<unsigned>(j),
+                           s_flag + 1)) {
+        if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        abort = true;
+        break;
+      }
       load_rows(pc, p.B, BP, c.mode == 2 ? 2 : 1, r0, nr, stage);
     }
     __syncthreads();
@@ -474,7 +523,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
         prep_block<G, BP>(p, c, stage, krow0, nkrow, ones, blk, (blk - blk0) * (kFwhtBlock / G), L, xh, V, Fv,
-                          p.ssq, lane);
+                          ssq, lane);
     }
     __syncthreads();
 
@@ -629,7 +678,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
         }
         constexpr int nwq = BP >= 2 ? BP / 2 : 1;  // quad threads holding distinct batch rows
         if (q < nwq) {
-          float* dst = p.part + (static_cast<size_t>(ku) * c.nru + ru) * BP * kRows;
+          float* dst = part + (static_cast<size_t>(ku) * c.nru + ru) * BP * kRows;
 #pragma unroll
           for (int s = 0; s < 2; ++s)
 #pragma unroll
@@ -664,14 +713,14 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       if (warp == kNW - 1) {
 #pragma unroll
         for (int b = 0; b < BP; ++b) {
-          const float sc = b < p.B ? out_scale_warp(c, p.ssq, BP, b, lane) : 1.f;
+          const float sc = b < p.B ? out_scale_warp(c, ssq, BP, b, lane) : 1.f;
           if (lane == 0) s_scale[b] = sc;
         }
       }
-      const int fr0 = (cta * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
-      const int fr1 = ((cta + 1) * (c.N / 4)) / static_cast<int>(gridDim.x) * 4;
+      int fr0, fr1;
+      fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
       const int r0[3] = {fr0, 0, 0}, nr[3] = {fr1 - fr0, 0, 0};
-      gather(c, p.part, p.B, BP, 1, r0, nr, stage, (kNW - 1) * 32);
+      gather(c, part, p.B, BP, 1, r0, nr, stage, (kNW - 1) * 32);
       __syncthreads();
       for (int e = threadIdx.x; e < (fr1 - fr0) / 4 * p.B; e += blockDim.x) {
         const int b = e % p.B, k = 4 * (e / p.B);
@@ -679,14 +728,11 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
             in_row4(stage, 0, BP, b, k, s_scale[b]);
       }
     }
-    // ---- barrier: the whole output is final before the next call reads it or overwrites the
-    //      partial sums ----
-    if (j + 1 < p.ncalls) {
-      grid_arrive(p.sync);
-      if (!grid_wait(p.sync, nbar++, s_flag + 1)) {
-        if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
-        abort = true;
-      }
+    // ---- this CTA's rows are final: raise its flag ----
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      __threadfence();
+      st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
     }
   }
 
@@ -706,6 +752,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     __threadfence();
     const unsigned prev = atomicAdd(p.sync + 1, 1u);
     if (prev == gridDim.x - 1 && !abort) {
+      for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
       p.sync[0] = 0u;
       p.sync[1] = 0u;
       __threadfence();
@@ -896,9 +943,9 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   s->part_stride = static_cast<size_t>(Tmax) * s->Bp * kRows;
   s->ssq_stride = (Kmax / kFwhtBlock) * s->Bp;
   s->ws_calls = align256(sizeof(CallDev) * ncalls);
-  s->ws_sync = 256;
-  s->ws_part = align256(s->part_stride * 4);
-  s->ws_ssq = align256(static_cast<size_t>(s->ssq_stride) * 4);
+  s->ws_sync = align256((kFlagBase + static_cast<size_t>(sms)) * 4);
+  s->ws_part = align256(2 * s->part_stride * 4);
+  s->ws_ssq = align256(static_cast<size_t>(2) * s->ssq_stride * 4);
   s->ws_bytes = s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq;
   *out = s;
   return TQ_OK;
@@ -935,6 +982,8 @@ extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) 
   prm.sync = reinterpret_cast<unsigned*>(ws + s->ws_calls);
   prm.part = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync);
   prm.ssq = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync + s->ws_part);
+  prm.part_stride = s->part_stride;
+  prm.ssq_stride = s->ssq_stride;
   prm.nkc = s->nkc;
   prm.off_scales = s->off_scales;
   prm.off_xh = s->off_xh;
