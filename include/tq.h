@@ -214,7 +214,10 @@ tq_status tq_moe_route(const float* logits, int T, int E, int topk, int32_t* idx
  * gate_up: desc with N = 2F, K = H; down: desc with N = H, K = F (same packing/group/fwht).
  * gu_codes [E][2F][P_H], gu_scales [E][2F][H/group], d_codes [E][H][P_F], d_scales [E][H][F/group].
  * x: bf16 [T][H]; idx/gate as tq_moe_route; h_out: float [T][topk][F] or NULL; y: float [T][H].
- * Each active expert's codes are read once per call for all the tokens routed to it. */
+ * Three launches: routing and the chunk table (one CTA), the gate/up GEMV, the down GEMV with the
+ * combine fused into it.  The tokens routed to an expert are processed in chunks of 1 (T = 1) or 2
+ * tokens; each chunk streams its expert's codes once, so an expert with n routed tokens is read
+ * ceil(n / 2) times per call. */
 size_t tq_moe_workspace_bytes(int T, int E, int topk, int H, int F);
 tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, int E, int topk,
                       const uint32_t* gu_codes, const uint16_t* gu_scales,

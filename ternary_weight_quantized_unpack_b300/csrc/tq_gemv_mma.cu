@@ -294,6 +294,10 @@ struct Params {
   const uint16_t* x;
   const float* gu;
   float* h_out;
+  // Fused combine of the expert layer (count == nullptr: none); see ChunkCombine.
+  int* cmb_count;
+  const float* cmb_gate;
+  float* cmb_y;
 };
 
 // Operands of this CTA: the whole call, or one chunk of routed tokens.
@@ -460,6 +464,44 @@ __device__ __forceinline__ void fused_prologue(const Params& p, const Cta& c, co
 // Partial sums red[kl][RT][B] (in shared memory) -> y.  K-lanes are added in lane order, then the
 // cluster's CTAs in rank order through distributed shared memory.  Every thread calls this.
 // ---------------------------------------------------------------------------------------------
+// The expert layer's combine, fused into the down projection: count this CTA's finished slot for each
+// of its tokens; for the tokens whose topk slots are now all finished, add the slots' outputs (rows of
+// this tile) in slot order, weighted by the gates.  flags: shared scratch (one int per batch slot).
+// The CTA's output stores precede the count (barrier, then a device-scope fence by the counting
+// thread); the combining CTA fences after reading the count, before it loads the other slots' rows.
+__device__ __forceinline__ void combine_tokens(const Params& p, const Cta& c, const Sel& sel, int* flags) {
+  __syncthreads();  // every thread's stores (and, before this, any use of the scratch) are done
+  const int tile = static_cast<int>(blockIdx.x), tiles = static_cast<int>(gridDim.x);
+  if (threadIdx.x == 0) {
+    __threadfence();
+    for (int b = 0; b < p.B; ++b) {
+      flags[b] = -1;
+      if (b >= sel.count) continue;
+      const int t = sel.rows[b] / p.topk;
+      if (atomicAdd(p.cmb_count + static_cast<size_t>(t) * tiles + tile, 1) == p.topk - 1) flags[b] = t;
+    }
+    __threadfence();
+  }
+  __syncthreads();
+  for (int b = 0; b < p.B; ++b) {
+    const int t = flags[b];
+    if (t < 0) continue;
+    const float* gate = p.cmb_gate + static_cast<size_t>(t) * p.topk;
+    for (int rl = threadIdx.x; rl < c.RT; rl += blockDim.x) {
+      const int row = c.row0 + rl;
+      if (row >= p.N) continue;
+      float acc = 0.f;
+      for (int j = 0; j < p.topk; ++j)
+        acc = fmaf(gate[j], __ldcg(p.y + (static_cast<size_t>(t) * p.topk + j) * p.N + row), acc);
+      p.cmb_y[static_cast<size_t>(t) * p.N + row] = acc;
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    for (int b = 0; b < p.B; ++b)
+      if (flags[b] >= 0) p.cmb_count[static_cast<size_t>(flags[b]) * tiles + tile] = 0;
+}
+
 __device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, const Sel& sel, float* red) {
   const int E = c.RT * p.B;
   if (p.kl > 1) {
@@ -476,6 +518,7 @@ __device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, cons
       const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
       if (row < p.N && b < sel.count) p.y[static_cast<size_t>(sel.rows ? sel.rows[b] : b) * p.N + row] = red[e];
     }
+    if (p.cmb_count) combine_tokens(p, c, sel, reinterpret_cast<int*>(red));
     return;
   }
   cluster_sync();  // every CTA's red[0] is complete
@@ -496,7 +539,9 @@ __device__ __forceinline__ void reduce_store(const Params& p, const Cta& c, cons
     const int rl = e / p.B, b = e - rl * p.B, row = c.row0 + rl;
     if (row < p.N && b < sel.count) p.y[static_cast<size_t>(sel.rows ? sel.rows[b] : b) * p.N + row] = v;
   }
-  cluster_sync();  // keep this CTA's shared memory alive until the peers have read it
+  cluster_sync();  // keep this CTA's shared memory alive until the peers have read it; and every
+                   // rank's stores precede the combine count of rank 0
+  if (p.cmb_count && rank == 0) combine_tokens(p, c, sel, reinterpret_cast<int*>(red));
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -1742,10 +1787,18 @@ size_t gemv_chunks_workspace_bytes(const tq_desc* d, int B, int max_chunks) {
   return static_cast<size_t>(max_chunks) * (xh_bytes(d, B) + vp_bytes(d, B));
 }
 
+int gemv_chunks_row_tiles(const tq_desc* d, int B) {
+  using namespace gemv;
+  if (gemv_workspace_bytes(d, B) == 0) return -1;
+  Plan pl{};
+  if (choose_plan(gemv_kernel(d, B), d, B, &pl) != cudaSuccess) return -1;
+  return pl.n_rg;
+}
+
 cudaError_t launch_gemv_chunks(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, size_t codes_estride,
                                size_t scales_estride, int mode, const uint16_t* x, const float* gu, float* h_out,
                                int topk, const int* chunks, int B, int max_chunks, float* y, void* ws,
-                               cudaStream_t s) {
+                               cudaStream_t s, const ChunkCombine* combine) {
   using namespace gemv;
   PrepParams pp{};
   pp.x = x;
@@ -1768,6 +1821,12 @@ cudaError_t launch_gemv_chunks(const tq_desc* d, const uint32_t* codes, const ui
   prm.scales_estride = scales_estride;
   prm.xh_cstride = pp.xh_cstride;
   prm.vp_cstride = pp.vp_cstride;
+  prm.topk = topk;
+  if (combine) {
+    prm.cmb_count = combine->count;
+    prm.cmb_gate = combine->gate;
+    prm.cmb_y = combine->y;
+  }
   return launch_pair(d, pp, prm, B, max_chunks, s);
 }
 

@@ -25,11 +25,23 @@ int gemv_kernel_count(const tq_desc* d, int batch);
 // gu (float, gate then up, 2K wide), copied to h_out (K wide) when h_out is not null.  Output row
 // rows[b] of y (N wide) receives the expert's product.  Codes / scales of expert e start
 // e * codes_estride / e * scales_estride elements in.
+// combine (may be null): after a CTA has stored its output rows it counts, per token t = rows[b] /
+// topk, one more finished slot in combine->count[t * row_tiles + row tile]; the CTA that completes a
+// token's topk slots writes combine->y[t][rows of the tile] = sum_j gate[t][j] * y[t * topk + j][rows]
+// (slots in order j = 0..topk-1, so the sum does not depend on which CTA forms it) and sets the count
+// back to 0.  The counts must be zero before the launch; row_tiles_out receives the tile count.
+struct ChunkCombine {
+  int* count;
+  const float* gate;
+  float* y;
+};
 size_t gemv_chunks_workspace_bytes(const tq_desc* d, int B, int max_chunks);
+// Row tiles (CTAs along N) of the chunked GEMV for this shape and batch, or -1.
+int gemv_chunks_row_tiles(const tq_desc* d, int B);
 cudaError_t launch_gemv_chunks(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, size_t codes_estride,
                                size_t scales_estride, int mode, const uint16_t* x, const float* gu, float* h_out,
                                int topk, const int* chunks, int B, int max_chunks, float* y, void* ws,
-                               cudaStream_t s);
+                               cudaStream_t s, const ChunkCombine* combine = nullptr);
 
 // Prefill GEMM (weights decoded to FP16 once per call, tcgen05 tensor cores); workspace from
 // gemm_workspace_bytes.

@@ -1,10 +1,14 @@
 // Routed MoE expert layer at decode time: top-k routing of 256 experts (8 active per token, router
 // in full precision - the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, section "为什么 1.58bit 没变成乱码", point 1), then the
-// ternary SwiGLU experts.  The (token, slot) assignments are sorted by expert into chunks of up to
-// 1 / 2 / 4 tokens; the gate/up and down projections run as the decode GEMV kernels over those
-// chunks (blockIdx.z = chunk), so each chunk streams its expert's packed codes once, the prep kernel
-// gathers the tokens (gate/up) or forms FWHT(silu(gate) * up) (down), and a last kernel adds the
-// expert outputs in slot order (deterministic).
+// ternary SwiGLU experts, in three launches:
+//  1. one CTA routes every token (warp per token), counts the assignments per expert, scans the
+//     per-expert chunk counts and writes the chunk table: the (token, slot) assignments of each
+//     expert in ascending order, cut into chunks of 1 token (a single token) or 2 tokens;
+//  2. the gate/up projection as the decode GEMV over those chunks (blockIdx.z = chunk), each chunk
+//     streaming its expert's packed codes once and transforming its tokens' inputs itself;
+//  3. the down projection the same way on FWHT(silu(gate) * up); as each CTA stores its rows it
+//     counts the finished slot of each of its tokens, and the CTA that finishes a token's last slot
+//     adds the slots' rows in slot order, weighted by the gates (deterministic).
 #include <float.h>
 
 #include <algorithm>
@@ -18,13 +22,10 @@ namespace {
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 8;
 
-// One warp per token: k rounds of a warp-wide argmax with the order (logit descending, expert
-// index ascending); gate = softmax over the chosen logits, summed in slot order.
-__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int topk, int* __restrict__ idx,
-                             float* __restrict__ gate) {
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int t = blockIdx.x * (blockDim.x >> 5) + warp;
-  if (t >= T) return;
+// Token t, one warp: k rounds of a warp-wide argmax with the order (logit descending, expert index
+// ascending); gate = softmax over the chosen logits, summed in slot order.
+__device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int topk,
+                                            int* __restrict__ idx, float* __restrict__ gate, int lane) {
   float v[kMaxExperts / 32];
 #pragma unroll
   for (int i = 0; i < kMaxExperts / 32; ++i) {
@@ -71,29 +72,70 @@ __global__ void route_kernel(const float* __restrict__ logits, int T, int E, int
   }
 }
 
-// One block, one thread per expert: the (token, slot) assignments routed to each expert, in ascending
-// order, cut into chunks of at most CB.  table[0] = number of chunks; chunk c is the record
-// table[1 + c * (2 + CB)] = {expert, count, a_0 .. a_(CB-1)}; chunks are in expert order.  Unused
-// slots repeat a_0 (they are never read as data).  Deterministic.
-__global__ void chunks_kernel(const int* __restrict__ idx, int n_assign, int E, int CB, int* __restrict__ table) {
-  __shared__ int s_off[kMaxExperts + 1];
-  const int e = threadIdx.x;
-  int c = 0;
-  if (e < E)
-    for (int a = 0; a < n_assign; ++a) c += idx[a] == e;
-  s_off[e + 1] = e < E ? (c + CB - 1) / CB : 0;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    s_off[0] = 0;
-    for (int i = 0; i < kMaxExperts; ++i) s_off[i + 1] += s_off[i];
-    table[0] = s_off[kMaxExperts];
+__global__ void route_kernel(const float* __restrict__ logits, int T, int E, int topk, int* __restrict__ idx,
+                             float* __restrict__ gate) {
+  const int t = blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+  if (t < T) route_token(logits, t, E, topk, idx, gate, threadIdx.x & 31);
+}
+
+constexpr int kPlanThreads = 1024;
+constexpr int kPlanSmemAssign = 8192;  // assignments kept in shared memory (larger batches read global)
+
+// Step 1 of the expert layer, one CTA: route every token, then the chunk table.  table[0] = number of
+// chunks; chunk c is the record table[1 + c * (2 + CB)] = {expert, count, a_0 .. a_(CB-1)}, chunks
+// in expert order and each expert's assignments in ascending order (unused slots repeat a_0; they
+// are never read as data).  Also zeroes the combine counts.  Deterministic: counts are order-free
+// and each expert's assignments are placed by a scan in assignment order.
+__global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const float* __restrict__ logits, int T, int E,
+                                                                int topk, int CB, int* __restrict__ idx,
+                                                                float* __restrict__ gate, int* __restrict__ table,
+                                                                int* __restrict__ count, int ncount) {
+  extern __shared__ int s_assign[];  // min(A, kPlanSmemAssign) expert indices
+  __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts], s_wsum[kMaxExperts / 32];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, A = T * topk;
+  for (int t = warp; t < T; t += kPlanThreads / 32) route_token(logits, t, E, topk, idx, gate, lane);
+  for (int i = threadIdx.x; i < ncount; i += kPlanThreads) count[i] = 0;
+  for (int e = threadIdx.x; e < kMaxExperts; e += kPlanThreads) s_cnt[e] = 0;
+  __syncthreads();  // idx is complete (global writes of this CTA, read back below)
+  const bool in_smem = A <= kPlanSmemAssign;
+  for (int a = threadIdx.x; a < A; a += kPlanThreads) {
+    const int e = __ldcg(idx + a);
+    if (in_smem) s_assign[a] = e;
+    atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
-  if (e < E && c > 0) {
+  // exclusive scan of the chunk counts over the experts: per warp, then across warps
+  if (threadIdx.x < kMaxExperts) {
+    const int e = threadIdx.x;
+    const int nch = e < E ? (s_cnt[e] + CB - 1) / CB : 0;
+    int incl = nch;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int v = __shfl_up_sync(0xffffffffu, incl, o);
+      if (lane >= o) incl += v;
+    }
+    if (lane == 31) s_wsum[warp] = incl;
+    s_off[e] = incl - nch;
+  }
+  __syncthreads();
+  if (threadIdx.x < kMaxExperts) {
+    int base = 0;
+    for (int w = 0; w < warp; ++w) base += s_wsum[w];
+    s_off[threadIdx.x] += base;
+    if (threadIdx.x == kMaxExperts - 1) {
+      int total = 0;
+      for (int w = 0; w < kMaxExperts / 32; ++w) total += s_wsum[w];
+      table[0] = total;
+    }
+  }
+  __syncthreads();
+  // one thread per expert places its assignments, in order
+  if (threadIdx.x < E && s_cnt[threadIdx.x] > 0) {
+    const int e = threadIdx.x;
     int chunk = s_off[e], slot = 0;
     int* rec = table + 1 + static_cast<size_t>(chunk) * (2 + CB);
-    for (int a = 0; a < n_assign; ++a) {
-      if (idx[a] != e) continue;
+    for (int a = 0; a < A; ++a) {
+      if ((in_smem ? s_assign[a] : __ldcg(idx + a)) != e) continue;
       rec[2 + slot] = a;
       if (++slot == CB) {
         rec[0] = e;
@@ -111,26 +153,19 @@ __global__ void chunks_kernel(const int* __restrict__ idx, int n_assign, int E, 
   }
 }
 
-// y[t][r] = sum_j gate[t][j] * ypart[t*topk + j][r], summed in slot order j = 0..topk-1.
-__global__ void combine_kernel(const float* __restrict__ ypart, const float* __restrict__ gate, int T, int H,
-                               int topk, float* __restrict__ y) {
-  const size_t i = static_cast<size_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<size_t>(T) * H) return;
-  const int t = static_cast<int>(i / H), r = static_cast<int>(i % H);
-  float acc = 0.f;
-  for (int j = 0; j < topk; ++j)
-    acc = fmaf(gate[static_cast<size_t>(t) * topk + j], ypart[(static_cast<size_t>(t) * topk + j) * H + r], acc);
-  y[i] = acc;
-}
-
 // Tokens per chunk: one token never routes twice to an expert; larger batches share an expert's
-// weights among up to 2 or 4 routed tokens per pass.
-int chunk_batch(int T) { return T == 1 ? 1 : (T <= 16 ? 2 : 4); }
+// weights between 2 routed tokens per pass (the GEMV then transforms its inputs itself: no separate
+// transform launch).
+int chunk_batch(int T) { return T == 1 ? 1 : 2; }
+
+// Row tiles of the down projection's chunked GEMV are at most H / 16 (one 16-row slab each).
+size_t combine_count_ints(int T, int H) { return static_cast<size_t>(T) * ((H + 15) / 16); }
 
 struct MoeWs {
   int* table;   // chunk records
   float* gu;    // gate / up outputs per assignment [T * topk][2F]
   float* ypart; // down outputs per assignment [T * topk][H]
+  int* count;   // combine counts [T][row tiles]
   void* prep;   // prep output of the current stage (shared by both stages)
   size_t bytes;
 };
@@ -145,6 +180,7 @@ MoeWs moe_ws_layout(void* base, int T, int topk, int H, int F) {
   w.table = reinterpret_cast<int*>(take((1 + static_cast<size_t>(A) * (2 + CB)) * 4));
   w.gu = reinterpret_cast<float*>(take(static_cast<size_t>(A) * 2 * F * 4));
   w.ypart = reinterpret_cast<float*>(take(static_cast<size_t>(A) * H * 4));
+  w.count = reinterpret_cast<int*>(take(combine_count_ints(T, H) * 4));
   const tq_desc gu{2 * F, H, 64, TQ_PACK_B3, kFwhtBlock, 0}, dn{H, F, 64, TQ_PACK_B3, kFwhtBlock, 0};
   const size_t prep = std::max(gemv_chunks_workspace_bytes(&gu, CB, A), gemv_chunks_workspace_bytes(&dn, CB, A));
   w.prep = take(prep);
@@ -205,24 +241,24 @@ extern "C" tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, in
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   MoeWs w = moe_ws_layout(workspace, T, topk, H, F);
   const int G = gate_up->group, A = T * topk, CB = chunk_batch(T);
+  const int tiles = gemv_chunks_row_tiles(down, CB);
+  if (tiles < 1 || static_cast<size_t>(T) * tiles > combine_count_ints(T, H)) return TQ_ERR_UNSUPPORTED;
   cudaError_t e;
-  if ((e = launch_route(router_logits, T, E, topk, topk_idx, topk_gate, s)) != cudaSuccess) return cuda_fail(e);
-  chunks_kernel<<<1, kMaxExperts, 0, s>>>(topk_idx, A, E, CB, w.table);
+  const int A_smem = std::min(A, kPlanSmemAssign);
+  moe_plan_kernel<<<1, kPlanThreads, static_cast<size_t>(A_smem) * 4, s>>>(router_logits, T, E, topk, CB, topk_idx,
+                                                                           topk_gate, w.table, w.count, T * tiles);
   if ((e = cudaPeekAtLastError()) != cudaSuccess) return cuda_fail(e);
   // gate / up: chunk slot b holds assignment a, fed with x row a / topk; output row a of gu
   e = launch_gemv_chunks(gate_up, gu_codes, gu_scales, static_cast<size_t>(2 * F) * pitch_words(H, gate_up->packing),
                          static_cast<size_t>(2 * F) * (H / G), 1, x, nullptr, nullptr, topk, w.table, CB, A, w.gu,
                          w.prep, s);
   if (e != cudaSuccess) return cuda_fail(e);
-  // down: fed with FWHT(silu(gate) * up) of assignment a; output row a of ypart
+  // down: fed with FWHT(silu(gate) * up) of assignment a; output row a of ypart; the combine into y
+  // is done by the CTA that finishes a token's last slot
+  const ChunkCombine cmb{w.count, topk_gate, y};
   e = launch_gemv_chunks(down, d_codes, d_scales, static_cast<size_t>(H) * pitch_words(F, down->packing),
                          static_cast<size_t>(H) * (F / G), 2, nullptr, w.gu, h_out, topk, w.table, CB, A, w.ypart,
-                         w.prep, s);
+                         w.prep, s, &cmb);
   if (e != cudaSuccess) return cuda_fail(e);
-  {
-    const size_t n = static_cast<size_t>(T) * H;
-    combine_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(w.ypart, topk_gate, T, H, topk, y);
-    if ((e = cudaPeekAtLastError()) != cudaSuccess) return cuda_fail(e);
-  }
   return TQ_OK;
 }

@@ -101,3 +101,40 @@ def test_moe_route_ties_and_order():
     assert np.array_equal(idx.cpu().numpy(), idx_ref)
     assert np.max(np.abs(gate.cpu().numpy() - gate_ref)) <= 1e-6
     assert idx_ref[1, :3].tolist() == [3, 9, 200] and idx_ref[2].tolist() == list(range(8))
+
+
+def test_moe_repeat_and_graph_replay_deterministic():
+    """The fused combine is done by whichever CTA finishes a token's last slot, adding the slots in
+    slot order: repeated calls (the per-token counts reset themselves) and a CUDA-graph replay give
+    bit-identical outputs.  Also a batch with more tokens than shared-memory assignments would not
+    matter here (T = 64)."""
+    m = inputs.MOE
+    case = MoeCase(inputs.seed_of(3) + 99, m["E"], m["H"], m["F"], m["group"], m["packing"], 64, m["topk"])
+    logits, x = case.logits.cuda(), case.x_host.cuda()
+    ws = torch.empty(tq.tq_moe_workspace_bytes(64, m["E"], m["topk"], m["H"], m["F"]), dtype=torch.uint8, device="cuda")
+    y = torch.empty((64, m["H"]), dtype=torch.float32, device="cuda")
+    idx = torch.empty((64, m["topk"]), dtype=torch.int32, device="cuda")
+    gate = torch.empty((64, m["topk"]), dtype=torch.float32, device="cuda")
+
+    def call():
+        tq.tq_moe_gemv(case.gu, case.dn, m["E"], m["topk"], case.gu_codes, case.gu_scales, case.d_codes,
+                       case.d_scales, logits, x, topk_idx=idx, topk_gate=gate, y=y, workspace=ws)
+
+    call()
+    torch.cuda.synchronize()
+    first = y.clone()
+    for _ in range(3):
+        y.fill_(float("nan"))
+        call()
+        torch.cuda.synchronize()
+        assert torch.equal(y, first)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        call()
+    y.fill_(float("nan"))
+    g.replay()
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    assert torch.equal(y, first)
