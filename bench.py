@@ -319,23 +319,24 @@ class _Null:
 
 
 def traffic_from_profiles(kernel_key: str):
-    """DRAM bytes recorded by an ncu capture (profiles/ncu_traffic.txt: key, bytes, source hash), if
-    the kernel sources it was taken on are unchanged."""
+    """DRAM bytes recorded by an ncu capture (profiles/ncu_traffic.txt: key, bytes, hash, source files),
+    if the kernel sources it was taken on (the files listed, under the package's csrc/) are unchanged."""
     p = os.path.join(ROOT, "profiles", "ncu_traffic.txt")
     if not os.path.exists(p):
         return None
-    cur = source_hash()
     for line in open(p):
         parts = line.split()
-        if len(parts) >= 3 and not line.startswith("#") and parts[0] == kernel_key and parts[2] == cur:
-            return float(parts[1])
+        if len(parts) >= 4 and not line.startswith("#") and parts[0] == kernel_key:
+            if parts[2] == source_hash(parts[3].split(",")):
+                return float(parts[1])
     return None
 
 
-def source_hash():
+def source_hash(files=None):
+    """First 16 hex digits of the SHA-256 of the kernel sources (all of csrc/, or the files named)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "ternary_weight_quantized_unpack_b300", "csrc")
-    for f in sorted(os.listdir(csrc)):
+    for f in sorted(files if files else os.listdir(csrc)):
         with open(os.path.join(csrc, f), "rb") as fh:
             h.update(fh.read())
     return h.hexdigest()[:16]
@@ -391,6 +392,27 @@ def bench_moe(T, steps, warmup, seed=inputs.seed_of(3)):
     byts = n_active * per_expert + logits.numel() * 4
     return {"tokens": T, "active_experts": n_active, "ms": ms, "GB_s": byts / (ms * 1e-3) / GB,
             "tok_s_40_layers": T / (40 * ms * 1e-3), "bytes": byts}
+
+
+def bench_quantize(reps, seed=inputs.seed_of(2)):
+    """The offline quantizer on the 27B-class gate/up shape (17408 x 5120 dense bf16 W): rotate, scale,
+    ternarize and pack, timed per call; GB/s of W read."""
+    N, K = 17408, 5120
+    w = (inputs.activations(seed, 900, N, K, outlier_frac=0.001).float() * 2.0 ** -6).to(torch.bfloat16).cuda()
+    out = {}
+    for name, pk in (("2bit", tq.TQ_PACK_2BIT), ("base3", tq.TQ_PACK_B3)):
+        d = tq.desc(N, K, 128, pk)
+        codes, scales = tq.tq_quantize(d, w)
+        torch.cuda.synchronize()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        for _ in range(reps):
+            tq.tq_quantize(d, w, codes, scales)
+        b.record()
+        torch.cuda.synchronize()
+        ms = a.elapsed_time(b) / reps
+        out[name] = {"N": N, "K": K, "ms": ms, "GB_s_of_W": N * K * 2 / (ms * 1e-3) / GB}
+    return out
 
 
 def bench_prefill(shape, steps, warmup, seed=inputs.seed_of(4)):
@@ -687,7 +709,7 @@ def run_tq(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(packing, batch)
     if args.extras and world == 1:
         ex = {"decode_step": [], "per_call_stream": [], "single_linear": None, "layer_linears": [],
-              "moe": [], "prefill": []}
+              "moe": [], "prefill": [], "quantize": None}
         reps = max(5, args.steps // 4)
         if seq:   # the same weights called one launch per call
             g2, ms2, _ = bench_per_call(st, reps)
@@ -719,7 +741,11 @@ def run_tq(args, rank, world, local):
             ex["layer_linears"] += bench_layer_linears(pk, inputs.DENSE_DECODE["batches"], max(10, args.steps // 5))
         torch.cuda.empty_cache()
         for T in inputs.MOE["tokens"]:
-            ex["moe"].append(bench_moe(T, max(10, args.steps // 2), 3))
+            r = bench_moe(T, max(10, args.steps // 2), 3)
+            r["latency_us"] = r["ms"] * 1e3
+            r["launches_per_call"] = 3
+            ex["moe"].append(r)
+        ex["quantize"] = bench_quantize(5)
         for shape in inputs.PREFILL["shapes"]:
             ex["prefill"].append(bench_prefill(shape, 20, 3))
         for p in ex["prefill"]:

@@ -85,7 +85,7 @@ constexpr int kPlanSmemAssign = 8192;  // assignments kept in shared memory (lar
 // chunks; chunk c is the record table[1 + c * (2 + CB)] = {expert, count, a_0 .. a_(CB-1)}, chunks
 // in expert order and each expert's assignments in ascending order (unused slots repeat a_0; they
 // are never read as data).  Also zeroes the combine counts.  Deterministic: counts are order-free
-// and each expert's assignments are placed by a scan in assignment order.
+// and each assignment's place follows from the number of earlier assignments to its expert.
 __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const float* __restrict__ logits, int T, int E,
                                                                 int topk, int CB, int* __restrict__ idx,
                                                                 float* __restrict__ gate, int* __restrict__ table,
@@ -129,13 +129,30 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const float* __r
     }
   }
   __syncthreads();
-  // one thread per expert places its assignments, in order
-  if (threadIdx.x < E && s_cnt[threadIdx.x] > 0) {
+  if (in_smem) {
+    // one thread per assignment: its rank among the earlier assignments to the same expert gives its
+    // chunk and slot
+    for (int a = threadIdx.x; a < A; a += kPlanThreads) {
+      const int e = s_assign[a];
+      int rank = 0;
+      for (int b = 0; b < a; ++b) rank += s_assign[b] == e;
+      const int ci = rank / CB, slot = rank - ci * CB;
+      int* rec = table + 1 + static_cast<size_t>(s_off[e] + ci) * (2 + CB);
+      rec[2 + slot] = a;
+      if (slot == 0) {
+        const int n = min(CB, s_cnt[e] - ci * CB);
+        rec[0] = e;
+        rec[1] = n;
+        for (int j = n; j < CB; ++j) rec[2 + j] = a;
+      }
+    }
+  } else if (threadIdx.x < E && s_cnt[threadIdx.x] > 0) {
+    // large batches: one thread per expert places its assignments, in order
     const int e = threadIdx.x;
     int chunk = s_off[e], slot = 0;
     int* rec = table + 1 + static_cast<size_t>(chunk) * (2 + CB);
     for (int a = 0; a < A; ++a) {
-      if ((in_smem ? s_assign[a] : __ldcg(idx + a)) != e) continue;
+      if (__ldcg(idx + a) != e) continue;
       rec[2 + slot] = a;
       if (++slot == CB) {
         rec[0] = e;
