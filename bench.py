@@ -415,6 +415,48 @@ def bench_quantize(reps, seed=inputs.seed_of(2)):
     return out
 
 
+def bench_moe_prefill(T, steps, warmup, seed=inputs.seed_of(3)):
+    """The expert layer at prefill sizes (tq_moe_gemm: grouped tcgen05 GEMM), T tokens; TFLOP/s of the
+    expert GEMMs (2 * T * topk * (2F * H + H * F))."""
+    m = inputs.MOE
+    E, H, F, G, k = m["E"], m["H"], m["F"], m["group"], m["topk"]
+    gu, dn = tq.desc(2 * F, H, G, m["packing"]), tq.desc(H, F, G, m["packing"])
+    dev = "cuda"
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(seed + T)
+    gu_all, dn_all = tq.desc(E * 2 * F, H, G, m["packing"]), tq.desc(E * H, F, G, m["packing"])
+    gu_codes = tq.tq_pack(gu_all, torch.randint(-1, 2, (E * 2 * F, H), dtype=torch.int8, device=dev, generator=gen))
+    d_codes = tq.tq_pack(dn_all, torch.randint(-1, 2, (E * H, F), dtype=torch.int8, device=dev, generator=gen))
+    gu_s = torch.exp(torch.randn((E * 2 * F, H // G), generator=gen, device=dev) * 0.5 - 4).half()
+    d_s = torch.exp(torch.randn((E * H, F // G), generator=gen, device=dev) * 0.5 - 4).half()
+    logits = inputs.router_logits(seed, T, T, E).to(dev)
+    x = inputs.activations(seed, T, T, H).to(dev)
+    y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    idx = torch.empty((T, k), dtype=torch.int32, device=dev)
+    gate = torch.empty((T, k), dtype=torch.float32, device=dev)
+    ws = torch.empty(tq.tq_moe_gemm_workspace_bytes(T, E, k, H, F), dtype=torch.uint8, device=dev)
+
+    def call():
+        tq.tq_moe_gemm(gu, dn, E, k, gu_codes, gu_s, d_codes, d_s, logits, x, topk_idx=idx, topk_gate=gate, y=y,
+                       workspace=ws)
+
+    for _ in range(warmup):
+        call()
+    torch.cuda.synchronize()
+    times = []
+    for _ in range(steps):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record()
+        call()
+        b.record()
+        torch.cuda.synchronize()
+        times.append(a.elapsed_time(b))
+    ms = statistics.median(times)
+    flops = 2.0 * T * k * (2 * F * H + H * F)
+    return {"tokens": T, "ms": ms, "TFLOP_s": flops / (ms * 1e-3) / 1e12, "tok_s_40_layers": T / (40 * ms * 1e-3),
+            "launches_per_call": 9}
+
+
 def bench_prefill(shape, steps, warmup, seed=inputs.seed_of(4)):
     M, K, N = shape
     d = tq.desc(N, K, 128, tq.TQ_PACK_2BIT)
@@ -709,7 +751,7 @@ def run_tq(args, rank, world, local):
         line["cpu_baseline"] = cpu_baseline(packing, batch)
     if args.extras and world == 1:
         ex = {"decode_step": [], "per_call_stream": [], "single_linear": None, "layer_linears": [],
-              "moe": [], "prefill": [], "quantize": None}
+              "moe": [], "prefill": [], "quantize": None, "moe_prefill": []}
         reps = max(5, args.steps // 4)
         if seq:   # the same weights called one launch per call
             g2, ms2, _ = bench_per_call(st, reps)
@@ -746,6 +788,9 @@ def run_tq(args, rank, world, local):
             r["launches_per_call"] = 3
             ex["moe"].append(r)
         ex["quantize"] = bench_quantize(5)
+        ex["moe_prefill"] = [bench_moe_prefill(T, 10, 3) for T in (256, 1024, 4096)]
+        for r in ex["moe_prefill"]:
+            r["pct_of_bf16_peak"] = 100.0 * r["TFLOP_s"] / peaks["bf16_tflops"]
         for shape in inputs.PREFILL["shapes"]:
             ex["prefill"].append(bench_prefill(shape, 20, 3))
         for p in ex["prefill"]:
@@ -769,8 +814,9 @@ def main():
                     help="seq: the whole step as one tq_seq launch (2-bit, batch <= 8); per_call: one tq_gemv per call")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
-    ap.add_argument("--workload", choices=["stream", "prefill", "moe"], default="stream",
-                    help="stream: the headline decode line; prefill / moe: one line per shape of those workloads")
+    ap.add_argument("--workload", choices=["stream", "prefill", "moe", "moe_prefill"], default="stream",
+                    help="stream: the headline decode line; prefill / moe / moe_prefill: one line per shape of "
+                         "those workloads")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank, world, local = dist_setup()
@@ -787,6 +833,10 @@ def main():
         if rank == 0:
             for T in inputs.MOE["tokens"]:
                 print(json.dumps({"workload": "moe", **bench_moe(T, args.steps, args.warmup)}))
+    elif args.workload == "moe_prefill":
+        if rank == 0:
+            for T in (256, 1024, 4096):
+                print(json.dumps({"workload": "moe_prefill", **bench_moe_prefill(T, args.steps, args.warmup)}))
     else:
         run_tq(args, rank, world, local)
     if world > 1:

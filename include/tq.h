@@ -226,6 +226,24 @@ tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, int E, int to
                       int32_t* topk_idx, float* topk_gate, float* h_out, float* y,
                       void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- tq_moe_gemm: the same expert layer at prefill sizes (many tokens per expert) -------------------
+ * Same computation, arguments and layouts as tq_moe_gemv (tantan.ink, "为什么 1.58bit 没变成乱码",
+ * points 1-2), organised as a grouped tensor-core GEMM: the (token, slot) assignments are sorted by
+ * expert, the tokens' block-transformed inputs are gathered in that order as FP16 (|x~| below 65504,
+ * else TQ_ERR_RANGE), every expert's weights are decoded to FP16 s * t, one persistent tcgen05 launch
+ * per projection walks a tile list over (expert, 128 sorted rows, 256 weight rows), silu(gate) * up
+ * and its transform go to FP16 for the down projection, and the combine adds the slots in slot order
+ * (deterministic).  Nine launches.  Requires H and 2F multiples of 256 and T * topk < 2^24.
+ * workspace >= tq_moe_gemm_workspace_bytes(T, E, topk, H, F): it holds every expert's decoded
+ * weights (E * 3 * H * F * 2 bytes) besides per-assignment rows. */
+size_t tq_moe_gemm_workspace_bytes(int T, int E, int topk, int H, int F);
+tq_status tq_moe_gemm(const tq_desc* gate_up, const tq_desc* down, int E, int topk,
+                      const uint32_t* gu_codes, const uint16_t* gu_scales,
+                      const uint32_t* d_codes, const uint16_t* d_scales,
+                      const float* router_logits, const uint16_t* x, int T,
+                      int32_t* topk_idx, float* topk_gate, float* h_out, float* y,
+                      void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- tq_gemm: batched prefill, Y[m][n] = bf16( sum_k s[n][k/group] t[n][k] x~[m][k] ) -------------
  * x: bf16 [M][K]; y: bf16 [M][N]; fp32 accumulation.  x~ is held as FP16 (|x~| must stay below
  * 65504, else TQ_ERR_RANGE is recorded).  Requires K a multiple of 128.

@@ -77,6 +77,8 @@ _SIGS = {
     "tq_moe_route": (_I, [_P, _I, _I, _I, _P, _P, _P]),
     "tq_moe_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
     "tq_moe_gemv": (_I, [_D, _D, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
+    "tq_moe_gemm_workspace_bytes": (_SZ, [_I, _I, _I, _I, _I]),
+    "tq_moe_gemm": (_I, [_D, _D, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tq_gemm_workspace_bytes": (_SZ, [_D, _I]),
     "tq_gemm": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "tq_seq_create": (_I, [ctypes.POINTER(tq_seq_call), _I, _I, ctypes.POINTER(ctypes.c_void_p)]),
@@ -262,6 +264,36 @@ def tq_moe_gemv(gate_up: tq_desc, down: tq_desc, E: int, topk: int, gu_codes, gu
                              _ptr(topk_gate), _ptr(h_out), _ptr(y), _ptr(workspace),
                              workspace.numel() * workspace.element_size(), _stream(stream)), "tq_moe_gemv")
     return y, topk_idx, topk_gate, h_out
+
+
+def tq_moe_gemm(gate_up: tq_desc, down: tq_desc, E: int, topk: int, gu_codes, gu_scales, d_codes, d_scales,
+                router_logits, x, topk_idx=None, topk_gate=None, h_out=None, y=None, workspace=None,
+                want_h: bool = False, stream=None):
+    """Routed SwiGLU expert layer at prefill sizes (grouped tensor-core GEMM).  Same arguments and
+    returns as tq_moe_gemv."""
+    T, H = x.shape
+    F = down.K
+    dev = x.device
+    if topk_idx is None:
+        topk_idx = torch.empty((T, topk), dtype=torch.int32, device=dev)
+    if topk_gate is None:
+        topk_gate = torch.empty((T, topk), dtype=torch.float32, device=dev)
+    if h_out is None and want_h:
+        h_out = torch.empty((T, topk, F), dtype=torch.float32, device=dev)
+    if y is None:
+        y = torch.empty((T, H), dtype=torch.float32, device=dev)
+    nbytes = tq_moe_gemm_workspace_bytes(T, E, topk, H, F)
+    if workspace is None:
+        workspace = _ws(nbytes, dev)
+    _check(lib().tq_moe_gemm(ctypes.byref(gate_up), ctypes.byref(down), E, topk, _ptr(gu_codes), _ptr(gu_scales),
+                             _ptr(d_codes), _ptr(d_scales), _ptr(router_logits), _ptr(x), T, _ptr(topk_idx),
+                             _ptr(topk_gate), _ptr(h_out), _ptr(y), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream)), "tq_moe_gemm")
+    return y, topk_idx, topk_gate, h_out
+
+
+def tq_moe_gemm_workspace_bytes(T: int, E: int, topk: int, H: int, F: int) -> int:
+    return lib().tq_moe_gemm_workspace_bytes(T, E, topk, H, F)
 
 
 def tq_gemm(d: tq_desc, codes, scales, x, y=None, workspace=None, stream=None) -> torch.Tensor:

@@ -17,6 +17,12 @@
 //   warps 2-5  epilogue: tcgen05.ld of a full accumulator, bf16 conversion, stores; then the
 //              accumulator is released, so one tile's epilogue overlaps the next tile's MMAs
 // Every mbarrier wait is bounded; a wait that runs out records TQ_ERR_TIMEOUT and the warp stops.
+//
+// Grouped mode (the expert layer at prefill sizes): instead of the M x N tile grid the kernel walks a
+// tile list written on the device - {first A row, valid rows, first B row, first output column} -
+// so one launch covers every routed expert: A holds the tokens sorted by expert, B the decoded
+// weights of all experts stacked, and rows past an expert's token count are computed but not stored.
+// Output fp32.
 // Activations are the block Walsh-Hadamard transform of x in FP16 ("27B 大模型塞进
 // 5.9GB", section 二 ①); group scales per 64 or 128 weights (same page, section 二 ②).
 #include <cuda_bf16.h>
@@ -55,14 +61,37 @@ struct Smem {
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment of the base to 1024
 
+// Tile list of the grouped mode (tiles == nullptr: the plain M x N grid).
+struct GroupedTiles {
+  const int4* tiles;  // {A row, valid rows, B row, output column}
+  const int* count;   // number of tiles
+  float* y;           // fp32 output, row r at y + r * ldy
+  int ldy;
+};
+
+__device__ __forceinline__ void tile_of(const GroupedTiles& gt, int t, int n_mt, int& m0, int& rows, int& nb, int& no) {
+  if (gt.tiles) {
+    const int4 v = gt.tiles[t];
+    m0 = v.x;
+    rows = v.y;
+    nb = v.z;
+    no = v.w;
+  } else {
+    m0 = (t % n_mt) * BM;
+    rows = BM;
+    nb = no = (t / n_mt) * BN;
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, uint16_t* y,
-                   int M, int N, int K, int* status) {
+                   int M, int N, int K, int* status, const __grid_constant__ GroupedTiles gt) {
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nk = K / BK;
-  const int n_mt = (M + BM - 1) / BM, n_tiles = n_mt * ((N + BN - 1) / BN);
+  const int n_mt = (M + BM - 1) / BM;
+  const int n_tiles = gt.tiles ? *gt.count : n_mt * ((N + BN - 1) / BN);
   // tile t: token tile t % n_mt, weight tile t / n_mt (the CTAs running together share few weight tiles)
   if (threadIdx.x == 0) {
 #pragma unroll
@@ -89,7 +118,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int g = 0;  // K steps issued so far, over all tiles
     bool ok = true;
     for (int t = blockIdx.x; t < n_tiles && ok; t += gridDim.x) {
-      const int m0 = (t % n_mt) * BM, n0 = (t / n_mt) * BN;
+      int m0, rows, nb, no;
+      tile_of(gt, t, n_mt, m0, rows, nb, no);
       for (int kb = 0; kb < nk; ++kb, ++g) {
         const int s = g % STAGES;
         if (g >= STAGES && !mbar_wait(&sm.empty[s], ((g / STAGES) & 1) ^ 1)) {
@@ -99,7 +129,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
         tma_load_2d(sm.a[s], &tm_x, kb * BK, m0, &sm.full[s]);
-        tma_load_2d(sm.b[s], &tm_w, kb * BK, n0, &sm.full[s]);
+        tma_load_2d(sm.b[s], &tm_w, kb * BK, nb, &sm.full[s]);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -136,7 +166,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     int it = 0;
     for (int t = blockIdx.x; t < n_tiles; t += gridDim.x, ++it) {
       const int b = it & 1;
-      const int m0 = (t % n_mt) * BM, n0 = (t / n_mt) * BN;
+      int m0, rows, nb, n0;
+      tile_of(gt, t, n_mt, m0, rows, nb, n0);
       if (!mbar_wait(&sm.acc_full[b], (it >> 1) & 1)) {
         if (lane == 0) record_error(status, TQ_ERR_TIMEOUT);
         break;
@@ -149,7 +180,15 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_ld<32>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN + c), v);
         tmem_wait_ld();
         const int n = n0 + c;
-        if (m < M && n < N) {
+        if (gt.tiles) {
+          if (32 * q + lane < rows) {
+            float4* dst = reinterpret_cast<float4*>(gt.y + static_cast<size_t>(m) * gt.ldy + n);
+#pragma unroll
+            for (int j = 0; j < 32; j += 4)
+              dst[j / 4] = make_float4(__uint_as_float(v[j]), __uint_as_float(v[j + 1]), __uint_as_float(v[j + 2]),
+                                       __uint_as_float(v[j + 3]));
+          }
+        } else if (m < M && n < N) {
           uint16_t* dst = y + static_cast<size_t>(m) * N + n;
           if (vec && n + 32 <= N) {
 #pragma unroll
@@ -227,6 +266,31 @@ __global__ void decode_b3_kernel(const uint32_t* __restrict__ codes, const uint1
   const int k0 = 80 * j, kn = min(80, K - k0);
   uint16_t* dst = w + static_cast<size_t>(n) * K + k0;
   const uint16_t* srow = scales + static_cast<size_t>(n) * ng;
+  if (kn == 80 && (K & 7) == 0) {
+    // whole quad: the four words in one 16-byte load, 80 values in ten 16-byte stores
+    const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<size_t>(n) * P + 4 * j));
+    const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
+    uint32_t o[40];
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t v = min(wv[wi], kB3Max);
+#pragma unroll
+      for (int d = 0; d < 20; d += 2) {
+        const uint32_t q1 = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
+        const int t0 = static_cast<int>(v - 3u * q1) - 1;
+        const uint32_t q2 = __umulhi(q1, 0xAAAAAAABu) >> 1;
+        const int t1 = static_cast<int>(q1 - 3u * q2) - 1;
+        v = q2;
+        const int k = 20 * wi + d;
+        const uint16_t s0 = __ldg(srow + (k0 + k) / G), s1 = __ldg(srow + (k0 + k + 1) / G);
+        o[k / 2] = static_cast<uint32_t>(signed_scale(t0, s0)) | (static_cast<uint32_t>(signed_scale(t1, s1)) << 16);
+      }
+    }
+    uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int c = 0; c < 10; ++c) d4[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    return;
+  }
   for (int wi = 0; wi < 4; ++wi) {
     if (20 * wi >= kn) break;
     uint32_t v = min(__ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi), kB3Max);
@@ -294,7 +358,40 @@ cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t*
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
   const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, sms));
-  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status_ptr());
+  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status_ptr(), GroupedTiles{});
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_gemm_grouped(const uint16_t* xa, int a_rows, const uint16_t* wa, int w_rows, int K, const int* tiles,
+                                const int* count, int max_tiles, float* y, int ldy, cudaStream_t s) {
+  using namespace gemm;
+  CUtensorMap tm_x, tm_w;
+  if (!make_tmap_2d(&tm_x, xa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, a_rows, static_cast<uint64_t>(K) * 2, BK, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_w, wa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, w_rows, static_cast<uint64_t>(K) * 2, BK, BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  cudaError_t e;
+  if ((e = ensure_attr()) != cudaSuccess) return e;
+  int dev = 0, sms = 148;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
+  const unsigned grid = static_cast<unsigned>(std::max(1, std::min(max_tiles, sms)));
+  const GroupedTiles gt{reinterpret_cast<const int4*>(tiles), count, y, ldy};
+  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, nullptr, a_rows, 0, K, status_ptr(), gt);
+  return cudaPeekAtLastError();
+}
+
+cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, uint16_t* w, cudaStream_t s) {
+  using namespace gemm;
+  const int N = d->N, K = d->K, G = d->group, P = pitch_words(K, d->packing), ng = K / G;
+  if (d->packing == TQ_PACK_2BIT) {
+    const long long n = static_cast<long long>(N) * (K / 16);
+    decode_2b_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, w, N, K, P, ng, G);
+  } else {
+    const long long n = static_cast<long long>(N) * ((K + 79) / 80);
+    decode_b3_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, w, N, K, P, ng, G);
+  }
   return cudaPeekAtLastError();
 }
 

@@ -49,6 +49,14 @@ size_t gemm_workspace_bytes(const tq_desc* d, int M);
 cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int M,
                         uint16_t* y, void* ws, cudaStream_t s);
 
+// Grouped prefill GEMM (expert layer): one persistent tcgen05 launch over a device-written tile list;
+// tiles[4 i .. 4 i + 3] = {A row, valid rows, B row, output column}, *count tiles (at most max_tiles).
+// xa: FP16 [a_rows][K]; wa: FP16 [w_rows][K]; y: fp32, row r at y + r * ldy.
+cudaError_t launch_gemm_grouped(const uint16_t* xa, int a_rows, const uint16_t* wa, int w_rows, int K, const int* tiles,
+                                const int* count, int max_tiles, float* y, int ldy, cudaStream_t s);
+// Weights of one matrix (or of stacked experts viewed as one matrix) decoded to FP16 s * t [N][K].
+cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, uint16_t* w, cudaStream_t s);
+
 // Host-side descriptor checks shared by the contraction entry points.
 tq_status check_linear_desc(const tq_desc* d);
 

@@ -53,6 +53,9 @@ def test_invalid_descriptors():
     assert tq.tq_gemv_workspace_bytes(tq.desc(64, 128, flags=tq.TQ_STATIC_WEIGHTS), 1) == 512
     assert tq.tq_moe_workspace_bytes(1, 257, 8, 2048, 512) == 0
     assert tq.tq_moe_workspace_bytes(8, 256, 8, 2048, 512) > 0
+    assert tq.tq_moe_gemm_workspace_bytes(256, 256, 8, 2048, 512) > 256 * 3 * 2048 * 512 * 2  # decoded experts
+    assert tq.tq_moe_gemm_workspace_bytes(256, 256, 8, 2000, 512) == 0   # H not a multiple of 256
+    assert tq.tq_moe_gemm_workspace_bytes(256, 256, 8, 2048, 64) == 0    # 2F not a multiple of 256
 
 
 def _call(name, *args):
