@@ -234,75 +234,122 @@ __device__ __forceinline__ uint16_t signed_scale(int t, uint16_t s) {
   return t == 0 ? static_cast<uint16_t>(0) : (t > 0 ? s : static_cast<uint16_t>(s ^ 0x8000u));
 }
 
-__global__ void decode_2b_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
-                                 uint16_t* __restrict__ w, int N, int K, int P, int ng, int G) {
-  const int wpr = K / 16;  // words with data per row
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<long long>(N) * wpr) return;
-  const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
-  const uint32_t word = __ldg(codes + static_cast<size_t>(n) * P + j);
-  const uint16_t s = __ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G);
-  uint32_t o[8];
-#pragma unroll
-  for (int h = 0; h < 8; ++h) {
-    const int d0 = static_cast<int>((word >> (4 * h)) & 3u), d1 = static_cast<int>((word >> (4 * h + 2)) & 3u);
-    // a field of 3 is not a valid code: it decodes as t = 0, as tq_unpack reads it
-    const int t0 = d0 == 3 ? 0 : d0 - 1, t1 = d1 == 3 ? 0 : d1 - 1;
-    o[h] = static_cast<uint32_t>(signed_scale(t0, s)) | (static_cast<uint32_t>(signed_scale(t1, s)) << 16);
-  }
-  uint4* dst = reinterpret_cast<uint4*>(w + static_cast<size_t>(n) * K + 16 * j);
-  dst[0] = make_uint4(o[0], o[1], o[2], o[3]);
-  dst[1] = make_uint4(o[4], o[5], o[6], o[7]);
+// The output of a CTA's threads is one contiguous range of W (threads take consecutive words or quads
+// of consecutive rows), so each thread writes its 16-byte pieces into shared memory at their offset
+// in that range and the CTA then stores the range with consecutive lanes on consecutive 16 bytes:
+// whole 32-byte sectors per store instead of half sectors.
+constexpr int kDecThreads = 256;
+
+__device__ __forceinline__ void flush_stage(const uint4* stage, uint16_t* w, long long base, long long end) {
+  __syncthreads();
+  uint4* out = reinterpret_cast<uint4*>(w + base);
+  const int nchunks = static_cast<int>((end - base) / 8);
+  for (int c = threadIdx.x; c < nchunks; c += blockDim.x) out[c] = stage[c];
 }
 
-__global__ void decode_b3_kernel(const uint32_t* __restrict__ codes, const uint16_t* __restrict__ scales,
-                                 uint16_t* __restrict__ w, int N, int K, int P, int ng, int G) {
+__global__ void __launch_bounds__(kDecThreads) decode_2b_kernel(const uint32_t* __restrict__ codes,
+                                                                const uint16_t* __restrict__ scales,
+                                                                uint16_t* __restrict__ w, int N, int K, int P, int ng,
+                                                                int G) {
+  __shared__ uint4 stage[kDecThreads * 2];
+  const int wpr = K / 16;  // words with data per row
+  const long long total = static_cast<long long>(N) * wpr;
+  const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x;
+  const long long i = i0 + threadIdx.x;
+  // word i writes W[16 i .. 16 i + 15] (rows are K = 16 * wpr wide): the CTA's range is contiguous
+  const long long base = 16 * i0, end = 16 * min(total, i0 + blockDim.x);
+  if (i < total) {
+    const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
+    const uint32_t word = __ldg(codes + static_cast<size_t>(n) * P + j);
+    const uint16_t s = __ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G);
+    uint32_t o[8];
+#pragma unroll
+    for (int h = 0; h < 8; ++h) {
+      const int d0 = static_cast<int>((word >> (4 * h)) & 3u), d1 = static_cast<int>((word >> (4 * h + 2)) & 3u);
+      // a field of 3 is not a valid code: it decodes as t = 0, as tq_unpack reads it
+      const int t0 = d0 == 3 ? 0 : d0 - 1, t1 = d1 == 3 ? 0 : d1 - 1;
+      o[h] = static_cast<uint32_t>(signed_scale(t0, s)) | (static_cast<uint32_t>(signed_scale(t1, s)) << 16);
+    }
+    stage[2 * threadIdx.x] = make_uint4(o[0], o[1], o[2], o[3]);
+    stage[2 * threadIdx.x + 1] = make_uint4(o[4], o[5], o[6], o[7]);
+  }
+  flush_stage(stage, w, base, end);
+}
+
+// base-3: one thread per 4 words (80 trits) of a row, digits by exact reciprocal multiplies.  With K a
+// multiple of 8 the quads' outputs are whole 16-byte pieces and go through the staging above; otherwise
+// each value is stored on its own.
+__global__ void __launch_bounds__(kDecThreads) decode_b3_kernel(const uint32_t* __restrict__ codes,
+                                                                const uint16_t* __restrict__ scales,
+                                                                uint16_t* __restrict__ w, int N, int K, int P, int ng,
+                                                                int G) {
+  __shared__ uint4 stage[kDecThreads * 10];
   const int qpr = K / 80;  // groups of 4 words (80 trits, 160 bytes of output) per row; K % 80 handled below
   const int tail = K - qpr * 80;
   const int per_row = qpr + (tail > 0 ? 1 : 0);
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<long long>(N) * per_row) return;
-  const int n = static_cast<int>(i / per_row), j = static_cast<int>(i - static_cast<long long>(n) * per_row);
-  const int k0 = 80 * j, kn = min(80, K - k0);
-  uint16_t* dst = w + static_cast<size_t>(n) * K + k0;
-  const uint16_t* srow = scales + static_cast<size_t>(n) * ng;
-  if (kn == 80 && (K & 7) == 0) {
-    // whole quad: the four words in one 16-byte load, 80 values in ten 16-byte stores
-    const uint4 q4 = __ldg(reinterpret_cast<const uint4*>(codes + static_cast<size_t>(n) * P + 4 * j));
-    const uint32_t wv[4] = {q4.x, q4.y, q4.z, q4.w};
-    uint32_t o[40];
+  const long long total = static_cast<long long>(N) * per_row;
+  const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x;
+  const long long i = i0 + threadIdx.x;
+  auto out_of = [&](long long q) {  // first element of W that quad q writes
+    const long long n = q / per_row;
+    return n * K + 80 * (q - n * per_row);
+  };
+  const bool staged = (K & 7) == 0;
+  const long long base = out_of(i0);
+  const long long last = min(total, i0 + blockDim.x) - 1;
+  const long long end = out_of(last) + min(80, K - 80 * static_cast<int>(last % per_row));
+  if (i < total) {
+    const int n = static_cast<int>(i / per_row), j = static_cast<int>(i - static_cast<long long>(n) * per_row);
+    const int k0 = 80 * j, kn = min(80, K - k0);
+    const uint16_t* srow = scales + static_cast<size_t>(n) * ng;
+    if (staged) {
+      uint32_t wv[4];
 #pragma unroll
-    for (int wi = 0; wi < 4; ++wi) {
-      uint32_t v = min(wv[wi], kB3Max);
+      for (int wi = 0; wi < 4; ++wi) wv[wi] = 20 * wi < kn ? __ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi) : 0u;
+      // the (at most three) groups the 80 trits touch, and where the next two start (relative to k0)
+      const int g0 = k0 / G;
+      const int b1 = (g0 + 1) * G - k0, b2 = b1 + G;
+      const uint16_t sa = __ldg(srow + g0);
+      const uint16_t sb = b1 < kn ? __ldg(srow + g0 + 1) : sa;
+      const uint16_t sc = b2 < kn ? __ldg(srow + g0 + 2) : sb;
+      uint32_t o[40];
 #pragma unroll
-      for (int d = 0; d < 20; d += 2) {
-        const uint32_t q1 = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
-        const int t0 = static_cast<int>(v - 3u * q1) - 1;
-        const uint32_t q2 = __umulhi(q1, 0xAAAAAAABu) >> 1;
-        const int t1 = static_cast<int>(q1 - 3u * q2) - 1;
-        v = q2;
-        const int k = 20 * wi + d;
-        const uint16_t s0 = __ldg(srow + (k0 + k) / G), s1 = __ldg(srow + (k0 + k + 1) / G);
-        o[k / 2] = static_cast<uint32_t>(signed_scale(t0, s0)) | (static_cast<uint32_t>(signed_scale(t1, s1)) << 16);
+      for (int wi = 0; wi < 4; ++wi) {
+        uint32_t v = min(wv[wi], kB3Max);
+#pragma unroll
+        for (int d = 0; d < 20; d += 2) {
+          const uint32_t q1 = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
+          const int t0 = static_cast<int>(v - 3u * q1) - 1;
+          const uint32_t q2 = __umulhi(q1, 0xAAAAAAABu) >> 1;
+          const int t1 = static_cast<int>(q1 - 3u * q2) - 1;
+          v = q2;
+          const int k = 20 * wi + d;
+          // scale of trits k, k + 1 (group boundaries fall on even k: groups are 64 or 128)
+          const uint16_t sk = k < b1 ? sa : (k < b2 ? sb : sc);
+          o[k / 2] = static_cast<uint32_t>(signed_scale(t0, sk)) | (static_cast<uint32_t>(signed_scale(t1, sk)) << 16);
+        }
+      }
+      uint4* st = stage + (out_of(i) - base) / 8;
+#pragma unroll
+      for (int c = 0; c < 10; ++c)
+        if (8 * c < kn) st[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+    } else {
+      uint16_t* dst = w + static_cast<size_t>(n) * K + k0;
+      for (int wi = 0; wi < 4; ++wi) {
+        if (20 * wi >= kn) break;
+        uint32_t v = min(__ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi), kB3Max);
+#pragma unroll
+        for (int d = 0; d < 20; ++d) {
+          const uint32_t qd = __umulhi(v, 0xAAAAAAABu) >> 1;
+          const int t = static_cast<int>(v - 3u * qd) - 1;
+          v = qd;
+          const int k = 20 * wi + d;
+          if (k < kn) dst[k] = signed_scale(t, __ldg(srow + (k0 + k) / G));
+        }
       }
     }
-    uint4* d4 = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-    for (int c = 0; c < 10; ++c) d4[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-    return;
   }
-  for (int wi = 0; wi < 4; ++wi) {
-    if (20 * wi >= kn) break;
-    uint32_t v = min(__ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi), kB3Max);
-#pragma unroll
-    for (int d = 0; d < 20; ++d) {
-      const uint32_t qd = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
-      const int t = static_cast<int>(v - 3u * qd) - 1;
-      v = qd;
-      const int k = 20 * wi + d;
-      if (k < kn) dst[k] = signed_scale(t, __ldg(srow + (k0 + k) / G));
-    }
-  }
+  if (staged) flush_stage(stage, w, base, end);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -339,10 +386,10 @@ cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t*
   // W = s * t in FP16
   if (d->packing == TQ_PACK_2BIT) {
     const long long n = static_cast<long long>(N) * (K / 16);
-    decode_2b_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
+    decode_2b_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
   } else {
     const long long n = static_cast<long long>(N) * ((K + 79) / 80);
-    decode_b3_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
+    decode_b3_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
   }
   if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
   CUtensorMap tm_x, tm_w;
@@ -387,10 +434,10 @@ cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_
   const int N = d->N, K = d->K, G = d->group, P = pitch_words(K, d->packing), ng = K / G;
   if (d->packing == TQ_PACK_2BIT) {
     const long long n = static_cast<long long>(N) * (K / 16);
-    decode_2b_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, w, N, K, P, ng, G);
+    decode_2b_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, w, N, K, P, ng, G);
   } else {
     const long long n = static_cast<long long>(N) * ((K + 79) / 80);
-    decode_b3_kernel<<<static_cast<unsigned>((n + 255) / 256), 256, 0, s>>>(codes, scales, w, N, K, P, ng, G);
+    decode_b3_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, w, N, K, P, ng, G);
   }
   return cudaPeekAtLastError();
 }
