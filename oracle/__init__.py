@@ -44,9 +44,19 @@ import numpy as np
 
 PACK_B3 = 1
 PACK_2BIT = 2
+PACK_3BIT = 3
 B3_TRITS = 20      # [TT] point 3: base-3 code packs 20 ternary indices into one 32-bit integer
 B2_TRITS = 16
 B3_MAX = 3 ** 20 - 1  # largest valid base-3 word
+# [TT] point 1: the non-expert linears (attention, GDN projections, lm_head) stay at 3 bits.  This
+# build's reading of that format: integer codes q in {-4..3} (digit d = q + 4) times the group's
+# FP16 scale; 10 digits per 32-bit word at bits 3j (bits 30-31 zero); each block of 64 codes takes 7
+# words (codes 10i..10i+9 of the block in word i; word 6 holds codes 60..63 and six padding digits),
+# so no word straddles a group of 64 or 128.
+Q3_PER_WORD = 10
+Q3_BLOCK = 64
+Q3_WORDS_PER_BLOCK = 7
+Q3_PAD_DIGIT = 4   # q = 0
 
 
 # ----------------------------------------------------------------------------------------------
@@ -54,7 +64,9 @@ B3_MAX = 3 ** 20 - 1  # largest valid base-3 word
 # ----------------------------------------------------------------------------------------------
 
 def words_per_row(K: int, packing: int) -> int:
-    """Words that hold one row of K trits, before pitch padding."""
+    """Words that hold one row of K trits (or 3-bit codes), before pitch padding."""
+    if packing == PACK_3BIT:
+        return -(-K // Q3_BLOCK) * Q3_WORDS_PER_BLOCK
     per = B3_TRITS if packing == PACK_B3 else B2_TRITS
     return -(-K // per)
 
@@ -86,7 +98,11 @@ def pack(trits: np.ndarray, packing: int) -> np.ndarray:
 
     base-3: word j of a row = sum_{i<20} (t[20j+i] + 1) * 3**i.
     2-bit : word j of a row = sum_{i<16} (t[16j+i] + 1) << 2i.
+    3-bit : codes q in {-4..3}; word i of 64-code block b = sum_{j<10} (q[64b + 10i + j] + 4) << 3j
+            (padding digits 4, i.e. q = 0).
     """
+    if packing == PACK_3BIT:
+        return _pack3(trits)
     trits = np.asarray(trits)
     assert trits.ndim == 2 and np.isin(trits, (-1, 0, 1)).all()
     N, K = trits.shape
@@ -103,13 +119,44 @@ def pack(trits: np.ndarray, packing: int) -> np.ndarray:
     return words.astype(np.uint32)
 
 
+def _pack3(q: np.ndarray) -> np.ndarray:
+    q = np.asarray(q)
+    assert q.ndim == 2 and ((q >= -4) & (q <= 3)).all()
+    N, K = q.shape
+    nb = -(-K // Q3_BLOCK)
+    P = row_pitch_words(K, PACK_3BIT)
+    digits = np.full((N, nb * Q3_BLOCK), Q3_PAD_DIGIT, dtype=np.int64)
+    digits[:, :K] = q.astype(np.int64) + 4
+    slots = np.full((N, nb, Q3_WORDS_PER_BLOCK * Q3_PER_WORD), Q3_PAD_DIGIT, dtype=np.int64)
+    slots[:, :, :Q3_BLOCK] = digits.reshape(N, nb, Q3_BLOCK)
+    slots = slots.reshape(N, nb * Q3_WORDS_PER_BLOCK, Q3_PER_WORD)
+    words = (slots << (3 * np.arange(Q3_PER_WORD, dtype=np.int64))).sum(axis=2)
+    out = np.full((N, P), sum(Q3_PAD_DIGIT << (3 * j) for j in range(Q3_PER_WORD)), dtype=np.int64)
+    out[:, :nb * Q3_WORDS_PER_BLOCK] = words
+    return out.astype(np.uint32)
+
+
+def _unpack3(codes: np.ndarray, K: int):
+    codes = np.asarray(codes, dtype=np.uint32).astype(np.int64)
+    N, P = codes.shape
+    nb = -(-K // Q3_BLOCK)
+    invalid = codes >= (1 << 30)
+    w = codes[:, :nb * Q3_WORDS_PER_BLOCK].reshape(N, nb, Q3_WORDS_PER_BLOCK)
+    digits = np.stack([(w >> (3 * j)) & 7 for j in range(Q3_PER_WORD)], axis=3)  # [N, nb, 7, 10]
+    digits = digits.reshape(N, nb, Q3_WORDS_PER_BLOCK * Q3_PER_WORD)[:, :, :Q3_BLOCK].reshape(N, nb * Q3_BLOCK)
+    return (digits[:, :K] - 4).astype(np.int8), int(invalid.sum())
+
+
 def unpack(codes: np.ndarray, K: int, packing: int):
     """uint32 codes [N, P] -> (int8 trits [N, K], number of invalid words).
 
     base-3: digit i of word v is (v // 3**i) % 3, t = digit - 1; a word above 3**20 - 1 is invalid.
     2-bit : field i is (v >> 2i) & 3, t = field - 1; a word holding a field equal to 3 is invalid.
+    3-bit : digit j of word v is (v >> 3j) & 7, q = digit - 4; a word with bit 30 or 31 set is invalid.
     Every word of the row pitch is validated; the values of padding digits are not.
     """
+    if packing == PACK_3BIT:
+        return _unpack3(codes, K)
     codes = np.asarray(codes, dtype=np.uint32).astype(np.int64)
     N, P = codes.shape
     if packing == PACK_B3:

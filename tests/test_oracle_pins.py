@@ -196,6 +196,48 @@ def pin_contraction_bruteforce(O):
                 assert abs(A[b, nn] - aab) <= 1e-12 * max(1.0, aab)
 
 
+def pin_pack_3bit(O):
+    """3-bit codes against Python's own base-8 parsing of each word's ten digits (digit q + 4, least
+    significant first; blocks of 64 codes in 7 words, the last word of a block holding four codes and
+    six q = 0 digits), a hand-worked block, the row pitch, the invalid-word count and the contraction
+    by brute force."""
+    r = rng(31)
+    for K in (1, 10, 63, 64, 65, 200, 640):
+        q = r.integers(-4, 4, size=(3, K)).astype(np.int8)
+        codes = O.pack(q, O.PACK_3BIT)
+        nb = -(-K // 64)
+        assert codes.shape == (3, -(-nb * 7 // 4) * 4)
+        for n in range(3):
+            for b in range(nb):
+                for i in range(7):
+                    digits = []
+                    for j in range(10):
+                        k = 64 * b + 10 * i + j
+                        digits.append(int(q[n, k]) + 4 if (10 * i + j < 64 and k < K) else 4)
+                    assert int(codes[n, 7 * b + i]) == int("".join(str(d) for d in reversed(digits)), 8)
+        back, bad = O.unpack(codes, K, O.PACK_3BIT)
+        assert bad == 0 and np.array_equal(back, q)
+    q = np.array([[k % 8 - 4 for k in range(64)]], dtype=np.int8)
+    c = O.pack(q, O.PACK_3BIT)
+    assert int(c[0, 0]) == sum((k % 8) << (3 * k) for k in range(10))
+    assert int(c[0, 6]) == sum(d << (3 * j) for j, d in enumerate([4, 5, 6, 7, 4, 4, 4, 4, 4, 4]))
+    bad_codes = c.copy()
+    bad_codes[0, 2] |= np.uint32(1 << 30)
+    assert O.unpack(bad_codes, 64, O.PACK_3BIT)[1] == 1
+    # the contraction on 3-bit codes: y = sum_k s q x~, brute force
+    N, K, B, group = 2, 256, 2, 64
+    q = r.integers(-4, 4, size=(N, K)).astype(np.int8)
+    sc = np.exp(r.normal(-4, 0.5, size=(N, K // group))).astype(np.float16)
+    x = r.standard_normal((B, K)).astype(np.float32)
+    y, A, bad = O.ternary_linear(O.pack(q, O.PACK_3BIT), sc, x, K, group, O.PACK_3BIT, 128)
+    assert bad == 0
+    for b in range(B):
+        xt = fwht_closed_form([float(v) for v in x[b]], 128)
+        for nn in range(N):
+            terms = [float(sc[nn, k // group]) * int(q[nn, k]) * xt[k] for k in range(K)]
+            assert abs(y[b, nn] - sum(terms)) <= 1e-12 * max(1.0, sum(abs(v) for v in terms))
+
+
 def pin_special_cases(O):
     r = rng(8)
     N, K, B = 4, 384, 3
@@ -445,7 +487,7 @@ def pin_quantize_round_trip(O):
 PINS = [pin_pack_b3, pin_pack_2b, pin_unpack, pin_format_constants, pin_hadamard, pin_fwht,
         pin_rotation_identity, pin_contraction_bruteforce, pin_special_cases, pin_moe_route, pin_moe_layer,
         pin_silu, pin_moe_down_from_h, pin_quantize_closed_form, pin_quantize_nearest_level,
-        pin_quantize_round_trip]
+        pin_quantize_round_trip, pin_pack_3bit]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -459,6 +501,19 @@ def test_oracle_pin(pin):
 
 ORIG = {k: getattr(O_real, k) for k in ("pack", "unpack", "hadamard", "block_fwht", "moe_route", "dequant",
                                         "silu", "moe_down_from_h", "quantize")}
+
+
+def _pack3_blocks_of_60(trits, packing):
+    """3-bit codes packed densely (no block padding: 6 words of 10 per 60 codes)."""
+    if packing != O_real.PACK_3BIT:
+        return ORIG["pack"](trits, packing)
+    q = np.asarray(trits)
+    N, K = q.shape
+    P = O_real.row_pitch_words(K, packing)
+    d = np.full((N, P * 10), 4, dtype=np.int64)
+    d[:, :K] = q.astype(np.int64) + 4
+    w = (d.reshape(N, P, 10) << (3 * np.arange(10))).sum(axis=2)
+    return w.astype(np.uint32)
 
 
 def _pack_msd_first(trits, packing):
@@ -541,6 +596,7 @@ def _quantize_with(stat="mean", thr=0.5, rotate=True, c=None, ties_up=False, int
 
 
 MUTANTS = {
+    "3-bit blocks not padded to 64": dict(pack=_pack3_blocks_of_60),
     "quantize scale from max": dict(quantize=_quantize_with(stat="max")),
     "quantize threshold 0.7 S": dict(quantize=_quantize_with(thr=0.7)),
     "quantize without rotation": dict(quantize=_quantize_with(rotate=False)),
