@@ -48,6 +48,7 @@ from ternary_weight_quantized_unpack_b300 import inputs  # noqa: E402
 GB = 1e9
 LAYERS = 64
 PACKINGS = {"2bit": tq.TQ_PACK_2BIT, "base3": tq.TQ_PACK_B3}
+PACKING_NAMES = {tq.TQ_PACK_2BIT: "2bit", tq.TQ_PACK_B3: "base3", tq.TQ_PACK_3BIT: "3bit"}
 METRIC = "packed-weight HBM GB/s (% of B300 peak) and model-equivalent decode tok/s"
 
 
@@ -539,7 +540,8 @@ def bench_layer_linears(packing, batches, reps, seed=inputs.seed_of(2)):
     w = []
     for lin in lins:
         d = tq.desc(lin.N, lin.K, 128, packing)
-        codes = tq.tq_pack(d, torch.randint(-1, 2, (lin.N, lin.K), dtype=torch.int8, device="cuda", generator=gen))
+        lo, hi = (-4, 4) if packing == tq.TQ_PACK_3BIT else (-1, 2)
+        codes = tq.tq_pack(d, torch.randint(lo, hi, (lin.N, lin.K), dtype=torch.int8, device="cuda", generator=gen))
         s = torch.exp(torch.randn((lin.N, lin.K // 128), generator=gen, device="cuda") * 0.5 - 4).half()
         w.append((lin, d, codes, s))
     out = []
@@ -553,7 +555,7 @@ def bench_layer_linears(packing, batches, reps, seed=inputs.seed_of(2)):
             per[lin.name] = l2_cold_times(call, reps, flush) * 1e3
         tot_us = sum(per.values())
         byts = sum(tq.tq_packed_bytes(d) + tq.tq_scale_bytes(d) for _, d, _, _ in w)
-        out.append({"packing": "base3" if packing == tq.TQ_PACK_B3 else "2bit", "batch": b,
+        out.append({"packing": PACKING_NAMES[packing], "batch": b,
                     "us_per_linear_l2_cold": per, "us_sum_7": tot_us,
                     "GB_s": byts / (tot_us * 1e-6) / GB,
                     "tok_s_64_layers": b / (LAYERS * tot_us * 1e-6)})
@@ -781,6 +783,9 @@ def run_tq(args, rank, world, local):
         ex["single_linear"] = bench_single_linear(max(20, args.steps // 2))
         for pk in (tq.TQ_PACK_2BIT, tq.TQ_PACK_B3):
             ex["layer_linears"] += bench_layer_linears(pk, inputs.DENSE_DECODE["batches"], max(10, args.steps // 5))
+        # 3-bit codes (the precision the non-expert linears keep)
+        ex["layer_linears"] += bench_layer_linears(tq.TQ_PACK_3BIT, inputs.DENSE_DECODE["batches"],
+                                                   max(10, args.steps // 5))
         torch.cuda.empty_cache()
         for T in inputs.MOE["tokens"]:
             r = bench_moe(T, max(10, args.steps // 2), 3)

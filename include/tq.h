@@ -55,8 +55,19 @@ typedef enum {
 
 typedef enum {
   TQ_PACK_B3 = 1,   /* base-3: word = sum_{i<20} (t[20j+i]+1) * 3^i; pad trits t=0; row pitch multiple of 4 words */
-  TQ_PACK_2BIT = 2  /* 2-bit : word = sum_{i<16} (t[16j+i]+1) << 2i;  field 3 invalid; pad trits t=0 */
+  TQ_PACK_2BIT = 2, /* 2-bit : word = sum_{i<16} (t[16j+i]+1) << 2i;  field 3 invalid; pad trits t=0 */
+  TQ_PACK_3BIT = 3  /* 3-bit codes q in -4..3 (the non-expert linears; see below) */
 } tq_packing;
+/* TQ_PACK_3BIT (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, "为什么 1.58bit 没变成乱码", point 1:
+ * attention, GDN projections and lm_head stay at 3 bits; the page gives no format, this is the
+ * library's): W = s * q with q in {-4..3}, digit d = q + 4.  A word has ten 3-bit slots, five per
+ * 16-bit half: slot j < 5 at bits 3j, slot j >= 5 at bits 16 + 3(j - 5); bits 15 and 31 are zero (a
+ * word with either set is invalid).  Each block of 64 codes takes 7 words: word i < 6 holds codes
+ * 10i..10i+9 of the block in slots 0..9; word 6 holds codes 60, 61 in slots 0, 1 and 62, 63 in slots
+ * 5, 6, digit 4 (q = 0) elsewhere; so no word straddles a group.  Row pitch ceil(K/64) * 7 words,
+ * rounded up to a multiple of 4.  Supported by the size functions, tq_pack / tq_unpack (trits hold
+ * q), tq_gemv and tq_gemv_noalloc (batch 1..16, tensor-core decode as for base-3); the other
+ * contractions (tq_gemm, tq_seq_*, tq_moe_*) return TQ_ERR_UNSUPPORTED. */
 
 /* One ternary weight matrix W [N][K] (y = W x~). */
 typedef struct {

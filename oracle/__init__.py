@@ -48,15 +48,24 @@ PACK_3BIT = 3
 B3_TRITS = 20      # [TT] point 3: base-3 code packs 20 ternary indices into one 32-bit integer
 B2_TRITS = 16
 B3_MAX = 3 ** 20 - 1  # largest valid base-3 word
-# [TT] point 1: the non-expert linears (attention, GDN projections, lm_head) stay at 3 bits.  This
-# build's reading of that format: integer codes q in {-4..3} (digit d = q + 4) times the group's
-# FP16 scale; 10 digits per 32-bit word at bits 3j (bits 30-31 zero); each block of 64 codes takes 7
-# words (codes 10i..10i+9 of the block in word i; word 6 holds codes 60..63 and six padding digits),
-# so no word straddles a group of 64 or 128.
+# [TT] point 1: the non-expert linears (attention, GDN projections, lm_head) stay at 3 bits.  The
+# page fixes no bit layout; this build's reading: integer codes q in {-4..3} (digit d = q + 4) times
+# the group's FP16 scale.  A 32-bit word has ten 3-bit slots, five per 16-bit half: slot j < 5 at
+# bits 3j, slot j >= 5 at bits 16 + 3(j - 5); bits 15 and 31 are zero.  Each block of 64 codes takes
+# 7 words: word i < 6 holds codes 10i..10i+9 of the block in slots 0..9; word 6 holds codes 60, 61 in
+# slots 0, 1 and codes 62, 63 in slots 5, 6, its other slots the padding digit.  No word straddles a
+# group of 64 or 128.
 Q3_PER_WORD = 10
 Q3_BLOCK = 64
 Q3_WORDS_PER_BLOCK = 7
 Q3_PAD_DIGIT = 4   # q = 0
+# (word, slot) of each code of a block, in code order
+Q3_CODE_SLOTS = [(c // 10, c % 10) for c in range(60)] + [(6, 0), (6, 1), (6, 5), (6, 6)]
+
+
+def q3_slot_bit(j: int) -> int:
+    """Lowest bit of slot j of a 3-bit word."""
+    return 3 * j if j < 5 else 16 + 3 * (j - 5)
 
 
 # ----------------------------------------------------------------------------------------------
@@ -98,8 +107,8 @@ def pack(trits: np.ndarray, packing: int) -> np.ndarray:
 
     base-3: word j of a row = sum_{i<20} (t[20j+i] + 1) * 3**i.
     2-bit : word j of a row = sum_{i<16} (t[16j+i] + 1) << 2i.
-    3-bit : codes q in {-4..3}; word i of 64-code block b = sum_{j<10} (q[64b + 10i + j] + 4) << 3j
-            (padding digits 4, i.e. q = 0).
+    3-bit : codes q in {-4..3}; code c of 64-code block b sits as digit q + 4 in slot
+            Q3_CODE_SLOTS[c] = (i, j) of word 7b + i, at bit q3_slot_bit(j) (padding digits 4, q = 0).
     """
     if packing == PACK_3BIT:
         return _pack3(trits)
@@ -125,13 +134,15 @@ def _pack3(q: np.ndarray) -> np.ndarray:
     N, K = q.shape
     nb = -(-K // Q3_BLOCK)
     P = row_pitch_words(K, PACK_3BIT)
-    digits = np.full((N, nb * Q3_BLOCK), Q3_PAD_DIGIT, dtype=np.int64)
-    digits[:, :K] = q.astype(np.int64) + 4
-    slots = np.full((N, nb, Q3_WORDS_PER_BLOCK * Q3_PER_WORD), Q3_PAD_DIGIT, dtype=np.int64)
-    slots[:, :, :Q3_BLOCK] = digits.reshape(N, nb, Q3_BLOCK)
-    slots = slots.reshape(N, nb * Q3_WORDS_PER_BLOCK, Q3_PER_WORD)
-    words = (slots << (3 * np.arange(Q3_PER_WORD, dtype=np.int64))).sum(axis=2)
-    out = np.full((N, P), sum(Q3_PAD_DIGIT << (3 * j) for j in range(Q3_PER_WORD)), dtype=np.int64)
+    digits = np.full((N, nb, Q3_BLOCK), Q3_PAD_DIGIT, dtype=np.int64)
+    digits.reshape(N, nb * Q3_BLOCK)[:, :K] = q.astype(np.int64) + 4
+    slots = np.full((N, nb, Q3_WORDS_PER_BLOCK, Q3_PER_WORD), Q3_PAD_DIGIT, dtype=np.int64)
+    for c, (i, j) in enumerate(Q3_CODE_SLOTS):
+        slots[:, :, i, j] = digits[:, :, c]
+    shifts = np.array([q3_slot_bit(j) for j in range(Q3_PER_WORD)], dtype=np.int64)
+    words = (slots << shifts).sum(axis=3).reshape(N, nb * Q3_WORDS_PER_BLOCK)
+    pad_word = sum(Q3_PAD_DIGIT << q3_slot_bit(j) for j in range(Q3_PER_WORD))
+    out = np.full((N, P), pad_word, dtype=np.int64)
     out[:, :nb * Q3_WORDS_PER_BLOCK] = words
     return out.astype(np.uint32)
 
@@ -140,11 +151,12 @@ def _unpack3(codes: np.ndarray, K: int):
     codes = np.asarray(codes, dtype=np.uint32).astype(np.int64)
     N, P = codes.shape
     nb = -(-K // Q3_BLOCK)
-    invalid = codes >= (1 << 30)
+    invalid = (codes & ((1 << 15) | (1 << 31))) != 0
     w = codes[:, :nb * Q3_WORDS_PER_BLOCK].reshape(N, nb, Q3_WORDS_PER_BLOCK)
-    digits = np.stack([(w >> (3 * j)) & 7 for j in range(Q3_PER_WORD)], axis=3)  # [N, nb, 7, 10]
-    digits = digits.reshape(N, nb, Q3_WORDS_PER_BLOCK * Q3_PER_WORD)[:, :, :Q3_BLOCK].reshape(N, nb * Q3_BLOCK)
-    return (digits[:, :K] - 4).astype(np.int8), int(invalid.sum())
+    digits = np.empty((N, nb, Q3_BLOCK), dtype=np.int64)
+    for c, (i, j) in enumerate(Q3_CODE_SLOTS):
+        digits[:, :, c] = (w[:, :, i] >> q3_slot_bit(j)) & 7
+    return (digits.reshape(N, nb * Q3_BLOCK)[:, :K] - 4).astype(np.int8), int(invalid.sum())
 
 
 def unpack(codes: np.ndarray, K: int, packing: int):
@@ -152,7 +164,8 @@ def unpack(codes: np.ndarray, K: int, packing: int):
 
     base-3: digit i of word v is (v // 3**i) % 3, t = digit - 1; a word above 3**20 - 1 is invalid.
     2-bit : field i is (v >> 2i) & 3, t = field - 1; a word holding a field equal to 3 is invalid.
-    3-bit : digit j of word v is (v >> 3j) & 7, q = digit - 4; a word with bit 30 or 31 set is invalid.
+    3-bit : slot j of word v is (v >> q3_slot_bit(j)) & 7, q = digit - 4; a word with bit 15 or 31 set
+            is invalid.
     Every word of the row pitch is validated; the values of padding digits are not.
     """
     if packing == PACK_3BIT:

@@ -19,6 +19,7 @@ LIB_PATH = os.path.join(PKG_DIR, "libtq.so")
 
 TQ_PACK_B3 = 1
 TQ_PACK_2BIT = 2
+TQ_PACK_3BIT = 3
 TQ_STATIC_WEIGHTS = 1
 
 STATUS = {0: "TQ_OK", 1: "TQ_ERR_INVALID_ARG", 2: "TQ_ERR_UNSUPPORTED", 3: "TQ_ERR_MISALIGNED",

@@ -40,22 +40,29 @@ int* status_ptr() {
   return g_status_addr[dev];
 }
 
-tq_status check_linear_desc(const tq_desc* d) {
+namespace {
+tq_status check_desc_rules(const tq_desc* d, bool allow_3bit) {
   if (!d || d->N < 1 || d->K < 1) return TQ_ERR_INVALID_ARG;
-  if (d->packing != TQ_PACK_B3 && d->packing != TQ_PACK_2BIT) return TQ_ERR_INVALID_ARG;
+  if (d->packing == TQ_PACK_3BIT && !allow_3bit) return TQ_ERR_UNSUPPORTED;
+  if (d->packing != TQ_PACK_B3 && d->packing != TQ_PACK_2BIT && d->packing != TQ_PACK_3BIT) return TQ_ERR_INVALID_ARG;
   if (d->group != 64 && d->group != 128) return TQ_ERR_UNSUPPORTED;
   if (d->fwht_block != 0 && d->fwht_block != kFwhtBlock) return TQ_ERR_UNSUPPORTED;
   if (d->K % kFwhtBlock != 0) return TQ_ERR_UNSUPPORTED;
   if (d->flags & ~TQ_STATIC_WEIGHTS) return TQ_ERR_INVALID_ARG;
   return TQ_OK;
 }
+}  // namespace
+
+tq_status check_linear_desc(const tq_desc* d) { return check_desc_rules(d, false); }
+tq_status check_gemv_desc(const tq_desc* d) { return check_desc_rules(d, true); }
 
 }  // namespace tq
 
 using namespace tq;
 
 static bool desc_ok(const tq_desc* d) {
-  return d && d->N >= 1 && d->K >= 1 && (d->packing == TQ_PACK_B3 || d->packing == TQ_PACK_2BIT);
+  return d && d->N >= 1 && d->K >= 1 &&
+         (d->packing == TQ_PACK_B3 || d->packing == TQ_PACK_2BIT || d->packing == TQ_PACK_3BIT);
 }
 
 extern "C" size_t tq_row_pitch_words(const tq_desc* d) {

@@ -3,8 +3,10 @@
 // base-3: 20 trits per 32-bit word, word = sum_i (t_i + 1) 3^i (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B page, section
 // "为什么 1.58bit 没变成乱码", point 3: base-3 code, 20 ternary indices per 32-bit integer, ~1.6 bpw).
 // 2-bit : 16 trits per word, field (t + 1) at bits 2i; field 3 is not a valid code.
+// 3-bit : codes q in -4..3 of the non-expert linears, digit q + 4 at bits 3j of a word, 10 per word,
+// each block of 64 codes in 7 words (word 6 holds four codes and six q = 0 digits).
 // Rows are padded to a multiple of 4 words (16 bytes) so every row starts 16-byte aligned; every
-// padding trit is t = 0.
+// padding trit (code) is 0.
 #include "tq_internal.cuh"
 
 namespace tq {
@@ -18,7 +20,15 @@ __global__ void pack_kernel(const int8_t* __restrict__ trits, uint32_t* __restri
   const int8_t* row = trits + static_cast<size_t>(n) * K;
   bool bad = false;
   uint32_t w = 0;
-  if (packing == TQ_PACK_B3) {
+  if (packing == TQ_PACK_3BIT) {
+    const int b = j / kQ3WordsPerBlock, i = j - b * kQ3WordsPerBlock;
+    for (int q = 0; q < kQ3PerWord; ++q) {
+      const int c = q3_slot_code(i, q), k = kQ3Block * b + c;
+      int v = c >= 0 && k < K ? row[k] : 0;
+      if (v < -4 || v > 3) { bad = true; v = 0; }
+      w |= static_cast<uint32_t>(v + 4) << q3_slot_bit(q);
+    }
+  } else if (packing == TQ_PACK_B3) {
     // Horner from the most significant digit: w = (((d19) 3 + d18) 3 + ...) 3 + d0
     for (int q = kB3Trits - 1; q >= 0; --q) {
       const int k = j * kB3Trits + q;
@@ -46,7 +56,14 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ codes, int8_t* __rest
   uint32_t v = codes[i];
   int8_t* row = trits + static_cast<size_t>(n) * K;
   bool bad;
-  if (packing == TQ_PACK_B3) {
+  if (packing == TQ_PACK_3BIT) {
+    bad = (v & 0x80008000u) != 0u;
+    const int b = j / kQ3WordsPerBlock, i = j - b * kQ3WordsPerBlock;
+    for (int q = 0; q < kQ3PerWord; ++q) {
+      const int c = q3_slot_code(i, q), k = kQ3Block * b + c;
+      if (c >= 0 && k < K) row[k] = static_cast<int8_t>(static_cast<int>((v >> q3_slot_bit(q)) & 7u) - 4);
+    }
+  } else if (packing == TQ_PACK_B3) {
     bad = v > kB3Max;
     for (int q = 0; q < kB3Trits; ++q) {
       const uint32_t d = v % 3u;
@@ -71,7 +88,7 @@ __global__ void unpack_kernel(const uint32_t* __restrict__ codes, int8_t* __rest
 
 tq_status check_desc_basic(const tq_desc* d) {
   if (!d || d->N < 1 || d->K < 1) return TQ_ERR_INVALID_ARG;
-  if (d->packing != TQ_PACK_B3 && d->packing != TQ_PACK_2BIT) return TQ_ERR_INVALID_ARG;
+  if (d->packing != TQ_PACK_B3 && d->packing != TQ_PACK_2BIT && d->packing != TQ_PACK_3BIT) return TQ_ERR_INVALID_ARG;
   return TQ_OK;
 }
 

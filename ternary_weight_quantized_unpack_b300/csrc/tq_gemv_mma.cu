@@ -85,6 +85,13 @@ struct Geo<TQ_PACK_2BIT> {
   static constexpr int UT = 512;
   static constexpr int SLAB = 16;
 };
+template <>
+struct Geo<TQ_PACK_3BIT> {
+  static constexpr int UT = 256;   // codes per unit (28 words = 4 blocks of 64; 2 groups of 128 or 4 of 64)
+  static constexpr int SLAB = 64;  // rows per warp (column layout)
+};
+__host__ __device__ constexpr int unit_codes(int pack) { return pack == TQ_PACK_B3 ? 640 : pack == TQ_PACK_3BIT ? 256 : 512; }
+__host__ __device__ constexpr int slab_rows(int pack) { return pack == TQ_PACK_2BIT ? 16 : 64; }
 
 // Row length of VP[group][.]: V for each batch row, then zeros, then the block factor 2^(16+e) in the
 // last slot; a multiple of 4 floats so that every group's row is a whole number of 16-byte chunks.
@@ -121,6 +128,8 @@ __device__ const LutTable g_lut = make_lut();
 // x^ layout (halves), K-major so that any K-range is one contiguous slice starting at k * B:
 //   base-3: ((((m >> 1) * B + b) * 2 + (m & 1)) * 4 + r  for trit k = 4m + r (an MMA pair shares
 //           16 bytes);
+//   3-bit : the same with m = 16 * (k / 64) + reg / 2 and r = 2 * (reg % 2) + half, where (reg, half)
+//           is the operand register of the 64-block (0..31) and the FP16 half the code decodes into;
 //   2-bit : ((((((gi*WPT + u)*2 + jj/2)*B + b)*4 + q)*2 + jj%2)*2 + pair%2)*2 + half for the trit at
 //           word u of quad thread q in group gi, pair index jp (MMA jj = jp / 2), half = trit / 8.
 // ---------------------------------------------------------------------------------------------
@@ -206,22 +215,39 @@ __device__ __forceinline__ void prep_block(const uint16_t* __restrict__ x, const
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const int k = kr + j;
-      int pos, off;
+      int pb, off;  // pb: lowest mantissa bit of the weight's digit in its decoded FP16 half
       if (PACK == TQ_PACK_B3) {
-        pos = ((k % 20) % 10) >> 1;
+        pb = 2 * (((k % 20) % 10) >> 1);
         const int m = k >> 2, r4 = k & 3;
+        off = (((m >> 1) * B + b) * 2 + (m & 1)) * 4 + r4;
+      } else if (PACK == TQ_PACK_3BIT) {
+        // code c of its 64-block -> operand register r (0..31) of the block, half h, bit pb
+        const int c = k & 63;
+        int r, h;
+        if (c < 60) {
+          const int i = c / 10, jj = c - 10 * i;
+          h = jj >= 5 ? 1 : 0;
+          const int jr = jj - 5 * h;
+          r = 5 * i + jr;
+          pb = jr < 3 ? 3 * jr : 3 * jr - 8;
+        } else {
+          h = (c - 60) >> 1;
+          r = 30 + ((c - 60) & 1);
+          pb = 3 * ((c - 60) & 1);
+        }
+        const int m = (k >> 6) * 16 + (r >> 1), r4 = 2 * (r & 1) + h;
         off = (((m >> 1) * B + b) * 2 + (m & 1)) * 4 + r4;
       } else {
         constexpr int WPT = G / 64;
         const int gi = k / G, pg = k % G, wg = pg >> 4, f = pg & 15, jp = f & 7;
-        pos = jp < 5 ? jp : jp - 5;
+        pb = 2 * (jp < 5 ? jp : jp - 5);
         const int qq = wg / WPT, u = wg % WPT, jj = jp >> 1;
         off = ((((((gi * WPT + u) * 2 + (jj >> 1)) * B + b) * 4 + qq) * 2 + (jj & 1)) * 2 + (jp & 1)) * 2 + (f >> 3);
       }
-      const float F = __int_as_float((127 + 8 - 2 * pos) << 23);
+      const float F = __int_as_float((127 + 8 - pb) << 23);
       const __half h = __float2half_rn(v[b][j] * down * F);
       xh[off] = __half_as_ushort(h);
-      vs += __half2float(h) * __int_as_float((127 - 8 + 2 * pos) << 23);
+      vs += __half2float(h) * __int_as_float((127 - 8 + pb) << 23);
     }
     if (G == 128) {
 #pragma unroll
@@ -230,7 +256,9 @@ __device__ __forceinline__ void prep_block(const uint16_t* __restrict__ x, const
 #pragma unroll
       for (int o = 8; o > 0; o >>= 1) vs += __shfl_xor_sync(0xffffffffu, vs, o);
     }
-    if ((lane & (G == 128 ? 31 : 15)) == 0) vpo[(kr / G) * R + b] = -1.52587890625e-05f * vs;
+    // the digit offset: t = d - 1 (ternary), q = d - 4 (3-bit)
+    constexpr float kOff = PACK == TQ_PACK_3BIT ? -4.f * 1.52587890625e-05f : -1.52587890625e-05f;
+    if ((lane & (G == 128 ? 31 : 15)) == 0) vpo[(kr / G) * R + b] = kOff * vs;
   }
   if (lane < kFwhtBlock / G) {  // per group of the block: padding zeros and the block factor
     const int gi = (blk - blk0) * (kFwhtBlock / G) + lane;
@@ -934,6 +962,201 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
 }
 
 // ---------------------------------------------------------------------------------------------
+// 3-bit codes, column layout (the base-3 kernel's thread / row / accumulator arrangement).
+// A 64-code block is 7 words; word i < 6 yields five operand registers and word 6 two, 32 in all:
+// register j < 3 of a word is w & (7 << 3j | 7 << (16 + 3j)) (codes of slots j and j + 5 at bit 3j of
+// their halves), j = 3, 4 take the same mask of w >> 8 (bit 3j - 8).  A digit d at bit p of a zero-
+// exponent half is d * 2^(p - 24); the prep kernel folds 2^(8 - p) into the activations and the
+// offset q = d - 4 into the group's starting value.  MMA m of a block takes registers 2m, 2m + 1 of
+// both rows of the thread, so a block is 16 MMAs and a group 16 (G = 64) or 32 (G = 128).
+// A unit is 28 words (7 steps of four); the code ring has one slot per step of a unit, so every ring
+// index is a compile-time constant while three steps stay in flight.
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t q3_reg(uint32_t w, int i, int j) {
+  if (i == 6) return w & (j == 0 ? 0x00070007u : 0x00380038u);
+  return j < 3 ? (w & (0x00070007u << (3 * j))) : ((w >> 8) & (0x00070007u << (3 * j - 8)));
+}
+
+constexpr int kQ3Steps = 7;  // 16-byte steps per unit
+
+template <int G, int NT, bool FULL>
+__device__ __forceinline__ void q3_unit(const Params& p, const Cta& c, int u, int ngp, const uint4* __restrict__ cR,
+                                        const uint4* __restrict__ cR2, int s_last, uint4 (&ra)[kQ3Steps],
+                                        uint4 (&rb)[kQ3Steps], const uint32_t* const (&bptr)[NT],
+                                        const int (&bstr)[NT], const float* __restrict__ V,
+                                        const uint16_t* __restrict__ swr, float (&acc)[NT][4]) {
+  constexpr int GM = G / 4;     // MMAs per group
+  constexpr int GPS = 256 / G;  // groups per unit
+  const int bq = (c.lane & 3) >> 1;
+  const int ul = u - c.u0;
+  float cc[NT][4];
+  uint4 bp[NT];
+  uint32_t ea = 0u, eb = 0u;  // the even register of the MMA being formed (rows R, R + 32)
+#pragma unroll
+  for (int st = 0; st < kQ3Steps; ++st) {
+    {
+      const int s = min(u * kQ3Steps + st + 3, s_last);  // past this warp's range: re-read its last step
+      ra[(st + 3) % kQ3Steps] = __ldg(cR + s);
+      rb[(st + 3) % kQ3Steps] = __ldg(cR2 + s);
+    }
+    const uint4 cur = ra[st], cur2 = rb[st];
+    const uint32_t wr[4] = {cur.x, cur.y, cur.z, cur.w};
+    const uint32_t wr2[4] = {cur2.x, cur2.y, cur2.z, cur2.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      const int w = 4 * st + wi, blk = w / 7, i = w % 7;
+#pragma unroll
+      for (int j = 0; j < (i < 6 ? 5 : 2); ++j) {
+        const int reg = 5 * i + j;  // operand register of the block
+        const uint32_t xa = q3_reg(wr[wi], i, j), xb = q3_reg(wr2[wi], i, j);
+        if ((reg & 1) == 0) {
+          ea = xa;
+          eb = xb;
+          continue;
+        }
+        const int mloc = blk * 16 + (reg >> 1);  // MMA index within the unit
+        const int gl = mloc / GM;
+        if (!FULL && gl >= ngp) continue;
+        const int gla = ul * GPS + gl;  // group index within the CTA
+        if (mloc % GM == 0) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const float v0 = V[gla * p.R + min(2 * t + bq, p.B - 1)];  // columns past B are not stored
+            cc[t][0] = v0;
+            cc[t][1] = v0;
+            cc[t][2] = v0;
+            cc[t][3] = v0;
+          }
+        }
+        if ((mloc & 1) == 0) {
+          const int mp = ul * 32 + (mloc >> 1);  // MMA pair index within the CTA
+#pragma unroll
+          for (int t = 0; t < NT; ++t) bp[t] = *reinterpret_cast<const uint4*>(bptr[t] + mp * bstr[t]);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint32_t b0 = (mloc & 1) ? bp[t].z : bp[t].x, b1 = (mloc & 1) ? bp[t].w : bp[t].y;
+          mma16816(cc[t], ea, eb, xa, xb, b0, b1);
+        }
+        if ((mloc + 1) % GM == 0) {
+          const float p2 = V[gla * p.R + p.R - 1];
+          const float2 m01 = scale_pair(swr + gl * 64, p2);
+          const float2 m23 = scale_pair(swr + gl * 64 + 32, p2);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            acc[t][0] = fmaf(m01.x, cc[t][0], acc[t][0]);
+            acc[t][1] = fmaf(m01.y, cc[t][1], acc[t][1]);
+            acc[t][2] = fmaf(m23.x, cc[t][2], acc[t][2]);
+            acc[t][3] = fmaf(m23.y, cc[t][3], acc[t][3]);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int G, int NT>
+__global__ void __launch_bounds__(kMaxThreads) gemv_q3_kernel(const __grid_constant__ Params p) {
+  extern __shared__ __align__(16) uint8_t smem[];
+  pdl_launch_dependents();
+  const Cta c = cta_geometry<TQ_PACK_3BIT>(p);
+  Sel sel;
+  if (!select_operands(p, sel)) return;
+  Bars* bars = reinterpret_cast<Bars*>(smem + p.bar_off);
+  init_bars(bars);
+  const int g = c.lane >> 2, q = c.lane & 3;
+  // rows past N compute on row 0 and are not stored
+  const int R = c.row0 + c.slab * 64 + c.lane, R2 = R + 32;
+  const uint4* cR = reinterpret_cast<const uint4*>(sel.codes + static_cast<size_t>(R < p.N ? R : 0) * p.P);
+  const uint4* cR2 = reinterpret_cast<const uint4*>(sel.codes + static_cast<size_t>(R2 < p.N ? R2 : 0) * p.P);
+  const int s_begin = c.ua * kQ3Steps;
+  const int s_end = min(c.ub * kQ3Steps, p.P >> 2);
+  const int s_last = s_end - 1;  // this warp's last 4-word step
+  constexpr int GPS = 256 / G;
+  const int row_w0 = c.row0 + c.slab * 64;
+  uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + c.warp * (GPS * 64);
+  UnitScales<64, GPS, false> us;
+  auto unit_groups = [&](int u) { return min(GPS, (min((u + 1) * 256, p.K) - u * 256) / G); };
+  uint4 ra[kQ3Steps], rb[kQ3Steps];
+#pragma unroll
+  for (int i = 0; i < kQ3Steps; ++i) {
+    ra[i] = make_uint4(0u, 0u, 0u, 0u);
+    rb[i] = ra[i];
+  }
+  auto prime = [&]() {
+    if (c.ua < c.ub) {
+#pragma unroll
+      for (int i = 0; i < 3; ++i) {
+        ra[i] = __ldg(cR + min(s_begin + i, s_last));
+        rb[i] = __ldg(cR2 + min(s_begin + i, s_last));
+      }
+      us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
+    }
+  };
+  if (kPrefetchL2 && p.early && c.ua < c.ub) {
+    const uint32_t bytes = static_cast<uint32_t>(s_end - s_begin) * 16u;
+    if (R < p.N) bulk_prefetch_l2(cR + s_begin, bytes);
+    if (R2 < p.N) bulk_prefetch_l2(cR2 + s_begin, bytes);
+  }
+  if (p.early) prime();
+  pdl_wait();
+  if (!p.fused) copy_prep_slice(p, c, sel, smem, bars);
+  if (!p.early) prime();
+  if (p.fused) {
+    fused_prologue<TQ_PACK_3BIT, G>(p, c, sel, smem);
+  } else {
+    wait_bar(p, &bars->x);
+  }
+
+  const uint32_t* xh = reinterpret_cast<const uint32_t*>(smem + p.xh_off);
+  const float* V = reinterpret_cast<const float*>(smem + p.vp_off);
+  // B operand: lane (g, q) supplies batch 2t + g/4 of tile t when g % 4 == q, else 16 zero bytes
+  const uint32_t* bptr[NT];
+  int bstr[NT];
+  {
+    const bool bsup = (g & 3) == q;
+#pragma unroll
+    for (int t = 0; t < NT; ++t) {
+      bptr[t] = bsup ? xh + min(2 * t + (g >> 2), p.B - 1) * 4 : bars->zero;
+      bstr[t] = bsup ? p.B * 4 : 0;
+    }
+  }
+  const int cq = (2 * q) & 3;
+  const int rl0 = c.slab * 64 + 4 * g + cq;
+  const uint16_t* swr = sw + 4 * g + cq;
+  float acc[NT][4];
+#pragma unroll
+  for (int t = 0; t < NT; ++t)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) acc[t][i] = 0.f;
+  for (int u = c.ua; u < c.ub; ++u) {
+    const int ngp = unit_groups(u);
+    __syncwarp();
+    us.store(sw, c.lane);
+    __syncwarp();
+    if (u + 1 < c.ub) us.load(p, sel.scales, row_w0, u + 1, unit_groups(u + 1), c.lane);
+    if (ngp == GPS)
+      q3_unit<G, NT, true>(p, c, u, ngp, cR, cR2, s_last, ra, rb, bptr, bstr, V, swr, acc);
+    else
+      q3_unit<G, NT, false>(p, c, u, ngp, cR, cR2, s_last, ra, rb, bptr, bstr, V, swr, acc);
+  }
+
+  __syncthreads();  // the partial sums reuse the x^ region
+  float* red = reinterpret_cast<float*>(smem);
+  const int rows[4] = {rl0, rl0 + 1, rl0 + 32, rl0 + 33};
+#pragma unroll
+  for (int t = 0; t < NT; ++t) {
+    const int b = 2 * t + (q >> 1);
+    if (b < p.B) {
+#pragma unroll
+      for (int i = 0; i < 4; ++i) red[(c.kln * c.RT + rows[i]) * p.B + b] = acc[t][i];
+    }
+  }
+  __syncthreads();
+  reduce_store(p, c, sel, red);
+}
+
+// ---------------------------------------------------------------------------------------------
 // 2-bit dense decode, streamed ("stream" kernel).  One CTA per SM: nw consumer warps, each owning a
 // 16-row slab of the CTA's 16*nw-row block, and one producer warp whose elected lane streams the
 // block's codes through a ring of S shared-memory stages with 2-D TMA (32 words = 512 trits x 16*nw
@@ -1247,12 +1470,12 @@ struct Plan {
 
 // Shared-memory layout of a candidate split; returns the total bytes.  The partial-sum buffer of
 // the epilogue reuses the table / x^ region.
-size_t layout(Plan& pl, bool b3, int B, int G, int K) {
-  const int UT = b3 ? 640 : 512, SLAB = b3 ? 64 : 16;
+size_t layout(Plan& pl, int pack, int B, int G, int K) {
+  const int UT = unit_codes(pack), SLAB = slab_rows(pack);
   const int RT = pl.rs * SLAB;
   const int kr = std::min(pl.kl * pl.ppl * UT, K);
   const int ngr = kr / G;
-  pl.xh_off = b3 ? kLutBytes : 0;
+  pl.xh_off = pack == TQ_PACK_B3 ? kLutBytes : 0;
   const size_t main = pl.xh_off + align256(static_cast<size_t>(kr) * B * 2);
   const size_t red = static_cast<size_t>(pl.kl) * RT * B * 4;
   pl.vp_off = align256(std::max(main, red));
@@ -1265,8 +1488,7 @@ size_t layout(Plan& pl, bool b3, int B, int G, int K) {
 // Candidate splits in order of estimated time: per-warp units x busiest-SM warps (at least 12, below
 // which a warp's own latency dominates); ties go to fewer CTAs, then to smaller clusters.
 std::vector<Plan> candidates(const tq_desc* d, int B) {
-  const bool b3 = d->packing == TQ_PACK_B3;
-  const int UT = b3 ? 640 : 512, SLAB = b3 ? 64 : 16;
+  const int UT = unit_codes(d->packing), SLAB = slab_rows(d->packing);
   const int upr = (d->K + UT - 1) / UT;
   const int slabs = (d->N + SLAB - 1) / SLAB;
   std::vector<std::tuple<double, int, int, Plan>> list;
@@ -1282,7 +1504,7 @@ std::vector<Plan> candidates(const tq_desc* d, int B) {
         if ((ks - 1) * kl * pl.ppl >= upr) continue;  // a CTA without work
         if (kl > 1 && (kl - 1) * pl.ppl >= upr) continue;  // a K-lane that can never have work
         pl.n_rg = (slabs + rs - 1) / rs;
-        if (layout(pl, b3, B, d->group, d->K) > kSmemLimit) continue;
+        if (layout(pl, d->packing, B, d->group, d->K) > kSmemLimit) continue;
         const long long C = static_cast<long long>(pl.n_rg) * ks;
         const long long k = (C + kSMs - 1) / kSMs;
         const double cost = pl.ppl * std::max<double>(static_cast<double>(k * rs * kl), 12.0);
@@ -1435,11 +1657,22 @@ const void* kernel_b3(int B) {
   }
 }
 template <int G>
+const void* kernel_q3(int B) {
+  switch ((B + 1) / 2) {
+    case 1: return reinterpret_cast<const void*>(gemv_q3_kernel<G, 1>);
+    case 2: return reinterpret_cast<const void*>(gemv_q3_kernel<G, 2>);
+    case 3:
+    case 4: return reinterpret_cast<const void*>(gemv_q3_kernel<G, 4>);
+    default: return reinterpret_cast<const void*>(gemv_q3_kernel<G, 8>);
+  }
+}
+template <int G>
 const void* kernel_2b(int B) {
   return B <= 8 ? reinterpret_cast<const void*>(gemv_2b_kernel<G, 1>) : reinterpret_cast<const void*>(gemv_2b_kernel<G, 2>);
 }
 const void* gemv_kernel(const tq_desc* d, int B) {
   if (d->packing == TQ_PACK_B3) return d->group == 128 ? kernel_b3<128>(B) : kernel_b3<64>(B);
+  if (d->packing == TQ_PACK_3BIT) return d->group == 128 ? kernel_q3<128>(B) : kernel_q3<64>(B);
   return d->group == 128 ? kernel_2b<128>(B) : kernel_2b<64>(B);
 }
 
@@ -1706,9 +1939,13 @@ cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int 
     prm.gu = pp.gu;
     prm.h_out = pp.h_out;
   } else {
-    e = b3 ? (d->group == 128 ? launch_prep<TQ_PACK_B3, 128>(pp, s, zdim) : launch_prep<TQ_PACK_B3, 64>(pp, s, zdim))
-           : (d->group == 128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s, zdim)
-                              : launch_prep<TQ_PACK_2BIT, 64>(pp, s, zdim));
+    const bool g128 = d->group == 128;
+    if (b3)
+      e = g128 ? launch_prep<TQ_PACK_B3, 128>(pp, s, zdim) : launch_prep<TQ_PACK_B3, 64>(pp, s, zdim);
+    else if (d->packing == TQ_PACK_3BIT)
+      e = g128 ? launch_prep<TQ_PACK_3BIT, 128>(pp, s, zdim) : launch_prep<TQ_PACK_3BIT, 64>(pp, s, zdim);
+    else
+      e = g128 ? launch_prep<TQ_PACK_2BIT, 128>(pp, s, zdim) : launch_prep<TQ_PACK_2BIT, 64>(pp, s, zdim);
     if (e != cudaSuccess) return e;
   }
   prm.xh_g = pp.xh;
@@ -1742,14 +1979,13 @@ cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int 
 size_t gemv_workspace_bytes(const tq_desc* d, int batch) {
   using namespace gemv;
   // the smallest split (one slab, one K-lane, eight CTAs along K) must fit shared memory
-  const bool b3 = d->packing == TQ_PACK_B3;
   Plan pl{};
-  pl.upr = (d->K + (b3 ? 640 : 512) - 1) / (b3 ? 640 : 512);
+  pl.upr = (d->K + unit_codes(d->packing) - 1) / unit_codes(d->packing);
   pl.rs = 1;
   pl.kl = 1;
   pl.ks = std::min(kMaxCluster, pl.upr);
   pl.ppl = (pl.upr + pl.ks - 1) / pl.ks;
-  if (layout(pl, b3, batch, d->group, d->K) > kSmemLimit) return 0;
+  if (layout(pl, d->packing, batch, d->group, d->K) > kSmemLimit) return 0;
   return xh_bytes(d, batch) + vp_bytes(d, batch);
 }
 

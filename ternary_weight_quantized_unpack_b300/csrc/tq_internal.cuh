@@ -28,11 +28,26 @@ tq_status cuda_fail(cudaError_t e);
 
 __device__ __forceinline__ void record_error(int* status, int code) { atomicCAS(status, 0, code); }
 
+// 3-bit codes: a word has ten 3-bit slots, five per 16-bit half (bits 15 and 31 zero), so that one
+// mask takes a code from each half.  A block of 64 codes takes 7 words: word i < 6 holds codes
+// 10i..10i+9 of the block in slots 0..9, word 6 holds codes 60, 61 in slots 0, 1 and 62, 63 in slots
+// 5, 6 (its other slots hold digit 4, q = 0).  Digit = q + 4.
+constexpr int kQ3PerWord = 10;
+constexpr int kQ3Block = 64;
+constexpr int kQ3WordsPerBlock = 7;
+__host__ __device__ __forceinline__ int q3_slot_bit(int slot) { return slot < 5 ? 3 * slot : 3 * slot + 1; }
+// code of slot `slot` of word i (0..6) of a block, or -1 for a padding slot
+__host__ __device__ __forceinline__ int q3_slot_code(int i, int slot) {
+  if (i < 6) return 10 * i + slot;
+  return slot == 0 || slot == 1 ? 60 + slot : slot == 5 || slot == 6 ? 57 + slot : -1;
+}
+
 __host__ __device__ __forceinline__ int trits_per_word(int packing) {
   return packing == TQ_PACK_B3 ? kB3Trits : kB2Trits;
 }
 __host__ __device__ __forceinline__ int pitch_words(int K, int packing) {
-  int w = (K + trits_per_word(packing) - 1) / trits_per_word(packing);
+  const int w = packing == TQ_PACK_3BIT ? (K + kQ3Block - 1) / kQ3Block * kQ3WordsPerBlock
+                                        : (K + trits_per_word(packing) - 1) / trits_per_word(packing);
   return (w + 3) & ~3;
 }
 __host__ __device__ __forceinline__ int groups_of(int K, int group) { return (K + group - 1) / group; }

@@ -59,6 +59,8 @@ cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_
 
 // Host-side descriptor checks shared by the contraction entry points.
 tq_status check_linear_desc(const tq_desc* d);
+// check_linear_desc, also accepting 3-bit codes (the decode GEMV takes them)
+tq_status check_gemv_desc(const tq_desc* d);
 
 // Round up to a multiple of 256 bytes (workspace sub-buffer alignment).
 inline size_t align256(size_t b) { return (b + 255) & ~static_cast<size_t>(255); }

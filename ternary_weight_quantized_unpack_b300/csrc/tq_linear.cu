@@ -19,13 +19,13 @@ tq_status check_ptrs(const uint32_t* codes, const uint16_t* scales, const uint16
 using namespace tq;
 
 extern "C" size_t tq_gemv_workspace_bytes(const tq_desc* d, int batch) {
-  if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return 0;
+  if (check_gemv_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return 0;
   return gemv_workspace_bytes(d, batch);
 }
 
 extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                              int batch, float* y, void* workspace, size_t workspace_bytes, void* stream) {
-  tq_status st = check_linear_desc(d);
+  tq_status st = check_gemv_desc(d);
   if (st != TQ_OK) return st;
   if (batch < 1 || batch > kMaxBatch) return TQ_ERR_INVALID_ARG;
   if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
@@ -40,7 +40,7 @@ extern "C" tq_status tq_gemv(const tq_desc* d, const uint32_t* codes, const uint
 }
 
 extern "C" int tq_gemv_kernel_count(const tq_desc* d, int batch) {
-  if (check_linear_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return -1;
+  if (check_gemv_desc(d) != TQ_OK || batch < 1 || batch > kMaxBatch) return -1;
   return gemv_kernel_count(d, batch);
 }
 

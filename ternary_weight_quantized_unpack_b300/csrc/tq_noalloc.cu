@@ -51,7 +51,7 @@ using namespace tq;
 
 extern "C" tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_t* scales,
                                      const uint16_t* x, int batch, float* y, void* stream) {
-  tq_status st = check_linear_desc(d);
+  tq_status st = check_gemv_desc(d);
   if (st != TQ_OK) return st;
   if (batch < 1 || batch > kMaxBatch) return TQ_ERR_INVALID_ARG;
   if (!codes || !scales || !x || !y) return TQ_ERR_INVALID_ARG;

@@ -67,6 +67,20 @@ def trits(seed: int, tid: int, N: int, K: int, rows=None, device="cpu", chunk_ro
     return out
 
 
+def codes3(seed: int, tid: int, N: int, K: int, rows=None, device="cpu", chunk_rows: int = 2048) -> torch.Tensor:
+    """int8 3-bit codes [len(rows) or N, K], uniform on {-4..3}; element (n,k) depends only on
+    (seed, tid, n*K+k)."""
+    assert N * K < 2**32
+    row_list = torch.arange(N, dtype=torch.int64) if rows is None else torch.as_tensor(rows, dtype=torch.int64)
+    out = torch.empty((row_list.numel(), K), dtype=torch.int8, device=device)
+    kk = torch.arange(K, dtype=torch.int64, device=device)
+    for r0 in range(0, row_list.numel(), chunk_rows):
+        r = row_list[r0:r0 + chunk_rows].to(device)
+        idx = r[:, None] * K + kk[None, :]
+        out[r0:r0 + r.numel()] = ((hash_u32(seed, tid, idx) >> 8) % 8 - 4).to(torch.int8)
+    return out
+
+
 _SCALE_TABLE_CACHE: dict = {}
 
 

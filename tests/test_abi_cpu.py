@@ -28,7 +28,7 @@ def test_library_exports_every_declared_symbol():
     assert all(hasattr(tq, n) for n in names), [n for n in names if not hasattr(tq, n)]
 
 
-@pytest.mark.parametrize("packing", [tq.TQ_PACK_B3, tq.TQ_PACK_2BIT])
+@pytest.mark.parametrize("packing", [tq.TQ_PACK_B3, tq.TQ_PACK_2BIT, tq.TQ_PACK_3BIT])
 @pytest.mark.parametrize("K", [1, 20, 21, 128, 1000, 1024, 2048, 512, 5120, 17408])
 def test_sizes_match_oracle(packing, K):
     for N in (1, 7, 1024):
@@ -41,7 +41,14 @@ def test_sizes_match_oracle(packing, K):
 
 def test_invalid_descriptors():
     assert tq.tq_row_pitch_words(tq.desc(0, 128)) == 0
-    assert tq.tq_packed_bytes(tq.desc(4, 128, packing=3)) == 0
+    assert tq.tq_packed_bytes(tq.desc(4, 128, packing=4)) == 0
+    # 3-bit codes: the decode GEMV takes batch 1..16 with the same workspace as the ternary packings
+    # (x^ halves, then 40 groups x 12 floats rounded to 256 bytes); the other contractions do not
+    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, packing=tq.TQ_PACK_3BIT), 1) == 512
+    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 5120, packing=tq.TQ_PACK_3BIT), 8) == 5120 * 8 * 2 + 2048
+    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, packing=tq.TQ_PACK_3BIT), 17) == 0
+    assert tq.tq_gemv_workspace_bytes(tq.desc(4, 100, packing=tq.TQ_PACK_3BIT), 1) == 0
+    assert tq.tq_gemm_workspace_bytes(tq.desc(4, 128, packing=tq.TQ_PACK_3BIT), 16) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 100), 1) == 0        # K not a multiple of 128
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, group=32), 1) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 17) == 0        # batch above 16

@@ -197,11 +197,15 @@ def pin_contraction_bruteforce(O):
 
 
 def pin_pack_3bit(O):
-    """3-bit codes against Python's own base-8 parsing of each word's ten digits (digit q + 4, least
-    significant first; blocks of 64 codes in 7 words, the last word of a block holding four codes and
-    six q = 0 digits), a hand-worked block, the row pitch, the invalid-word count and the contraction
-    by brute force."""
+    """3-bit codes against Python's own base-8 parsing of each 16-bit half of a word (five digits
+    q + 4, least significant first, bit 15 left zero; blocks of 64 codes in 7 words, word 6 holding
+    codes 60, 61 in its low half and 62, 63 in its high half, every other digit q = 0), a hand-worked
+    block, the row pitch, the invalid-word count and the contraction by brute force."""
     r = rng(31)
+
+    def half(digits):
+        return int("".join(str(d) for d in reversed(digits)), 8)
+
     for K in (1, 10, 63, 64, 65, 200, 640):
         q = r.integers(-4, 4, size=(3, K)).astype(np.int8)
         codes = O.pack(q, O.PACK_3BIT)
@@ -209,21 +213,33 @@ def pin_pack_3bit(O):
         assert codes.shape == (3, -(-nb * 7 // 4) * 4)
         for n in range(3):
             for b in range(nb):
-                for i in range(7):
-                    digits = []
-                    for j in range(10):
-                        k = 64 * b + 10 * i + j
-                        digits.append(int(q[n, k]) + 4 if (10 * i + j < 64 and k < K) else 4)
-                    assert int(codes[n, 7 * b + i]) == int("".join(str(d) for d in reversed(digits)), 8)
+                def dig(c):
+                    k = 64 * b + c
+                    return int(q[n, k]) + 4 if k < K else 4
+                for i in range(6):
+                    lo = [dig(10 * i + j) for j in range(5)]
+                    hi = [dig(10 * i + 5 + j) for j in range(5)]
+                    assert int(codes[n, 7 * b + i]) == half(lo) + (half(hi) << 16)
+                lo6 = [dig(60), dig(61), 4, 4, 4]
+                hi6 = [dig(62), dig(63), 4, 4, 4]
+                assert int(codes[n, 7 * b + 6]) == half(lo6) + (half(hi6) << 16)
         back, bad = O.unpack(codes, K, O.PACK_3BIT)
         assert bad == 0 and np.array_equal(back, q)
-    q = np.array([[k % 8 - 4 for k in range(64)]], dtype=np.int8)
+    q = np.array([[k % 8 - 4 for k in range(64)]], dtype=np.int8)   # digit of code k is k % 8
     c = O.pack(q, O.PACK_3BIT)
-    assert int(c[0, 0]) == sum((k % 8) << (3 * k) for k in range(10))
-    assert int(c[0, 6]) == sum(d << (3 * j) for j, d in enumerate([4, 5, 6, 7, 4, 4, 4, 4, 4, 4]))
-    bad_codes = c.copy()
-    bad_codes[0, 2] |= np.uint32(1 << 30)
-    assert O.unpack(bad_codes, 64, O.PACK_3BIT)[1] == 1
+    assert int(c[0, 0]) == 0o43210 | (0o10765 << 16)
+    assert int(c[0, 1]) == 0o65432 | (0o32107 << 16)
+    assert int(c[0, 6]) == 0o44454 | (0o44476 << 16)
+    back, bad = O.unpack(c, 64, O.PACK_3BIT)
+    assert bad == 0 and np.array_equal(back, q)
+    for bit in (15, 31):
+        bad_codes = c.copy()
+        bad_codes[0, 2] |= np.uint32(1 << bit)
+        assert O.unpack(bad_codes, 64, O.PACK_3BIT)[1] == 1
+    ok_codes = c.copy()
+    ok_codes[0, 6] ^= np.uint32(7 << 6)    # a padding slot of word 6: not validated, not read
+    back, bad = O.unpack(ok_codes, 64, O.PACK_3BIT)
+    assert bad == 0 and np.array_equal(back, q)
     # the contraction on 3-bit codes: y = sum_k s q x~, brute force
     N, K, B, group = 2, 256, 2, 64
     q = r.integers(-4, 4, size=(N, K)).astype(np.int8)
@@ -512,8 +528,18 @@ def _pack3_blocks_of_60(trits, packing):
     P = O_real.row_pitch_words(K, packing)
     d = np.full((N, P * 10), 4, dtype=np.int64)
     d[:, :K] = q.astype(np.int64) + 4
-    w = (d.reshape(N, P, 10) << (3 * np.arange(10))).sum(axis=2)
+    shifts = np.array([O_real.q3_slot_bit(j) for j in range(10)])
+    w = (d.reshape(N, P, 10) << shifts).sum(axis=2)
     return w.astype(np.uint32)
+
+
+def _pack3_no_half_gap(trits, packing):
+    """3-bit slots at bits 3j for all ten slots (the high half starting at bit 15)."""
+    if packing != O_real.PACK_3BIT:
+        return ORIG["pack"](trits, packing)
+    w = ORIG["pack"](trits, packing).astype(np.int64)
+    hi = (w >> 16) & 0x7FFF
+    return ((w & 0x7FFF) | (hi << 15)).astype(np.uint32)
 
 
 def _pack_msd_first(trits, packing):
@@ -597,6 +623,7 @@ def _quantize_with(stat="mean", thr=0.5, rotate=True, c=None, ties_up=False, int
 
 MUTANTS = {
     "3-bit blocks not padded to 64": dict(pack=_pack3_blocks_of_60),
+    "3-bit high half starting at bit 15": dict(pack=_pack3_no_half_gap),
     "quantize scale from max": dict(quantize=_quantize_with(stat="max")),
     "quantize threshold 0.7 S": dict(quantize=_quantize_with(thr=0.7)),
     "quantize without rotation": dict(quantize=_quantize_with(rotate=False)),
