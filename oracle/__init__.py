@@ -387,3 +387,54 @@ def quantize(W, group: int, packing: int, fwht_block: int = 128):
     half = np.repeat(scales.astype(np.float64) / 2.0, group, axis=1)
     trits = np.where(np.abs(u) * c > half, np.sign(u), 0.0).astype(np.int8)
     return pack(trits, packing), scales, trits
+
+
+# ----------------------------------------------------------------------------------------------
+# FP8 prefill variant.  No passage states it: it is this build's variant of the batched contraction
+# ([CC] §二 ③ computes on the packed format; the FP8 operand type is the reading).  Each activation
+# row and each weight row is brought to FP8 E4M3 under its own power-of-two factor; the tolerance
+# against the exact result is the variant's own, stated with the GPU test.
+# ----------------------------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def e4m3(v):
+    """Nearest FP8 E4M3 value (4 exponent bits with bias 7, 3 mantissa bits, subnormals m * 2^-9,
+    largest finite 448, no infinities), ties to the even mantissa; magnitudes that round above 448
+    give 448.  fp64 in, fp64 out."""
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))       # a = f * 2^ex, f in [0.5, 1): floor(log2 a) = ex - 1
+    E = np.maximum(ex - 1, -6)                      # binade; below 2^-6 the subnormal spacing 2^-9
+    step = np.ldexp(1.0, E - 3)                     # grid spacing: 3 mantissa bits
+    q = np.minimum(np.round(a / step) * step, E4M3_MAX)   # np.round: half to even
+    return np.copysign(q, v)
+
+
+def pow2_exponent(m):
+    """e = floor(log2 m) - 7 for m > 0, so that m * 2^-e lies in [128, 256); 0 for m = 0."""
+    m = np.asarray(m, dtype=np.float64)
+    _, ex = np.frexp(np.where(m > 0, m, 1.0))
+    return np.where(m > 0, ex - 1 - 7, 0).astype(np.int64)
+
+
+def linear_fp8(codes, scales, x, K: int, group: int, packing: int, fwht_block: int = 128):
+    """The contraction with FP8 E4M3 operands:
+
+        y[b, n] = 2^(ea_b + eb_n) * sum_k e4m3(x~[b, k] * 2^-ea_b) * e4m3(s[n, g(k)] t[n, k] * 2^-eb_n)
+
+    with ea_b = pow2_exponent(max_k |x~[b, k]|) and eb_n = pow2_exponent(max_g |s[n, g]|) (over the
+    row's scales).  Products of E4M3 values and their sums are exact in fp64 at these sizes, so y is
+    the exact value of the quantised operands' contraction.  Returns (y, A, n_invalid) with A the
+    exact operands' sum_k |s t x~| (as ``ternary_linear``)."""
+    t, n_invalid = unpack(codes, K, packing)
+    W = dequant(t, scales, group)
+    xt = block_fwht(np.asarray(x, dtype=np.float64), fwht_block)
+    ea = pow2_exponent(np.abs(xt).max(axis=1))
+    eb = pow2_exponent(np.abs(np.asarray(scales, dtype=np.float64)).max(axis=1))
+    aq = e4m3(xt * np.ldexp(1.0, -ea)[:, None])
+    wq = e4m3(W * np.ldexp(1.0, -eb)[:, None])
+    y = np.matmul(aq, wq.T) * np.ldexp(1.0, ea[:, None] + eb[None, :])
+    A = np.matmul(np.abs(xt), np.abs(W).T)
+    return y, A, n_invalid

@@ -13,6 +13,7 @@ import os
 
 import numpy as np
 import pytest
+import torch
 
 import oracle as O_real
 from ternary_weight_quantized_unpack_b300 import inputs
@@ -500,10 +501,118 @@ def pin_quantize_round_trip(O):
             assert np.allclose(S_q.astype(np.float64), S * frac, rtol=4e-3, atol=0)
 
 
+def e4m3_grid():
+    """Every finite FP8 E4M3 value from its bit fields (exponent e, mantissa m), by Python
+    arithmetic, with the mantissa field of each."""
+    grid = {}
+    for e in range(16):
+        for m in range(8):
+            if e == 15 and m == 7:
+                continue  # the NaN pattern
+            v = m * 2.0 ** -9 if e == 0 else (1 + m / 8) * 2.0 ** (e - 7)
+            grid[v] = m
+            grid[-v] = m
+    return grid
+
+
+def pin_e4m3(O):
+    """Rounding to FP8 E4M3: the grid enumerated from its bit fields is fixed, midpoints go to the
+    even mantissa, points just off a midpoint to the nearer neighbour, magnitudes past 448 to 448, and
+    torch's own E4M3 conversion agrees on random values in range."""
+    grid = e4m3_grid()
+    vals = np.array(sorted(grid))
+    assert vals.max() == 448.0 and vals[vals > 0].min() == 2.0 ** -9 and len(vals) == 253
+    assert np.array_equal(O.e4m3(vals), vals)
+    pos = [v for v in sorted(grid) if v >= 0]
+    for lo, hi in zip(pos[:-1], pos[1:]):
+        mid = (lo + hi) / 2
+        even = lo if grid[lo] % 2 == 0 else hi
+        assert O.e4m3(mid) == even and O.e4m3(-mid) == -even, (lo, hi)
+        assert O.e4m3(mid - (hi - lo) / 8) == lo and O.e4m3(mid + (hi - lo) / 8) == hi
+    assert O.e4m3(1000.0) == 448.0 and O.e4m3(-470.0) == -448.0 and O.e4m3(2.0 ** -11) == 0.0
+    r = rng(41)
+    v = r.standard_normal(4000) * 10.0 ** r.uniform(-4, 2.5, 4000)
+    v = v[np.abs(v) < 440]
+    lib = torch.tensor(v).to(torch.float8_e4m3fn).to(torch.float64).numpy()
+    assert np.array_equal(O.e4m3(v), lib)
+
+
+def pin_pow2_exponent(O):
+    """e = floor(log2 m) - 7: m * 2^-e in [128, 256), by Python's frexp; 0 for m = 0."""
+    assert list(O.pow2_exponent([0.0, 1.0, 128.0, 255.9, 256.0, 2.0 ** -20])) == [0, -7, 0, 0, 1, -27]
+    r = rng(42)
+    m = np.exp(r.uniform(-30, 30, 500))
+    e = O.pow2_exponent(m)
+    scaled = m * np.exp2(-e.astype(np.float64))
+    assert ((scaled >= 128) & (scaled < 256)).all()
+
+
+def fp8_bound(xt, W, ea, eb):
+    """|y_fp8 - y| for the E4M3 operands: relative 2^-4 per operand (normals, half a 3-bit ulp) and,
+    below 2^-6 after scaling, an absolute 2^-10 (half the subnormal spacing) times the row factor."""
+    ax, aw = np.abs(xt), np.abs(W)
+    A = ax @ aw.T
+    fa = np.ldexp(1.0, ea)[:, None]
+    fb = np.ldexp(1.0, eb)[None, :]
+    K = xt.shape[1]
+    return ((2.0 ** -3 + 2.0 ** -8) * A + 2.0 ** -10 * 1.07 * (fb * ax.sum(axis=1)[:, None] + fa * aw.sum(axis=1)[None, :])
+            + K * 2.0 ** -20 * fa * fb)
+
+
+def pin_linear_fp8(O):
+    """The FP8 contraction: (a) operands already on the E4M3 grid under their row factors give the
+    exact ternary result; (b) brute force with Python loops (frexp exponents, the pinned rounding) on a
+    small case; (c) the distance to the exact result stays inside the derived bound."""
+    r = rng(43)
+    grid = np.array(sorted(v for v in e4m3_grid() if 16 <= abs(v) < 256))
+    # (a) rows of x with a maximum in [128, 256), weights with group scales on the grid in [128, 256)
+    N, K, B, group = 5, 256, 3, 64
+    x = r.choice(grid, size=(B, K))
+    x[:, 0] = 240.0
+    t = r.integers(-1, 2, size=(N, K)).astype(np.int8)
+    sc = r.choice(grid[(grid >= 128)], size=(N, K // group)).astype(np.float16)
+    codes = O.pack(t, O.PACK_2BIT)
+    y8, A8, bad = O.linear_fp8(codes, sc, x, K, group, O.PACK_2BIT, 0)
+    y, A, _ = O.ternary_linear(codes, sc, x, K, group, O.PACK_2BIT, 0)
+    assert bad == 0 and np.array_equal(y8, y) and np.array_equal(A8, A)
+    # (b) brute force
+    N, K, B, group = 3, 256, 2, 128
+    t = r.integers(-1, 2, size=(N, K)).astype(np.int8)
+    sc = np.exp(r.normal(-4, 0.5, size=(N, K // group))).astype(np.float16)
+    x = (r.standard_normal((B, K)) * np.array([[1e-3], [50.0]])).astype(np.float32)
+    codes = O.pack(t, O.PACK_B3)
+    y8, _, _ = O.linear_fp8(codes, sc, x, K, group, O.PACK_B3, 128)
+    for b in range(B):
+        xt = fwht_closed_form([float(v) for v in x[b]], 128)
+        ea = math.frexp(max(abs(v) for v in xt))[1] - 1 - 7
+        for n in range(N):
+            eb = math.frexp(max(abs(float(v)) for v in sc[n]))[1] - 1 - 7
+            acc = 0.0
+            for k in range(K):
+                w = float(sc[n, k // group]) * int(t[n, k])
+                acc += float(O.e4m3(xt[k] * 2.0 ** -ea)) * float(O.e4m3(w * 2.0 ** -eb))
+            ref = acc * 2.0 ** (ea + eb)
+            assert abs(y8[b, n] - ref) <= 1e-12 * max(1.0, abs(ref)), (b, n, y8[b, n], ref)
+    # (c) the bound, on a case with a wide range of magnitudes
+    N, K, B, group = 16, 512, 4, 64
+    t = r.integers(-1, 2, size=(N, K)).astype(np.int8)
+    sc = np.exp(r.normal(-4, 1.5, size=(N, K // group))).astype(np.float16)
+    x = (r.standard_normal((B, K)) * np.exp(r.normal(0, 3, size=(B, K)))).astype(np.float32)
+    codes = O.pack(t, O.PACK_2BIT)
+    y8, _, _ = O.linear_fp8(codes, sc, x, K, group, O.PACK_2BIT, 128)
+    y, _, _ = O.ternary_linear(codes, sc, x, K, group, O.PACK_2BIT, 128)
+    xt = O.block_fwht(x, 128)
+    W = O.dequant(t, sc, group)
+    ea = np.array([math.frexp(np.abs(row).max())[1] - 8 for row in xt])
+    eb = np.array([math.frexp(float(np.abs(row.astype(np.float64)).max()))[1] - 8 for row in sc])
+    assert (np.abs(y8 - y) <= fp8_bound(xt, W, ea, eb)).all()
+    assert np.abs(y8 - y).max() > 0   # the quantisation is not a no-op here
+
+
 PINS = [pin_pack_b3, pin_pack_2b, pin_unpack, pin_format_constants, pin_hadamard, pin_fwht,
         pin_rotation_identity, pin_contraction_bruteforce, pin_special_cases, pin_moe_route, pin_moe_layer,
         pin_silu, pin_moe_down_from_h, pin_quantize_closed_form, pin_quantize_nearest_level,
-        pin_quantize_round_trip, pin_pack_3bit]
+        pin_quantize_round_trip, pin_pack_3bit, pin_e4m3, pin_pow2_exponent, pin_linear_fp8]
 
 
 @pytest.mark.parametrize("pin", PINS, ids=lambda p: p.__name__)
@@ -621,6 +730,27 @@ def _quantize_with(stat="mean", thr=0.5, rotate=True, c=None, ties_up=False, int
     return q
 
 
+def _e4m3_ties_away(v):
+    v = np.asarray(v, dtype=np.float64)
+    a = np.abs(v)
+    _, ex = np.frexp(np.where(a > 0, a, 1.0))
+    step = np.ldexp(1.0, np.maximum(ex - 1, -6) - 3)
+    return np.copysign(np.minimum(np.floor(a / step + 0.5) * step, 448.0), v)
+
+
+def _pow2_exponent_one_high(m):
+    return ORIG_FP8["pow2_exponent"](m) + 1
+
+
+def _linear_fp8_without_weight_factor(codes, scales, x, K, group, packing, fwht_block=128):
+    y, A, bad = ORIG_FP8["linear_fp8"](codes, scales, x, K, group, packing, fwht_block)
+    eb = ORIG_FP8["pow2_exponent"](np.abs(np.asarray(scales, dtype=np.float64)).max(axis=1))
+    return y * np.ldexp(1.0, -eb)[None, :], A, bad
+
+
+ORIG_FP8 = {k: getattr(O_real, k) for k in ("e4m3", "pow2_exponent", "linear_fp8")}
+
+
 MUTANTS = {
     "3-bit blocks not padded to 64": dict(pack=_pack3_blocks_of_60),
     "3-bit high half starting at bit 15": dict(pack=_pack3_no_half_gap),
@@ -642,6 +772,9 @@ MUTANTS = {
     "unpack shifted by one trit": dict(unpack=_unpack_off_by_one),
     "silu with sigmoid(-z)": dict(silu=_silu_mirrored),
     "down stage ignores the gates": dict(moe_down_from_h=_down_without_gates),
+    "e4m3 ties away from zero": dict(e4m3=_e4m3_ties_away),
+    "fp8 row exponent one too high": dict(pow2_exponent=_pow2_exponent_one_high),
+    "fp8 result missing the weight factor": dict(linear_fp8=_linear_fp8_without_weight_factor),
 }
 
 
