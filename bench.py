@@ -458,7 +458,8 @@ def bench_moe_prefill(T, steps, warmup, seed=inputs.seed_of(3)):
             "launches_per_call": 9}
 
 
-def bench_prefill(shape, steps, warmup, seed=inputs.seed_of(4)):
+def bench_prefill(shape, steps, warmup, seed=inputs.seed_of(4), fp8=False):
+    """One prefill call (FP16 operands, or FP8 E4M3 with tq_gemm_fp8), device time per call."""
     M, K, N = shape
     d = tq.desc(N, K, 128, tq.TQ_PACK_2BIT)
     dev = "cuda"
@@ -468,21 +469,24 @@ def bench_prefill(shape, steps, warmup, seed=inputs.seed_of(4)):
     s = torch.exp(torch.randn((N, K // 128), generator=gen, device=dev) * 0.5 - 4).half()
     x = inputs.activations(seed, K, M, K).to(dev)
     y = torch.empty((M, N), dtype=torch.bfloat16, device=dev)
-    ws = torch.empty(tq.tq_gemm_workspace_bytes(d, M), dtype=torch.uint8, device=dev)
+    gemm = tq.tq_gemm_fp8 if fp8 else tq.tq_gemm
+    ws_bytes = (tq.tq_gemm_fp8_workspace_bytes if fp8 else tq.tq_gemm_workspace_bytes)(d, M)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     for _ in range(warmup):
-        tq.tq_gemm(d, codes, s, x, y=y, workspace=ws)
+        gemm(d, codes, s, x, y=y, workspace=ws)
     torch.cuda.synchronize()
     times = []
     for _ in range(steps):
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record()
-        tq.tq_gemm(d, codes, s, x, y=y, workspace=ws)
+        gemm(d, codes, s, x, y=y, workspace=ws)
         b.record()
         torch.cuda.synchronize()
         times.append(a.elapsed_time(b))
     ms = statistics.median(times)
     flops = 2.0 * M * N * K
-    return {"M": M, "K": K, "N": N, "ms": ms, "TFLOP_s": flops / (ms * 1e-3) / 1e12}
+    return {"M": M, "K": K, "N": N, "operands": "fp8_e4m3" if fp8 else "fp16", "ms": ms,
+            "TFLOP_s": flops / (ms * 1e-3) / 1e12}
 
 
 def l2_cold_times(fn, reps, flush):
@@ -798,8 +802,12 @@ def run_tq(args, rank, world, local):
             r["pct_of_bf16_peak"] = 100.0 * r["TFLOP_s"] / peaks["bf16_tflops"]
         for shape in inputs.PREFILL["shapes"]:
             ex["prefill"].append(bench_prefill(shape, 20, 3))
+            ex["prefill"].append(bench_prefill(shape, 20, 3, fp8=True))
         for p in ex["prefill"]:
-            p["pct_of_bf16_peak"] = 100.0 * p["TFLOP_s"] / peaks["bf16_tflops"]
+            if p["operands"] == "fp16":
+                p["pct_of_bf16_peak"] = 100.0 * p["TFLOP_s"] / peaks["bf16_tflops"]
+            else:  # FP8 peak: the measured bf16 burst x the nominal FP8 / BF16 ratio (4.5 / 2.25)
+                p["pct_of_fp8_peak"] = 100.0 * p["TFLOP_s"] / (2.0 * peaks["bf16_tflops"])
         line["extras"] = ex
     if rank == 0:
         print(json.dumps(line))

@@ -263,6 +263,22 @@ size_t tq_gemm_workspace_bytes(const tq_desc* d, int M);
 tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
                   int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream);
 
+/* ---- tq_gemm_fp8: tq_gemm with FP8 E4M3 operands ----------------------------------------------------
+ * No page states this variant; it is the library's: the batched contraction on the packed codes
+ * ("27B 大模型塞进 5.9GB", section 二 ③) with both operands in FP8 E4M3 for the tensor cores' FP8 rate
+ * (tcgen05.mma kind::f8f6f4).  Each token row is scaled by 2^-ea[m], each weight row by 2^-eb[n],
+ * ea[m] = floor(log2 max_k |x~[m][k]|) - 7, eb[n] = floor(log2 max_g |s[n][g]|) - 7 (0 for an all-zero
+ * row), and rounded to E4M3 to nearest even:
+ *   Y[m][n] = bf16( 2^(ea[m] + eb[n]) * sum_k e4m3(x~[m][k] 2^-ea[m]) e4m3(s[n][k/group] t[n][k] 2^-eb[n]) ).
+ * t is exact in E4M3; s and x~ keep 4 significant bits, so |Y - exact| <= (2^-3 + 2^-8) sum_k |s t x~|
+ * plus a subnormal term of 2^-10 times the row factors (and fp32 accumulation, bf16 output rounding).
+ * Inf / NaN in a row of x~ or of the scales records TQ_ERR_RANGE.  x, y, requirements as tq_gemm
+ * (no FP16 range limit on x~).  workspace >= tq_gemm_fp8_workspace_bytes(d, M): the E4M3 operands
+ * (M * K and N * K bytes) and the row exponents. */
+size_t tq_gemm_fp8_workspace_bytes(const tq_desc* d, int M);
+tq_status tq_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                      int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream);
+
 /* ---- tq_selftest_wait: the bounded-wait path, made to run out on purpose ------------------------------
  * Launches one CTA that waits on something nothing completes, with a wait limit of limit_ns
  * (1 .. 1e9 ns) instead of the kernels' 4 s: kind 0 an mbarrier that is never arrived on (the

@@ -82,6 +82,8 @@ _SIGS = {
     "tq_moe_gemm": (_I, [_D, _D, _I, _I, _P, _P, _P, _P, _P, _P, _I, _P, _P, _P, _P, _P, _SZ, _P]),
     "tq_gemm_workspace_bytes": (_SZ, [_D, _I]),
     "tq_gemm": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
+    "tq_gemm_fp8_workspace_bytes": (_SZ, [_D, _I]),
+    "tq_gemm_fp8": (_I, [_D, _P, _P, _P, _I, _P, _P, _SZ, _P]),
     "tq_seq_create": (_I, [ctypes.POINTER(tq_seq_call), _I, _I, ctypes.POINTER(ctypes.c_void_p)]),
     "tq_seq_workspace_bytes": (_SZ, [_P]),
     "tq_seq_upload": (_I, [_P, _P, _SZ]),
@@ -159,6 +161,10 @@ def tq_gemv_kernel_count(d: tq_desc, batch: int) -> int:
 
 def tq_gemm_workspace_bytes(d: tq_desc, M: int) -> int:
     return lib().tq_gemm_workspace_bytes(ctypes.byref(d), M)
+
+
+def tq_gemm_fp8_workspace_bytes(d: tq_desc, M: int) -> int:
+    return lib().tq_gemm_fp8_workspace_bytes(ctypes.byref(d), M)
 
 
 def tq_moe_workspace_bytes(T: int, E: int, topk: int, H: int, F: int) -> int:
@@ -307,6 +313,19 @@ def tq_gemm(d: tq_desc, codes, scales, x, y=None, workspace=None, stream=None) -
         workspace = _ws(nbytes, x.device)
     _check(lib().tq_gemm(ctypes.byref(d), _ptr(codes), _ptr(scales), _ptr(x), M, _ptr(y), _ptr(workspace),
                          workspace.numel() * workspace.element_size(), _stream(stream)), "tq_gemm")
+    return y
+
+
+def tq_gemm_fp8(d: tq_desc, codes, scales, x, y=None, workspace=None, stream=None) -> torch.Tensor:
+    """Prefill with FP8 E4M3 operands: x bf16 [M, K] -> y bf16 [M, N]."""
+    M = x.shape[0]
+    if y is None:
+        y = torch.empty((M, d.N), dtype=torch.bfloat16, device=x.device)
+    nbytes = tq_gemm_fp8_workspace_bytes(d, M)
+    if workspace is None:
+        workspace = _ws(nbytes, x.device)
+    _check(lib().tq_gemm_fp8(ctypes.byref(d), _ptr(codes), _ptr(scales), _ptr(x), M, _ptr(y), _ptr(workspace),
+                             workspace.numel() * workspace.element_size(), _stream(stream)), "tq_gemm_fp8")
     return y
 
 

@@ -26,6 +26,7 @@
 // Activations are the block Walsh-Hadamard transform of x in FP16 ("27B 大模型塞进
 // 5.9GB", section 二 ①); group scales per 64 or 128 weights (same page, section 二 ②).
 #include <cuda_bf16.h>
+#include <cuda_fp8.h>
 
 #include <algorithm>
 #include <map>
@@ -43,7 +44,8 @@ using namespace sm100;
 
 constexpr int BM = 128;  // tokens per tile (MMA M, TMEM lanes)
 constexpr int BN = 256;  // weight rows per tile (MMA N, TMEM columns)
-constexpr int BK = 64;   // K per stage: one 128-byte swizzle row of FP16
+constexpr int BK = 64;   // K per stage: one 128-byte swizzle row of FP16 ...
+constexpr int BK8 = 128; // ... or of FP8
 constexpr int STAGES = 4;
 constexpr uint32_t kABytes = BM * BK * 2;
 constexpr uint32_t kBBytes = BN * BK * 2;
@@ -83,13 +85,18 @@ __device__ __forceinline__ void tile_of(const GroupedTiles& gt, int t, int n_mt,
   }
 }
 
+// F8: operands FP8 E4M3 (kind::f8f6f4), each row of x~ and of W under its own power-of-two factor
+// 2^ea[m] / 2^eb[n], which the epilogue applies exactly.
+template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, uint16_t* y,
-                   int M, int N, int K, int* status, const __grid_constant__ GroupedTiles gt) {
+                   int M, int N, int K, int* status, const __grid_constant__ GroupedTiles gt, const int* ea,
+                   const int* eb) {
+  constexpr int BKE = F8 ? BK8 : BK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int nk = K / BK;
+  const int nk = K / BKE;
   const int n_mt = (M + BM - 1) / BM;
   const int n_tiles = gt.tiles ? *gt.count : n_mt * ((N + BN - 1) / BN);
   // tile t: token tile t % n_mt, weight tile t / n_mt (the CTAs running together share few weight tiles)
@@ -128,8 +135,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         mbar_arrive_expect_tx(&sm.full[s], kABytes + kBBytes);
-        tma_load_2d(sm.a[s], &tm_x, kb * BK, m0, &sm.full[s]);
-        tma_load_2d(sm.b[s], &tm_w, kb * BK, nb, &sm.full[s]);
+        tma_load_2d(sm.a[s], &tm_x, kb * BKE, m0, &sm.full[s]);
+        tma_load_2d(sm.b[s], &tm_w, kb * BKE, nb, &sm.full[s]);
       }
     }
   } else if (warp == 1 && lane == 0) {
@@ -154,8 +161,12 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         const uint32_t a0 = smem_addr(sm.a[s]), b0 = smem_addr(sm.b[s]);
 #pragma unroll
-        for (int k = 0; k < BK / 16; ++k)
-          mma_f16_ss(d, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc, (kb | k) != 0);
+        for (int k = 0; k < 4; ++k) {  // 32 bytes of K each: 16 FP16 or 32 FP8
+          if (F8)
+            mma_f8_ss(d, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc, (kb | k) != 0);
+          else
+            mma_f16_ss(d, smem_desc_sw128(a0 + 32u * k), smem_desc_sw128(b0 + 32u * k), idesc, (kb | k) != 0);
+        }
         mma_commit(&sm.empty[s]);  // the stage is free once these MMAs have read it
       }
       mma_commit(&sm.acc_full[b]);
@@ -174,12 +185,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int m = m0 + 32 * q + lane;
+      const int eam = F8 && m < M ? ea[m] : 0;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t v[32];
         tmem_ld<32>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN + c), v);
         tmem_wait_ld();
         const int n = n0 + c;
+        if (F8) {  // y = acc * 2^(ea[m] + eb[n]), exact
+#pragma unroll
+          for (int j = 0; j < 32; ++j)
+            v[j] = __float_as_uint(ldexpf(__uint_as_float(v[j]), eam + (n + j < N ? __ldg(eb + n + j) : 0)));
+        }
         if (gt.tiles) {
           if (32 * q + lane < rows) {
             float4* dst = reinterpret_cast<float4*>(gt.y + static_cast<size_t>(m) * gt.ldy + n);
@@ -353,8 +370,162 @@ __global__ void __launch_bounds__(kDecThreads) decode_b3_kernel(const uint32_t* 
 }
 
 // ---------------------------------------------------------------------------------------------
+// FP8 operands.  Row factors: ea[m] = floor(log2 max_k |x~[m][k]|) - 7 and eb[n] = floor(log2
+// max_g |s[n][g]|) - 7 (0 for an all-zero row), so each row's largest magnitude lands in [128, 256),
+// below the E4M3 maximum 448; values are rounded to E4M3 to nearest even (cvt .satfinite).
+// ---------------------------------------------------------------------------------------------
+__device__ __forceinline__ int row_exponent(float mx) {
+  if (!(mx > 0.f)) return 0;
+  int ex = 0;
+  (void)frexpf(mx, &ex);  // mx = f * 2^ex, f in [0.5, 1)
+  return ex - 1 - 7;
+}
+
+__device__ __forceinline__ uint8_t to_e4m3(float v) {
+  return static_cast<uint8_t>(__nv_cvt_float_to_fp8(v, __NV_SATFINITE, __NV_E4M3));
+}
+
+// One CTA per token row: the block transform of the row (bf16 in, fp32), its largest magnitude, then
+// the E4M3 values of x~ * 2^-ea (the transform is recomputed in the second pass from the bf16 input).
+constexpr int kActThreads = 256;
+__global__ void __launch_bounds__(kActThreads) fp8_act_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xq,
+                                                              int* __restrict__ ea, int K, int apply, int* status) {
+  __shared__ float red[kActThreads / 32];
+  const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = K / kFwhtBlock;
+  const uint16_t* xr = x + static_cast<size_t>(m) * K;
+  auto block_values = [&](int blk, float (&v)[4]) {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + blk * kFwhtBlock + 4 * lane));
+    v[0] = bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu));
+    v[1] = bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16));
+    v[2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
+    v[3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
+    if (apply) {
+      fwht128_warp(v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] *= 0.08838834764831845f;
+    }
+  };
+  float mx = 0.f;
+  for (int blk = warp; blk < nblk; blk += kActThreads / 32) {
+    float v[4];
+    block_values(blk, v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[j]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int w = 1; w < kActThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+  if (!(mx <= 3.0e38f)) {  // inf or NaN in the row
+    if (threadIdx.x == 0) record_error(status, TQ_ERR_RANGE);
+    mx = 0.f;
+  }
+  const int e = row_exponent(mx);
+  if (threadIdx.x == 0) ea[m] = e;
+  for (int blk = warp; blk < nblk; blk += kActThreads / 32) {
+    float v[4];
+    block_values(blk, v);
+    uint32_t o = 0;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) o |= static_cast<uint32_t>(to_e4m3(ldexpf(v[j], -e))) << (8 * j);
+    *reinterpret_cast<uint32_t*>(xq + static_cast<size_t>(m) * K + blk * kFwhtBlock + 4 * lane) = o;
+  }
+}
+
+// eb[n] from the row's scales (one thread per row).
+__global__ void fp8_wexp_kernel(const uint16_t* __restrict__ scales, int* __restrict__ eb, int N, int ng, int* status) {
+  const int n = blockIdx.x * blockDim.x + threadIdx.x;
+  if (n >= N) return;
+  float mx = 0.f;
+  for (int g = 0; g < ng; ++g) mx = fmaxf(mx, fabsf(__half2float(__ushort_as_half(__ldg(scales + static_cast<size_t>(n) * ng + g)))));
+  if (!(mx <= 65504.f)) {
+    record_error(status, TQ_ERR_RANGE);
+    mx = 0.f;
+  }
+  eb[n] = row_exponent(mx);
+}
+
+// E4M3 of +-s * 2^-eb: the byte for +s; -s flips the sign bit, t = 0 is the byte 0.
+__device__ __forceinline__ uint8_t signed_e4m3(int t, uint8_t pos) {
+  return t == 0 ? static_cast<uint8_t>(0) : (t > 0 ? pos : static_cast<uint8_t>(pos ^ 0x80u));
+}
+
+// 2-bit: one thread per word (16 weights of one group), one 16-byte store.
+__global__ void __launch_bounds__(kDecThreads) decode_2b_f8_kernel(const uint32_t* __restrict__ codes,
+                                                                   const uint16_t* __restrict__ scales,
+                                                                   const int* __restrict__ eb, uint8_t* __restrict__ w,
+                                                                   int N, int K, int P, int ng, int G) {
+  const int wpr = K / 16;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(N) * wpr) return;
+  const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
+  const uint32_t word = __ldg(codes + static_cast<size_t>(n) * P + j);
+  const float s = __half2float(__ushort_as_half(__ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G)));
+  const uint8_t pos = to_e4m3(ldexpf(s, -__ldg(eb + n)));
+  uint32_t o[4];
+#pragma unroll
+  for (int q = 0; q < 4; ++q) {
+    uint32_t v = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const int d = static_cast<int>((word >> (2 * (4 * q + h))) & 3u);
+      v |= static_cast<uint32_t>(signed_e4m3(d == 3 ? 0 : d - 1, pos)) << (8 * h);  // field 3 reads as t = 0
+    }
+    o[q] = v;
+  }
+  *reinterpret_cast<uint4*>(w + static_cast<size_t>(n) * K + 16 * j) = make_uint4(o[0], o[1], o[2], o[3]);
+}
+
+// base-3: one thread per 4 words (80 weights) of a row; K is a multiple of 128, so every 80-weight
+// piece and the row tail are whole 16-byte pieces.
+__global__ void __launch_bounds__(kDecThreads) decode_b3_f8_kernel(const uint32_t* __restrict__ codes,
+                                                                   const uint16_t* __restrict__ scales,
+                                                                   const int* __restrict__ eb, uint8_t* __restrict__ w,
+                                                                   int N, int K, int P, int ng, int G) {
+  const int per_row = (K + 79) / 80;
+  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
+  if (i >= static_cast<long long>(N) * per_row) return;
+  const int n = static_cast<int>(i / per_row), j = static_cast<int>(i - static_cast<long long>(n) * per_row);
+  const int k0 = 80 * j, kn = min(80, K - k0);
+  const uint16_t* srow = scales + static_cast<size_t>(n) * ng;
+  const int e = __ldg(eb + n);
+  const int g0 = k0 / G;
+  const int b1 = (g0 + 1) * G - k0, b2 = b1 + G;
+  const uint8_t pa = to_e4m3(ldexpf(__half2float(__ushort_as_half(__ldg(srow + g0))), -e));
+  const uint8_t pb = b1 < kn ? to_e4m3(ldexpf(__half2float(__ushort_as_half(__ldg(srow + g0 + 1))), -e)) : pa;
+  const uint8_t pc = b2 < kn ? to_e4m3(ldexpf(__half2float(__ushort_as_half(__ldg(srow + g0 + 2))), -e)) : pb;
+  uint32_t o[20];
+#pragma unroll
+  for (int wi = 0; wi < 4; ++wi) {
+    uint32_t v = 20 * wi < kn ? min(__ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi), kB3Max) : kB3Zero;
+#pragma unroll
+    for (int d4 = 0; d4 < 5; ++d4) {
+      uint32_t out = 0;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const uint32_t qd = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
+        const int t = static_cast<int>(v - 3u * qd) - 1;
+        v = qd;
+        const int k = 20 * wi + 4 * d4 + h;
+        out |= static_cast<uint32_t>(signed_e4m3(t, k < b1 ? pa : (k < b2 ? pb : pc))) << (8 * h);
+      }
+      o[5 * wi + d4] = out;
+    }
+  }
+  uint4* dst = reinterpret_cast<uint4*>(w + static_cast<size_t>(n) * K + k0);
+#pragma unroll
+  for (int c = 0; c < 5; ++c)
+    if (16 * c < kn) dst[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
+}
+
+// ---------------------------------------------------------------------------------------------
 // host side
 // ---------------------------------------------------------------------------------------------
+template <bool F8>
 cudaError_t ensure_attr() {
   static std::map<int, bool> done;
   static std::mutex mu;
@@ -363,9 +534,19 @@ cudaError_t ensure_attr() {
   if (e != cudaSuccess) return e;
   std::lock_guard<std::mutex> lock(mu);
   if (done[dev]) return cudaSuccess;
-  e = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kSmemBytes));
+  e = cudaFuncSetAttribute(gemm_tc_kernel<F8>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           static_cast<int>(kSmemBytes));
   if (e == cudaSuccess) done[dev] = true;
   return e;
+}
+
+int sm_count() {
+  int dev = 0, sms = 148;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    sms = 148;
+  }
+  return sms;
 }
 
 }  // namespace gemm
@@ -398,14 +579,15 @@ cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t*
       !make_tmap_2d(&tm_w, wa, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, K, N, static_cast<uint64_t>(K) * 2, BK, BN,
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
-  if ((e = ensure_attr()) != cudaSuccess) return e;
+  if ((e = ensure_attr<false>()) != cudaSuccess) return e;
   // persistent: one CTA per SM, each walking the tiles with a stride of the grid
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
   const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, sms));
-  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status_ptr(), GroupedTiles{});
+  gemm_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status_ptr(), GroupedTiles{},
+                                                           nullptr, nullptr);
   return cudaPeekAtLastError();
 }
 
@@ -419,13 +601,14 @@ cudaError_t launch_gemm_grouped(const uint16_t* xa, int a_rows, const uint16_t* 
                     CU_TENSOR_MAP_SWIZZLE_128B))
     return cudaErrorInvalidValue;
   cudaError_t e;
-  if ((e = ensure_attr()) != cudaSuccess) return e;
+  if ((e = ensure_attr<false>()) != cudaSuccess) return e;
   int dev = 0, sms = 148;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
   if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) sms = 148;
   const unsigned grid = static_cast<unsigned>(std::max(1, std::min(max_tiles, sms)));
   const GroupedTiles gt{reinterpret_cast<const int4*>(tiles), count, y, ldy};
-  gemm_tc_kernel<<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, nullptr, a_rows, 0, K, status_ptr(), gt);
+  gemm_tc_kernel<false><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, nullptr, a_rows, 0, K, status_ptr(), gt,
+                                                           nullptr, nullptr);
   return cudaPeekAtLastError();
 }
 
@@ -439,6 +622,46 @@ cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_
     const long long n = static_cast<long long>(N) * ((K + 79) / 80);
     decode_b3_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, w, N, K, P, ng, G);
   }
+  return cudaPeekAtLastError();
+}
+
+size_t gemm_fp8_workspace_bytes(const tq_desc* d, int M) {
+  return align256(static_cast<size_t>(M) * d->K) + align256(static_cast<size_t>(d->N) * d->K) +
+         align256(static_cast<size_t>(M) * 4) + align256(static_cast<size_t>(d->N) * 4);
+}
+
+cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int M,
+                            uint16_t* y, void* ws, cudaStream_t s) {
+  using namespace gemm;
+  const int N = d->N, K = d->K, G = d->group, P = pitch_words(K, d->packing), ng = K / G;
+  uint8_t* xq = static_cast<uint8_t*>(ws);
+  uint8_t* wq = xq + align256(static_cast<size_t>(M) * K);
+  int* ea = reinterpret_cast<int*>(wq + align256(static_cast<size_t>(N) * K));
+  int* eb = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ea) + align256(static_cast<size_t>(M) * 4));
+  int* status = status_ptr();
+  fp8_act_kernel<<<M, kActThreads, 0, s>>>(x, xq, ea, K, d->fwht_block != 0, status);
+  fp8_wexp_kernel<<<(N + 255) / 256, 256, 0, s>>>(scales, eb, N, ng, status);
+  if (d->packing == TQ_PACK_2BIT) {
+    const long long n = static_cast<long long>(N) * (K / 16);
+    decode_2b_f8_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(
+        codes, scales, eb, wq, N, K, P, ng, G);
+  } else {
+    const long long n = static_cast<long long>(N) * ((K + 79) / 80);
+    decode_b3_f8_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(
+        codes, scales, eb, wq, N, K, P, ng, G);
+  }
+  cudaError_t e = cudaPeekAtLastError();
+  if (e != cudaSuccess) return e;
+  CUtensorMap tm_x, tm_w;
+  if (!make_tmap_2d(&tm_x, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, static_cast<uint64_t>(K), BK8, BM,
+                    CU_TENSOR_MAP_SWIZZLE_128B) ||
+      !make_tmap_2d(&tm_w, wq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, N, static_cast<uint64_t>(K), BK8, BN,
+                    CU_TENSOR_MAP_SWIZZLE_128B))
+    return cudaErrorInvalidValue;
+  if ((e = ensure_attr<true>()) != cudaSuccess) return e;
+  const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
+  const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, sm_count()));
+  gemm_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status, GroupedTiles{}, ea, eb);
   return cudaPeekAtLastError();
 }
 

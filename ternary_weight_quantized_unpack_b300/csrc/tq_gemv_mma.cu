@@ -310,6 +310,7 @@ struct Params {
   int early;  // 1: codes and scales may be read before the preceding kernel has completed
   int v8;     // base-3: rows and code base are 32-byte aligned, codes are read 32 bytes at a time
   uint32_t xh_off, vp_off, sw_off, bar_off;  // shared-memory offsets: x^, VP, per-warp scales, barriers
+  uint32_t ring_off;                         // 3-bit: per-warp code rings
   // Routed-token chunks (nullptr: one dense matrix).  blockIdx.z selects record {expert, count,
   // rows[B]} of chunks[1 + z * (2 + B)] (chunks[0] = number of records); the expert's codes and
   // scales start expert * *_estride elements in, the chunk's prep slice z * *_cstride in, and batch
@@ -969,20 +970,24 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
 // exponent half is d * 2^(p - 24); the prep kernel folds 2^(8 - p) into the activations and the
 // offset q = d - 4 into the group's starting value.  MMA m of a block takes registers 2m, 2m + 1 of
 // both rows of the thread, so a block is 16 MMAs and a group 16 (G = 64) or 32 (G = 128).
-// A unit is 28 words (7 steps of four); the code ring has one slot per step of a unit, so every ring
-// index is a compile-time constant while three steps stay in flight.
+// A unit is 28 words (7 steps of four).  Code words reach the warp through a shared-memory ring of
+// 16-byte cp.async copies, each lane copying and later reading its own two rows' step, kQ3Ahead steps
+// in flight: the copies do not hold registers, so the depth does not cost occupancy.
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t q3_reg(uint32_t w, int i, int j) {
   if (i == 6) return w & (j == 0 ? 0x00070007u : 0x00380038u);
   return j < 3 ? (w & (0x00070007u << (3 * j))) : ((w >> 8) & (0x00070007u << (3 * j - 8)));
 }
 
-constexpr int kQ3Steps = 7;  // 16-byte steps per unit
+constexpr int kQ3Steps = 7;       // 16-byte steps per unit
+constexpr int kQ3Ring = 8;        // ring slots per warp: one step of the warp's 64 rows (1 KB) each
+constexpr int kQ3Ahead = 6;       // steps in flight
+constexpr uint32_t kQ3RingBytes = kQ3Ring * 1024u;
 
 template <int G, int NT, bool FULL>
 __device__ __forceinline__ void q3_unit(const Params& p, const Cta& c, int u, int ngp, const uint4* __restrict__ cR,
-                                        const uint4* __restrict__ cR2, int s_last, uint4 (&ra)[kQ3Steps],
-                                        uint4 (&rb)[kQ3Steps], const uint32_t* const (&bptr)[NT],
+                                        const uint4* __restrict__ cR2, int s_last, uint32_t ring,
+                                        const uint32_t* const (&bptr)[NT],
                                         const int (&bstr)[NT], const float* __restrict__ V,
                                         const uint16_t* __restrict__ swr, float (&acc)[NT][4]) {
   constexpr int GM = G / 4;     // MMAs per group
@@ -994,12 +999,17 @@ __device__ __forceinline__ void q3_unit(const Params& p, const Cta& c, int u, in
   uint32_t ea = 0u, eb = 0u;  // the even register of the MMA being formed (rows R, R + 32)
 #pragma unroll
   for (int st = 0; st < kQ3Steps; ++st) {
+    const int sa = u * kQ3Steps + st;  // absolute step; slot sa % kQ3Ring holds it
     {
-      const int s = min(u * kQ3Steps + st + 3, s_last);  // past this warp's range: re-read its last step
-      ra[(st + 3) % kQ3Steps] = __ldg(cR + s);
-      rb[(st + 3) % kQ3Steps] = __ldg(cR2 + s);
+      const int s = min(sa + kQ3Ahead, s_last);  // past this warp's range: re-read its last step
+      const uint32_t slot = ring + static_cast<uint32_t>((sa + kQ3Ahead) & (kQ3Ring - 1)) * 1024u;
+      cp_async16(slot, cR + s);
+      cp_async16(slot + 512u, cR2 + s);
+      cp_async_commit();
     }
-    const uint4 cur = ra[st], cur2 = rb[st];
+    cp_async_wait<kQ3Ahead>();  // the group of step sa has landed (this lane's own copies)
+    const uint32_t cs = ring + static_cast<uint32_t>(sa & (kQ3Ring - 1)) * 1024u;
+    const uint4 cur = lds128(cs), cur2 = lds128(cs + 512u);
     const uint32_t wr[4] = {cur.x, cur.y, cur.z, cur.w};
     const uint32_t wr2[4] = {cur2.x, cur2.y, cur2.z, cur2.w};
 #pragma unroll
@@ -1077,18 +1087,17 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_q3_kernel(const __grid_const
   uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + c.warp * (GPS * 64);
   UnitScales<64, GPS, false> us;
   auto unit_groups = [&](int u) { return min(GPS, (min((u + 1) * 256, p.K) - u * 256) / G); };
-  uint4 ra[kQ3Steps], rb[kQ3Steps];
-#pragma unroll
-  for (int i = 0; i < kQ3Steps; ++i) {
-    ra[i] = make_uint4(0u, 0u, 0u, 0u);
-    rb[i] = ra[i];
-  }
+  // the warp's ring: slot i holds one step, 16 bytes of row R per lane, then 16 bytes of row R + 32
+  const uint32_t ring = smem_addr(smem + p.ring_off) + c.warp * kQ3RingBytes + c.lane * 16u;
   auto prime = [&]() {
     if (c.ua < c.ub) {
 #pragma unroll
-      for (int i = 0; i < 3; ++i) {
-        ra[i] = __ldg(cR + min(s_begin + i, s_last));
-        rb[i] = __ldg(cR2 + min(s_begin + i, s_last));
+      for (int i = 0; i < kQ3Ahead; ++i) {
+        const int s = min(s_begin + i, s_last);
+        const uint32_t slot = ring + static_cast<uint32_t>((s_begin + i) & (kQ3Ring - 1)) * 1024u;
+        cp_async16(slot, cR + s);
+        cp_async16(slot + 512u, cR2 + s);
+        cp_async_commit();
       }
       us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
@@ -1136,10 +1145,11 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_q3_kernel(const __grid_const
     __syncwarp();
     if (u + 1 < c.ub) us.load(p, sel.scales, row_w0, u + 1, unit_groups(u + 1), c.lane);
     if (ngp == GPS)
-      q3_unit<G, NT, true>(p, c, u, ngp, cR, cR2, s_last, ra, rb, bptr, bstr, V, swr, acc);
+      q3_unit<G, NT, true>(p, c, u, ngp, cR, cR2, s_last, ring, bptr, bstr, V, swr, acc);
     else
-      q3_unit<G, NT, false>(p, c, u, ngp, cR, cR2, s_last, ra, rb, bptr, bstr, V, swr, acc);
+      q3_unit<G, NT, false>(p, c, u, ngp, cR, cR2, s_last, ring, bptr, bstr, V, swr, acc);
   }
+  cp_async_wait<0>();  // the ring's trailing copies (re-reads of the last step) land before exit
 
   __syncthreads();  // the partial sums reuse the x^ region
   float* red = reinterpret_cast<float*>(smem);
@@ -1465,7 +1475,7 @@ constexpr size_t kSmemLimit = 227 * 1024;
 struct Plan {
   bool ok;
   int rs, kl, ppl, ks, upr, n_rg;
-  size_t smem, xh_off, vp_off, sw_off, bar_off;
+  size_t smem, xh_off, vp_off, sw_off, bar_off, ring_off;
 };
 
 // Shared-memory layout of a candidate split; returns the total bytes.  The partial-sum buffer of
@@ -1481,7 +1491,8 @@ size_t layout(Plan& pl, int pack, int B, int G, int K) {
   pl.vp_off = align256(std::max(main, red));
   pl.sw_off = pl.vp_off + align256(static_cast<size_t>(ngr) * vp_row(B) * 4);
   pl.bar_off = pl.sw_off + align256(static_cast<size_t>(pl.rs) * pl.kl * (UT / G) * SLAB * 2);
-  pl.smem = pl.bar_off + 256;
+  pl.ring_off = pl.bar_off + 256;
+  pl.smem = pl.ring_off + (pack == TQ_PACK_3BIT ? static_cast<size_t>(pl.rs) * pl.kl * kQ3RingBytes : 0);
   return pl.smem;
 }
 
@@ -1966,6 +1977,7 @@ cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int 
   prm.vp_off = static_cast<uint32_t>(pl.vp_off);
   prm.sw_off = static_cast<uint32_t>(pl.sw_off);
   prm.bar_off = static_cast<uint32_t>(pl.bar_off);
+  prm.ring_off = static_cast<uint32_t>(pl.ring_off);
   prm.v8 = b3 && prm.P % 8 == 0 && reinterpret_cast<uintptr_t>(prm.codes) % 32 == 0 &&
            (!prm.chunks || prm.codes_estride % 8 == 0);
   cudaLaunchAttribute attr[2];

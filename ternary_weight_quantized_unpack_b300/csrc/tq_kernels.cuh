@@ -54,6 +54,10 @@ cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t*
 // xa: FP16 [a_rows][K]; wa: FP16 [w_rows][K]; y: fp32, row r at y + r * ldy.
 cudaError_t launch_gemm_grouped(const uint16_t* xa, int a_rows, const uint16_t* wa, int w_rows, int K, const int* tiles,
                                 const int* count, int max_tiles, float* y, int ldy, cudaStream_t s);
+// Prefill GEMM with FP8 E4M3 operands (per-row power-of-two factors; tcgen05 kind::f8f6f4).
+size_t gemm_fp8_workspace_bytes(const tq_desc* d, int M);
+cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int M,
+                            uint16_t* y, void* ws, cudaStream_t s);
 // Weights of one matrix (or of stacked experts viewed as one matrix) decoded to FP16 s * t [N][K].
 cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, uint16_t* w, cudaStream_t s);
 

@@ -61,3 +61,22 @@ extern "C" tq_status tq_gemm(const tq_desc* d, const uint32_t* codes, const uint
   if (const cudaError_t e = launch_gemm(d, codes, scales, x, M, y, workspace, s); e != cudaSuccess) return cuda_fail(e);
   return TQ_OK;
 }
+
+extern "C" size_t tq_gemm_fp8_workspace_bytes(const tq_desc* d, int M) {
+  if (check_linear_desc(d) != TQ_OK || M < 1) return 0;
+  return gemm_fp8_workspace_bytes(d, M);
+}
+
+extern "C" tq_status tq_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x,
+                                 int M, uint16_t* y, void* workspace, size_t workspace_bytes, void* stream) {
+  tq_status st = check_linear_desc(d);
+  if (st != TQ_OK) return st;
+  if (M < 1) return TQ_ERR_INVALID_ARG;
+  if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
+  if (workspace_bytes < tq_gemm_fp8_workspace_bytes(d, M)) return TQ_ERR_WORKSPACE;
+  if (!status_ptr()) return TQ_ERR_CUDA;
+  if (const cudaError_t e = launch_gemm_fp8(d, codes, scales, x, M, y, workspace, static_cast<cudaStream_t>(stream));
+      e != cudaSuccess)
+    return cuda_fail(e);
+  return TQ_OK;
+}

@@ -17,6 +17,7 @@ import torch
 
 import oracle as O_real
 from ternary_weight_quantized_unpack_b300 import inputs
+from tq_testlib import fp8_bound
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "format_constants.txt")
 
@@ -545,18 +546,6 @@ def pin_pow2_exponent(O):
     e = O.pow2_exponent(m)
     scaled = m * np.exp2(-e.astype(np.float64))
     assert ((scaled >= 128) & (scaled < 256)).all()
-
-
-def fp8_bound(xt, W, ea, eb):
-    """|y_fp8 - y| for the E4M3 operands: relative 2^-4 per operand (normals, half a 3-bit ulp) and,
-    below 2^-6 after scaling, an absolute 2^-10 (half the subnormal spacing) times the row factor."""
-    ax, aw = np.abs(xt), np.abs(W)
-    A = ax @ aw.T
-    fa = np.ldexp(1.0, ea)[:, None]
-    fb = np.ldexp(1.0, eb)[None, :]
-    K = xt.shape[1]
-    return ((2.0 ** -3 + 2.0 ** -8) * A + 2.0 ** -10 * 1.07 * (fb * ax.sum(axis=1)[:, None] + fa * aw.sum(axis=1)[None, :])
-            + K * 2.0 ** -20 * fa * fb)
 
 
 def pin_linear_fp8(O):

@@ -110,3 +110,15 @@ def moe_bounds(out, down_dense, fwht_block):
             extra[ti] += out["gate"][ti, j] * (Wd_abs @ dht[ti, j]) + 1e-6 * np.abs(out["y_parts"][ti, j])
     A_e2e = np.einsum("tj,tjh->th", out["gate"], out["A_d"])
     return hb, A_e2e, extra
+
+
+def fp8_bound(xt, W, ea, eb):
+    """|y_fp8 - y| for the E4M3 operands: relative 2^-4 per operand (normals, half a 3-bit ulp) and,
+    below 2^-6 after scaling, an absolute 2^-10 (half the subnormal spacing) times the row factor."""
+    ax, aw = np.abs(xt), np.abs(W)
+    A = ax @ aw.T
+    fa = np.ldexp(1.0, ea)[:, None]
+    fb = np.ldexp(1.0, eb)[None, :]
+    K = xt.shape[1]
+    return ((2.0 ** -3 + 2.0 ** -8) * A + 2.0 ** -10 * 1.07 * (fb * ax.sum(axis=1)[:, None] + fa * aw.sum(axis=1)[None, :])
+            + K * 2.0 ** -20 * fa * fb)
