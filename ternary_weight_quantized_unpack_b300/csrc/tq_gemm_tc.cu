@@ -454,30 +454,48 @@ __device__ __forceinline__ uint8_t signed_e4m3(int t, uint8_t pos) {
   return t == 0 ? static_cast<uint8_t>(0) : (t > 0 ? pos : static_cast<uint8_t>(pos ^ 0x80u));
 }
 
-// 2-bit: one thread per word (16 weights of one group), one 16-byte store.
+// 2-bit: a warp takes 128 consecutive words (of the flattened [N][K/16] word grid), lane l the words
+// l + 32 q (q < 4): every load and every 16-byte store of the warp is one contiguous 128- / 512-byte
+// range, and each lane has four independent loads in flight.  A word is 16 weights of one group.
+constexpr int kF8WordsPerLane = 4;
 __global__ void __launch_bounds__(kDecThreads) decode_2b_f8_kernel(const uint32_t* __restrict__ codes,
                                                                    const uint16_t* __restrict__ scales,
                                                                    const int* __restrict__ eb, uint8_t* __restrict__ w,
                                                                    int N, int K, int P, int ng, int G) {
   const int wpr = K / 16;
-  const long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  if (i >= static_cast<long long>(N) * wpr) return;
-  const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
-  const uint32_t word = __ldg(codes + static_cast<size_t>(n) * P + j);
-  const float s = __half2float(__ushort_as_half(__ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G)));
-  const uint8_t pos = to_e4m3(ldexpf(s, -__ldg(eb + n)));
-  uint32_t o[4];
+  const long long total = static_cast<long long>(N) * wpr;
+  const long long base = (static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31)) * kF8WordsPerLane +
+                         (threadIdx.x & 31);
+  uint32_t word[kF8WordsPerLane];
+  float sv[kF8WordsPerLane];
+  int ev[kF8WordsPerLane];
 #pragma unroll
-  for (int q = 0; q < 4; ++q) {
-    uint32_t v = 0;
-#pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      const int d = static_cast<int>((word >> (2 * (4 * q + h))) & 3u);
-      v |= static_cast<uint32_t>(signed_e4m3(d == 3 ? 0 : d - 1, pos)) << (8 * h);  // field 3 reads as t = 0
-    }
-    o[q] = v;
+  for (int q = 0; q < kF8WordsPerLane; ++q) {
+    const long long i = min(base + 32 * q, total - 1);
+    const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
+    word[q] = __ldg(codes + static_cast<size_t>(n) * P + j);
+    sv[q] = __half2float(__ushort_as_half(__ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G)));
+    ev[q] = __ldg(eb + n);
   }
-  *reinterpret_cast<uint4*>(w + static_cast<size_t>(n) * K + 16 * j) = make_uint4(o[0], o[1], o[2], o[3]);
+#pragma unroll
+  for (int q = 0; q < kF8WordsPerLane; ++q) {
+    const long long i = base + 32 * q;
+    if (i >= total) break;
+    const uint8_t pos = to_e4m3(ldexpf(sv[q], -ev[q]));
+    uint32_t o[4];
+#pragma unroll
+    for (int c = 0; c < 4; ++c) {
+      uint32_t v = 0;
+#pragma unroll
+      for (int h = 0; h < 4; ++h) {
+        const int d = static_cast<int>((word[q] >> (2 * (4 * c + h))) & 3u);
+        v |= static_cast<uint32_t>(signed_e4m3(d == 3 ? 0 : d - 1, pos)) << (8 * h);  // field 3 reads as t = 0
+      }
+      o[c] = v;
+    }
+    // word i of the flattened grid is weights 16 i .. 16 i + 15 of W (rows are K = 16 * wpr wide)
+    *reinterpret_cast<uint4*>(w + 16 * static_cast<size_t>(i)) = make_uint4(o[0], o[1], o[2], o[3]);
+  }
 }
 
 // base-3: one thread per 4 words (80 weights) of a row; K is a multiple of 128, so every 80-weight
@@ -643,7 +661,8 @@ cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint1
   fp8_wexp_kernel<<<(N + 255) / 256, 256, 0, s>>>(scales, eb, N, ng, status);
   if (d->packing == TQ_PACK_2BIT) {
     const long long n = static_cast<long long>(N) * (K / 16);
-    decode_2b_f8_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(
+    const long long per_cta = static_cast<long long>(kDecThreads) * kF8WordsPerLane;
+    decode_2b_f8_kernel<<<static_cast<unsigned>((n + per_cta - 1) / per_cta), kDecThreads, 0, s>>>(
         codes, scales, eb, wq, N, K, P, ng, G);
   } else {
     const long long n = static_cast<long long>(N) * ((K + 79) / 80);
