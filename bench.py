@@ -532,6 +532,32 @@ def bench_single_linear(reps, seed=inputs.seed_of(1)):
             "kernels_per_call": tq.tq_gemv_kernel_count(d, c["B"])}
 
 
+# 3-bit linears timed alone: a 27B-class gate/up-sized matrix and a wide-output one (the shape class of
+# an lm_head over a 2048-wide hidden state; no page gives the model's vocabulary size)
+GEMV3_SHAPES = ((17408, 5120), (131072, 2048))
+
+
+def bench_gemv_linear(N, K, packing, batch, reps, seed=inputs.seed_of(2)):
+    """One linear called alone with L2 flushed before each call: device time and GB/s of codes + scales."""
+    d = tq.desc(N, K, 128, packing)
+    gen = torch.Generator(device="cuda")
+    gen.manual_seed(seed + N + packing)
+    lo, hi = (-4, 4) if packing == tq.TQ_PACK_3BIT else (-1, 2)
+    codes = tq.tq_pack(d, torch.randint(lo, hi, (N, K), dtype=torch.int8, device="cuda", generator=gen))
+    s = torch.exp(torch.randn((N, K // 128), generator=gen, device="cuda") * 0.5 - 4).half()
+    x = inputs.activations(seed, N, batch, K).cuda()
+    y = torch.empty((batch, N), dtype=torch.float32, device="cuda")
+    ws = torch.empty(max(1, tq.tq_gemv_workspace_bytes(d, batch)), dtype=torch.uint8, device="cuda")
+    call = lambda: tq.tq_gemv(d, codes, s, x, y=y, workspace=ws)  # noqa: E731
+    for _ in range(3):
+        call()
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    ms = l2_cold_times(call, max(3, reps), flush)
+    byts = tq.tq_packed_bytes(d) + tq.tq_scale_bytes(d)
+    return {"N": N, "K": K, "packing": PACKING_NAMES[packing], "batch": batch, "us_l2_cold": ms * 1e3,
+            "GB_s": byts / (ms * 1e-3) / GB, "kernels_per_call": tq.tq_gemv_kernel_count(d, batch)}
+
+
 def bench_layer_linears(packing, batches, reps, seed=inputs.seed_of(2)):
     """The seven linears of one 27B-class layer, each called alone with L2 flushed before it; per
     batch: per-linear device times and tok/s = batch / (64 x sum of the seven times)."""
@@ -790,6 +816,7 @@ def run_tq(args, rank, world, local):
         # 3-bit codes (the precision the non-expert linears keep)
         ex["layer_linears"] += bench_layer_linears(tq.TQ_PACK_3BIT, inputs.DENSE_DECODE["batches"],
                                                    max(10, args.steps // 5))
+        ex["gemv3"] = [bench_gemv_linear(N, K, tq.TQ_PACK_3BIT, 1, 20) for N, K in GEMV3_SHAPES]
         torch.cuda.empty_cache()
         for T in inputs.MOE["tokens"]:
             r = bench_moe(T, max(10, args.steps // 2), 3)
@@ -827,21 +854,28 @@ def main():
                     help="seq: the whole step as one tq_seq launch (2-bit, batch <= 8); per_call: one tq_gemv per call")
     ap.add_argument("--no-extras", dest="extras", action="store_false")
     ap.add_argument("--no-cpu-baseline", dest="cpu", action="store_false")
-    ap.add_argument("--workload", choices=["stream", "prefill", "moe", "moe_prefill"], default="stream",
-                    help="stream: the headline decode line; prefill / moe / moe_prefill: one line per shape of "
-                         "those workloads")
+    ap.add_argument("--workload", choices=["stream", "prefill", "prefill_fp8", "moe", "moe_prefill", "gemv3"],
+                    default="stream",
+                    help="stream: the headline decode line; prefill / prefill_fp8 / moe / moe_prefill / gemv3: one "
+                         "line per shape of those workloads")
     args = ap.parse_args()
     assert args.warmup >= 3, "at least 3 warm-up steps"
     rank, world, local = dist_setup()
     if args.impl == "reference":
         run_reference(args, rank, world)
-    elif args.workload == "prefill":
+    elif args.workload in ("prefill", "prefill_fp8"):
         if rank == 0:
             peaks = measured_peaks()
+            fp8 = args.workload == "prefill_fp8"
             for shape in inputs.PREFILL["shapes"]:
-                r = bench_prefill(shape, args.steps, args.warmup)
-                r["pct_of_bf16_peak"] = 100.0 * r["TFLOP_s"] / peaks["bf16_tflops"]
-                print(json.dumps({"workload": "prefill", **r}))
+                r = bench_prefill(shape, args.steps, args.warmup, fp8=fp8)
+                r["pct_of_peak"] = 100.0 * r["TFLOP_s"] / (peaks["bf16_tflops"] * (2.0 if fp8 else 1.0))
+                print(json.dumps({"workload": args.workload, **r}))
+    elif args.workload == "gemv3":
+        if rank == 0:
+            for N, K in GEMV3_SHAPES:
+                for b in (1, 16):
+                    print(json.dumps({"workload": "gemv3", **bench_gemv_linear(N, K, tq.TQ_PACK_3BIT, b, args.steps)}))
     elif args.workload == "moe":
         if rank == 0:
             for T in inputs.MOE["tokens"]:

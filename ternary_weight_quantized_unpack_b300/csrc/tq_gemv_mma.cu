@@ -296,6 +296,7 @@ __global__ void __launch_bounds__(128) gemv_prep_kernel(const __grid_constant__ 
 // GEMV kernels
 // ---------------------------------------------------------------------------------------------
 struct Params {
+  CUtensorMap tm;  // 3-bit: the codes [N][P] as a 2-D map (box 28 words x 64 rows); unused otherwise
   const uint32_t* codes;
   const uint16_t* scales;
   const uint16_t* xh_g;  // prep output: x^ for all of K
@@ -970,24 +971,25 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_b3_kernel(const __grid_const
 // exponent half is d * 2^(p - 24); the prep kernel folds 2^(8 - p) into the activations and the
 // offset q = d - 4 into the group's starting value.  MMA m of a block takes registers 2m, 2m + 1 of
 // both rows of the thread, so a block is 16 MMAs and a group 16 (G = 64) or 32 (G = 128).
-// A unit is 28 words (7 steps of four).  Code words reach the warp through a shared-memory ring of
-// 16-byte cp.async copies, each lane copying and later reading its own two rows' step, kQ3Ahead steps
-// in flight: the copies do not hold registers, so the depth does not cost occupancy.
+// A unit is 28 words (7 steps of four).  A warp's codes arrive one unit at a time as a 2-D TMA box
+// (its 64 rows x 112 bytes) in a two-slot shared-memory ring, the next unit in flight while this one
+// is decoded: one request per box instead of 32 scattered 16-byte requests per warp-wide load (the
+// L1 would take those one 128-byte line at a time).  Lane l reads rows l and l + 32 of the box (a row
+// stride of 112 bytes keeps 16-byte reads free of bank conflicts).
 // ---------------------------------------------------------------------------------------------
 __device__ __forceinline__ uint32_t q3_reg(uint32_t w, int i, int j) {
   if (i == 6) return w & (j == 0 ? 0x00070007u : 0x00380038u);
   return j < 3 ? (w & (0x00070007u << (3 * j))) : ((w >> 8) & (0x00070007u << (3 * j - 8)));
 }
 
-constexpr int kQ3Steps = 7;       // 16-byte steps per unit
-constexpr int kQ3Ring = 8;        // ring slots per warp: one step of the warp's 64 rows (1 KB) each
-constexpr int kQ3Ahead = 6;       // steps in flight
-constexpr uint32_t kQ3RingBytes = kQ3Ring * 1024u;
+constexpr int kQ3Steps = 7;                       // 16-byte steps per unit
+constexpr int kQ3UnitWords = 28;
+constexpr uint32_t kQ3Box = 64u * kQ3UnitWords * 4u;  // one unit of the warp's 64 rows: 7168 bytes
+constexpr uint32_t kQ3WarpRing = 2u * kQ3Box + 128u;  // two slots, then the two slots' mbarriers
 
 template <int G, int NT, bool FULL>
-__device__ __forceinline__ void q3_unit(const Params& p, const Cta& c, int u, int ngp, const uint4* __restrict__ cR,
-                                        const uint4* __restrict__ cR2, int s_last, uint32_t ring,
-                                        const uint32_t* const (&bptr)[NT],
+__device__ __forceinline__ void q3_unit(const Params& p, const Cta& c, int u, int ngp,
+                                        const uint4* __restrict__ box, const uint32_t* const (&bptr)[NT],
                                         const int (&bstr)[NT], const float* __restrict__ V,
                                         const uint16_t* __restrict__ swr, float (&acc)[NT][4]) {
   constexpr int GM = G / 4;     // MMAs per group
@@ -999,17 +1001,7 @@ __device__ __forceinline__ void q3_unit(const Params& p, const Cta& c, int u, in
   uint32_t ea = 0u, eb = 0u;  // the even register of the MMA being formed (rows R, R + 32)
 #pragma unroll
   for (int st = 0; st < kQ3Steps; ++st) {
-    const int sa = u * kQ3Steps + st;  // absolute step; slot sa % kQ3Ring holds it
-    {
-      const int s = min(sa + kQ3Ahead, s_last);  // past this warp's range: re-read its last step
-      const uint32_t slot = ring + static_cast<uint32_t>((sa + kQ3Ahead) & (kQ3Ring - 1)) * 1024u;
-      cp_async16(slot, cR + s);
-      cp_async16(slot + 512u, cR2 + s);
-      cp_async_commit();
-    }
-    cp_async_wait<kQ3Ahead>();  // the group of step sa has landed (this lane's own copies)
-    const uint32_t cs = ring + static_cast<uint32_t>(sa & (kQ3Ring - 1)) * 1024u;
-    const uint4 cur = lds128(cs), cur2 = lds128(cs + 512u);
+    const uint4 cur = box[st], cur2 = box[32 * kQ3Steps + st];  // rows l and l + 32 of the box
     const uint32_t wr[4] = {cur.x, cur.y, cur.z, cur.w};
     const uint32_t wr2[4] = {cur2.x, cur2.y, cur2.z, cur2.w};
 #pragma unroll
@@ -1075,38 +1067,34 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_q3_kernel(const __grid_const
   Bars* bars = reinterpret_cast<Bars*>(smem + p.bar_off);
   init_bars(bars);
   const int g = c.lane >> 2, q = c.lane & 3;
-  // rows past N compute on row 0 and are not stored
-  const int R = c.row0 + c.slab * 64 + c.lane, R2 = R + 32;
-  const uint4* cR = reinterpret_cast<const uint4*>(sel.codes + static_cast<size_t>(R < p.N ? R : 0) * p.P);
-  const uint4* cR2 = reinterpret_cast<const uint4*>(sel.codes + static_cast<size_t>(R2 < p.N ? R2 : 0) * p.P);
-  const int s_begin = c.ua * kQ3Steps;
-  const int s_end = min(c.ub * kQ3Steps, p.P >> 2);
-  const int s_last = s_end - 1;  // this warp's last 4-word step
+  // rows past N are zero-filled by the TMA box, computed and not stored
   constexpr int GPS = 256 / G;
   const int row_w0 = c.row0 + c.slab * 64;
   uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.sw_off) + c.warp * (GPS * 64);
   UnitScales<64, GPS, false> us;
   auto unit_groups = [&](int u) { return min(GPS, (min((u + 1) * 256, p.K) - u * 256) / G); };
-  // the warp's ring: slot i holds one step, 16 bytes of row R per lane, then 16 bytes of row R + 32
-  const uint32_t ring = smem_addr(smem + p.ring_off) + c.warp * kQ3RingBytes + c.lane * 16u;
+  uint8_t* wring = smem + p.ring_off + c.warp * kQ3WarpRing;
+  uint64_t* ubar = reinterpret_cast<uint64_t*>(wring + 2 * kQ3Box);
+  if (c.lane == 0) {
+    mbar_init(&ubar[0], 1);
+    mbar_init(&ubar[1], 1);
+    fence_mbar_init();
+  }
+  __syncwarp();
+  auto issue = [&](int u) {  // unit u of the warp's rows into slot (u - ua) & 1
+    if (c.lane == 0) {
+      const int slot = (u - c.ua) & 1;
+      mbar_arrive_expect_tx(&ubar[slot], kQ3Box);
+      tma_load_2d(wring + slot * kQ3Box, &p.tm, kQ3UnitWords * u, row_w0, &ubar[slot]);
+    }
+  };
   auto prime = [&]() {
     if (c.ua < c.ub) {
-#pragma unroll
-      for (int i = 0; i < kQ3Ahead; ++i) {
-        const int s = min(s_begin + i, s_last);
-        const uint32_t slot = ring + static_cast<uint32_t>((s_begin + i) & (kQ3Ring - 1)) * 1024u;
-        cp_async16(slot, cR + s);
-        cp_async16(slot + 512u, cR2 + s);
-        cp_async_commit();
-      }
+      issue(c.ua);
+      if (c.ua + 1 < c.ub) issue(c.ua + 1);
       us.load(p, sel.scales, row_w0, c.ua, unit_groups(c.ua), c.lane);
     }
   };
-  if (kPrefetchL2 && p.early && c.ua < c.ub) {
-    const uint32_t bytes = static_cast<uint32_t>(s_end - s_begin) * 16u;
-    if (R < p.N) bulk_prefetch_l2(cR + s_begin, bytes);
-    if (R2 < p.N) bulk_prefetch_l2(cR2 + s_begin, bytes);
-  }
   if (p.early) prime();
   pdl_wait();
   if (!p.fused) copy_prep_slice(p, c, sel, smem, bars);
@@ -1144,12 +1132,19 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_q3_kernel(const __grid_const
     us.store(sw, c.lane);
     __syncwarp();
     if (u + 1 < c.ub) us.load(p, sel.scales, row_w0, u + 1, unit_groups(u + 1), c.lane);
+    const int slot = (u - c.ua) & 1;
+    if (!mbar_wait(&ubar[slot], ((u - c.ua) >> 1) & 1) && c.lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+    const uint4* box = reinterpret_cast<const uint4*>(wring + slot * kQ3Box) + c.lane * kQ3Steps;
     if (ngp == GPS)
-      q3_unit<G, NT, true>(p, c, u, ngp, cR, cR2, s_last, ring, bptr, bstr, V, swr, acc);
+      q3_unit<G, NT, true>(p, c, u, ngp, box, bptr, bstr, V, swr, acc);
     else
-      q3_unit<G, NT, false>(p, c, u, ngp, cR, cR2, s_last, ring, bptr, bstr, V, swr, acc);
+      q3_unit<G, NT, false>(p, c, u, ngp, box, bptr, bstr, V, swr, acc);
+    if (u + 2 < c.ub) {  // the slot is free once every lane has read it
+      __syncwarp();
+      fence_proxy_async_smem();
+      issue(u + 2);
+    }
   }
-  cp_async_wait<0>();  // the ring's trailing copies (re-reads of the last step) land before exit
 
   __syncthreads();  // the partial sums reuse the x^ region
   float* red = reinterpret_cast<float*>(smem);
@@ -1492,7 +1487,7 @@ size_t layout(Plan& pl, int pack, int B, int G, int K) {
   pl.sw_off = pl.vp_off + align256(static_cast<size_t>(ngr) * vp_row(B) * 4);
   pl.bar_off = pl.sw_off + align256(static_cast<size_t>(pl.rs) * pl.kl * (UT / G) * SLAB * 2);
   pl.ring_off = pl.bar_off + 256;
-  pl.smem = pl.ring_off + (pack == TQ_PACK_3BIT ? static_cast<size_t>(pl.rs) * pl.kl * kQ3RingBytes : 0);
+  pl.smem = pl.ring_off + (pack == TQ_PACK_3BIT ? static_cast<size_t>(pl.rs) * pl.kl * kQ3WarpRing : 0);
   return pl.smem;
 }
 
@@ -1978,6 +1973,11 @@ cudaError_t launch_pair(const tq_desc* d, PrepParams pp, Params prm, int B, int 
   prm.sw_off = static_cast<uint32_t>(pl.sw_off);
   prm.bar_off = static_cast<uint32_t>(pl.bar_off);
   prm.ring_off = static_cast<uint32_t>(pl.ring_off);
+  if (d->packing == TQ_PACK_3BIT &&
+      !make_tmap_2d(&prm.tm, prm.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<uint64_t>(prm.P),
+                    static_cast<uint64_t>(d->N), static_cast<uint64_t>(prm.P) * 4u, kQ3UnitWords, 64,
+                    CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
   prm.v8 = b3 && prm.P % 8 == 0 && reinterpret_cast<uintptr_t>(prm.codes) % 32 == 0 &&
            (!prm.chunks || prm.codes_estride % 8 == 0);
   cudaLaunchAttribute attr[2];
