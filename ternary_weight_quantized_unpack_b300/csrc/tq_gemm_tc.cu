@@ -436,6 +436,61 @@ __global__ void __launch_bounds__(kActThreads) fp8_act_kernel(const uint16_t* __
   }
 }
 
+// The same in one pass over the input: the row's transformed values wait in shared memory (K floats)
+// while the CTA takes the maximum; then each thread converts and stores 16 consecutive values.
+constexpr int kActSmemThreads = 512;
+__global__ void __launch_bounds__(kActSmemThreads) fp8_act_smem_kernel(const uint16_t* __restrict__ x,
+                                                                   uint8_t* __restrict__ xq, int* __restrict__ ea,
+                                                                   int K, int apply, int* status) {
+  extern __shared__ float4 xs4[];
+  __shared__ float red[kActSmemThreads / 32];
+  const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nblk = K / kFwhtBlock;
+  const uint16_t* xr = x + static_cast<size_t>(m) * K;
+  float mx = 0.f;
+  for (int blk = warp; blk < nblk; blk += kActSmemThreads / 32) {
+    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + blk * kFwhtBlock + 4 * lane));
+    float v[4] = {bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu)),
+                  bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16)),
+                  bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu)),
+                  bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16))};
+    if (apply) {
+      fwht128_warp(v);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) v[j] *= 0.08838834764831845f;
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[j]));
+    xs4[blk * (kFwhtBlock / 4) + lane] = make_float4(v[0], v[1], v[2], v[3]);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+  if (lane == 0) red[warp] = mx;
+  __syncthreads();
+  mx = red[0];
+#pragma unroll
+  for (int w = 1; w < kActSmemThreads / 32; ++w) mx = fmaxf(mx, red[w]);
+  if (!(mx <= 3.0e38f)) {  // inf or NaN in the row
+    if (threadIdx.x == 0) record_error(status, TQ_ERR_RANGE);
+    mx = 0.f;
+  }
+  const int e = row_exponent(mx);
+  if (threadIdx.x == 0) ea[m] = e;
+  uint4* out = reinterpret_cast<uint4*>(xq + static_cast<size_t>(m) * K);
+  for (int c = threadIdx.x; c < K / 16; c += kActSmemThreads) {
+    uint32_t o[4];
+#pragma unroll
+    for (int w = 0; w < 4; ++w) {
+      const float4 v = xs4[4 * c + w];
+      o[w] = static_cast<uint32_t>(to_e4m3(ldexpf(v.x, -e))) | (static_cast<uint32_t>(to_e4m3(ldexpf(v.y, -e))) << 8) |
+             (static_cast<uint32_t>(to_e4m3(ldexpf(v.z, -e))) << 16) |
+             (static_cast<uint32_t>(to_e4m3(ldexpf(v.w, -e))) << 24);
+    }
+    out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+  }
+}
+constexpr int kActSmemMaxK = 200 * 1024 / 4;  // K up to which the one-pass kernel is used
+
 // eb[n] from the row's scales (one thread per row).
 __global__ void fp8_wexp_kernel(const uint16_t* __restrict__ scales, int* __restrict__ eb, int N, int ng, int* status) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
@@ -457,41 +512,52 @@ __device__ __forceinline__ uint8_t signed_e4m3(int t, uint8_t pos) {
 // 2-bit: a warp takes 128 consecutive words (of the flattened [N][K/16] word grid), lane l the words
 // l + 32 q (q < 4): every load and every 16-byte store of the warp is one contiguous 128- / 512-byte
 // range, and each lane has four independent loads in flight.  A word is 16 weights of one group.
+// A byte of a code word (four 2-bit fields) becomes four output bytes through two tables built in
+// shared memory: nz (0xFF where t != 0) and neg (0x80 where t = -1); out = (nz & 4 x pos) | neg, pos
+// the E4M3 byte of +s * 2^-eb.
 constexpr int kF8WordsPerLane = 4;
 __global__ void __launch_bounds__(kDecThreads) decode_2b_f8_kernel(const uint32_t* __restrict__ codes,
                                                                    const uint16_t* __restrict__ scales,
                                                                    const int* __restrict__ eb, uint8_t* __restrict__ w,
                                                                    int N, int K, int P, int ng, int G) {
+  __shared__ uint32_t nz_t[256], neg_t[256];
+  {
+    const uint32_t b = threadIdx.x;  // kDecThreads == 256: one entry per thread
+    uint32_t nz = 0, ng8 = 0;
+#pragma unroll
+    for (int h = 0; h < 4; ++h) {
+      const uint32_t f = (b >> (2 * h)) & 3u;  // field 1 is t = 0, field 3 reads as t = 0
+      if (f == 0u || f == 2u) nz |= 0xFFu << (8 * h);
+      if (f == 0u) ng8 |= 0x80u << (8 * h);
+    }
+    nz_t[b] = nz;
+    neg_t[b] = ng8;
+  }
+  __syncthreads();
   const int wpr = K / 16;
-  const long long total = static_cast<long long>(N) * wpr;
-  const long long base = (static_cast<long long>(blockIdx.x) * blockDim.x + (threadIdx.x & ~31)) * kF8WordsPerLane +
-                         (threadIdx.x & 31);
+  const unsigned total = static_cast<unsigned>(N) * static_cast<unsigned>(wpr);  // < 2^31 (checked on the host)
+  const unsigned base = (blockIdx.x * blockDim.x + (threadIdx.x & ~31u)) * kF8WordsPerLane + (threadIdx.x & 31u);
   uint32_t word[kF8WordsPerLane];
   float sv[kF8WordsPerLane];
   int ev[kF8WordsPerLane];
 #pragma unroll
   for (int q = 0; q < kF8WordsPerLane; ++q) {
-    const long long i = min(base + 32 * q, total - 1);
-    const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
+    const unsigned i = min(base + 32u * q, total - 1u);
+    const unsigned n = i / static_cast<unsigned>(wpr), j = i - n * static_cast<unsigned>(wpr);
     word[q] = __ldg(codes + static_cast<size_t>(n) * P + j);
     sv[q] = __half2float(__ushort_as_half(__ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G)));
     ev[q] = __ldg(eb + n);
   }
 #pragma unroll
   for (int q = 0; q < kF8WordsPerLane; ++q) {
-    const long long i = base + 32 * q;
+    const unsigned i = base + 32u * q;
     if (i >= total) break;
-    const uint8_t pos = to_e4m3(ldexpf(sv[q], -ev[q]));
+    const uint32_t pos4 = static_cast<uint32_t>(to_e4m3(ldexpf(sv[q], -ev[q]))) * 0x01010101u;
     uint32_t o[4];
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
-      uint32_t v = 0;
-#pragma unroll
-      for (int h = 0; h < 4; ++h) {
-        const int d = static_cast<int>((word[q] >> (2 * (4 * c + h))) & 3u);
-        v |= static_cast<uint32_t>(signed_e4m3(d == 3 ? 0 : d - 1, pos)) << (8 * h);  // field 3 reads as t = 0
-      }
-      o[c] = v;
+      const uint32_t b = (word[q] >> (8 * c)) & 0xFFu;
+      o[c] = (nz_t[b] & pos4) | neg_t[b];
     }
     // word i of the flattened grid is weights 16 i .. 16 i + 15 of W (rows are K = 16 * wpr wide)
     *reinterpret_cast<uint4*>(w + 16 * static_cast<size_t>(i)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -657,7 +723,26 @@ cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint1
   int* ea = reinterpret_cast<int*>(wq + align256(static_cast<size_t>(N) * K));
   int* eb = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ea) + align256(static_cast<size_t>(M) * 4));
   int* status = status_ptr();
-  fp8_act_kernel<<<M, kActThreads, 0, s>>>(x, xq, ea, K, d->fwht_block != 0, status);
+  cudaError_t e;
+  if (K <= kActSmemMaxK) {
+    const size_t sm = static_cast<size_t>(K) * 4;
+    static std::map<int, size_t> attr_done;
+    static std::mutex attr_mu;
+    int dev = 0;
+    if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+    {
+      std::lock_guard<std::mutex> lock(attr_mu);
+      if (attr_done[dev] < sm) {
+        if ((e = cudaFuncSetAttribute(fp8_act_smem_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                      static_cast<int>(sm))) != cudaSuccess)
+          return e;
+        attr_done[dev] = sm;
+      }
+    }
+    fp8_act_smem_kernel<<<M, kActSmemThreads, sm, s>>>(x, xq, ea, K, d->fwht_block != 0, status);
+  } else {
+    fp8_act_kernel<<<M, kActThreads, 0, s>>>(x, xq, ea, K, d->fwht_block != 0, status);
+  }
   fp8_wexp_kernel<<<(N + 255) / 256, 256, 0, s>>>(scales, eb, N, ng, status);
   if (d->packing == TQ_PACK_2BIT) {
     const long long n = static_cast<long long>(N) * (K / 16);
@@ -669,7 +754,7 @@ cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint1
     decode_b3_f8_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(
         codes, scales, eb, wq, N, K, P, ng, G);
   }
-  cudaError_t e = cudaPeekAtLastError();
+  e = cudaPeekAtLastError();
   if (e != cudaSuccess) return e;
   CUtensorMap tm_x, tm_w;
   if (!make_tmap_2d(&tm_x, xq, CU_TENSOR_MAP_DATA_TYPE_UINT8, K, M, static_cast<uint64_t>(K), BK8, BM,

@@ -72,6 +72,7 @@ extern "C" tq_status tq_gemm_fp8(const tq_desc* d, const uint32_t* codes, const 
   tq_status st = check_linear_desc(d);
   if (st != TQ_OK) return st;
   if (M < 1) return TQ_ERR_INVALID_ARG;
+  if (static_cast<long long>(d->N) * (d->K / 16) >= (1ll << 31)) return TQ_ERR_UNSUPPORTED;  // decode index range
   if ((st = check_ptrs(codes, scales, x, y, workspace)) != TQ_OK) return st;
   if (workspace_bytes < tq_gemm_fp8_workspace_bytes(d, M)) return TQ_ERR_WORKSPACE;
   if (!status_ptr()) return TQ_ERR_CUDA;
