@@ -63,6 +63,12 @@ struct Smem {
 };
 constexpr size_t kSmemBytes = sizeof(Smem) + 1024;  // + alignment of the base to 1024
 
+// v * 2^e: one multiply by the exact power of two while 2^e is a normal float (one rounding only where
+// the product leaves the normal range, as ldexpf), ldexpf beyond.
+__device__ __forceinline__ float scale2(float v, int e) {
+  return e >= -126 && e <= 127 ? v * __int_as_float((127 + e) << 23) : ldexpf(v, e);
+}
+
 // Tile list of the grouped mode (tiles == nullptr: the plain M x N grid).
 struct GroupedTiles {
   const int4* tiles;  // {A row, valid rows, B row, output column}
@@ -86,12 +92,12 @@ __device__ __forceinline__ void tile_of(const GroupedTiles& gt, int t, int n_mt,
 }
 
 // F8: operands FP8 E4M3 (kind::f8f6f4), each row of x~ and of W under its own power-of-two factor
-// 2^ea[m] / 2^eb[n], which the epilogue applies exactly.
+// fa[m] = 2^ea[m] / fb[n] = 2^eb[n] (floats), which the epilogue applies as one exact power of two.
 template <bool F8>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap tm_x, const __grid_constant__ CUtensorMap tm_w, uint16_t* y,
-                   int M, int N, int K, int* status, const __grid_constant__ GroupedTiles gt, const int* ea,
-                   const int* eb) {
+                   int M, int N, int K, int* status, const __grid_constant__ GroupedTiles gt, const float* fa,
+                   const float* fb) {
   constexpr int BKE = F8 ? BK8 : BK;  // K elements per stage
   extern __shared__ uint8_t smem_raw[];
   Smem& sm = *reinterpret_cast<Smem*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -185,17 +191,17 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       tc_fence_after();
       const int m = m0 + 32 * q + lane;
-      const int eam = F8 && m < M ? ea[m] : 0;
+      const float fam = F8 && m < M ? fa[m] : 1.f;
 #pragma unroll 1
       for (int c = 0; c < BN; c += 32) {
         uint32_t v[32];
         tmem_ld<32>(tmem + (static_cast<uint32_t>(32 * q) << 16) + static_cast<uint32_t>(b * BN + c), v);
         tmem_wait_ld();
         const int n = n0 + c;
-        if (F8) {  // y = acc * 2^(ea[m] + eb[n]), exact
+        if (F8) {  // y = acc * (2^ea[m] * 2^eb[n]): the factor is an exact power of two, one rounding
 #pragma unroll
           for (int j = 0; j < 32; ++j)
-            v[j] = __float_as_uint(ldexpf(__uint_as_float(v[j]), eam + (n + j < N ? __ldg(eb + n + j) : 0)));
+            v[j] = __float_as_uint(__uint_as_float(v[j]) * (fam * (n + j < N ? __ldg(fb + n + j) : 1.f)));
         }
         if (gt.tiles) {
           if (32 * q + lane < rows) {
@@ -389,7 +395,7 @@ __device__ __forceinline__ uint8_t to_e4m3(float v) {
 // the E4M3 values of x~ * 2^-ea (the transform is recomputed in the second pass from the bf16 input).
 constexpr int kActThreads = 256;
 __global__ void __launch_bounds__(kActThreads) fp8_act_kernel(const uint16_t* __restrict__ x, uint8_t* __restrict__ xq,
-                                                              int* __restrict__ ea, int K, int apply, int* status) {
+                                                              float* __restrict__ fa, int K, int apply, int* status) {
   __shared__ float red[kActThreads / 32];
   const int m = blockIdx.x, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int nblk = K / kFwhtBlock;
@@ -425,13 +431,13 @@ __global__ void __launch_bounds__(kActThreads) fp8_act_kernel(const uint16_t* __
     mx = 0.f;
   }
   const int e = row_exponent(mx);
-  if (threadIdx.x == 0) ea[m] = e;
+  if (threadIdx.x == 0) fa[m] = ldexpf(1.f, e);
   for (int blk = warp; blk < nblk; blk += kActThreads / 32) {
     float v[4];
     block_values(blk, v);
     uint32_t o = 0;
 #pragma unroll
-    for (int j = 0; j < 4; ++j) o |= static_cast<uint32_t>(to_e4m3(ldexpf(v[j], -e))) << (8 * j);
+    for (int j = 0; j < 4; ++j) o |= static_cast<uint32_t>(to_e4m3(scale2(v[j], -e))) << (8 * j);
     *reinterpret_cast<uint32_t*>(xq + static_cast<size_t>(m) * K + blk * kFwhtBlock + 4 * lane) = o;
   }
 }
@@ -440,7 +446,7 @@ __global__ void __launch_bounds__(kActThreads) fp8_act_kernel(const uint16_t* __
 // while the CTA takes the maximum; then each thread converts and stores 16 consecutive values.
 constexpr int kActSmemThreads = 512;
 __global__ void __launch_bounds__(kActSmemThreads) fp8_act_smem_kernel(const uint16_t* __restrict__ x,
-                                                                   uint8_t* __restrict__ xq, int* __restrict__ ea,
+                                                                   uint8_t* __restrict__ xq, float* __restrict__ fa,
                                                                    int K, int apply, int* status) {
   extern __shared__ float4 xs4[];
   __shared__ float red[kActSmemThreads / 32];
@@ -448,20 +454,31 @@ __global__ void __launch_bounds__(kActSmemThreads) fp8_act_smem_kernel(const uin
   const int nblk = K / kFwhtBlock;
   const uint16_t* xr = x + static_cast<size_t>(m) * K;
   float mx = 0.f;
-  for (int blk = warp; blk < nblk; blk += kActSmemThreads / 32) {
-    const uint2 raw = __ldg(reinterpret_cast<const uint2*>(xr + blk * kFwhtBlock + 4 * lane));
-    float v[4] = {bf16_bits_to_float(static_cast<uint16_t>(raw.x & 0xffffu)),
-                  bf16_bits_to_float(static_cast<uint16_t>(raw.x >> 16)),
-                  bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu)),
-                  bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16))};
-    if (apply) {
-      fwht128_warp(v);
+  constexpr int kNWarps = kActSmemThreads / 32, kBatch = 8;  // a warp's blocks, 8 loads in flight at a time
+  for (int base = warp; base < nblk; base += kNWarps * kBatch) {
+    uint2 raw[kBatch];
 #pragma unroll
-      for (int j = 0; j < 4; ++j) v[j] *= 0.08838834764831845f;
+    for (int i = 0; i < kBatch; ++i) {
+      const int blk = base + kNWarps * i;
+      if (blk < nblk) raw[i] = __ldg(reinterpret_cast<const uint2*>(xr + blk * kFwhtBlock + 4 * lane));
     }
 #pragma unroll
-    for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[j]));
-    xs4[blk * (kFwhtBlock / 4) + lane] = make_float4(v[0], v[1], v[2], v[3]);
+    for (int i = 0; i < kBatch; ++i) {
+      const int blk = base + kNWarps * i;
+      if (blk >= nblk) break;
+      float v[4] = {bf16_bits_to_float(static_cast<uint16_t>(raw[i].x & 0xffffu)),
+                    bf16_bits_to_float(static_cast<uint16_t>(raw[i].x >> 16)),
+                    bf16_bits_to_float(static_cast<uint16_t>(raw[i].y & 0xffffu)),
+                    bf16_bits_to_float(static_cast<uint16_t>(raw[i].y >> 16))};
+      if (apply) {
+        fwht128_warp(v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] *= 0.08838834764831845f;
+      }
+#pragma unroll
+      for (int j = 0; j < 4; ++j) mx = fmaxf(mx, fabsf(v[j]));
+      xs4[blk * (kFwhtBlock / 4) + lane] = make_float4(v[0], v[1], v[2], v[3]);
+    }
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
@@ -475,16 +492,16 @@ __global__ void __launch_bounds__(kActSmemThreads) fp8_act_smem_kernel(const uin
     mx = 0.f;
   }
   const int e = row_exponent(mx);
-  if (threadIdx.x == 0) ea[m] = e;
+  if (threadIdx.x == 0) fa[m] = ldexpf(1.f, e);
   uint4* out = reinterpret_cast<uint4*>(xq + static_cast<size_t>(m) * K);
   for (int c = threadIdx.x; c < K / 16; c += kActSmemThreads) {
     uint32_t o[4];
 #pragma unroll
     for (int w = 0; w < 4; ++w) {
       const float4 v = xs4[4 * c + w];
-      o[w] = static_cast<uint32_t>(to_e4m3(ldexpf(v.x, -e))) | (static_cast<uint32_t>(to_e4m3(ldexpf(v.y, -e))) << 8) |
-             (static_cast<uint32_t>(to_e4m3(ldexpf(v.z, -e))) << 16) |
-             (static_cast<uint32_t>(to_e4m3(ldexpf(v.w, -e))) << 24);
+      o[w] = static_cast<uint32_t>(to_e4m3(scale2(v.x, -e))) | (static_cast<uint32_t>(to_e4m3(scale2(v.y, -e))) << 8) |
+             (static_cast<uint32_t>(to_e4m3(scale2(v.z, -e))) << 16) |
+             (static_cast<uint32_t>(to_e4m3(scale2(v.w, -e))) << 24);
     }
     out[c] = make_uint4(o[0], o[1], o[2], o[3]);
   }
@@ -492,7 +509,8 @@ __global__ void __launch_bounds__(kActSmemThreads) fp8_act_smem_kernel(const uin
 constexpr int kActSmemMaxK = 200 * 1024 / 4;  // K up to which the one-pass kernel is used
 
 // eb[n] from the row's scales (one thread per row).
-__global__ void fp8_wexp_kernel(const uint16_t* __restrict__ scales, int* __restrict__ eb, int N, int ng, int* status) {
+__global__ void fp8_wexp_kernel(const uint16_t* __restrict__ scales, int* __restrict__ eb, float* __restrict__ fb,
+                                int N, int ng, int* status) {
   const int n = blockIdx.x * blockDim.x + threadIdx.x;
   if (n >= N) return;
   float mx = 0.f;
@@ -501,7 +519,9 @@ __global__ void fp8_wexp_kernel(const uint16_t* __restrict__ scales, int* __rest
     record_error(status, TQ_ERR_RANGE);
     mx = 0.f;
   }
-  eb[n] = row_exponent(mx);
+  const int e = row_exponent(mx);
+  eb[n] = e;
+  fb[n] = ldexpf(1.f, e);
 }
 
 // E4M3 of +-s * 2^-eb: the byte for +s; -s flips the sign bit, t = 0 is the byte 0.
@@ -711,7 +731,7 @@ cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_
 
 size_t gemm_fp8_workspace_bytes(const tq_desc* d, int M) {
   return align256(static_cast<size_t>(M) * d->K) + align256(static_cast<size_t>(d->N) * d->K) +
-         align256(static_cast<size_t>(M) * 4) + align256(static_cast<size_t>(d->N) * 4);
+         align256(static_cast<size_t>(M) * 4) + 2 * align256(static_cast<size_t>(d->N) * 4);
 }
 
 cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint16_t* scales, const uint16_t* x, int M,
@@ -720,8 +740,9 @@ cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint1
   const int N = d->N, K = d->K, G = d->group, P = pitch_words(K, d->packing), ng = K / G;
   uint8_t* xq = static_cast<uint8_t*>(ws);
   uint8_t* wq = xq + align256(static_cast<size_t>(M) * K);
-  int* ea = reinterpret_cast<int*>(wq + align256(static_cast<size_t>(N) * K));
-  int* eb = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(ea) + align256(static_cast<size_t>(M) * 4));
+  float* fa = reinterpret_cast<float*>(wq + align256(static_cast<size_t>(N) * K));
+  int* eb = reinterpret_cast<int*>(reinterpret_cast<uint8_t*>(fa) + align256(static_cast<size_t>(M) * 4));
+  float* fb = reinterpret_cast<float*>(reinterpret_cast<uint8_t*>(eb) + align256(static_cast<size_t>(N) * 4));
   int* status = status_ptr();
   cudaError_t e;
   if (K <= kActSmemMaxK) {
@@ -739,11 +760,11 @@ cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint1
         attr_done[dev] = sm;
       }
     }
-    fp8_act_smem_kernel<<<M, kActSmemThreads, sm, s>>>(x, xq, ea, K, d->fwht_block != 0, status);
+    fp8_act_smem_kernel<<<M, kActSmemThreads, sm, s>>>(x, xq, fa, K, d->fwht_block != 0, status);
   } else {
-    fp8_act_kernel<<<M, kActThreads, 0, s>>>(x, xq, ea, K, d->fwht_block != 0, status);
+    fp8_act_kernel<<<M, kActThreads, 0, s>>>(x, xq, fa, K, d->fwht_block != 0, status);
   }
-  fp8_wexp_kernel<<<(N + 255) / 256, 256, 0, s>>>(scales, eb, N, ng, status);
+  fp8_wexp_kernel<<<(N + 255) / 256, 256, 0, s>>>(scales, eb, fb, N, ng, status);
   if (d->packing == TQ_PACK_2BIT) {
     const long long n = static_cast<long long>(N) * (K / 16);
     const long long per_cta = static_cast<long long>(kDecThreads) * kF8WordsPerLane;
@@ -765,7 +786,7 @@ cudaError_t launch_gemm_fp8(const tq_desc* d, const uint32_t* codes, const uint1
   if ((e = ensure_attr<true>()) != cudaSuccess) return e;
   const long long tiles = static_cast<long long>((M + BM - 1) / BM) * ((N + BN - 1) / BN);
   const unsigned grid = static_cast<unsigned>(std::min<long long>(tiles, sm_count()));
-  gemm_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status, GroupedTiles{}, ea, eb);
+  gemm_tc_kernel<true><<<grid, kThreads, kSmemBytes, s>>>(tm_x, tm_w, y, M, N, K, status, GroupedTiles{}, fa, fb);
   return cudaPeekAtLastError();
 }
 
