@@ -238,8 +238,8 @@ tq_status tq_moe_gemv(const tq_desc* gate_up, const tq_desc* down, int E, int to
                       void* workspace, size_t workspace_bytes, void* stream);
 
 /* ---- tq_moe_gemm: the same expert layer at prefill sizes (many tokens per expert) -------------------
- * Same computation, arguments and layouts as tq_moe_gemv (tantan.ink, "为什么 1.58bit 没变成乱码",
- * points 1-2), organised as a grouped tensor-core GEMM: the (token, slot) assignments are sorted by
+ * Same computation, arguments and layouts as tq_moe_gemv (the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B
+ * page, "为什么 1.58bit 没变成乱码", points 1-2), organised as a grouped tensor-core GEMM: the (token, slot) assignments are sorted by
  * expert, the tokens' block-transformed inputs are gathered in that order as FP16 (|x~| below 65504,
  * else TQ_ERR_RANGE), every expert's weights are decoded to FP16 s * t, one persistent tcgen05 launch
  * per projection walks a tile list over (expert, 128 sorted rows, 256 weight rows), silu(gate) * up

@@ -49,6 +49,12 @@ def test_invalid_descriptors():
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, packing=tq.TQ_PACK_3BIT), 17) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 100, packing=tq.TQ_PACK_3BIT), 1) == 0
     assert tq.tq_gemm_workspace_bytes(tq.desc(4, 128, packing=tq.TQ_PACK_3BIT), 16) == 0
+    # FP8 prefill: E4M3 operands (M x K, N x K bytes), per-row float factors of x, int exponents and
+    # float factors of W, each 256-byte aligned; 3-bit codes and a K off the 128-grid are refused
+    assert tq.tq_gemm_fp8_workspace_bytes(tq.desc(300, 1024), 77) == 77 * 1024 + 300 * 1024 + 512 + 2 * 1280
+    assert tq.tq_gemm_fp8_workspace_bytes(tq.desc(300, 1024, packing=tq.TQ_PACK_3BIT), 77) == 0
+    assert tq.tq_gemm_fp8_workspace_bytes(tq.desc(300, 1000), 77) == 0
+    assert tq.tq_gemm_fp8_workspace_bytes(tq.desc(300, 1024), 0) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 100), 1) == 0        # K not a multiple of 128
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128, group=32), 1) == 0
     assert tq.tq_gemv_workspace_bytes(tq.desc(4, 128), 17) == 0        # batch above 16
