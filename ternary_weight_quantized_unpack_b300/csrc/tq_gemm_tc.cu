@@ -253,10 +253,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 // 2-bit: one thread per word (16 trits, one group), two 16-byte stores.
 // base-3: one thread per 4 words (80 trits), digits by exact reciprocal multiplies.
 // ---------------------------------------------------------------------------------------------
-__device__ __forceinline__ uint16_t signed_scale(int t, uint16_t s) {
-  return t == 0 ? static_cast<uint16_t>(0) : (t > 0 ? s : static_cast<uint16_t>(s ^ 0x8000u));
-}
-
 // The output of a CTA's threads is one contiguous range of W (threads take consecutive words or quads
 // of consecutive rows), so each thread writes its 16-byte pieces into shared memory at their offset
 // in that range and the CTA then stores the range with consecutive lanes on consecutive 16 bytes:
@@ -270,11 +266,29 @@ __device__ __forceinline__ void flush_stage(const uint4* stage, uint16_t* w, lon
   for (int c = threadIdx.x; c < nchunks; c += blockDim.x) out[c] = stage[c];
 }
 
+// Pair tables: a pair of trits becomes two FP16 halves (t0 in the low half) as (mask & s2) ^ sign,
+// s2 = the scale in both halves: mask has 0xFFFF in a half whose trit is non-zero, sign 0x8000 (the
+// FP16 sign bit, flipped) in a half whose trit is -1.  2-bit: indexed by the pair's 4 code bits (field 3 reads as t = 0, as
+// tq_unpack reads it); base-3: by the pair's value d0 + 3 d1 (0..8, d = t + 1).
+__device__ __forceinline__ void pair_entry(int t0, int t1, uint32_t& mask, uint32_t& sign) {
+  mask = (t0 != 0 ? 0x0000FFFFu : 0u) | (t1 != 0 ? 0xFFFF0000u : 0u);
+  sign = (t0 < 0 ? 0x00008000u : 0u) | (t1 < 0 ? 0x80000000u : 0u);
+}
+
+// 2-bit: one thread per word (16 weights of one group), eight pairs, two 16-byte pieces.
 __global__ void __launch_bounds__(kDecThreads) decode_2b_kernel(const uint32_t* __restrict__ codes,
                                                                 const uint16_t* __restrict__ scales,
                                                                 uint16_t* __restrict__ w, int N, int K, int P, int ng,
                                                                 int G) {
   __shared__ uint4 stage[kDecThreads * 2];
+  __shared__ uint2 pairs[16];
+  if (threadIdx.x < 16) {
+    const int f0 = threadIdx.x & 3, f1 = threadIdx.x >> 2;
+    uint32_t m, sg;
+    pair_entry(f0 == 3 ? 0 : f0 - 1, f1 == 3 ? 0 : f1 - 1, m, sg);
+    pairs[threadIdx.x] = make_uint2(m, sg);
+  }
+  __syncthreads();
   const int wpr = K / 16;  // words with data per row
   const long long total = static_cast<long long>(N) * wpr;
   const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x;
@@ -284,14 +298,13 @@ __global__ void __launch_bounds__(kDecThreads) decode_2b_kernel(const uint32_t* 
   if (i < total) {
     const int n = static_cast<int>(i / wpr), j = static_cast<int>(i - static_cast<long long>(n) * wpr);
     const uint32_t word = __ldg(codes + static_cast<size_t>(n) * P + j);
-    const uint16_t s = __ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G);
+    const uint32_t s = __ldg(scales + static_cast<size_t>(n) * ng + (16 * j) / G);
+    const uint32_t s2 = s | (s << 16);
     uint32_t o[8];
 #pragma unroll
     for (int h = 0; h < 8; ++h) {
-      const int d0 = static_cast<int>((word >> (4 * h)) & 3u), d1 = static_cast<int>((word >> (4 * h + 2)) & 3u);
-      // a field of 3 is not a valid code: it decodes as t = 0, as tq_unpack reads it
-      const int t0 = d0 == 3 ? 0 : d0 - 1, t1 = d1 == 3 ? 0 : d1 - 1;
-      o[h] = static_cast<uint32_t>(signed_scale(t0, s)) | (static_cast<uint32_t>(signed_scale(t1, s)) << 16);
+      const uint2 e = pairs[(word >> (4 * h)) & 15u];
+      o[h] = (e.x & s2) ^ e.y;
     }
     stage[2 * threadIdx.x] = make_uint4(o[0], o[1], o[2], o[3]);
     stage[2 * threadIdx.x + 1] = make_uint4(o[4], o[5], o[6], o[7]);
@@ -299,80 +312,67 @@ __global__ void __launch_bounds__(kDecThreads) decode_2b_kernel(const uint32_t* 
   flush_stage(stage, w, base, end);
 }
 
-// base-3: one thread per 4 words (80 trits) of a row, digits by exact reciprocal multiplies.  With K a
-// multiple of 8 the quads' outputs are whole 16-byte pieces and go through the staging above; otherwise
-// each value is stored on its own.
+// base-3: one thread per 2 words (40 trits, 80 bytes of output) of a row; a pair of trits is the
+// word's value mod 9, taken by an exact reciprocal multiply.  K is a multiple of 8 here (the FWHT
+// block), so every piece and the row tail are whole 16-byte pieces and go through the staging above.
+constexpr int kB3DecWords = 2;
 __global__ void __launch_bounds__(kDecThreads) decode_b3_kernel(const uint32_t* __restrict__ codes,
                                                                 const uint16_t* __restrict__ scales,
                                                                 uint16_t* __restrict__ w, int N, int K, int P, int ng,
                                                                 int G) {
-  __shared__ uint4 stage[kDecThreads * 10];
-  const int qpr = K / 80;  // groups of 4 words (80 trits, 160 bytes of output) per row; K % 80 handled below
-  const int tail = K - qpr * 80;
-  const int per_row = qpr + (tail > 0 ? 1 : 0);
-  const long long total = static_cast<long long>(N) * per_row;
+  constexpr int kT = 20 * kB3DecWords;  // trits per thread
+  __shared__ uint4 stage[kDecThreads * (kT / 8)];
+  __shared__ uint2 pairs[9];
+  if (threadIdx.x < 9) {
+    uint32_t m, sg;
+    pair_entry(static_cast<int>(threadIdx.x % 3) - 1, static_cast<int>(threadIdx.x / 3) - 1, m, sg);
+    pairs[threadIdx.x] = make_uint2(m, sg);
+  }
+  __syncthreads();
+  const int ppr = (K + kT - 1) / kT;  // pieces per row
+  const long long total = static_cast<long long>(N) * ppr;
   const long long i0 = static_cast<long long>(blockIdx.x) * blockDim.x;
   const long long i = i0 + threadIdx.x;
-  auto out_of = [&](long long q) {  // first element of W that quad q writes
-    const long long n = q / per_row;
-    return n * K + 80 * (q - n * per_row);
+  auto out_of = [&](long long q) {  // first element of W that piece q writes
+    const long long n = q / ppr;
+    return n * K + static_cast<long long>(kT) * (q - n * ppr);
   };
-  const bool staged = (K & 7) == 0;
   const long long base = out_of(i0);
   const long long last = min(total, i0 + blockDim.x) - 1;
-  const long long end = out_of(last) + min(80, K - 80 * static_cast<int>(last % per_row));
+  const long long end = out_of(last) + min(kT, K - kT * static_cast<int>(last % ppr));
   if (i < total) {
-    const int n = static_cast<int>(i / per_row), j = static_cast<int>(i - static_cast<long long>(n) * per_row);
-    const int k0 = 80 * j, kn = min(80, K - k0);
+    const int n = static_cast<int>(i / ppr), j = static_cast<int>(i - static_cast<long long>(n) * ppr);
+    const int k0 = kT * j, kn = min(kT, K - k0);
     const uint16_t* srow = scales + static_cast<size_t>(n) * ng;
-    if (staged) {
-      uint32_t wv[4];
+    // the (at most two) groups the piece touches (groups are 64 or 128 >= 40), and where the second
+    // starts (relative to k0)
+    const int g0 = k0 / G;
+    const int b1 = (g0 + 1) * G - k0;
+    const uint32_t sa = __ldg(srow + g0);
+    const uint32_t sb = b1 < kn ? __ldg(srow + g0 + 1) : sa;
+    const uint32_t s2a = sa | (sa << 16), s2b = sb | (sb << 16);
+    uint32_t wv[kB3DecWords];
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) wv[wi] = 20 * wi < kn ? __ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi) : 0u;
-      // the (at most three) groups the 80 trits touch, and where the next two start (relative to k0)
-      const int g0 = k0 / G;
-      const int b1 = (g0 + 1) * G - k0, b2 = b1 + G;
-      const uint16_t sa = __ldg(srow + g0);
-      const uint16_t sb = b1 < kn ? __ldg(srow + g0 + 1) : sa;
-      const uint16_t sc = b2 < kn ? __ldg(srow + g0 + 2) : sb;
-      uint32_t o[40];
+    for (int wi = 0; wi < kB3DecWords; ++wi)
+      wv[wi] = 20 * wi < kn ? min(__ldg(codes + static_cast<size_t>(n) * P + kB3DecWords * j + wi), kB3Max) : kB3Zero;
+    uint4* st = stage + (out_of(i) - base) / 8;
 #pragma unroll
-      for (int wi = 0; wi < 4; ++wi) {
-        uint32_t v = min(wv[wi], kB3Max);
+    for (int c = 0; c < kT / 8; ++c) {
+      uint32_t o[4];
 #pragma unroll
-        for (int d = 0; d < 20; d += 2) {
-          const uint32_t q1 = __umulhi(v, 0xAAAAAAABu) >> 1;  // v / 3, exact for every 32-bit v
-          const int t0 = static_cast<int>(v - 3u * q1) - 1;
-          const uint32_t q2 = __umulhi(q1, 0xAAAAAAABu) >> 1;
-          const int t1 = static_cast<int>(q1 - 3u * q2) - 1;
-          v = q2;
-          const int k = 20 * wi + d;
-          // scale of trits k, k + 1 (group boundaries fall on even k: groups are 64 or 128)
-          const uint16_t sk = k < b1 ? sa : (k < b2 ? sb : sc);
-          o[k / 2] = static_cast<uint32_t>(signed_scale(t0, sk)) | (static_cast<uint32_t>(signed_scale(t1, sk)) << 16);
-        }
+      for (int h = 0; h < 4; ++h) {
+        const int pr = 4 * c + h;        // pair within the piece
+        const int wi = pr / 10;          // its word
+        const uint32_t v = wv[wi];
+        const uint32_t q = __umulhi(v, 0x38E38E39u) >> 1;  // v / 9, exact for every 32-bit v
+        wv[wi] = q;
+        const uint2 e = pairs[v - 9u * q];
+        o[h] = (e.x & (2 * pr < b1 ? s2a : s2b)) ^ e.y;
       }
-      uint4* st = stage + (out_of(i) - base) / 8;
-#pragma unroll
-      for (int c = 0; c < 10; ++c)
-        if (8 * c < kn) st[c] = make_uint4(o[4 * c], o[4 * c + 1], o[4 * c + 2], o[4 * c + 3]);
-    } else {
-      uint16_t* dst = w + static_cast<size_t>(n) * K + k0;
-      for (int wi = 0; wi < 4; ++wi) {
-        if (20 * wi >= kn) break;
-        uint32_t v = min(__ldg(codes + static_cast<size_t>(n) * P + 4 * j + wi), kB3Max);
-#pragma unroll
-        for (int d = 0; d < 20; ++d) {
-          const uint32_t qd = __umulhi(v, 0xAAAAAAABu) >> 1;
-          const int t = static_cast<int>(v - 3u * qd) - 1;
-          v = qd;
-          const int k = 20 * wi + d;
-          if (k < kn) dst[k] = signed_scale(t, __ldg(srow + (k0 + k) / G));
-        }
-      }
+      if (8 * c < kn) st[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
   }
-  if (staged) flush_stage(stage, w, base, end);
+  flush_stage(stage, w, base, end);
 }
 
 // ---------------------------------------------------------------------------------------------
@@ -533,8 +533,8 @@ __device__ __forceinline__ uint8_t signed_e4m3(int t, uint8_t pos) {
 // l + 32 q (q < 4): every load and every 16-byte store of the warp is one contiguous 128- / 512-byte
 // range, and each lane has four independent loads in flight.  A word is 16 weights of one group.
 // A byte of a code word (four 2-bit fields) becomes four output bytes through two tables built in
-// shared memory: nz (0xFF where t != 0) and neg (0x80 where t = -1); out = (nz & 4 x pos) | neg, pos
-// the E4M3 byte of +s * 2^-eb.
+// shared memory: nz (0xFF where t != 0) and neg (0x80 where t = -1); out = (nz & 4 x pos) ^ neg, pos
+// the E4M3 byte of s * 2^-eb (the sign bit flips for t = -1, whatever the sign of s).
 constexpr int kF8WordsPerLane = 4;
 __global__ void __launch_bounds__(kDecThreads) decode_2b_f8_kernel(const uint32_t* __restrict__ codes,
                                                                    const uint16_t* __restrict__ scales,
@@ -577,7 +577,7 @@ __global__ void __launch_bounds__(kDecThreads) decode_2b_f8_kernel(const uint32_
 #pragma unroll
     for (int c = 0; c < 4; ++c) {
       const uint32_t b = (word[q] >> (8 * c)) & 0xFFu;
-      o[c] = (nz_t[b] & pos4) | neg_t[b];
+      o[c] = (nz_t[b] & pos4) ^ neg_t[b];
     }
     // word i of the flattened grid is weights 16 i .. 16 i + 15 of W (rows are K = 16 * wpr wide)
     *reinterpret_cast<uint4*>(w + 16 * static_cast<size_t>(i)) = make_uint4(o[0], o[1], o[2], o[3]);
@@ -673,7 +673,7 @@ cudaError_t launch_gemm(const tq_desc* d, const uint32_t* codes, const uint16_t*
     const long long n = static_cast<long long>(N) * (K / 16);
     decode_2b_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
   } else {
-    const long long n = static_cast<long long>(N) * ((K + 79) / 80);
+    const long long n = static_cast<long long>(N) * ((K + 20 * kB3DecWords - 1) / (20 * kB3DecWords));
     decode_b3_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, wa, N, K, P, ng, G);
   }
   if ((e = cudaPeekAtLastError()) != cudaSuccess) return e;
@@ -723,7 +723,7 @@ cudaError_t launch_decode(const tq_desc* d, const uint32_t* codes, const uint16_
     const long long n = static_cast<long long>(N) * (K / 16);
     decode_2b_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, w, N, K, P, ng, G);
   } else {
-    const long long n = static_cast<long long>(N) * ((K + 79) / 80);
+    const long long n = static_cast<long long>(N) * ((K + 20 * kB3DecWords - 1) / (20 * kB3DecWords));
     decode_b3_kernel<<<static_cast<unsigned>((n + kDecThreads - 1) / kDecThreads), kDecThreads, 0, s>>>(codes, scales, w, N, K, P, ng, G);
   }
   return cudaPeekAtLastError();

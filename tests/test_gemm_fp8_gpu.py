@@ -151,3 +151,14 @@ def test_matches_fp16_path_closely():
     y16 = tq.tq_gemm(case.desc, case.codes, case.scales, case.x).float().cpu().numpy()
     r = refs(case)
     assert (np.abs(y8 - y16) <= r["bound"] + ACC * r["Aq"] + 2e-3 * r["A"] + 1e-30).all()
+
+
+@pytest.mark.parametrize("packing", [B2, B3])
+def test_negative_scales(packing):
+    """Negative FP16 scales (the E4M3 sign bit flips for t = -1 whatever the scale's sign)."""
+    case = LinearCase(36, 8, 200, 1024, 64, packing, 64, fwht_block=0)
+    case.scales[:, 1::2] = -case.scales[:, 1::2]
+    yg = run(case)
+    t, _ = case.host_rows(np.arange(case.N))
+    check(yg, refs_with_scales(case, case.scales.cpu().numpy(), t), False)
+

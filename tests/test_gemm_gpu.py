@@ -84,3 +84,17 @@ def test_out_of_fp16_range_is_reported():
     case2 = LinearCase(23, 5, 128, 512, 128, B2, 64)
     y_ref, A = case2.oracle()
     check_bf16(run(case2), y_ref, A)
+
+
+@pytest.mark.parametrize("packing", [B2, B3])
+def test_negative_scales(packing):
+    """FP16 scales of either sign (the decode flips the sign bit for t = -1): every other group negated."""
+    import oracle as O
+    case = LinearCase(24, 5, 136, 1280, 64, packing, 96)
+    case.scales[:, ::2] = -case.scales[:, ::2]
+    y = run(case)
+    t, _ = case.host_rows(np.arange(case.N))
+    y_ref, A, _ = O.ternary_linear(O.pack(t, packing), case.scales.cpu().numpy(), case.x_host.float().numpy(),
+                                   case.K, case.group, packing, 128)
+    check_bf16(y, y_ref, A)
+
