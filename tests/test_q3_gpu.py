@@ -126,3 +126,19 @@ def test_unsupported_elsewhere():
     assert tq.tq_gemv_kernel_count(d, 1) == 2
     assert tq.tq_gemv_kernel_count(d, 17) == -1
     assert tq.tq_gemm_workspace_bytes(d, 64) == 0
+
+
+def test_gemv_wide_output_sampled():
+    """The wide-output 3-bit shape the bench times (131072 x 2048, lm_head-like): rows sampled across
+    the whole output (the first and last 2048 and two chunks between), batch 1 and 3."""
+    for batch in (1, 3):
+        c = Q3Case(77, batch, 131072, 2048, 128, batch)
+        y = tq.tq_gemv(c.desc, c.codes, c.scales, c.x)
+        torch.cuda.synchronize()
+        assert tq.tq_device_status() == 0
+        yh = y.cpu().numpy()
+        for r0 in (0, 40960, 90112, 131072 - 2048):
+            rows = np.arange(r0, r0 + 2048)
+            y_ref, A = c.oracle(rows)
+            check_tolerance(yh[:, rows], y_ref, A, what=f"rows {r0}..")
+
