@@ -1797,12 +1797,12 @@ bool codes_tmap(const uint32_t* codes, int N, int P, int BR, CUtensorMap* out) {
 
 // The stream kernel's plan for a shape on the current device (cached), or !ok when it does not apply.
 cudaError_t choose_stream_plan(const tq_desc* d, int B, SPlan* out) {
-  static std::map<std::tuple<int, int, int, int, int>, SPlan> cache;
+  static std::map<std::tuple<int, int, int, int, int, int>, SPlan> cache;  // per packing: only 2-bit streams
   static std::mutex mu;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  const auto key = std::make_tuple(d->N, d->K, d->group, B, dev);
+  const auto key = std::make_tuple(d->N, d->K, d->group, B, dev, d->packing);
   {
     std::lock_guard<std::mutex> lock(mu);
     auto it = cache.find(key);

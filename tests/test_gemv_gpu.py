@@ -196,3 +196,29 @@ def test_stacked_projections_graph_replayed_every_output(packing, batch):
             y_ref, A = c.oracle(rows)
             check_tolerance(yh[:, rows], y_ref, A, what=f"N={c.N} rows {r0}..")
     assert torch.equal(y_again, ys[0])
+
+
+def test_same_shape_every_packing_in_one_process():
+    """A 2-bit call, then base-3 and 3-bit calls of the same shape and batch in the same process: each
+    packing takes its own kernel (the work-split caches are per packing) and matches the oracle."""
+    import oracle as O
+    N, K, B = 2048, 5120, 1
+    for packing in (tq.TQ_PACK_2BIT, tq.TQ_PACK_B3):
+        case = LinearCase(61, packing, N, K, 128, packing, B)
+        y = tq.tq_gemv(case.desc, case.codes, case.scales, case.x)
+        torch.cuda.synchronize()
+        assert tq.tq_device_status() == 0
+        y_ref, A = case.oracle()
+        check_tolerance(y.cpu().numpy(), y_ref, A, what=f"packing {packing}")
+    q = inputs.codes3(61, 3, N, K)
+    d3 = tq.desc(N, K, 128, tq.TQ_PACK_3BIT)
+    s3 = inputs.scales(61, 4, N, K // 128)
+    x3 = inputs.activations(61, 5, B, K)
+    y3 = tq.tq_gemv(d3, tq.tq_pack(d3, q.cuda()), s3.cuda(), x3.cuda())
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    y_ref, A, _ = O.ternary_linear(O.pack(q.numpy(), O.PACK_3BIT), s3.numpy(), x3.float().numpy(), K, 128,
+                                   O.PACK_3BIT)
+    check_tolerance(y3.cpu().numpy(), y_ref, A, what="3-bit")
+    assert tq.tq_gemv_kernel_count(d3, B) == 2
+
