@@ -50,9 +50,7 @@ namespace seq {
 using namespace sm100;
 
 constexpr int kNW = 12;                        // warps per CTA
-// Ring stages per warp: three while the batch is small, two when the staging of eight batch rows needs
-// the shared memory.
-__host__ __device__ constexpr int ring_depth(int Bp) { return Bp <= 2 ? 3 : 2; }
+constexpr int kD = 3;                          // ring stages per warp
 constexpr int kGatherKu = 12;                  // partial sums one thread adds in one go
 constexpr int kRows = 32;                      // rows per item: two 16-row MMA slabs
 constexpr int kItemTrits = 512;                // trits per item along K: 32 code words of a row
@@ -94,8 +92,7 @@ struct Params {
   size_t part_stride;     // floats per parity of part
   int ssq_stride;         // floats per parity of ssq
   int nkc;                // K slices one CTA may cover (x^ capacity)
-  int stage_floats;       // capacity of the gather staging buffer
-  uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc, off_stage;
+  uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc;
 };
 
 // ---- static work split (K-major) ---------------------------------------------------------------
@@ -111,14 +108,13 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 }
 
 // Grid barrier number k (after call k), in two halves so that work that does not depend on it can
-// run in between: grid_arrive (every thread; thread 0 arrives once this CTA's writes are visible) and
-// grid_wait (every thread; thread 0 waits until every CTA has arrived, false if limit_ns passed first).
+// run in between: grid_arrive (every thread; after a CTA barrier, thread 0 adds one with release
+// semantics, so every write of the CTA before the barrier is visible to a thread that acquires the
+// count) and grid_wait (every thread; thread 0 waits with acquire loads until every CTA has arrived,
+// false if limit_ns passed first).
 __device__ __forceinline__ void grid_arrive(unsigned* sync) {
   __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    atomicAdd(sync, 1u);
-  }
+  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sync) : "memory");
 }
 __device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag, uint64_t limit_ns = kWaitNs) {
   if (threadIdx.x == 0) {
@@ -134,13 +130,13 @@ __device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag,
         }
       }
     }
-    __threadfence();
   }
-  __syncthreads();
+  __syncthreads();  // the acquire above and this barrier order every thread's later reads
   return *flag != 0;
 }
 
-// Ready flags: CTA c stores j + 1 in flags[c] (release) once its rows of call j's output are final.
+// Ready flags: CTA c stores j + 1 in flags[c] (release, after a CTA barrier) once its rows of call
+// j's output are final.
 constexpr int kFlagBase = 64;  // flags start at this word of the sync area
 __device__ __forceinline__ void st_release(unsigned* p, unsigned v) {
   asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
@@ -150,90 +146,75 @@ __device__ __forceinline__ void fin_rows(int N, int c, int grid, int& fr0, int& 
   fr0 = (c * (N / 4)) / grid * 4;
   fr1 = ((c + 1) * (N / 4)) / grid * 4;
 }
-// Every thread t < grid whose CTA finalized any of the rows [r0[sg], r0[sg] + nr[sg]) of call pc
-// waits (bounded) for that CTA's flag to reach `want`; then the CTA synchronises.  False on timeout.
-__device__ __forceinline__ bool wait_rows_ready(const unsigned* flags, const CallLite& pc, int nseg, const int (&r0)[3],
-                                                const int (&nr)[3], unsigned want, int* flag) {
-  if (threadIdx.x == 0) *flag = 1;
-  __syncthreads();
-  const int grid = static_cast<int>(gridDim.x);
-  for (int t = threadIdx.x; t < grid; t += blockDim.x) {
-    int fr0, fr1;
-    fin_rows(pc.N, t, grid, fr0, fr1);
-    bool need = false;
-    for (int sg = 0; sg < nseg; ++sg) need = need || (fr0 < r0[sg] + nr[sg] && r0[sg] < fr1);
-    if (!need || ld_acquire(flags + t) >= want) continue;
-    const uint64_t t0 = global_timer_ns();
-    for (uint32_t i = 0;; ++i) {
-      if (ld_acquire(flags + t) >= want) break;
-      if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) {
-        *flag = 0;
-        break;
-      }
-    }
+// The CTA whose fin_rows range holds row r (a multiple of 4): the least c with r < fr1(c).
+__device__ __forceinline__ int fin_owner(int N, int grid, int r) {
+  return static_cast<int>((static_cast<long long>(r / 4 + 1) * grid - 1) / (N / 4));
+}
+// One thread waits (bounded) until a ready flag reaches `want`; its later loads are ordered after the
+// acquire.  False on timeout.
+__device__ __forceinline__ bool wait_flag(const unsigned* flag, unsigned want) {
+  if (ld_acquire(flag) >= want) return true;
+  const uint64_t t0 = global_timer_ns();
+  for (uint32_t i = 0;; ++i) {
+    if (ld_acquire(flag) >= want) return true;
+    if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) return false;
   }
-  __threadfence();
-  __syncthreads();
-  return *flag != 0;
 }
 
-// ---- reading a previous call's output ---------------------------------------------------------
-// Its output scale for batch row b: 1 / rms of its own input (RMS mode), else 1.  One warp; the sum
-// of the per-block sums of squares is taken in a fixed order, so every CTA gets the same bits.
-__device__ __forceinline__ float out_scale_warp(const CallLite& c, const float* ssq, int Bp, int b, int lane) {
-  if (c.mode != 3) return 1.f;
-  float t = 0.f;
+// ---- finalizing a call's output rows -------------------------------------------------------------
+// Output scale of an RMS-mode call for batch row b (1 / rms of its own input), for the lane's b; one
+// warp, every batch row's loads in flight together.  The per-block sums of squares are added in a
+// fixed order, so every warp gets the same bits.
+template <int BP>
+__device__ __forceinline__ float out_scale_warp(const CallLite& c, const float* ssq, int B, int b, int lane) {
+  float t[BP];
+#pragma unroll
+  for (int bb = 0; bb < BP; ++bb) t[bb] = 0.f;
   const int nblk = c.K / kFwhtBlock;
-  for (int k = lane; k < nblk; k += 32) t += __ldcg(ssq + k * Bp + b);
-  t = warp_sum(t);
-  return rsqrtf(t / static_cast<float>(c.K) + kRmsEps);
-}
-
-// ---- gathering a finished call's output --------------------------------------------------------
-// Segments are stored one after another: segment sg starts after the rows of the segments before it.
-__host__ __device__ __forceinline__ int seg_offset(const int (&nr)[3], int Bp, int sg) {
-  int o = 0;
-  for (int i = 0; i < sg; ++i) o += nr[i];
-  return o * Bp;
-}
-
-// Rows [r0[sg], r0[sg] + nr[sg]) (multiples of 4) of the finished call pc, for every batch row, are
-// summed from its K slices' partial sums into the staging buffer: segment sg, 4-row chunk c4, batch
-// row b at float4 index c4 * Bp + b.  A group of NSP adjacent lanes shares one chunk: lane s adds the
-// slices [s * per, (s + 1) * per) (all its loads issued before the adds), then the group combines
-// its sums by a fixed butterfly.  The result does not depend on which CTA computes it, and the whole
-// gather costs about one L2 round trip.
-__device__ __forceinline__ void gather(const CallLite& pc, const float* ppart, int B, int Bp, int nseg,
-                                       const int (&r0)[3], const int (&nr)[3], float* stage, int nthreads) {
-  int nsp = 1;
-  while (nsp * kGatherKu < pc.nku) nsp <<= 1;  // lanes per chunk (a power of two up to 32)
-  const int per = (pc.nku + nsp - 1) / nsp;    // slices per lane (<= kGatherKu)
-  const size_t step = static_cast<size_t>(pc.nru) * Bp * kRows;
-  int items[3], total = 0;
-  for (int sg = 0; sg < 3; ++sg) {
-    items[sg] = sg < nseg ? (nr[sg] / 4) * B : 0;
-    total += items[sg];
+  for (int k = lane; k < nblk; k += 32)
+#pragma unroll
+    for (int bb = 0; bb < BP; ++bb)
+      if (bb < B) t[bb] += __ldcg(ssq + k * BP + bb);
+  float sc = 1.f;
+#pragma unroll
+  for (int bb = 0; bb < BP; ++bb) {
+    const float x = rsqrtf(warp_sum(t[bb]) / static_cast<float>(c.K) + kRmsEps);
+    if (bb == b) sc = x;
   }
+  return sc;
+}
+
+// Rows [fr0, fr0 + nr) (multiples of 4) of call c, for every batch row: the K slices' partial sums
+// added in ku order, times the output scale, stored to y.  A group of nsp adjacent lanes shares one
+// 4-row chunk: lane s adds the slices [s * per, (s + 1) * per) (all its loads issued before the
+// adds), then the group combines its sums by a fixed butterfly.  The result does not depend on which
+// CTA computes it, and the partial sums and the sums of squares of the scale are in flight together.
+template <int BP>
+__device__ __forceinline__ void finalize(const CallLite& c, const float* ppart, const float* ssq, int B, int fr0,
+                                         int nr) {
+  const int lane = static_cast<int>(threadIdx.x & 31);
+  int nsp = 1;
+  while (nsp * kGatherKu < c.nku) nsp <<= 1;  // lanes per chunk (a power of two up to 32)
+  const int per = (c.nku + nsp - 1) / nsp;    // slices per lane (<= kGatherKu)
+  const size_t step = static_cast<size_t>(c.nru) * BP * kRows;
+  const int total = (nr / 4) * B;
   const int nthr = (total * nsp + 31) & ~31;  // whole warps, so every lane takes part in the shuffles
-  if (static_cast<int>(threadIdx.x) >= nthreads) return;
-  for (int t = threadIdx.x; t < nthr; t += nthreads) {
-    const int s = t % nsp;
-    int u = t / nsp, sg = 0;
+  for (int t = threadIdx.x; t < nthr; t += blockDim.x) {
+    const int s = t % nsp, u = t / nsp;
     const bool valid = u < total;
-    if (valid)
-      while (u >= items[sg]) u -= items[sg++];
     const int b = valid ? u % B : 0, c4 = valid ? u / B : 0;
-    const int k = r0[sg] + 4 * c4;
-    const float* p0 = ppart + (static_cast<size_t>(k >> 5) * Bp + b) * kRows + (k & 31);
+    const int k = fr0 + 4 * c4;
+    const float* p0 = ppart + (static_cast<size_t>(k >> 5) * BP + b) * kRows + (k & 31);
     const int ku0 = s * per;
     float4 v[kGatherKu];
 #pragma unroll
     for (int i = 0; i < kGatherKu; ++i)
-      if (valid && i < per && ku0 + i < pc.nku) v[i] = __ldcg(reinterpret_cast<const float4*>(p0 + (ku0 + i) * step));
+      if (valid && i < per && ku0 + i < c.nku) v[i] = __ldcg(reinterpret_cast<const float4*>(p0 + (ku0 + i) * step));
+    const float sc = c.mode == 3 ? out_scale_warp<BP>(c, ssq, B, b, lane) : 1.f;
     float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
     for (int i = 0; i < kGatherKu; ++i)
-      if (valid && i < per && ku0 + i < pc.nku) {
+      if (valid && i < per && ku0 + i < c.nku) {
         a.x += v[i].x;
         a.y += v[i].y;
         a.z += v[i].z;
@@ -245,32 +226,9 @@ __device__ __forceinline__ void gather(const CallLite& pc, const float* ppart, i
       a.z += __shfl_xor_sync(0xffffffffu, a.z, m);
       a.w += __shfl_xor_sync(0xffffffffu, a.w, m);
     }
-    if (valid && s == 0) reinterpret_cast<float4*>(stage + seg_offset(nr, Bp, sg))[c4 * Bp + b] = a;
-  }
-}
-
-// Rows k..k+3 of the staging segment at soff (k relative to the segment start, a multiple of 4),
-// batch row b.
-__device__ __forceinline__ float4 in_row4(const float* stage, int soff, int Bp, int b, int k, float scale) {
-  float4 a = reinterpret_cast<const float4*>(stage + soff)[(k / 4) * Bp + b];
-  a.x *= scale;
-  a.y *= scale;
-  a.z *= scale;
-  a.w *= scale;
-  return a;
-}
-
-// Rows [r0[sg], r0[sg] + nr[sg]) (multiples of 4) of the finished call pc's final output, for every
-// batch row, into the staging buffer in the layout gather() writes.
-__device__ __forceinline__ void load_rows(const CallLite& pc, int B, int Bp, int nseg, const int (&r0)[3],
-                                          const int (&nr)[3], float* stage) {
-  for (int sg = 0; sg < nseg; ++sg) {
-    float4* dst = reinterpret_cast<float4*>(stage + seg_offset(nr, Bp, sg));
-    const int n4 = (nr[sg] / 4) * B;
-    for (int t = threadIdx.x; t < n4; t += blockDim.x) {
-      const int b = t % B, c4 = t / B;
-      dst[c4 * Bp + b] = __ldcg(reinterpret_cast<const float4*>(pc.y + static_cast<size_t>(b) * pc.N + r0[sg] + 4 * c4));
-    }
+    if (valid && s == 0)
+      *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + k) =
+          make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
   }
 }
 
@@ -310,12 +268,27 @@ struct LaneLayout {
 };
 
 // x^ and V / F of one 128-block (absolute index blk, local group index lg0 of its first group) for
-// all batch rows; one warp.  ssq: RMS mode, where the block's sums of squares go (global).
+// all batch rows; one warp.  Modes other than 0 read the previous call pc's final output: the CTAs
+// that finalized the block's 128 rows (SwiGLU: and the 128 matching rows of the up half) form one
+// or two contiguous ranges; one lane per CTA waits (bounded) for its flag, raising *abort on timeout,
+// and the warp barrier then orders every lane's reads after those acquires.  ssq: RMS mode, where
+// the block's sums of squares go (global).
 template <int G, int BP>
-__device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, const float* stage, int krow0, int krow_n, const float (&pscale)[BP], int blk, int lg0,
-                                           const LaneLayout<G>& L, uint8_t* xh, float* V, float* Fv, float* ssq,
-                                           int lane) {
+__device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, const CallLite& pc, unsigned want,
+                                           int* abort, int blk, int lg0, const LaneLayout<G>& L, uint8_t* xh,
+                                           float* V, float* Fv, float* ssq, int lane) {
   const int k0 = blk * kFwhtBlock + 4 * lane;
+  if (c.mode != 0) {
+    const unsigned* flags = p.sync + kFlagBase;
+    const int grid = static_cast<int>(gridDim.x), kb = blk * kFwhtBlock;
+    const int lo = fin_owner(pc.N, grid, kb), n1 = fin_owner(pc.N, grid, kb + kFwhtBlock - 4) - lo + 1;
+    const int lo2 = c.mode == 2 ? fin_owner(pc.N, grid, c.K + kb) : 0;
+    const int n2 = c.mode == 2 ? fin_owner(pc.N, grid, c.K + kb + kFwhtBlock - 4) - lo2 + 1 : 0;
+    bool ok = true;
+    for (int i = lane; i < n1 + n2; i += 32) ok = wait_flag(flags + (i < n1 ? lo + i : lo2 + i - n1), want) && ok;
+    if (!ok) *abort = 1;
+    __syncwarp();
+  }
   float v[BP][4];
 #pragma unroll
   for (int b = 0; b < BP; ++b) {
@@ -328,14 +301,15 @@ __device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, c
       v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
       v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
     } else if (c.mode == 2) {
-      const float4 g4 = in_row4(stage, 0, BP, b, k0 - krow0, pscale[b]);
-      const float4 u4 = in_row4(stage, krow_n * BP, BP, b, k0 - krow0, pscale[b]);
+      const float* yb = pc.y + static_cast<size_t>(b) * pc.N;
+      const float4 g4 = __ldcg(reinterpret_cast<const float4*>(yb + k0));
+      const float4 u4 = __ldcg(reinterpret_cast<const float4*>(yb + c.K + k0));
       v[b][0] = silu_f(g4.x) * u4.x;
       v[b][1] = silu_f(g4.y) * u4.y;
       v[b][2] = silu_f(g4.z) * u4.z;
       v[b][3] = silu_f(g4.w) * u4.w;
     } else {
-      const float4 a = in_row4(stage, 0, BP, b, k0 - krow0, pscale[b]);
+      const float4 a = __ldcg(reinterpret_cast<const float4*>(pc.y + static_cast<size_t>(b) * pc.N + k0));
       v[b][0] = a.x, v[b][1] = a.y, v[b][2] = a.z, v[b][3] = a.w;
     }
   }
@@ -407,7 +381,6 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   constexpr int CPG = GPI < 8 / BP ? GPI : 8 / BP;  // groups per accumulation cycle
   constexpr int NCYC = GPI / CPG;
   constexpr int BPI = kItemTrits / kFwhtBlock;     // 128-blocks per item
-  constexpr int kD = ring_depth(BP);
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
@@ -416,14 +389,12 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   uint8_t* codes_st = smem + static_cast<size_t>(warp) * kD * kCodeStage;
   const uint16_t* scales_st = reinterpret_cast<const uint16_t*>(smem + p.off_scales) + warp * kD * (kScaleStage / 2);
   uint8_t* scales_w = smem + p.off_scales + static_cast<size_t>(warp) * kD * kScaleStage;
-  float* stage = reinterpret_cast<float*>(smem + p.off_stage);
   uint8_t* xh = smem + p.off_xh;
   const uint8_t* zero = smem + p.off_zero;
   float* V = reinterpret_cast<float*>(smem + p.off_v);
   float* Fv = reinterpret_cast<float*>(smem + p.off_f);
   uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar) + warp * kD;
   int* s_flag = reinterpret_cast<int*>(smem + p.off_misc);  // [0] abort, [1] barrier result
-  float* s_scale = reinterpret_cast<float*>(s_flag + 8);     // [8] output scale of the previous call
 
   for (uint32_t i = threadIdx.x; i < 64; i += blockDim.x) reinterpret_cast<uint32_t*>(smem + p.off_zero)[i] = 0u;
   const int vcap = (p.nkc * GPI + 8) * BP;
@@ -486,9 +457,6 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
 
   bool abort = false;
   const LaneLayout<G> L(lane);
-  float ones[BP];
-#pragma unroll
-  for (int b = 0; b < BP; ++b) ones[b] = 1.f;
   unsigned nbar = 0;  // grid barriers passed
   for (int j = 0; j < p.ncalls && !abort; ++j) {
     const CallLite c(p.calls[j]);
@@ -503,29 +471,21 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       ku_lo = ca / c.nru;
       if (cb > ca) ku_hi = (cb - 1) / c.nru;
     }
-    const int krow0 = ku_lo * kItemTrits;                                       // first input row needed
-    const int nkrow = ku_hi >= ku_lo ? min((ku_hi + 1) * kItemTrits, c.K) - krow0 : 0;
-    // ---- the input rows this CTA needs: the previous call's final output ----
-    if (j > 0 && c.mode != 0 && nkrow > 0) {
-      const int r0[3] = {krow0, c.K + krow0, 0}, nr[3] = {nkrow, c.mode == 2 ? nkrow : 0, 0};
-      if (!wait_rows_ready(p.sync + kFlagBase, pc, c.mode == 2 ? 2 : 1, r0, nr, static_cast<unsigned>(j),
-                           s_flag + 1)) {
-        if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
-        abort = true;
-        break;
-      }
-      load_rows(pc, p.B, BP, c.mode == 2 ? 2 : 1, r0, nr, stage);
-    }
-    __syncthreads();
-    // ---- input transform of this CTA's K slices ----
+    // ---- input transform of this CTA's K slices (reading the previous call's final output as each
+    //      warp's rows become ready) ----
     if (cb > ca) {
       const int blk0 = ku_lo * BPI;
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
-        prep_block<G, BP>(p, c, stage, krow0, nkrow, ones, blk, (blk - blk0) * (kFwhtBlock / G), L, xh, V, Fv,
-                          ssq, lane);
+        prep_block<G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G), L, xh,
+                          V, Fv, ssq, lane);
     }
     __syncthreads();
+    if (s_flag[0] != 0) {  // a ready flag did not come in time
+      if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      abort = true;
+      break;
+    }
 
     // ---- this warp's items ----
     int wa = 0, wb = 0;
@@ -708,32 +668,15 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       break;
     }
     // ---- this CTA's share of the call's output rows: partial sums in ku order, times the output
-    //      scale (the last warp forms the scale while the others add) ----
+    //      scale ----
     {
-      if (warp == kNW - 1) {
-#pragma unroll
-        for (int b = 0; b < BP; ++b) {
-          const float sc = b < p.B ? out_scale_warp(c, ssq, BP, b, lane) : 1.f;
-          if (lane == 0) s_scale[b] = sc;
-        }
-      }
       int fr0, fr1;
       fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
-      const int r0[3] = {fr0, 0, 0}, nr[3] = {fr1 - fr0, 0, 0};
-      gather(c, part, p.B, BP, 1, r0, nr, stage, (kNW - 1) * 32);
-      __syncthreads();
-      for (int e = threadIdx.x; e < (fr1 - fr0) / 4 * p.B; e += blockDim.x) {
-        const int b = e % p.B, k = 4 * (e / p.B);
-        *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + fr0 + k) =
-            in_row4(stage, 0, BP, b, k, s_scale[b]);
-      }
+      finalize<BP>(c, part, ssq, p.B, fr0, fr1 - fr0);
     }
     // ---- this CTA's rows are final: raise its flag ----
     __syncthreads();
-    if (threadIdx.x == 0) {
-      __threadfence();
-      st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
-    }
+    if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
   }
 
   if (abort) {
@@ -771,9 +714,9 @@ using namespace tq::seq;
 
 struct tq_seq {
   std::vector<CallDev> calls;
-  int ncalls = 0, B = 0, Bp = 0, G = 0, grid = 0, nkc = 0, dev = 0, stage_floats = 0;
+  int ncalls = 0, B = 0, Bp = 0, G = 0, grid = 0, nkc = 0, dev = 0;
   size_t smem = 0;
-  uint32_t off_scales = 0, off_xh = 0, off_zero = 0, off_v = 0, off_f = 0, off_bar = 0, off_misc = 0, off_stage = 0;
+  uint32_t off_scales = 0, off_xh = 0, off_zero = 0, off_v = 0, off_f = 0, off_bar = 0, off_misc = 0;
   size_t ws_calls = 0, ws_sync = 0, ws_part = 0, ws_ssq = 0, ws_bytes = 0, part_stride = 0;
   int ssq_stride = 0;
   const void* kern = nullptr;
@@ -851,7 +794,6 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   // per-call work split; the most K slices any CTA covers, the largest item count
   s->calls.resize(ncalls);
   long long Tmax = 0;
-  long long stage_rows = 4;  // largest gather of any call
   for (int j = 0; j < ncalls; ++j) {
     const tq_seq_call& c = calls[j];
     CallDev& d = s->calls[j];
@@ -873,26 +815,15 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
     d.T = static_cast<int>(T);
     d.gp = std::min(sms, d.T);
     Tmax = std::max(Tmax, T);
-    int kmax = 0;  // most input rows one CTA transforms
-    for (int cta = 0; cta < d.gp; ++cta) {
-      const int a = cta_start(d.T, d.gp, cta), b = cta_start(d.T, d.gp, cta + 1);
-      if (b > a) kmax = std::max(kmax, std::min(((b - 1) / d.nru + 1) * kItemTrits, d.K) - (a / d.nru) * kItemTrits);
-    }
-    const int segs = c.x_src == TQ_SEQ_X_BF16 ? 0 : c.x_src == TQ_SEQ_X_SWIGLU_PREV ? 2 : 1;
-    stage_rows = std::max<long long>(stage_rows, static_cast<long long>(segs) * kmax);
-    stage_rows = std::max<long long>(stage_rows, ((d.N / 4) / sms + 1) * 4);  // the rows it finalizes
     for (int cta = 0; cta < d.gp; ++cta) {
       const int a = cta_start(d.T, d.gp, cta), b = cta_start(d.T, d.gp, cta + 1);
       if (b > a) s->nkc = std::max(s->nkc, (b - 1) / d.nru - a / d.nru + 1);
     }
   }
-  // shared memory: rings, x^ of the CTA's K slices, zero chunk, V, F, barriers, flags, gather staging
+  // shared memory: rings, x^ of the CTA's K slices, zero chunk, V, F, barriers, flags
   const int GPI = kItemTrits / G;
-  const int kD = ring_depth(s->Bp);
-  s->stage_floats = static_cast<int>(stage_rows * s->Bp);
   const size_t xh = align256(static_cast<size_t>(s->nkc) * GPI * s->Bp * 2 * G);
   const size_t vf = align256(static_cast<size_t>(s->nkc * GPI + 8) * s->Bp * 4);
-  const size_t stage = align256(static_cast<size_t>(s->stage_floats) * 4);
   size_t off = static_cast<size_t>(kNW) * kD * kCodeStage;
   s->off_scales = static_cast<uint32_t>(off);
   off += static_cast<size_t>(kNW) * kD * kScaleStage;
@@ -908,8 +839,6 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   off += align256(static_cast<size_t>(kNW) * kD * 8);
   s->off_misc = static_cast<uint32_t>(off);
   off += 256;
-  s->off_stage = static_cast<uint32_t>(off);
-  off += stage;
   s->smem = off + 1024;  // alignment slack of the base
   if (s->smem > kSmemLimit || s->smem > static_cast<size_t>(optin)) {
     delete s;
@@ -992,8 +921,6 @@ extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) 
   prm.off_f = s->off_f;
   prm.off_bar = s->off_bar;
   prm.off_misc = s->off_misc;
-  prm.off_stage = s->off_stage;
-  prm.stage_floats = s->stage_floats;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s->grid);
   cfg.blockDim = dim3(kNW * 32);
