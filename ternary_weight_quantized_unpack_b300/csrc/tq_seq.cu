@@ -50,7 +50,8 @@ namespace seq {
 using namespace sm100;
 
 constexpr int kNW = 12;                        // warps per CTA
-constexpr int kD = 3;                          // ring stages per warp
+// Ring stages per warp: three while the batch is small, two at four or eight batch rows.
+__host__ __device__ constexpr int ring_depth(int Bp) { return Bp <= 2 ? 3 : 2; }
 constexpr int kGatherKu = 12;                  // partial sums one thread adds in one go
 constexpr int kRows = 32;                      // rows per item: two 16-row MMA slabs
 constexpr int kItemTrits = 512;                // trits per item along K: 32 code words of a row
@@ -108,13 +109,12 @@ __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
 }
 
 // Grid barrier number k (after call k), in two halves so that work that does not depend on it can
-// run in between: grid_arrive (every thread; after a CTA barrier, thread 0 adds one with release
+// run in between: grid_arrive_release (thread 0, after a CTA barrier: adds one with release
 // semantics, so every write of the CTA before the barrier is visible to a thread that acquires the
 // count) and grid_wait (every thread; thread 0 waits with acquire loads until every CTA has arrived,
 // false if limit_ns passed first).
-__device__ __forceinline__ void grid_arrive(unsigned* sync) {
-  __syncthreads();
-  if (threadIdx.x == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sync) : "memory");
+__device__ __forceinline__ void grid_arrive_release(unsigned* sync) {
+  asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(sync) : "memory");
 }
 __device__ __forceinline__ bool grid_wait(unsigned* sync, unsigned k, int* flag, uint64_t limit_ns = kWaitNs) {
   if (threadIdx.x == 0) {
@@ -383,6 +383,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   constexpr int BPI = kItemTrits / kFwhtBlock;     // 128-blocks per item
   extern __shared__ __align__(16) uint8_t smem_raw[];
   uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  constexpr int kD = ring_depth(BP);
   const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
   const int g = lane >> 2, q = lane & 3;
   const int cta = static_cast<int>(blockIdx.x);
@@ -655,13 +656,11 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
         ++ku;
       }
     }
-    __syncthreads();
-    if (abort) s_flag[0] = 1;
-    __syncthreads();
-    abort = s_flag[0] != 0;
+    abort = __syncthreads_or(abort) != 0;
     if (abort) break;
-    // ---- barrier: every partial sum and sum of squares of this call is written ----
-    grid_arrive(p.sync);
+    // ---- barrier: every partial sum and sum of squares of this call is written (the CTA barrier
+    //      just passed orders them before thread 0's release) ----
+    if (threadIdx.x == 0) grid_arrive_release(p.sync);
     if (!grid_wait(p.sync, nbar++, s_flag + 1)) {
       if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
       abort = true;
@@ -822,6 +821,7 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   }
   // shared memory: rings, x^ of the CTA's K slices, zero chunk, V, F, barriers, flags
   const int GPI = kItemTrits / G;
+  const int kD = ring_depth(s->Bp);
   const size_t xh = align256(static_cast<size_t>(s->nkc) * GPI * s->Bp * 2 * G);
   const size_t vf = align256(static_cast<size_t>(s->nkc * GPI + 8) * s->Bp * 4);
   size_t off = static_cast<size_t>(kNW) * kD * kCodeStage;
