@@ -240,14 +240,14 @@ class Stream:
 
 
 class SeqStep:
-    """The decode step of a Stream's weights (stacked, 2-bit) as one tq_seq launch: the dependent chain
-    qkv(RMS-normalised input) -> o(q part) -> gate_up(RMS-normalised) -> down(SwiGLU) per layer."""
+    """The decode step of a Stream's weights (stacked, 2-bit or base-3) as one tq_seq launch: the dependent
+    chain qkv(RMS-normalised input) -> o(q part) -> gate_up(RMS-normalised) -> down(SwiGLU) per layer."""
 
     SRC = {"qkv": tq.TQ_SEQ_X_RMS_PREV, "o": tq.TQ_SEQ_X_PREV, "gate_up": tq.TQ_SEQ_X_RMS_PREV,
            "down": tq.TQ_SEQ_X_SWIGLU_PREV}
 
     def __init__(self, stream: "Stream", device="cuda"):
-        assert stream.stacked and stream.packing == tq.TQ_PACK_2BIT
+        assert stream.stacked and stream.packing in (tq.TQ_PACK_2BIT, tq.TQ_PACK_B3)
         self.batch = stream.batch
         lins = {l.name: l for l in stream.linears}
         self.x_dev, self.x_host = stream.x_bufs["qkv"]
@@ -728,11 +728,12 @@ def run_tq(args, rank, world, local):
     peaks = measured_peaks()
     packing, batch = PACKINGS[args.packing], args.batch
     st = Stream(packing, batch, layers=args.layers)
-    seq = args.engine == "seq" and packing == tq.TQ_PACK_2BIT and batch <= 8
+    seq = args.engine == "seq" and packing in (tq.TQ_PACK_2BIT, tq.TQ_PACK_B3) and batch <= 8
     if seq:
         eng, g, ms_total, clocks = bench_seq(st, args.steps, world, clocks_index=local, warmup=args.warmup)
         launches_per_step = tq.tq_seq_kernel_count(eng.plan.handle)
-        kernel = ("gemv_seq_kernel: the whole step (256 dependent calls) is this one persistent launch; "
+        kname = "gemv_seq_b3_kernel" if packing == tq.TQ_PACK_B3 else "gemv_seq_kernel"
+        kernel = (f"{kname}: the whole step (256 dependent calls) is this one persistent launch; "
                   "duration = CUDA-event time of the graph-replayed steps / steps")
     else:
         eng = st
@@ -751,7 +752,7 @@ def run_tq(args, rank, world, local):
         eng.step_e2e(y_host)
     e2e_s = e2e_time(lambda: eng.step_e2e(y_host), args.steps, world)
     e2e_value = st.bytes_per_step * args.steps * world / e2e_s / GB
-    tkey = f"gemv_seq_2b_b{batch}_per_layer" if seq else \
+    tkey = f"gemv_seq_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_per_layer" if seq else \
         f"dense_decode_{'b3' if packing == tq.TQ_PACK_B3 else '2b'}_b{batch}_stacked_per_layer"
     per_layer = traffic_from_profiles(tkey)
     line = {
@@ -788,7 +789,8 @@ def run_tq(args, rank, world, local):
         if seq:   # the same weights called one launch per call
             g2, ms2, _ = bench_per_call(st, reps)
             ms2 /= reps
-            ex["per_call_stream"].append({"packing": "2bit", "batch": batch, "calls_per_layer": 4, "ms": ms2,
+            ex["per_call_stream"].append({"packing": PACKING_NAMES[packing], "batch": batch, "calls_per_layer": 4,
+                                          "ms": ms2,
                                           "GB_s": st.bytes_per_step / (ms2 * 1e-3) / GB,
                                           "tok_s": batch / (ms2 * 1e-3)})
             del g2
@@ -796,13 +798,13 @@ def run_tq(args, rank, world, local):
         torch.cuda.empty_cache()
         for pk, b in ((tq.TQ_PACK_2BIT, 8), (tq.TQ_PACK_B3, 1), (tq.TQ_PACK_B3, 8)):
             s2 = Stream(pk, b)
-            if pk == tq.TQ_PACK_2BIT:
-                e2, g2, ms2, _ = bench_seq(s2, reps)
-                ms2 /= reps
-                ex["decode_step"].append({"packing": "2bit", "batch": b, "engine": "tq_seq (one launch per step)",
-                                          "ms": ms2, "GB_s": s2.bytes_per_step / (ms2 * 1e-3) / GB,
-                                          "tok_s": b / (ms2 * 1e-3)})
-                del e2, g2
+            e2, g2, ms2, _ = bench_seq(s2, reps)
+            ms2 /= reps
+            ex["decode_step"].append({"packing": PACKING_NAMES[pk], "batch": b, "engine": "tq_seq (one launch per step)",
+                                      "ms": ms2, "GB_s": s2.bytes_per_step / (ms2 * 1e-3) / GB,
+                                      "pct_of_hbm_peak": 100.0 * s2.bytes_per_step / (ms2 * 1e-3) / GB / peaks["hbm_gbs"],
+                                      "tok_s": b / (ms2 * 1e-3)})
+            del e2, g2
             g2, ms2, _ = bench_per_call(s2, reps)
             ms2 /= reps
             ex["per_call_stream"].append({"packing": "base3" if pk == tq.TQ_PACK_B3 else "2bit", "batch": b,

@@ -173,10 +173,12 @@ tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_
  *                        row (RMS normalisation with unit gain, as a pre-norm decoder applies it
  *                        before its attention and FFN projections).
  * Then x~ = block FWHT(input) if fwht_block = 128, y[b][n] = sum_k s t x~ (float [batch][N]).
- * Limits: 2-bit packing; one group size for all calls; K a multiple of 8 * group (each row of scales
- * a multiple of 16 bytes: they are fetched by TMA); N a multiple of 4; 1 <= batch <= 8; K * batch
- * small enough for the transformed activations of the widest call to sit in shared memory (K up to
- * about 40000 at batch 1, 5120 at batch 8); TQ_STATIC_WEIGHTS is implied (weights must not change
+ * Limits: one packing (TQ_PACK_2BIT or TQ_PACK_B3; 3-bit codes: TQ_ERR_UNSUPPORTED) and one group
+ * size for all calls; 2-bit: K a multiple of 8 * group (each row of scales a multiple of 16 bytes:
+ * they are fetched by TMA); N a multiple of 4; 1 <= batch <= 8; K * batch small enough for the
+ * transformed activations of the widest call to sit in shared memory (2-bit: K up to about 40000 at
+ * batch 1, 5120 at batch 8; base-3 leaves less room, TQ_ERR_UNSUPPORTED where it does not fit);
+ * TQ_STATIC_WEIGHTS is implied (weights must not change
  * while the plan is in use).  A call's y must not be the x of any call, nor the y of the call before
  * it.  All pointers: device memory, 16-byte aligned.
  *
@@ -195,7 +197,7 @@ tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_
 #define TQ_SEQ_X_RMS_PREV 3
 
 typedef struct {
-  tq_desc d;               /* N, K, group, packing (TQ_PACK_2BIT), fwht_block; flags ignored */
+  tq_desc d;               /* N, K, group, packing (TQ_PACK_2BIT or TQ_PACK_B3), fwht_block; flags ignored */
   const uint32_t* codes;   /* [N][P] */
   const uint16_t* scales;  /* [N][K / group] FP16 */
   int32_t x_src;           /* TQ_SEQ_X_* */

@@ -362,7 +362,7 @@ def tq_seq_destroy(plan):
 
 
 class SeqPlan:
-    """A decode step (a chain of 2-bit GEMVs) prepared once and run with one launch per call of run().
+    """A decode step (a chain of 2-bit or base-3 GEMVs) prepared once and run with one launch per call of run().
 
     calls: list of (desc, codes, scales, x_src, x, y) as tq_seq_call; the tensors are kept alive by
     the plan.  The workspace is allocated here with torch unless one is given."""

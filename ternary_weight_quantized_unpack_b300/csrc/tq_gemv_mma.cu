@@ -47,6 +47,7 @@
 #include <tuple>
 #include <vector>
 
+#include "tq_b3.cuh"
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
 #include "tq_sm100.cuh"
@@ -70,8 +71,7 @@ constexpr bool kPrefetchL2 = true;
 // before the wait.
 constexpr int kStreamFuseMaxB = 4;
 constexpr int kEarlyStages = 0;
-constexpr uint32_t kLutWords = 2u * 243u * 32u;
-constexpr uint32_t kLutBytes = kLutWords * 4u;
+constexpr uint32_t kLutBytes = B3Lut<32>::kBytes;
 
 template <int PACK>
 struct Geo;
@@ -97,31 +97,9 @@ __host__ __device__ constexpr int slab_rows(int pack) { return pack == TQ_PACK_2
 // last slot; a multiple of 4 floats so that every group's row is a whole number of 16-byte chunks.
 __host__ __device__ constexpr int vp_row(int B) { return (B + 1 + 3) & ~3; }
 
-// Chunk lookup table (base-3): for a 5-trit chunk c (digits d0..d4), entry "A" places the digits at
-// FP16 pair fields (lo0, hi0, lo1, hi1, lo2) and entry "B" at (hi2, lo3, hi3, lo4, hi4), where
-// loI / hiI are bits 2I / 16 + 2I.  Each entry is replicated 32 times so that lane l reads bank l.
-struct __align__(128) LutTable {  // bulk-copied: 16-byte alignment required
-  uint32_t v[kLutWords];
-};
-constexpr LutTable make_lut() {
-  LutTable L{};
-  for (int c = 0; c < 243; ++c) {
-    int d[5] = {0, 0, 0, 0, 0};
-    int x = c;
-    for (int i = 0; i < 5; ++i) {
-      d[i] = x % 3;
-      x /= 3;
-    }
-    const uint32_t a = static_cast<uint32_t>(d[0] | (d[1] << 16) | (d[2] << 2) | (d[3] << 18) | (d[4] << 4));
-    const uint32_t b = static_cast<uint32_t>((d[0] << 20) | (d[1] << 6) | (d[2] << 22) | (d[3] << 8) | (d[4] << 24));
-    for (int l = 0; l < 32; ++l) {
-      L.v[c * 32 + l] = a;
-      L.v[243 * 32 + c * 32 + l] = b;
-    }
-  }
-  return L;
-}
-__device__ const LutTable g_lut = make_lut();
+// Chunk lookup table (base-3), one copy per lane (32): lane l reads bank l.
+using LutTable = B3Lut<32>;
+__device__ const LutTable g_lut = make_b3_lut<32>();
 
 // ---------------------------------------------------------------------------------------------
 // Prep kernel: x^ and VP for the whole of K, one warp per 128-block, all batch rows in registers.
@@ -737,31 +715,6 @@ __global__ void __launch_bounds__(kMaxThreads) gemv_2b_kernel(const __grid_const
 // Thread (g, q) owns rows R = r0 + 4g + q and R + 32 of its warp's 64-row slab.
 // ---------------------------------------------------------------------------------------------
 
-// Base-3 word -> the four table words of its chunks: L0/L1 (trits 0..9), L2/L3 (trits 10..19).
-__device__ __forceinline__ void b3_lut4(uint32_t w, const uint32_t* __restrict__ lutA,
-                                        const uint32_t* __restrict__ lutB, uint32_t (&L)[4]) {
-  const uint32_t v = min(w, kB3Max);
-  const uint32_t hi = __umulhi(v + 1u, 2383401723u) >> 15;  // v / 3^10, exact for v < 3^20
-  const uint32_t lo = v - hi * 59049u;
-  const uint32_t bl = __umulhi(lo, 17675008u);                // lo / 243, exact for lo < 3^10
-  const uint32_t al = lo - bl * 243u;
-  const uint32_t bh = __umulhi(hi, 17675008u);
-  const uint32_t ah = hi - bh * 243u;
-  L[0] = lutA[al * 32];
-  L[1] = lutB[bl * 32];
-  L[2] = lutA[ah * 32];
-  L[3] = lutB[bh * 32];
-}
-
-// Pair j (0..9) of a decoded word as an MMA operand register: (trit 2j, trit 2j+1) in the
-// (lo, hi) halves at field j % 5.  Fields 0, 1 come from the "A" entry, 3, 4 from "B", 2 from both.
-__device__ __forceinline__ uint32_t b3_pair(const uint32_t (&L)[4], int j) {
-  const uint32_t a = j < 5 ? L[0] : L[2], b = j < 5 ? L[1] : L[3];
-  const int f = j % 5;
-  const uint32_t m = 0x00030003u << (2 * f);
-  return f < 2 ? (a & m) : f == 2 ? ((a | b) & m) : (b & m);
-}
-
 template <int G, int NT, bool FULL>
 __device__ __forceinline__ void b3_unit(const Params& p, const Cta& c, int u, int ngp, const uint4* __restrict__ cR,
                                         const uint4* __restrict__ cR2, int s_last, uint4 (&ra)[4], uint4 (&rb)[4],
@@ -796,8 +749,8 @@ __device__ __forceinline__ void b3_unit(const Params& p, const Cta& c, int u, in
 #pragma unroll
     for (int wi = 0; wi < 4; ++wi) {
       uint32_t La[4], Lb[4];
-      b3_lut4(wr[wi], lutA, lutB, La);
-      b3_lut4(wr2[wi], lutA, lutB, Lb);
+      b3_chunks<32>(wr[wi], lutA, lutB, La);
+      b3_chunks<32>(wr2[wi], lutA, lutB, Lb);
 #pragma unroll
       for (int mj = 0; mj < 5; ++mj) {
         const int pair = (st * 4 + wi) * 10 + 2 * mj;  // first pair of this MMA within the unit

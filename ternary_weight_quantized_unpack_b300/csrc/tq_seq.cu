@@ -1,4 +1,5 @@
-// Decode step: a sequence of dependent 2-bit ternary GEMVs in one persistent launch.
+// Decode step: a sequence of dependent 2-bit or base-3 ternary GEMVs in one persistent launch (the
+// base-3 kernel, further down, shares everything but the item decode).
 //
 // Decoding one token runs every linear of the model once, each on the previous one's output.  Issued
 // as separate kernels, every call pays a launch, an activation fetch and transform, and a tail in
@@ -39,6 +40,7 @@
 #include <new>
 #include <vector>
 
+#include "tq_b3.cuh"
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
 #include "tq_sm100.cuh"
@@ -66,6 +68,7 @@ struct alignas(128) CallDev {
   CUtensorMap tm_codes;   // codes [N][P] uint32, box {32 words, 32 rows}, 128-byte swizzle
   CUtensorMap tm_scales;  // scales [N][ng] FP16, box {8 groups, 32 rows}
   const uint16_t* x;      // mode 0: bf16 [B][K]
+  const uint16_t* scales; // FP16 [N][ng] (base-3: read with plain loads; 2-bit: through tm_scales)
   float* y;               // [B][N]
   int T;                  // items = nru * nku (T * grid < 2^31)
   int N, K, ng, mode, apply;
@@ -76,10 +79,11 @@ static_assert(sizeof(CallDev) % 128 == 0, "call records are 128-byte aligned");
 // The fields of a call the kernel reads repeatedly, kept in registers.
 struct CallLite {
   const uint16_t* x;
+  const uint16_t* scales;
   float* y;
   int T, N, K, ng, mode, apply, nru, nku, gp;
   __device__ __forceinline__ explicit CallLite(const CallDev& c)
-      : x(c.x), y(c.y), T(c.T), N(c.N), K(c.K), ng(c.ng), mode(c.mode), apply(c.apply), nru(c.nru), nku(c.nku),
+      : x(c.x), scales(c.scales), y(c.y), T(c.T), N(c.N), K(c.K), ng(c.ng), mode(c.mode), apply(c.apply), nru(c.nru), nku(c.nku),
         gp(c.gp) {}
 };
 
@@ -93,7 +97,7 @@ struct Params {
   size_t part_stride;     // floats per parity of part
   int ssq_stride;         // floats per parity of ssq
   int nkc;                // K slices one CTA may cover (x^ capacity)
-  uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc;
+  uint32_t off_scales, off_xh, off_zero, off_v, off_f, off_bar, off_misc, off_lut;
 };
 
 // ---- static work split (K-major) ---------------------------------------------------------------
@@ -189,14 +193,14 @@ __device__ __forceinline__ float out_scale_warp(const CallLite& c, const float* 
 // 4-row chunk: lane s adds the slices [s * per, (s + 1) * per) (all its loads issued before the
 // adds), then the group combines its sums by a fixed butterfly.  The result does not depend on which
 // CTA computes it, and the partial sums and the sums of squares of the scale are in flight together.
-template <int BP>
+template <int BP, int ROWS>
 __device__ __forceinline__ void finalize(const CallLite& c, const float* ppart, const float* ssq, int B, int fr0,
                                          int nr) {
   const int lane = static_cast<int>(threadIdx.x & 31);
   int nsp = 1;
   while (nsp * kGatherKu < c.nku) nsp <<= 1;  // lanes per chunk (a power of two up to 32)
   const int per = (c.nku + nsp - 1) / nsp;    // slices per lane (<= kGatherKu)
-  const size_t step = static_cast<size_t>(c.nru) * BP * kRows;
+  const size_t step = static_cast<size_t>(c.nru) * BP * ROWS;
   const int total = (nr / 4) * B;
   const int nthr = (total * nsp + 31) & ~31;  // whole warps, so every lane takes part in the shuffles
   for (int t = threadIdx.x; t < nthr; t += blockDim.x) {
@@ -204,7 +208,7 @@ __device__ __forceinline__ void finalize(const CallLite& c, const float* ppart, 
     const bool valid = u < total;
     const int b = valid ? u % B : 0, c4 = valid ? u / B : 0;
     const int k = fr0 + 4 * c4;
-    const float* p0 = ppart + (static_cast<size_t>(k >> 5) * BP + b) * kRows + (k & 31);
+    const float* p0 = ppart + (static_cast<size_t>(k / ROWS) * BP + b) * ROWS + (k % ROWS);
     const int ku0 = s * per;
     float4 v[kGatherKu];
 #pragma unroll
@@ -272,8 +276,9 @@ struct LaneLayout {
 // that finalized the block's 128 rows (SwiGLU: and the 128 matching rows of the up half) form one
 // or two contiguous ranges; one lane per CTA waits (bounded) for its flag, raising *abort on timeout,
 // and the warp barrier then orders every lane's reads after those acquires.  ssq: RMS mode, where
-// the block's sums of squares go (global).
-template <int G, int BP>
+// the block's sums of squares go (global).  PACK selects the x^ layout of the decode loop (2-bit:
+// LaneLayout; base-3: MMA order, see the base-3 kernel).
+template <int PACK, int G, int BP>
 __device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, const CallLite& pc, unsigned want,
                                            int* abort, int blk, int lg0, const LaneLayout<G>& L, uint8_t* xh,
                                            float* V, float* Fv, float* ssq, int lane) {
@@ -345,13 +350,30 @@ __device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, c
       e = max(e, -100);
     }
     const float down = __int_as_float((127 - e) << 23) * norm;
-    uint8_t* gbase = xh + (static_cast<size_t>(lg) * BP + b) * (2 * G);
     float vs = 0.f;
+    if constexpr (PACK == TQ_PACK_2BIT) {
+      uint8_t* gbase = xh + (static_cast<size_t>(lg) * BP + b) * (2 * G);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const __half h = __float2half_rn(v[b][i] * down * L.up[i]);
-      *reinterpret_cast<__half*>(gbase + L.off[i]) = h;
-      vs += __half2float(h) * L.dn[i];
+      for (int i = 0; i < 4; ++i) {
+        const __half h = __float2half_rn(v[b][i] * down * L.up[i]);
+        *reinterpret_cast<__half*>(gbase + L.off[i]) = h;
+        vs += __half2float(h) * L.dn[i];
+      }
+    } else {
+      // base-3: trit k of the CTA's slice (which starts on a word boundary) is half k % 4 of MMA
+      // m = k / 4; its digit sits at bit pb = 2 ((k % 20 % 10) / 2) of the decoded half
+      const int kr = lg0 * G + 4 * lane, m = kr >> 2;
+      uint32_t hw[2];
+#pragma unroll
+      for (int i = 0; i < 4; i += 2) {
+        const int pb0 = 2 * (((kr + i) % 20 % 10) >> 1), pb1 = 2 * (((kr + i + 1) % 20 % 10) >> 1);
+        const __half h0 = __float2half_rn(v[b][i] * down * __int_as_float((127 + 8 - pb0) << 23));
+        const __half h1 = __float2half_rn(v[b][i + 1] * down * __int_as_float((127 + 8 - pb1) << 23));
+        vs += __half2float(h0) * __int_as_float((127 - 8 + pb0) << 23) +
+              __half2float(h1) * __int_as_float((127 - 8 + pb1) << 23);
+        hw[i >> 1] = static_cast<uint32_t>(__half_as_ushort(h0)) | (static_cast<uint32_t>(__half_as_ushort(h1)) << 16);
+      }
+      *reinterpret_cast<uint2*>(xh + ((static_cast<size_t>(m >> 1) * BP + b) * 2 + (m & 1)) * 8) = make_uint2(hw[0], hw[1]);
     }
     constexpr int lanes_per_group = G / 4;
 #pragma unroll
@@ -478,7 +500,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       const int blk0 = ku_lo * BPI;
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
-        prep_block<G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G), L, xh,
+        prep_block<TQ_PACK_2BIT, G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G), L, xh,
                           V, Fv, ssq, lane);
     }
     __syncthreads();
@@ -671,7 +693,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     {
       int fr0, fr1;
       fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
-      finalize<BP>(c, part, ssq, p.B, fr0, fr1 - fr0);
+      finalize<BP, kRows>(c, part, ssq, p.B, fr0, fr1 - fr0);
     }
     // ---- this CTA's rows are final: raise its flag ----
     __syncthreads();
@@ -702,6 +724,356 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   }
 }
 
+// ---- base-3 --------------------------------------------------------------------------------------
+// The same step over base-3 codes (20 trits per 32-bit word, the TurboQuant-MLX page, "为什么 1.58bit
+// 没变成乱码", point 3), in the column layout of the per-call base-3 decode: a warp owns 64 rows, lane l
+// decodes rows l and l + 32 word by word (two reciprocal multiplies split a word into four 5-trit
+// chunks, a table in shared memory places each chunk's digits in FP16 pair fields, one mask per
+// pair gives an operand register), and the B operand of an MMA is zero except in the column of the
+// lane that supplies a batch row, so each column of the m16n8k16 accumulator holds one row's dot
+// product.  An item is a warp's 64 rows x 640 trits (32 words of each row: one 2-D TMA box of 64 x
+// 128 bytes, 128-byte swizzle); scales are loaded one item ahead into registers and staged per warp
+// as [group][row].  Boundaries, work split, finalize and flags are those of the 2-bit kernel.
+namespace b3 {
+constexpr int kNW = 8;                         // warps per CTA (255 registers each; the rings and the table fill shared memory)
+constexpr int kD = 2;                          // ring stages per warp
+constexpr int kRows = 64;                      // rows per item
+constexpr int kItemTrits = 640;                // trits per item along K: 32 words, five 128-blocks
+constexpr uint32_t kCodeStage = kRows * 128u;  // one item's codes: 8 KB
+constexpr int kLutRep = 16;                    // table copies (lanes l and l + 16 share one)
+constexpr uint32_t kLutBytes = B3Lut<kLutRep>::kBytes;
+}  // namespace b3
+
+__device__ const B3Lut<b3::kLutRep> g_seq_lut = make_b3_lut<b3::kLutRep>();
+
+// Scales of one item (64 rows x GPI groups), loaded into registers one item ahead (two halves per
+// register) and staged in the warp's area as halves [group][row].  Rows past N and groups past the
+// matrix read a clamped (valid) address; their values reach only outputs that are never stored.
+template <int GPI>
+struct ItemScales {
+  static constexpr int PER_LANE = 64 * GPI / 32;
+  uint32_t v[PER_LANE / 2];
+  __device__ __forceinline__ void load(const CallLite& c, int ku, int ru, int lane) {
+#pragma unroll
+    for (int j = 0; j < PER_LANE; ++j) {
+      const int e = lane + 32 * j, r = e / GPI, g = e % GPI;
+      const int row = min(ru * 64 + r, c.N - 1), grp = min(ku * GPI + g, c.ng - 1);
+      const uint32_t h = __ldg(c.scales + static_cast<size_t>(row) * c.ng + grp);
+      if (j & 1)
+        v[j >> 1] |= h << 16;
+      else
+        v[j >> 1] = h;
+    }
+  }
+  __device__ __forceinline__ void store(uint16_t* sw, int lane) const {
+#pragma unroll
+    for (int j = 0; j < PER_LANE; ++j) {
+      const int e = lane + 32 * j, r = e / GPI, g = e % GPI;
+      sw[g * 64 + r] = static_cast<uint16_t>((j & 1) ? (v[j >> 1] >> 16) : (v[j >> 1] & 0xffffu));
+    }
+  }
+};
+
+// One item: the warp's 64 rows x the item's ngi groups, folded into acc (rows rl0, rl0 + 1, rl0 + 32,
+// rl0 + 33 of the item for batch row 2t + bq of tile t).  box: the item's swizzled codes; xh32: x^ of
+// the CTA's slice (MMA pair mp, batch row b at words (mp * BP + b) * 4); mp0: the item's first MMA pair
+// in the slice; V / Fv at local group lg_item0 + gl, batch row b: lg * BP + b.
+template <int G, int BP, bool FULL>
+__device__ __forceinline__ void b3_item(const uint4* __restrict__ box, int lane, int ngi, const uint32_t* __restrict__ lutA,
+                                        const uint32_t* __restrict__ lutB, const uint32_t* const (&bptr)[(BP + 1) / 2],
+                                        const int (&bstr)[(BP + 1) / 2], int mp0, const float* __restrict__ V,
+                                        const float* __restrict__ Fv, int lg_item0, const uint16_t* __restrict__ swr,
+                                        float (&acc)[(BP + 1) / 2][4]) {
+  constexpr int NT = (BP + 1) / 2;
+  constexpr int GP = G / 2;  // pairs per group
+  const int bq = (lane & 3) >> 1;
+  const int sl = lane & 7;   // 128-byte swizzle: 16-byte chunk c of row r sits at chunk c ^ (r % 8)
+  float cc[NT][4];
+  uint4 bp[NT];
+#pragma unroll
+  for (int st = 0; st < 8; ++st) {
+    if (!FULL && (st * 80) / G >= ngi) break;
+    const uint4 cur = box[lane * 8 + (st ^ sl)], cur2 = box[(lane + 32) * 8 + (st ^ sl)];
+    const uint32_t wr[4] = {cur.x, cur.y, cur.z, cur.w};
+    const uint32_t wr2[4] = {cur2.x, cur2.y, cur2.z, cur2.w};
+#pragma unroll
+    for (int wi = 0; wi < 4; ++wi) {
+      uint32_t La[4], Lb[4];
+      b3_chunks<b3::kLutRep>(wr[wi], lutA, lutB, La);
+      b3_chunks<b3::kLutRep>(wr2[wi], lutA, lutB, Lb);
+#pragma unroll
+      for (int mj = 0; mj < 5; ++mj) {
+        const int pair = (st * 4 + wi) * 10 + 2 * mj;  // first pair of this MMA within the item
+        const int gl = pair / GP;
+        if (!FULL && gl >= ngi) break;
+        const int lg = lg_item0 + gl;
+        if (pair % GP == 0) {  // a new group: the sum starts at -2^-16 * sum(x^) of its batch row
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int b = 2 * t + bq;
+            const float v0 = b < BP ? V[lg * BP + b] : 0.f;
+            cc[t][0] = cc[t][1] = cc[t][2] = cc[t][3] = v0;
+          }
+        }
+        const int mloc = (st * 4 + wi) * 5 + mj;  // MMA index within the item
+        if ((mloc & 1) == 0) {
+#pragma unroll
+          for (int t = 0; t < NT; ++t)
+            bp[t] = *reinterpret_cast<const uint4*>(bptr[t] + (mp0 + (mloc >> 1)) * bstr[t]);
+        }
+        const uint32_t a0 = b3_pair(La, 2 * mj), a2 = b3_pair(La, 2 * mj + 1);
+        const uint32_t a1 = b3_pair(Lb, 2 * mj), a3 = b3_pair(Lb, 2 * mj + 1);
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+          const uint32_t b0 = (mloc & 1) ? bp[t].z : bp[t].x, b1 = (mloc & 1) ? bp[t].w : bp[t].y;
+          mma16816(cc[t], a0, a1, a2, a3, b0, b1);
+        }
+        if ((pair + 2) % GP == 0) {  // the group's last MMA: fold scale(row, group) * 2^(16 + e) * cc
+          const float2 s01 = __half22float2(*reinterpret_cast<const __half2*>(swr + gl * 64));
+          const float2 s23 = __half22float2(*reinterpret_cast<const __half2*>(swr + gl * 64 + 32));
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            const int b = 2 * t + bq;
+            const float f = b < BP ? Fv[lg * BP + b] : 0.f;
+            acc[t][0] = fmaf(s01.x * f, cc[t][0], acc[t][0]);
+            acc[t][1] = fmaf(s01.y * f, cc[t][1], acc[t][1]);
+            acc[t][2] = fmaf(s23.x * f, cc[t][2], acc[t][2]);
+            acc[t][3] = fmaf(s23.y * f, cc[t][3], acc[t][3]);
+          }
+        }
+      }
+    }
+  }
+}
+
+template <int G, int BP>
+__global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __grid_constant__ Params p) {
+  using b3::kD;
+  using b3::kNW;
+  using b3::kRows;
+  using b3::kItemTrits;
+  using b3::kCodeStage;
+  constexpr int GPI = kItemTrits / G;           // groups per item (5 or 10)
+  constexpr int BPI = kItemTrits / kFwhtBlock;  // 128-blocks per item
+  constexpr int NT = (BP + 1) / 2;              // two-row batch tiles
+  extern __shared__ __align__(16) uint8_t smem_raw[];
+  uint8_t* smem = smem_raw + ((1024u - (smem_addr(smem_raw) & 1023u)) & 1023u);
+  const int warp = static_cast<int>(threadIdx.x >> 5), lane = static_cast<int>(threadIdx.x & 31);
+  const int g = lane >> 2, q = lane & 3;
+  const int cta = static_cast<int>(blockIdx.x);
+  uint8_t* codes_st = smem + static_cast<size_t>(warp) * kD * kCodeStage;
+  uint16_t* sw = reinterpret_cast<uint16_t*>(smem + p.off_scales) + warp * (GPI * 64);
+  uint8_t* xh = smem + p.off_xh;
+  const uint32_t* zero = reinterpret_cast<const uint32_t*>(smem + p.off_zero);
+  float* V = reinterpret_cast<float*>(smem + p.off_v);
+  float* Fv = reinterpret_cast<float*>(smem + p.off_f);
+  uint64_t* full = reinterpret_cast<uint64_t*>(smem + p.off_bar) + warp * kD;
+  uint64_t* lut_bar = reinterpret_cast<uint64_t*>(smem + p.off_bar) + kNW * kD;
+  int* s_flag = reinterpret_cast<int*>(smem + p.off_misc);  // [0] abort, [1] barrier result
+  uint32_t* lut = reinterpret_cast<uint32_t*>(smem + p.off_lut);
+
+  for (uint32_t i = threadIdx.x; i < 64; i += blockDim.x) reinterpret_cast<uint32_t*>(smem + p.off_zero)[i] = 0u;
+  const int vcap = (p.nkc * GPI + 8) * BP;
+  for (int i = threadIdx.x; i < vcap; i += blockDim.x) V[i] = Fv[i] = 0.f;
+  if (lane == 0)
+    for (int s = 0; s < kD; ++s) mbar_init(&full[s], 1);
+  if (threadIdx.x == 0) {
+    s_flag[0] = 0;
+    mbar_init(lut_bar, 1);
+  }
+  fence_mbar_init();
+  __syncthreads();
+  if (threadIdx.x == 0) {  // the chunk table (constant data of this library)
+    mbar_arrive_expect_tx(lut_bar, b3::kLutBytes);
+    bulk_g2s(lut, &g_seq_lut, b3::kLutBytes, lut_bar);
+  }
+
+  auto warp_range = [&](const CallLite& c, int& a, int& b) {
+    if (cta >= c.gp) {
+      a = b = 0;
+      return;
+    }
+    const int ca = cta_start(c.T, c.gp, cta), cb = cta_start(c.T, c.gp, cta + 1), tc = cb - ca;
+    a = ca + (tc * warp) / kNW;
+    b = ca + (tc * (warp + 1)) / kNW;
+  };
+
+  // ---- producer state (lane 0 issues; the cursor is kept warp-uniform) ----
+  int pcall = 0, pidx = 0, pend = 0, pru = 0, pku = 0, pnru = 0;
+  auto set_call = [&]() {
+    const CallLite c(p.calls[pcall]);
+    warp_range(c, pidx, pend);
+    pnru = c.nru;
+    pku = pidx / c.nru;
+    pru = pidx - pku * c.nru;
+  };
+  set_call();
+  unsigned issued = 0, consumed = 0;
+  int ist = 0, cst = 0;
+  uint32_t cph = 0;
+  const uint64_t pol = l2_evict_first_policy();
+  auto issue_next = [&]() {
+    while (pidx >= pend) {
+      if (++pcall >= p.ncalls) return;
+      set_call();
+    }
+    const CallDev* cd = p.calls + pcall;
+    const int s = ist;
+    ist = ist + 1 == kD ? 0 : ist + 1;
+    if (lane == 0) {
+      mbar_arrive_expect_tx(&full[s], kCodeStage);
+      tma_load_2d_hint(codes_st + static_cast<size_t>(s) * kCodeStage, &cd->tm_codes, pku * 32, pru * kRows, &full[s],
+                       pol);
+    }
+    ++issued;
+    ++pidx;
+    if (++pru == pnru) {
+      pru = 0;
+      ++pku;
+    }
+  };
+  for (int s = 0; s < kD; ++s) issue_next();
+
+  bool abort = !mbar_wait(lut_bar, 0);
+  if (abort && threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+  abort = __syncthreads_or(abort) != 0;
+  const LaneLayout<G> L(lane);
+  const uint32_t* lutA = lut + (lane & (b3::kLutRep - 1));
+  const uint32_t* lutB = lutA + 243 * b3::kLutRep;
+  // B operand: lane (g, q) supplies batch row 2t + g / 4 of tile t when g % 4 == q, else 16 zero bytes
+  const uint32_t* bptr[NT];
+  int bstr[NT];
+  const int bq = q >> 1;
+  const int rl0 = 4 * g + ((2 * q) & 3);  // this lane's accumulator rows: rl0, rl0 + 1, rl0 + 32, rl0 + 33
+  ItemScales<GPI> us;
+  unsigned nbar = 0;
+  for (int j = 0; j < p.ncalls && !abort; ++j) {
+    const CallLite c(p.calls[j]);
+    const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
+    float* part = p.part + static_cast<size_t>(j & 1) * p.part_stride;
+    float* ssq = p.ssq + (j & 1) * p.ssq_stride;
+    int ca = 0, cb = 0, ku_lo = 0, ku_hi = -1;
+    if (cta < c.gp) {
+      ca = cta_start(c.T, c.gp, cta);
+      cb = cta_start(c.T, c.gp, cta + 1);
+      ku_lo = ca / c.nru;
+      if (cb > ca) ku_hi = (cb - 1) / c.nru;
+    }
+    int wa = 0, wb = 0;
+    warp_range(c, wa, wb);
+    int ku = wb > wa ? wa / c.nru : 0, ru = wa - ku * c.nru;
+    if (wb > wa) us.load(c, ku, ru, lane);  // the first item's scales, in flight during the transform
+    // ---- input transform of this CTA's K slices ----
+    if (cb > ca) {
+      const int blk0 = ku_lo * BPI;
+      const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
+      for (int blk = blk0 + warp; blk < blk1; blk += kNW)
+        prep_block<TQ_PACK_B3, G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G),
+                                      L, xh, V, Fv, ssq, lane);
+    }
+    __syncthreads();
+    if (s_flag[0] != 0) {  // a ready flag did not come in time
+      if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      abort = true;
+      break;
+    }
+    {
+      const bool bsup = (g & 3) == q;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int b = 2 * t + (g >> 2);
+        bptr[t] = bsup && b < p.B ? reinterpret_cast<const uint32_t*>(xh) + b * 4 : zero;
+        bstr[t] = bsup && b < p.B ? BP * 4 : 0;  // words per MMA pair: 8 halves per batch row
+      }
+    }
+    // ---- this warp's items ----
+    for (int it = wa; it < wb; ++it) {
+      const int st = cst;
+      if (!mbar_wait(&full[st], cph)) {
+        if (lane == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+        abort = true;
+        break;
+      }
+      __syncwarp();
+      us.store(sw, lane);
+      __syncwarp();
+      if (it + 1 < wb) {
+        const int nru2 = ru + 1 == c.nru ? 0 : ru + 1, nku2 = ru + 1 == c.nru ? ku + 1 : ku;
+        us.load(c, nku2, nru2, lane);
+      }
+      const uint4* box = reinterpret_cast<const uint4*>(codes_st + static_cast<size_t>(st) * kCodeStage);
+      const int ngi = min(GPI, c.ng - ku * GPI);
+      float acc[NT][4];
+#pragma unroll
+      for (int t = 0; t < NT; ++t) acc[t][0] = acc[t][1] = acc[t][2] = acc[t][3] = 0.f;
+      const int lg_item0 = (ku - ku_lo) * GPI, mp0 = (ku - ku_lo) * (kItemTrits / 8);
+      if (ngi == GPI)
+        b3_item<G, BP, true>(box, lane, ngi, lutA, lutB, bptr, bstr, mp0, V, Fv, lg_item0, sw + rl0, acc);
+      else
+        b3_item<G, BP, false>(box, lane, ngi, lutA, lutB, bptr, bstr, mp0, V, Fv, lg_item0, sw + rl0, acc);
+      __syncwarp();
+      ++consumed;
+      if (++cst == kD) {
+        cst = 0;
+        cph ^= 1u;
+      }
+      fence_proxy_async_smem();  // this stage's reads before the copy that refills it
+      issue_next();
+      // the item's partial sums: each (row, batch row) is held by one lane
+      float* dst = part + static_cast<size_t>(ku * c.nru + ru) * BP * kRows;
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int b = 2 * t + bq;
+        if (b < p.B) {
+          __stcg(reinterpret_cast<float2*>(dst + b * kRows + rl0), make_float2(acc[t][0], acc[t][1]));
+          __stcg(reinterpret_cast<float2*>(dst + b * kRows + rl0 + 32), make_float2(acc[t][2], acc[t][3]));
+        }
+      }
+      if (++ru == c.nru) {
+        ru = 0;
+        ++ku;
+      }
+    }
+    abort = __syncthreads_or(abort) != 0;
+    if (abort) break;
+    // ---- barrier: every partial sum and sum of squares of this call is written ----
+    if (threadIdx.x == 0) grid_arrive_release(p.sync);
+    if (!grid_wait(p.sync, nbar++, s_flag + 1)) {
+      if (threadIdx.x == 0) record_error(p.status, TQ_ERR_TIMEOUT);
+      abort = true;
+      break;
+    }
+    {
+      int fr0, fr1;
+      fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
+      finalize<BP, kRows>(c, part, ssq, p.B, fr0, fr1 - fr0);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
+  }
+
+  if (abort) {
+    for (; consumed < issued; ++consumed) {
+      if (!mbar_wait(&full[cst], cph)) break;
+      if (++cst == kD) {
+        cst = 0;
+        cph ^= 1u;
+      }
+    }
+  }
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.sync + 1, 1u);
+    if (prev == gridDim.x - 1 && !abort) {
+      for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+      __threadfence();
+    }
+  }
+}
+
 }  // namespace seq
 }  // namespace tq
 
@@ -713,9 +1085,9 @@ using namespace tq::seq;
 
 struct tq_seq {
   std::vector<CallDev> calls;
-  int ncalls = 0, B = 0, Bp = 0, G = 0, grid = 0, nkc = 0, dev = 0;
+  int ncalls = 0, B = 0, Bp = 0, G = 0, grid = 0, nkc = 0, dev = 0, pack = 0, nw = 0;
   size_t smem = 0;
-  uint32_t off_scales = 0, off_xh = 0, off_zero = 0, off_v = 0, off_f = 0, off_bar = 0, off_misc = 0;
+  uint32_t off_scales = 0, off_xh = 0, off_zero = 0, off_v = 0, off_f = 0, off_bar = 0, off_misc = 0, off_lut = 0;
   size_t ws_calls = 0, ws_sync = 0, ws_part = 0, ws_ssq = 0, ws_bytes = 0, part_stride = 0;
   int ssq_stride = 0;
   const void* kern = nullptr;
@@ -723,25 +1095,30 @@ struct tq_seq {
 
 namespace {
 
-template <int G, int BP>
+template <int PACK, int G, int BP>
 const void* seq_kernel_t() {
+  if constexpr (PACK == TQ_PACK_B3) return reinterpret_cast<const void*>(gemv_seq_b3_kernel<G, BP>);
   return reinterpret_cast<const void*>(gemv_seq_kernel<G, BP>);
 }
-const void* seq_kernel(int G, int Bp) {
+template <int PACK>
+const void* seq_kernel_p(int G, int Bp) {
   if (G == 128) {
     switch (Bp) {
-      case 1: return seq_kernel_t<128, 1>();
-      case 2: return seq_kernel_t<128, 2>();
-      case 4: return seq_kernel_t<128, 4>();
-      default: return seq_kernel_t<128, 8>();
+      case 1: return seq_kernel_t<PACK, 128, 1>();
+      case 2: return seq_kernel_t<PACK, 128, 2>();
+      case 4: return seq_kernel_t<PACK, 128, 4>();
+      default: return seq_kernel_t<PACK, 128, 8>();
     }
   }
   switch (Bp) {
-    case 1: return seq_kernel_t<64, 1>();
-    case 2: return seq_kernel_t<64, 2>();
-    case 4: return seq_kernel_t<64, 4>();
-    default: return seq_kernel_t<64, 8>();
+    case 1: return seq_kernel_t<PACK, 64, 1>();
+    case 2: return seq_kernel_t<PACK, 64, 2>();
+    case 4: return seq_kernel_t<PACK, 64, 4>();
+    default: return seq_kernel_t<PACK, 64, 8>();
   }
+}
+const void* seq_kernel(int pack, int G, int Bp) {
+  return pack == TQ_PACK_B3 ? seq_kernel_p<TQ_PACK_B3>(G, Bp) : seq_kernel_p<TQ_PACK_2BIT>(G, Bp);
 }
 
 }  // namespace
@@ -750,15 +1127,15 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   if (!out) return TQ_ERR_INVALID_ARG;
   *out = nullptr;
   if (!calls || ncalls < 1 || batch < 1 || batch > 8) return TQ_ERR_INVALID_ARG;
-  const int G = calls[0].d.group;
+  const int G = calls[0].d.group, pack = calls[0].d.packing;
   int Kmax = 0;
   for (int j = 0; j < ncalls; ++j) {
     const tq_seq_call& c = calls[j];
     tq_status st = check_linear_desc(&c.d);
     if (st != TQ_OK) return st;
-    if (c.d.packing != TQ_PACK_2BIT || c.d.group != G) return TQ_ERR_UNSUPPORTED;
-    // FP16 scales are fetched by TMA: a scale row must be a multiple of 16 bytes
-    if ((c.d.K / c.d.group) % 8 != 0 || c.d.N % 4 != 0) return TQ_ERR_UNSUPPORTED;
+    if (c.d.packing != pack || c.d.group != G) return TQ_ERR_UNSUPPORTED;
+    // 2-bit: FP16 scales are fetched by TMA, so a scale row must be a multiple of 16 bytes
+    if ((pack == TQ_PACK_2BIT && (c.d.K / c.d.group) % 8 != 0) || c.d.N % 4 != 0) return TQ_ERR_UNSUPPORTED;
     if (!c.codes || !c.scales || !c.y) return TQ_ERR_INVALID_ARG;
     if (!aligned(c.codes, 16) || !aligned(c.scales, 16) || !aligned(c.y, 16)) return TQ_ERR_MISALIGNED;
     if (c.x_src == TQ_SEQ_X_BF16) {
@@ -790,6 +1167,10 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   s->G = G;
   s->grid = sms;
   s->dev = dev;
+  s->pack = pack;
+  const bool b3p = pack == TQ_PACK_B3;
+  const int rows = b3p ? b3::kRows : kRows, item = b3p ? b3::kItemTrits : kItemTrits;
+  s->nw = b3p ? b3::kNW : kNW;
   // per-call work split; the most K slices any CTA covers, the largest item count
   s->calls.resize(ncalls);
   long long Tmax = 0;
@@ -798,14 +1179,15 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
     CallDev& d = s->calls[j];
     std::memset(&d, 0, sizeof(d));
     d.x = c.x_src == TQ_SEQ_X_BF16 ? c.x : nullptr;
+    d.scales = c.scales;
     d.y = c.y;
     d.N = c.d.N;
     d.K = c.d.K;
     d.ng = c.d.K / G;
     d.mode = c.x_src;
     d.apply = c.d.fwht_block != 0;
-    d.nru = (c.d.N + kRows - 1) / kRows;
-    d.nku = (c.d.K + kItemTrits - 1) / kItemTrits;
+    d.nru = (c.d.N + rows - 1) / rows;
+    d.nku = (c.d.K + item - 1) / item;
     const long long T = static_cast<long long>(d.nru) * d.nku;
     if (T * sms >= (1ll << 31)) {
       delete s;
@@ -819,39 +1201,48 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
       if (b > a) s->nkc = std::max(s->nkc, (b - 1) / d.nru - a / d.nru + 1);
     }
   }
-  // shared memory: rings, x^ of the CTA's K slices, zero chunk, V, F, barriers, flags
-  const int GPI = kItemTrits / G;
-  const int kD = ring_depth(s->Bp);
+  // shared memory: rings, scales (2-bit: their ring; base-3: a per-warp staging area), x^ of the CTA's K
+  // slices, zero chunk, V, F, barriers, flags, and for base-3 the chunk table
+  const int GPI = item / G;
+  const int kD = b3p ? b3::kD : ring_depth(s->Bp);
   const size_t xh = align256(static_cast<size_t>(s->nkc) * GPI * s->Bp * 2 * G);
   const size_t vf = align256(static_cast<size_t>(s->nkc * GPI + 8) * s->Bp * 4);
-  size_t off = static_cast<size_t>(kNW) * kD * kCodeStage;
-  s->off_scales = static_cast<uint32_t>(off);
-  off += static_cast<size_t>(kNW) * kD * kScaleStage;
-  s->off_xh = static_cast<uint32_t>(off);
-  off += xh;
-  s->off_zero = static_cast<uint32_t>(off);
-  off += 256;
-  s->off_v = static_cast<uint32_t>(off);
-  off += vf;
-  s->off_f = static_cast<uint32_t>(off);
-  off += vf;
-  s->off_bar = static_cast<uint32_t>(off);
-  off += align256(static_cast<size_t>(kNW) * kD * 8);
-  s->off_misc = static_cast<uint32_t>(off);
-  off += 256;
-  s->smem = off + 1024;  // alignment slack of the base
+  auto layout = [&]() {
+    size_t off = static_cast<size_t>(s->nw) * kD * (b3p ? b3::kCodeStage : kCodeStage);
+    s->off_scales = static_cast<uint32_t>(off);
+    off += b3p ? align256(static_cast<size_t>(s->nw) * GPI * 64 * 2) : static_cast<size_t>(kNW) * kD * kScaleStage;
+    s->off_xh = static_cast<uint32_t>(off);
+    off += xh;
+    s->off_zero = static_cast<uint32_t>(off);
+    off += 256;
+    s->off_v = static_cast<uint32_t>(off);
+    off += vf;
+    s->off_f = static_cast<uint32_t>(off);
+    off += vf;
+    s->off_bar = static_cast<uint32_t>(off);
+    off += align256(static_cast<size_t>(s->nw) * kD * 8 + 8);  // base-3: one more, the table copy's
+    s->off_misc = static_cast<uint32_t>(off);
+    off += 256;
+    if (b3p) {
+      s->off_lut = static_cast<uint32_t>(off);
+      off += align256(b3::kLutBytes);
+    }
+    s->smem = off + 1024;  // alignment slack of the base
+  };
+  layout();
   if (s->smem > kSmemLimit || s->smem > static_cast<size_t>(optin)) {
     delete s;
     return TQ_ERR_UNSUPPORTED;  // the activations of the widest CTA range do not fit shared memory
   }
-  s->kern = seq_kernel(G, s->Bp);
+  s->kern = seq_kernel(pack, G, s->Bp);
   if ((e = cudaFuncSetAttribute(s->kern, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(s->smem))) !=
       cudaSuccess) {
     delete s;
     return cuda_fail(e);
   }
   int bps = 0;
-  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, s->kern, kNW * 32, s->smem)) != cudaSuccess || bps < 1) {
+  if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&bps, s->kern, s->nw * 32, s->smem)) != cudaSuccess ||
+      bps < 1) {
     delete s;
     return e != cudaSuccess ? cuda_fail(e) : TQ_ERR_UNSUPPORTED;
   }
@@ -859,17 +1250,18 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
     const tq_seq_call& c = calls[j];
     CallDev& d = s->calls[j];
     const int P = pitch_words(c.d.K, c.d.packing);
+    // codes: box of 32 words x one item's rows, 128-byte swizzle; 2-bit scales: box of 8 groups
     if (!make_tmap_2d(&d.tm_codes, c.codes, CU_TENSOR_MAP_DATA_TYPE_UINT32, static_cast<uint64_t>(P),
-                      static_cast<uint64_t>(c.d.N), static_cast<uint64_t>(P) * 4u, 32u, kRows,
+                      static_cast<uint64_t>(c.d.N), static_cast<uint64_t>(P) * 4u, 32u, static_cast<uint32_t>(rows),
                       CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_tmap_2d(&d.tm_scales, c.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, static_cast<uint64_t>(d.ng),
-                      static_cast<uint64_t>(c.d.N), static_cast<uint64_t>(d.ng) * 2u, 8u, kRows,
-                      CU_TENSOR_MAP_SWIZZLE_NONE)) {
+        (!b3p && !make_tmap_2d(&d.tm_scales, c.scales, CU_TENSOR_MAP_DATA_TYPE_UINT16, static_cast<uint64_t>(d.ng),
+                               static_cast<uint64_t>(c.d.N), static_cast<uint64_t>(d.ng) * 2u, 8u, kRows,
+                               CU_TENSOR_MAP_SWIZZLE_NONE))) {
       delete s;
       return TQ_ERR_CUDA;
     }
   }
-  s->part_stride = static_cast<size_t>(Tmax) * s->Bp * kRows;
+  s->part_stride = static_cast<size_t>(Tmax) * s->Bp * rows;
   s->ssq_stride = (Kmax / kFwhtBlock) * s->Bp;
   s->ws_calls = align256(sizeof(CallDev) * ncalls);
   s->ws_sync = align256((kFlagBase + static_cast<size_t>(sms)) * 4);
@@ -921,9 +1313,10 @@ extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) 
   prm.off_f = s->off_f;
   prm.off_bar = s->off_bar;
   prm.off_misc = s->off_misc;
+  prm.off_lut = s->off_lut;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(s->grid);
-  cfg.blockDim = dim3(kNW * 32);
+  cfg.blockDim = dim3(s->nw * 32);
   cfg.dynamicSmemBytes = s->smem;
   cfg.stream = static_cast<cudaStream_t>(stream);
   cudaLaunchAttribute attr[1];

@@ -1,4 +1,4 @@
-"""tq_seq (a decode step: a chain of dependent 2-bit GEMVs in one launch) against the oracle.
+"""tq_seq (a decode step: a chain of dependent 2-bit or base-3 GEMVs in one launch) against the oracle.
 
 Each call of the chain is checked on its own input: call 0 on the bf16 x, a TQ_SEQ_X_PREV call on
 the GPU's own output of the call before it, a TQ_SEQ_X_SWIGLU_PREV call on silu(gate) * up formed
@@ -19,18 +19,18 @@ from tq_testlib import check_tolerance
 
 pytestmark = pytest.mark.gpu
 
-B2 = tq.TQ_PACK_2BIT
+B2, B3 = tq.TQ_PACK_2BIT, tq.TQ_PACK_B3
 BF16, PREV, SWIGLU, RMS = tq.TQ_SEQ_X_BF16, tq.TQ_SEQ_X_PREV, tq.TQ_SEQ_X_SWIGLU_PREV, tq.TQ_SEQ_X_RMS_PREV
 
 
 class Chain:
     """Seeded weights for a list of (N, K, x_src) calls, the plan, and the per-call oracle check."""
 
-    def __init__(self, seed, shapes, batch, group=128, x_tid=999):
-        self.seed, self.shapes, self.batch, self.group = seed, shapes, batch, group
+    def __init__(self, seed, shapes, batch, group=128, x_tid=999, packing=B2):
+        self.seed, self.shapes, self.batch, self.group, self.packing = seed, shapes, batch, group, packing
         self.descs, self.codes, self.scales, self.ys = [], [], [], []
         for j, (N, K, _) in enumerate(shapes):
-            d = tq.desc(N, K, group, B2)
+            d = tq.desc(N, K, group, packing)
             self.descs.append(d)
             self.codes.append(tq.tq_pack(d, inputs.trits(seed, 2 * j, N, K, device="cuda")))
             self.scales.append(inputs.scales(seed, 2 * j + 1, N, K // group, device="cuda").contiguous())
@@ -69,7 +69,7 @@ class Chain:
             rr = rows[r0:r0 + chunk]
             t = inputs.trits(self.seed, 2 * j, N, K, rows=rr).numpy()
             s = inputs.scales(self.seed, 2 * j + 1, N, K // self.group, rows=rr).numpy()
-            y_ref, A, bad = O.ternary_linear(O.pack(t, B2), s, x, K, self.group, B2, 128)
+            y_ref, A, bad = O.ternary_linear(O.pack(t, self.packing), s, x, K, self.group, self.packing, 128)
             assert bad == 0
             extra = None
             if kind == "rms":
@@ -89,38 +89,54 @@ SMALL_G128 = [(2048, 1024, BF16), (1024, 1024, PREV), (4096, 1024, RMS), (1024, 
 SMALL_G64 = [(512, 512, BF16), (2048, 512, RMS), (512, 1024, SWIGLU), (96, 512, PREV)]
 
 
+# Base-3 items are 640 trits x 64 rows: K = 1024 and 512 end in a partial item (3 of 5 groups of 128,
+# 8 of 10 groups of 64), N = 1000 and 96 in a partial row unit (rows past N read as zero codes).
+@pytest.mark.parametrize("packing", [B2, B3])
 @pytest.mark.parametrize("batch", [1, 2, 3, 4])
-def test_chain_small_group128(batch):
-    c = Chain(41 + batch, SMALL_G128, batch)
+def test_chain_small_group128(packing, batch):
+    c = Chain(41 + batch, SMALL_G128, batch, packing=packing)
     ys = c.run()
     for j in range(len(SMALL_G128)):
         c.check_call(j, ys)
 
 
+@pytest.mark.parametrize("packing", [B2, B3])
 @pytest.mark.parametrize("batch", [1, 2, 8])
-def test_chain_small_group64(batch):
-    c = Chain(51 + batch, SMALL_G64, batch, group=64)
+def test_chain_small_group64(packing, batch):
+    c = Chain(51 + batch, SMALL_G64, batch, group=64, packing=packing)
     ys = c.run()
     for j in range(len(SMALL_G64)):
         c.check_call(j, ys)
 
 
-def test_chain_full_size_layer_every_output():
+@pytest.mark.parametrize("packing", [B2, B3])
+def test_chain_full_size_layer_every_output(packing):
     """One 27B-class decoder layer as the decode step calls it (qkv 7168 x 5120 on x; o on the
     attention stand-in = the q part of qkv; gate_up 34816 x 5120 on the RMS-normalised o output;
     down 5120 x 17408 on SwiGLU), then the next layer's qkv on the RMS-normalised layer output;
     batch 1, the configuration of the decode benchmark.
     Every output of every call is compared with the oracle."""
     shapes = [(7168, 5120, BF16), (5120, 5120, PREV), (34816, 5120, RMS), (5120, 17408, SWIGLU), (7168, 5120, RMS)]
-    c = Chain(inputs.seed_of(5) + 7, shapes, 1)
+    c = Chain(inputs.seed_of(5) + 7, shapes, 1, packing=packing)
     ys = c.run()
     for j in range(len(shapes)):
         c.check_call(j, ys)
 
 
-def test_determinism_and_graph_replay():
+def test_base3_full_size_batch8_sampled():
+    """The same layer in base-3 at batch 8 (the largest batch tile): 512 sampled rows of each call."""
+    shapes = [(7168, 5120, BF16), (5120, 5120, PREV), (34816, 5120, RMS), (5120, 17408, SWIGLU)]
+    c = Chain(inputs.seed_of(5) + 9, shapes, 8, packing=B3)
+    ys = c.run()
+    rng = np.random.default_rng(5)
+    for j, (N, _, _) in enumerate(shapes):
+        c.check_call(j, ys, rows=np.sort(rng.choice(N, 512, replace=False)))
+
+
+@pytest.mark.parametrize("packing", [B2, B3])
+def test_determinism_and_graph_replay(packing):
     """Results do not depend on timing: two runs and a CUDA-graph replay are bit-identical."""
-    c = Chain(61, SMALL_G128, 2)
+    c = Chain(61, SMALL_G128, 2, packing=packing)
     first = c.run()
     second = c.run()
     for a, b in zip(first, second):
@@ -157,17 +173,20 @@ def test_rejected_on_the_host():
     d640 = tq.desc(1024, 640, 128, B2)
     assert status([(d640, codes, scales, BF16, x, y)]) == 2                   # scale rows of 10 bytes
     d3 = tq.desc(1024, 1024, 128, tq.TQ_PACK_B3)
-    assert status([(d3, codes, scales, BF16, x, y)]) == 2                     # base-3 not supported here
+    assert status([(d, codes, scales, BF16, x, y), (d3, codes, scales, PREV, None, y)]) == 2  # mixed packings
+    dq = tq.desc(1024, 1024, 128, tq.TQ_PACK_3BIT)
+    assert status([(dq, codes, scales, BF16, x, y)]) == 2                     # 3-bit codes
     ok = tq.tq_seq_create([(d, codes, scales, BF16, x, y)], 1)
     assert tq.tq_seq_kernel_count(ok) == 1
     tq.tq_seq_destroy(ok)
 
 
+@pytest.mark.parametrize("packing", [B2, B3])
 @pytest.mark.parametrize("batch", [2, 8])
-def test_chain_mixed_magnitude_rows(batch):
+def test_chain_mixed_magnitude_rows(packing, batch):
     """Batch rows 1e7 apart in size in one decode step (even rows x 1e4, odd rows x 1e-3): every call
     holds each row to its own bound (per-row block exponents; RMS normalisation per row)."""
-    c = Chain(81 + batch, SMALL_G128[:4], batch)
+    c = Chain(81 + batch, SMALL_G128[:4], batch, packing=packing)
     mult = torch.tensor([1e4 if b % 2 == 0 else 1e-3 for b in range(batch)]).reshape(batch, 1)
     c.x_host = (c.x_host.float() * mult).to(torch.bfloat16)
     c.x.copy_(c.x_host.cuda())
