@@ -21,6 +21,7 @@
 
 #include "tq_internal.cuh"
 #include "tq_kernels.cuh"
+#include "tq_sm100.cuh"
 
 namespace tq {
 namespace {
@@ -29,9 +30,11 @@ constexpr int kMaxExperts = 256;
 constexpr int kMaxTopk = 8;
 
 // Token t, one warp: k rounds of a warp-wide argmax with the order (logit descending, expert index
-// ascending); gate = softmax over the chosen logits, summed in slot order.
+// ascending); gate = softmax over the chosen logits, summed in slot order.  s_idx (optional): a
+// shared-memory copy of the token's expert indices, at the same offsets as idx.
 __device__ __forceinline__ void route_token(const float* __restrict__ logits, int t, int E, int topk,
-                                            int* __restrict__ idx, float* __restrict__ gate, int lane) {
+                                            int* __restrict__ idx, float* __restrict__ gate, int lane,
+                                            int* s_idx = nullptr) {
   float v[kMaxExperts / 32];
 #pragma unroll
   for (int i = 0; i < kMaxExperts / 32; ++i) {
@@ -74,6 +77,7 @@ __device__ __forceinline__ void route_token(const float* __restrict__ logits, in
       if (j < topk) {
         idx[static_cast<size_t>(t) * topk + j] = sel_i[j];
         gate[static_cast<size_t>(t) * topk + j] = ex[j] / sum;
+        if (s_idx) s_idx[t * topk + j] = sel_i[j];
       }
   }
 }
@@ -99,14 +103,14 @@ __global__ void __launch_bounds__(kPlanThreads) moe_plan_kernel(const float* __r
   extern __shared__ int s_assign[];  // min(A, kPlanSmemAssign) expert indices
   __shared__ int s_cnt[kMaxExperts], s_off[kMaxExperts], s_wsum[kMaxExperts / 32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, A = T * topk;
-  for (int t = warp; t < T; t += kPlanThreads / 32) route_token(logits, t, E, topk, idx, gate, lane);
+  const bool in_smem = A <= kPlanSmemAssign;
+  for (int t = warp; t < T; t += kPlanThreads / 32)
+    route_token(logits, t, E, topk, idx, gate, lane, in_smem ? s_assign : nullptr);
   for (int i = threadIdx.x; i < ncount; i += kPlanThreads) count[i] = 0;
   for (int e = threadIdx.x; e < kMaxExperts; e += kPlanThreads) s_cnt[e] = 0;
-  __syncthreads();  // idx is complete (global writes of this CTA, read back below)
-  const bool in_smem = A <= kPlanSmemAssign;
+  __syncthreads();  // idx is complete (in shared memory, or global writes of this CTA read back below)
   for (int a = threadIdx.x; a < A; a += kPlanThreads) {
-    const int e = __ldcg(idx + a);
-    if (in_smem) s_assign[a] = e;
+    const int e = in_smem ? s_assign[a] : __ldcg(idx + a);
     atomicAdd(&s_cnt[e], 1);
   }
   __syncthreads();
