@@ -725,8 +725,8 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
 }
 
 // ---- base-3 --------------------------------------------------------------------------------------
-// The same step over base-3 codes (20 trits per 32-bit word, the TurboQuant-MLX page, "为什么 1.58bit
-// 没变成乱码", point 3), in the column layout of the per-call base-3 decode: a warp owns 64 rows, lane l
+// The same step over base-3 codes (20 trits per 32-bit word: the TurboQuant-MLX 1.58-bit Qwen3.6-35B-A3B
+// page, "为什么 1.58bit 没变成乱码", point 3), in the column layout of the per-call base-3 decode: a warp owns 64 rows, lane l
 // decodes rows l and l + 32 word by word (two reciprocal multiplies split a word into four 5-trit
 // chunks, a table in shared memory places each chunk's digits in FP16 pair fields, one mask per
 // pair gives an operand register), and the B operand of an MMA is zero except in the column of the
@@ -775,9 +775,11 @@ struct ItemScales {
 };
 
 // One item: the warp's 64 rows x the item's ngi groups, folded into acc (rows rl0, rl0 + 1, rl0 + 32,
-// rl0 + 33 of the item for batch row 2t + bq of tile t).  box: the item's swizzled codes; xh32: x^ of
-// the CTA's slice (MMA pair mp, batch row b at words (mp * BP + b) * 4); mp0: the item's first MMA pair
-// in the slice; V / Fv at local group lg_item0 + gl, batch row b: lg * BP + b.
+// rl0 + 33 of the item for batch row 2t + bq of tile t).  box: the item's swizzled codes; bptr / bstr:
+// where this lane's B operand of tile t comes from and its stride per MMA pair (x^ of the CTA's slice,
+// MMA pair mp and batch row b at words (mp * BP + b) * 4, or the zero chunk with stride 0); mp0: the
+// item's first MMA pair in the slice; V / Fv of local group lg = lg_item0 + gl, batch row b at
+// lg * BP + b; swr: the staged scales at this lane's first accumulator row.
 template <int G, int BP, bool FULL>
 __device__ __forceinline__ void b3_item(const uint4* __restrict__ box, int lane, int ngi, const uint32_t* __restrict__ lutA,
                                         const uint32_t* __restrict__ lutB, const uint32_t* const (&bptr)[(BP + 1) / 2],
