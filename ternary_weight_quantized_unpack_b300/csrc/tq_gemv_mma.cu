@@ -1444,10 +1444,13 @@ size_t layout(Plan& pl, int pack, int B, int G, int K) {
   return pl.smem;
 }
 
-// Candidate splits in order of estimated time: per-warp units x busiest-SM warps (at least 12, below
-// which a warp's own latency dominates); ties go to fewer CTAs, then to smaller clusters.
+// Candidate splits in order of estimated time: per-warp units x busiest-SM warps (at least 12, 24 for
+// 3-bit codes, below which a warp's own latency dominates); ties go to fewer CTAs, then to smaller
+// clusters.
 std::vector<Plan> candidates(const tq_desc* d, int B) {
   const int UT = unit_codes(d->packing), SLAB = slab_rows(d->packing);
+  // the 3-bit kernel (a serial chain per warp, one TMA box per unit) keeps gaining up to ~24 warps
+  const double min_warps = d->packing == TQ_PACK_3BIT ? 24.0 : 12.0;
   const int upr = (d->K + UT - 1) / UT;
   const int slabs = (d->N + SLAB - 1) / SLAB;
   std::vector<std::tuple<double, int, int, Plan>> list;
@@ -1466,7 +1469,7 @@ std::vector<Plan> candidates(const tq_desc* d, int B) {
         if (layout(pl, d->packing, B, d->group, d->K) > kSmemLimit) continue;
         const long long C = static_cast<long long>(pl.n_rg) * ks;
         const long long k = (C + kSMs - 1) / kSMs;
-        const double cost = pl.ppl * std::max<double>(static_cast<double>(k * rs * kl), 12.0);
+        const double cost = pl.ppl * std::max<double>(static_cast<double>(k * rs * kl), min_warps);
         list.emplace_back(cost, static_cast<int>(C), ks, pl);
       }
     }
