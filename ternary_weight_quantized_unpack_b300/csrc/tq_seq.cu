@@ -91,8 +91,11 @@ struct Params {
   const CallDev* calls;
   int ncalls, B;
   int* status;
-  unsigned* sync;         // [0]: barrier arrivals, [1]: CTAs that have exited, [64 + cta]: ready flags
+  unsigned* sync;         // [0]: barrier arrivals, [1]: CTAs that have exited, [2]: launches completed,
+                          // [64 + cta]: ready flags
   float* part;            // partial sums: [2][items][Bp][32] (parity of the call)
+  uint64_t* hand;         // batch 1-2: each call's output as (epoch << 32 | value bits): [2][Bp][N]
+  size_t hand_stride;     // words per parity of hand
   float* ssq;             // per 128-block sums of squares of an RMS-normalised input: [2][blocks][Bp]
   size_t part_stride;     // floats per parity of part
   int ssq_stride;         // floats per parity of ssq
@@ -165,6 +168,45 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag, unsigned want) {
   }
 }
 
+// ---- handoff of a finished call's output (base-3, batch 1 and 2) ------------------------------------
+// The lanes that finalize an output value also write it with its call's epoch in one 64-bit word
+// (epoch in the high half, the float's bits in the low half; launch-unique: launches completed x
+// calls + call + 1).  A consumer polls the words it reads: a word whose epoch matches carries the
+// value itself, so reading needs one L2 round trip and no ready flag.  One 64-bit access is
+// single-copy atomic, so a value is never seen with another call's epoch.  Used by the base-3 kernel
+// at batch 1 and 2 (4.07 instead of 4.27 ms per 64-layer token); the 2-bit kernel keeps the flags
+// (measured 3.42 instead of 3.02 ms with the handoff: there the consumers reach their polls while the
+// producers still finalize, and every lane's polling competes with the producers' L2 traffic).
+__host__ __device__ constexpr bool hand_batch(int pack, int Bp) { return pack == TQ_PACK_B3 && Bp <= 2; }
+__device__ __forceinline__ void st_hand2(uint64_t* p, uint64_t a, uint64_t b) {
+  asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
+}
+__device__ __forceinline__ void ld_hand2(const uint64_t* p, uint64_t& a, uint64_t& b) {
+  asm volatile("ld.relaxed.gpu.global.v2.u64 {%0, %1}, [%2];" : "=l"(a), "=l"(b) : "l"(p) : "memory");
+}
+__device__ __forceinline__ bool hand_ready(const uint64_t (&w)[4], uint32_t epoch) {
+  return static_cast<uint32_t>(w[0] >> 32) == epoch && static_cast<uint32_t>(w[1] >> 32) == epoch &&
+         static_cast<uint32_t>(w[2] >> 32) == epoch && static_cast<uint32_t>(w[3] >> 32) == epoch;
+}
+// Four consecutive values (rows k..k+3 of one batch row) whose first poll was w: poll again until
+// all four carry `epoch` (bounded; *abort on timeout), and return them.
+__device__ __forceinline__ float4 hand_take(const uint64_t* h, uint32_t epoch, uint64_t (&w)[4], int* abort) {
+  if (!hand_ready(w, epoch)) {
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 0;; ++i) {
+      ld_hand2(h, w[0], w[1]);
+      ld_hand2(h + 2, w[2], w[3]);
+      if (hand_ready(w, epoch)) break;
+      if ((i & 63u) == 63u && global_timer_ns() - t0 > kWaitNs) {
+        *abort = 1;
+        break;
+      }
+    }
+  }
+  return make_float4(__uint_as_float(static_cast<uint32_t>(w[0])), __uint_as_float(static_cast<uint32_t>(w[1])),
+                     __uint_as_float(static_cast<uint32_t>(w[2])), __uint_as_float(static_cast<uint32_t>(w[3])));
+}
+
 // ---- finalizing a call's output rows -------------------------------------------------------------
 // Output scale of an RMS-mode call for batch row b (1 / rms of its own input), for the lane's b; one
 // warp, every batch row's loads in flight together.  The per-block sums of squares are added in a
@@ -193,9 +235,9 @@ __device__ __forceinline__ float out_scale_warp(const CallLite& c, const float* 
 // 4-row chunk: lane s adds the slices [s * per, (s + 1) * per) (all its loads issued before the
 // adds), then the group combines its sums by a fixed butterfly.  The result does not depend on which
 // CTA computes it, and the partial sums and the sums of squares of the scale are in flight together.
-template <int BP, int ROWS>
+template <int BP, int ROWS, bool HAND>
 __device__ __forceinline__ void finalize(const CallLite& c, const float* ppart, const float* ssq, int B, int fr0,
-                                         int nr) {
+                                         int nr, uint64_t* hand, uint32_t epoch) {
   const int lane = static_cast<int>(threadIdx.x & 31);
   int nsp = 1;
   while (nsp * kGatherKu < c.nku) nsp <<= 1;  // lanes per chunk (a power of two up to 32)
@@ -230,9 +272,16 @@ __device__ __forceinline__ void finalize(const CallLite& c, const float* ppart, 
       a.z += __shfl_xor_sync(0xffffffffu, a.z, m);
       a.w += __shfl_xor_sync(0xffffffffu, a.w, m);
     }
-    if (valid && s == 0)
-      *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + k) =
-          make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+    if (valid && s == 0) {
+      const float4 r = make_float4(a.x * sc, a.y * sc, a.z * sc, a.w * sc);
+      *reinterpret_cast<float4*>(c.y + static_cast<size_t>(b) * c.N + k) = r;
+      if constexpr (HAND) {
+        uint64_t* h = hand + static_cast<size_t>(b) * c.N + k;
+        const uint64_t e = static_cast<uint64_t>(epoch) << 32;
+        st_hand2(h, e | __float_as_uint(r.x), e | __float_as_uint(r.y));
+        st_hand2(h + 2, e | __float_as_uint(r.z), e | __float_as_uint(r.w));
+      }
+    }
   }
 }
 
@@ -281,9 +330,27 @@ struct LaneLayout {
 template <int PACK, int G, int BP>
 __device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, const CallLite& pc, unsigned want,
                                            int* abort, int blk, int lg0, const LaneLayout<G>& L, uint8_t* xh,
-                                           float* V, float* Fv, float* ssq, int lane) {
+                                           float* V, float* Fv, float* ssq, int lane, const uint64_t* hand_prev,
+                                           uint32_t epoch_prev) {
   const int k0 = blk * kFwhtBlock + 4 * lane;
-  if (c.mode != 0) {
+  // handoff (base-3, batch 1-2): the previous output's words, all first polls in flight together
+  constexpr bool HAND = hand_batch(PACK, BP);
+  constexpr int HB = HAND ? BP : 1;
+  uint64_t hw[HB][2][4];
+  if constexpr (HAND) {
+    if (c.mode != 0) {
+#pragma unroll
+      for (int b = 0; b < BP; ++b)
+#pragma unroll
+        for (int sg = 0; sg < 2; ++sg)
+          if (b < p.B && (sg == 0 || c.mode == 2)) {
+            const uint64_t* h = hand_prev + static_cast<size_t>(b) * pc.N + (sg ? c.K : 0) + k0;
+            ld_hand2(h, hw[b][sg][0], hw[b][sg][1]);
+            ld_hand2(h + 2, hw[b][sg][2], hw[b][sg][3]);
+          }
+    }
+  }
+  if (!HAND && c.mode != 0) {
     const unsigned* flags = p.sync + kFlagBase;
     const int grid = static_cast<int>(gridDim.x), kb = blk * kFwhtBlock;
     const int lo = fin_owner(pc.N, grid, kb), n1 = fin_owner(pc.N, grid, kb + kFwhtBlock - 4) - lo + 1;
@@ -306,15 +373,26 @@ __device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, c
       v[b][2] = bf16_bits_to_float(static_cast<uint16_t>(raw.y & 0xffffu));
       v[b][3] = bf16_bits_to_float(static_cast<uint16_t>(raw.y >> 16));
     } else if (c.mode == 2) {
-      const float* yb = pc.y + static_cast<size_t>(b) * pc.N;
-      const float4 g4 = __ldcg(reinterpret_cast<const float4*>(yb + k0));
-      const float4 u4 = __ldcg(reinterpret_cast<const float4*>(yb + c.K + k0));
+      float4 g4, u4;
+      if constexpr (HAND) {
+        const uint64_t* h = hand_prev + static_cast<size_t>(b) * pc.N + k0;
+        g4 = hand_take(h, epoch_prev, hw[b][0], abort);
+        u4 = hand_take(h + c.K, epoch_prev, hw[b][1], abort);
+      } else {
+        const float* yb = pc.y + static_cast<size_t>(b) * pc.N;
+        g4 = __ldcg(reinterpret_cast<const float4*>(yb + k0));
+        u4 = __ldcg(reinterpret_cast<const float4*>(yb + c.K + k0));
+      }
       v[b][0] = silu_f(g4.x) * u4.x;
       v[b][1] = silu_f(g4.y) * u4.y;
       v[b][2] = silu_f(g4.z) * u4.z;
       v[b][3] = silu_f(g4.w) * u4.w;
     } else {
-      const float4 a = __ldcg(reinterpret_cast<const float4*>(pc.y + static_cast<size_t>(b) * pc.N + k0));
+      float4 a;
+      if constexpr (HAND)
+        a = hand_take(hand_prev + static_cast<size_t>(b) * pc.N + k0, epoch_prev, hw[b][0], abort);
+      else
+        a = __ldcg(reinterpret_cast<const float4*>(pc.y + static_cast<size_t>(b) * pc.N + k0));
       v[b][0] = a.x, v[b][1] = a.y, v[b][2] = a.z, v[b][3] = a.w;
     }
   }
@@ -481,6 +559,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   bool abort = false;
   const LaneLayout<G> L(lane);
   unsigned nbar = 0;  // grid barriers passed
+  const uint32_t launch_seq = __ldcg(p.sync + 2);  // launches completed (advanced by the last CTA out)
   for (int j = 0; j < p.ncalls && !abort; ++j) {
     const CallLite c(p.calls[j]);
     const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
@@ -501,7 +580,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
         prep_block<TQ_PACK_2BIT, G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G), L, xh,
-                          V, Fv, ssq, lane);
+                          V, Fv, ssq, lane, nullptr, 0);
     }
     __syncthreads();
     if (s_flag[0] != 0) {  // a ready flag did not come in time
@@ -693,7 +772,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     {
       int fr0, fr1;
       fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
-      finalize<BP, kRows>(c, part, ssq, p.B, fr0, fr1 - fr0);
+      finalize<BP, kRows, false>(c, part, ssq, p.B, fr0, fr1 - fr0, nullptr, 0);
     }
     // ---- this CTA's rows are final: raise its flag ----
     __syncthreads();
@@ -719,6 +798,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
       p.sync[0] = 0u;
       p.sync[1] = 0u;
+      p.sync[2] = launch_seq + 1u;
       __threadfence();
     }
   }
@@ -949,6 +1029,9 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
   const int rl0 = 4 * g + ((2 * q) & 3);  // this lane's accumulator rows: rl0, rl0 + 1, rl0 + 32, rl0 + 33
   ItemScales<GPI> us;
   unsigned nbar = 0;
+  // epochs of this launch's calls: launches completed (stable during a launch) x calls + call + 1
+  const uint32_t launch_seq = __ldcg(p.sync + 2);
+  const uint32_t epoch0 = launch_seq * static_cast<uint32_t>(p.ncalls);
   for (int j = 0; j < p.ncalls && !abort; ++j) {
     const CallLite c(p.calls[j]);
     const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
@@ -971,7 +1054,8 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
         prep_block<TQ_PACK_B3, G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G),
-                                      L, xh, V, Fv, ssq, lane);
+                                      L, xh, V, Fv, ssq, lane,
+                                      p.hand + static_cast<size_t>((j - 1) & 1) * p.hand_stride, epoch0 + j);
     }
     __syncthreads();
     if (s_flag[0] != 0) {  // a ready flag did not come in time
@@ -1048,10 +1132,14 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
     {
       int fr0, fr1;
       fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
-      finalize<BP, kRows>(c, part, ssq, p.B, fr0, fr1 - fr0);
+      finalize<BP, kRows, hand_batch(TQ_PACK_B3, BP)>(c, part, ssq, p.B, fr0, fr1 - fr0,
+                                                      p.hand + static_cast<size_t>(j & 1) * p.hand_stride, epoch0 + j + 1);
     }
-    __syncthreads();
-    if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
+    // ---- this CTA's rows are final: raise its flag (unless they were handed over with their epochs) ----
+    if constexpr (!hand_batch(TQ_PACK_B3, BP)) {
+      __syncthreads();
+      if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
+    }
   }
 
   if (abort) {
@@ -1071,6 +1159,7 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
       for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
       p.sync[0] = 0u;
       p.sync[1] = 0u;
+      p.sync[2] = launch_seq + 1u;
       __threadfence();
     }
   }
@@ -1090,7 +1179,7 @@ struct tq_seq {
   int ncalls = 0, B = 0, Bp = 0, G = 0, grid = 0, nkc = 0, dev = 0, pack = 0, nw = 0;
   size_t smem = 0;
   uint32_t off_scales = 0, off_xh = 0, off_zero = 0, off_v = 0, off_f = 0, off_bar = 0, off_misc = 0, off_lut = 0;
-  size_t ws_calls = 0, ws_sync = 0, ws_part = 0, ws_ssq = 0, ws_bytes = 0, part_stride = 0;
+  size_t ws_calls = 0, ws_sync = 0, ws_part = 0, ws_ssq = 0, ws_hand = 0, ws_bytes = 0, part_stride = 0, hand_stride = 0;
   int ssq_stride = 0;
   const void* kern = nullptr;
 };
@@ -1269,7 +1358,13 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   s->ws_sync = align256((kFlagBase + static_cast<size_t>(sms)) * 4);
   s->ws_part = align256(2 * s->part_stride * 4);
   s->ws_ssq = align256(static_cast<size_t>(2) * s->ssq_stride * 4);
-  s->ws_bytes = s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq;
+  if (hand_batch(pack, s->Bp)) {  // each call's output with its epoch, two parities
+    int Nmax = 0;
+    for (int j = 0; j < ncalls; ++j) Nmax = std::max(Nmax, calls[j].d.N);
+    s->hand_stride = static_cast<size_t>(s->Bp) * Nmax;
+    s->ws_hand = align256(2 * s->hand_stride * 8);
+  }
+  s->ws_bytes = s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq + s->ws_hand;
   *out = s;
   return TQ_OK;
 }
@@ -1284,6 +1379,10 @@ extern "C" tq_status tq_seq_upload(const tq_seq* s, void* workspace, size_t work
   cudaError_t e = cudaMemcpy(ws, s->calls.data(), sizeof(CallDev) * s->ncalls, cudaMemcpyHostToDevice);
   if (e != cudaSuccess) return cuda_fail(e);
   if ((e = cudaMemset(ws + s->ws_calls, 0, s->ws_sync)) != cudaSuccess) return cuda_fail(e);
+  // no stale epochs: the handoff words start at epoch 0, which no call of a run uses
+  if (s->ws_hand &&
+      (e = cudaMemset(ws + s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq, 0, s->ws_hand)) != cudaSuccess)
+    return cuda_fail(e);
   return TQ_OK;
 }
 
@@ -1305,6 +1404,8 @@ extern "C" tq_status tq_seq_run(const tq_seq* s, void* workspace, void* stream) 
   prm.sync = reinterpret_cast<unsigned*>(ws + s->ws_calls);
   prm.part = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync);
   prm.ssq = reinterpret_cast<float*>(ws + s->ws_calls + s->ws_sync + s->ws_part);
+  prm.hand = s->ws_hand ? reinterpret_cast<uint64_t*>(ws + s->ws_calls + s->ws_sync + s->ws_part + s->ws_ssq) : nullptr;
+  prm.hand_stride = s->hand_stride;
   prm.part_stride = s->part_stride;
   prm.ssq_stride = s->ssq_stride;
   prm.nkc = s->nkc;
