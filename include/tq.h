@@ -185,8 +185,8 @@ tq_status tq_gemv_noalloc(const tq_desc* d, const uint32_t* codes, const uint16_
  * tq_seq_create checks the calls and builds a host-side plan (tensor maps of every weight matrix,
  * work split for the current device); it allocates host memory only.  The plan needs a caller-owned
  * device workspace of tq_seq_workspace_bytes(plan) bytes (256-byte aligned), filled once by
- * tq_seq_upload (synchronous: copies the call records, clears the barrier and handoff words) and then used by
- * every tq_seq_run with that plan; tq_seq_run only enqueues the launch (no allocation, no
+ * tq_seq_upload (synchronous: copies the call records, clears the barrier and handoff words) and
+ * then used by every tq_seq_run with that plan; tq_seq_run only enqueues the launch (no allocation, no
  * synchronisation; capturable in a CUDA graph).  Two runs that share a workspace must not overlap.
  * A bounded wait that runs out records TQ_ERR_TIMEOUT in the device status and leaves the workspace's
  * barrier words dirty: call tq_seq_upload again before the next run.  The plan is tied to the device
