@@ -108,6 +108,18 @@ __host__ __device__ __forceinline__ int cta_start(int T, int gp, int cta) {
   return static_cast<int>(static_cast<unsigned>(T) * static_cast<unsigned>(cta) / static_cast<unsigned>(gp));
 }
 
+// This warp's items [a, b) of call c: the CTA's equal share of the call's items, split evenly over
+// its nw warps.
+__device__ __forceinline__ void warp_items(const CallLite& c, int cta, int warp, int nw, int& a, int& b) {
+  if (cta >= c.gp) {
+    a = b = 0;
+    return;
+  }
+  const int ca = cta_start(c.T, c.gp, cta), cb = cta_start(c.T, c.gp, cta + 1), tc = cb - ca;
+  a = ca + (tc * warp) / nw;
+  b = ca + (tc * (warp + 1)) / nw;
+}
+
 // ---- waits ---------------------------------------------------------------------------------------
 __device__ __forceinline__ unsigned ld_acquire(const unsigned* p) {
   unsigned v;
@@ -473,6 +485,35 @@ __device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a1
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }
 
+// ---- leaving a launch ------------------------------------------------------------------------------
+// After an abort, wait (bounded) for this warp's copies still in flight into its ring of kD stages.
+__device__ __forceinline__ void drain_ring(uint64_t* full, int kD, unsigned consumed, unsigned issued, int cst,
+                                           uint32_t cph) {
+  for (; consumed < issued; ++consumed) {
+    if (!mbar_wait(&full[cst], cph)) break;
+    if (++cst == kD) {
+      cst = 0;
+      cph ^= 1u;
+    }
+  }
+}
+// Every thread: the last CTA to leave resets the barrier words and the flags for the next launch and
+// advances the count of completed launches (not after an abort: tq_seq_upload resets them then).
+__device__ __forceinline__ void leave_launch(const Params& p, bool abort, unsigned launch_seq) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(p.sync + 1, 1u);
+    if (prev == gridDim.x - 1 && !abort) {
+      for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
+      p.sync[0] = 0u;
+      p.sync[1] = 0u;
+      p.sync[2] = launch_seq + 1u;
+      __threadfence();
+    }
+  }
+}
+
 // ---- the kernel ----------------------------------------------------------------------------------
 template <int G, int BP>
 __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_constant__ Params p) {
@@ -506,16 +547,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   fence_mbar_init();
   __syncthreads();
 
-  // this warp's item range of a call
-  auto warp_range = [&](const CallLite& c, int& a, int& b) {
-    if (cta >= c.gp) {
-      a = b = 0;
-      return;
-    }
-    const int ca = cta_start(c.T, c.gp, cta), cb = cta_start(c.T, c.gp, cta + 1), tc = cb - ca;
-    a = ca + (tc * warp) / kNW;
-    b = ca + (tc * (warp + 1)) / kNW;
-  };
+  auto warp_range = [&](const CallLite& c, int& a, int& b) { warp_items(c, cta, warp, kNW, a, b); };
 
   // ---- producer state (lane 0 issues; the cursor is kept warp-uniform) ----
   int pcall = 0, pidx = 0, pend = 0, pru = 0, pku = 0, pnru = 0;
@@ -779,29 +811,8 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
   }
 
-  if (abort) {
-    // wind down: wait (bounded) for this warp's copies still in flight before the CTA exits
-    for (; consumed < issued; ++consumed) {
-      if (!mbar_wait(&full[cst], cph)) break;
-      if (++cst == kD) {
-        cst = 0;
-        cph ^= 1u;
-      }
-    }
-  }
-  // the last CTA to leave resets the barrier words for the next launch
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(p.sync + 1, 1u);
-    if (prev == gridDim.x - 1 && !abort) {
-      for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
-      p.sync[0] = 0u;
-      p.sync[1] = 0u;
-      p.sync[2] = launch_seq + 1u;
-      __threadfence();
-    }
-  }
+  if (abort) drain_ring(full, kD, consumed, issued, cst, cph);
+  leave_launch(p, abort, launch_seq);
 }
 
 // ---- base-3 --------------------------------------------------------------------------------------
@@ -970,15 +981,7 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
     bulk_g2s(lut, &g_seq_lut, b3::kLutBytes, lut_bar);
   }
 
-  auto warp_range = [&](const CallLite& c, int& a, int& b) {
-    if (cta >= c.gp) {
-      a = b = 0;
-      return;
-    }
-    const int ca = cta_start(c.T, c.gp, cta), cb = cta_start(c.T, c.gp, cta + 1), tc = cb - ca;
-    a = ca + (tc * warp) / kNW;
-    b = ca + (tc * (warp + 1)) / kNW;
-  };
+  auto warp_range = [&](const CallLite& c, int& a, int& b) { warp_items(c, cta, warp, kNW, a, b); };
 
   // ---- producer state (lane 0 issues; the cursor is kept warp-uniform) ----
   int pcall = 0, pidx = 0, pend = 0, pru = 0, pku = 0, pnru = 0;
@@ -1142,27 +1145,8 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
     }
   }
 
-  if (abort) {
-    for (; consumed < issued; ++consumed) {
-      if (!mbar_wait(&full[cst], cph)) break;
-      if (++cst == kD) {
-        cst = 0;
-        cph ^= 1u;
-      }
-    }
-  }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    __threadfence();
-    const unsigned prev = atomicAdd(p.sync + 1, 1u);
-    if (prev == gridDim.x - 1 && !abort) {
-      for (unsigned c2 = 0; c2 < gridDim.x; ++c2) p.sync[kFlagBase + c2] = 0u;
-      p.sync[0] = 0u;
-      p.sync[1] = 0u;
-      p.sync[2] = launch_seq + 1u;
-      __threadfence();
-    }
-  }
+  if (abort) drain_ring(full, kD, consumed, issued, cst, cph);
+  leave_launch(p, abort, launch_seq);
 }
 
 }  // namespace seq
