@@ -134,6 +134,32 @@ def test_base3_full_size_batch8_sampled():
 
 
 @pytest.mark.parametrize("packing", [B2, B3])
+@pytest.mark.parametrize("batch", [1, 2])
+def test_many_runs_and_reupload(packing, batch):
+    """Forty back-to-back runs of one plan (each run a new launch: the base-3 kernel's handoff words
+    carry a launch-unique epoch from the count of completed launches), then a fresh upload (which
+    resets that count and clears the words) and ten more: every run's outputs are bit-identical to the
+    first run's, and the first run matches the oracle."""
+    c = Chain(71 + batch, SMALL_G128, batch, packing=packing)
+    first = c.run()
+    for j in range(len(SMALL_G128)):
+        c.check_call(j, first)
+    for _ in range(39):
+        c.plan.run()
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    for a, y in zip(first, c.ys):
+        assert np.array_equal(a, y.cpu().numpy())
+    tq.tq_seq_upload(c.plan.handle, c.plan.workspace)
+    for _ in range(10):
+        c.plan.run()
+    torch.cuda.synchronize()
+    assert tq.tq_device_status() == 0
+    for a, y in zip(first, c.ys):
+        assert np.array_equal(a, y.cpu().numpy())
+
+
+@pytest.mark.parametrize("packing", [B2, B3])
 def test_determinism_and_graph_replay(packing):
     """Results do not depend on timing: two runs and a CUDA-graph replay are bit-identical."""
     c = Chain(61, SMALL_G128, 2, packing=packing)
