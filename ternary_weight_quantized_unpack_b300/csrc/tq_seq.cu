@@ -12,10 +12,11 @@
 //    barrier and the next input is being transformed, the next call's weights are already in flight.
 //  * After a call's items, one grid-wide barrier (a counter in the workspace, bounded wait): every
 //    partial sum of the call is written.  Each CTA then turns its share of the call's output rows
-//    into final values (partial sums added in K order, times the output scale) and raises its ready
-//    flag; the next call's CTAs wait (bounded) only for the flags of the CTAs that finalized the
-//    rows they read.  Partial sums and sums of squares alternate between two buffers by the parity
-//    of the call, so a CTA may start the next call while others still finalize this one.
+//    into final values (partial sums added in K order, times the output scale) and hands them over:
+//    at batch 1 and 2 as (epoch, value) words that the next call's readers poll directly, at batch 4
+//    and 8 by raising a ready flag for which those readers wait (bounded) before loading the rows.
+//    Partial sums and sums of squares alternate between two buffers by the parity of the call, so a
+//    CTA may start the next call while others still finalize this one.
 //  * Work split, K-major: the items (32-row unit ru, 512-trit K slice ku) of a call are ordered by
 //    ku, then ru, and divided into equal contiguous ranges, one per CTA (and each into ranges for
 //    its warps).  A CTA therefore works on one or two K slices of many row units: it transforms only
@@ -180,16 +181,16 @@ __device__ __forceinline__ bool wait_flag(const unsigned* flag, unsigned want) {
   }
 }
 
-// ---- handoff of a finished call's output (base-3, batch 1 and 2) ------------------------------------
+// ---- handoff of a finished call's output (batch 1 and 2) -------------------------------------------
 // The lanes that finalize an output value also write it with its call's epoch in one 64-bit word
 // (epoch in the high half, the float's bits in the low half; launch-unique: launches completed x
 // calls + call + 1).  A consumer polls the words it reads: a word whose epoch matches carries the
-// value itself, so reading needs one L2 round trip and no ready flag.  One 64-bit access is
-// single-copy atomic, so a value is never seen with another call's epoch.  Used by the base-3 kernel
-// at batch 1 and 2 (4.07 instead of 4.27 ms per 64-layer token); the 2-bit kernel keeps the flags
-// (measured 3.42 instead of 3.02 ms with the handoff: there the consumers reach their polls while the
-// producers still finalize, and every lane's polling competes with the producers' L2 traffic).
-__host__ __device__ constexpr bool hand_batch(int pack, int Bp) { return pack == TQ_PACK_B3 && Bp <= 2; }
+// value itself, so reading needs one L2 round trip where a ready flag and then the rows took two.
+// One 64-bit access is single-copy atomic, so a value is never seen with another call's epoch.  A
+// CTA barrier still follows the finalize, so that no warp polls while its own CTA finalizes (without
+// it the spinning warps took the finalizing warps' issue slots: 3.4 instead of 3.0 ms per 2-bit
+// token).  Batch 4 and 8 keep the ready flags: their first polls would need too many registers.
+__host__ __device__ constexpr bool hand_batch(int Bp) { return Bp <= 2; }
 __device__ __forceinline__ void st_hand2(uint64_t* p, uint64_t a, uint64_t b) {
   asm volatile("st.relaxed.gpu.global.v2.u64 [%0], {%1, %2};" ::"l"(p), "l"(a), "l"(b) : "memory");
 }
@@ -345,8 +346,8 @@ __device__ __forceinline__ void prep_block(const Params& p, const CallLite& c, c
                                            float* V, float* Fv, float* ssq, int lane, const uint64_t* hand_prev,
                                            uint32_t epoch_prev) {
   const int k0 = blk * kFwhtBlock + 4 * lane;
-  // handoff (base-3, batch 1-2): the previous output's words, all first polls in flight together
-  constexpr bool HAND = hand_batch(PACK, BP);
+  // handoff (batch 1-2): the previous output's words, all first polls in flight together
+  constexpr bool HAND = hand_batch(BP);
   constexpr int HB = HAND ? BP : 1;
   uint64_t hw[HB][2][4];
   if constexpr (HAND) {
@@ -592,6 +593,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
   const LaneLayout<G> L(lane);
   unsigned nbar = 0;  // grid barriers passed
   const uint32_t launch_seq = __ldcg(p.sync + 2);  // launches completed (advanced by the last CTA out)
+  const uint32_t epoch0 = launch_seq * static_cast<uint32_t>(p.ncalls);
   for (int j = 0; j < p.ncalls && !abort; ++j) {
     const CallLite c(p.calls[j]);
     const CallLite pc(p.calls[j > 0 ? j - 1 : 0]);
@@ -612,7 +614,7 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
       const int blk1 = min((ku_hi + 1) * BPI, c.K / kFwhtBlock);
       for (int blk = blk0 + warp; blk < blk1; blk += kNW)
         prep_block<TQ_PACK_2BIT, G, BP>(p, c, pc, static_cast<unsigned>(j), s_flag, blk, (blk - blk0) * (kFwhtBlock / G), L, xh,
-                          V, Fv, ssq, lane, nullptr, 0);
+                          V, Fv, ssq, lane, p.hand + static_cast<size_t>((j - 1) & 1) * p.hand_stride, epoch0 + j);
     }
     __syncthreads();
     if (s_flag[0] != 0) {  // a ready flag did not come in time
@@ -804,11 +806,15 @@ __global__ void __launch_bounds__(kNW * 32, 1) gemv_seq_kernel(const __grid_cons
     {
       int fr0, fr1;
       fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
-      finalize<BP, kRows, false>(c, part, ssq, p.B, fr0, fr1 - fr0, nullptr, 0);
+      finalize<BP, kRows, hand_batch(BP)>(c, part, ssq, p.B, fr0, fr1 - fr0,
+                                                        p.hand + static_cast<size_t>(j & 1) * p.hand_stride,
+                                                        epoch0 + j + 1);
     }
-    // ---- this CTA's rows are final: raise its flag ----
+    // ---- this CTA's rows are final: raise its flag (with the handoff only the CTA barrier: warps
+    //      do not start polling for the next input while their CTA still finalizes) ----
     __syncthreads();
-    if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
+    if (!hand_batch(BP) && threadIdx.x == 0)
+      st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
   }
 
   if (abort) drain_ring(full, kD, consumed, issued, cst, cph);
@@ -1135,14 +1141,13 @@ __global__ void __launch_bounds__(b3::kNW * 32, 1) gemv_seq_b3_kernel(const __gr
     {
       int fr0, fr1;
       fin_rows(c.N, cta, static_cast<int>(gridDim.x), fr0, fr1);
-      finalize<BP, kRows, hand_batch(TQ_PACK_B3, BP)>(c, part, ssq, p.B, fr0, fr1 - fr0,
+      finalize<BP, kRows, hand_batch(BP)>(c, part, ssq, p.B, fr0, fr1 - fr0,
                                                       p.hand + static_cast<size_t>(j & 1) * p.hand_stride, epoch0 + j + 1);
     }
-    // ---- this CTA's rows are final: raise its flag (unless they were handed over with their epochs) ----
-    if constexpr (!hand_batch(TQ_PACK_B3, BP)) {
-      __syncthreads();
-      if (threadIdx.x == 0) st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
-    }
+    // ---- this CTA's rows are final: raise its flag (with the handoff only the CTA barrier) ----
+    __syncthreads();
+    if (!hand_batch(BP) && threadIdx.x == 0)
+      st_release(p.sync + kFlagBase + cta, static_cast<unsigned>(j + 1));
   }
 
   if (abort) drain_ring(full, kD, consumed, issued, cst, cph);
@@ -1342,7 +1347,7 @@ extern "C" tq_status tq_seq_create(const tq_seq_call* calls, int ncalls, int bat
   s->ws_sync = align256((kFlagBase + static_cast<size_t>(sms)) * 4);
   s->ws_part = align256(2 * s->part_stride * 4);
   s->ws_ssq = align256(static_cast<size_t>(2) * s->ssq_stride * 4);
-  if (hand_batch(pack, s->Bp)) {  // each call's output with its epoch, two parities
+  if (hand_batch(s->Bp)) {  // each call's output with its epoch, two parities
     int Nmax = 0;
     for (int j = 0; j < ncalls; ++j) Nmax = std::max(Nmax, calls[j].d.N);
     s->hand_stride = static_cast<size_t>(s->Bp) * Nmax;
